@@ -1,0 +1,226 @@
+/*
+ * CPU FP64 oracle for exact scaled-dot-product attention forward, its chunk-pair partials and the
+ * exact LSE merge of partials. TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the
+ * benchmark's CPU-baseline leg call it; the library's product path never does. It shares no code
+ * with the CUDA path.
+ *
+ * What it computes (the plain definition; the pages never print the formula, so this follows
+ * their statement of the problem):
+ *   - "stream-cqsa 2.2.0 -> 2.2.2" diff, stream_cqsa/api.py, `attention` docstring: the call is a
+ *     drop-in for torch's F.scaled_dot_product_attention (SDPA), "exact";
+ *   - "stream-cqsa 2.2.2 -> 2.2.3" diff, stream_cqsa/oom_fallback.py, `stream_cqsa_auto`: each
+ *     call yields a per-row log-sum-exp ("lse") besides the output;
+ *   - "stream-cqsa 2.2.0 -> 2.2.2" diff, README profile-sweep section: outputs of subproblems are
+ *     merged into an accumulator.
+ *
+ * For query row i of head (b, h), with absolute positions q_off + i and kv_off + j:
+ *   A_i   = { j : 0 <= j < Nkv and (not causal or kv_off + j <= q_off + i) }
+ *   s_ij  = scale * sum_c q_ic k_jc                (double; fp16/bf16 inputs widened exactly)
+ *   M_i   = max_{j in A_i} s_ij
+ *   p_ij  = exp(s_ij - M_i),   l_i = sum_j p_ij   (Neumaier-compensated sums)
+ *   O_ic  = (sum_j p_ij v_jc) / l_i
+ *   LSE_i = M_i + log(l_i)                         (natural log, scale included)
+ * A row with A_i empty (a chunk pair entirely above the causal diagonal, or Nkv = 0) has O = 0 and
+ * LSE = -inf. The whole score row is materialised. `scale` arrives as the fp32 value the GPU uses,
+ * widened to double, so both sides compute with the identical scale.
+ *
+ * Merge of n partials of the same rows over disjoint key sets (exact in exact arithmetic):
+ *   M = max_k LSE_k,  lse = M + log(sum_k exp(LSE_k - M)),  O = sum_k exp(LSE_k - lse) O_k;
+ * all-empty rows (M = -inf) give O = 0, lse = -inf.
+ *
+ * A second routine, written separately, evaluates tiny problems in long double without the max
+ * subtraction (p_ij = exp(s_ij) directly), as a brute-force cross-check of the first.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+/* ---- exact widening of the storage types -------------------------------------------------- */
+
+/* IEEE 754 binary16: 1 sign, 5 exponent (bias 15), 10 fraction bits. */
+static double half_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 10) & 0x1f;
+    int fr = h & 0x3ff;
+    double v;
+    if (ex == 0) {
+        v = ldexp((double)fr, -24);                 /* subnormal: fr * 2^-24 */
+    } else if (ex == 31) {
+        v = fr ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(fr | 0x400), ex - 25);   /* (1024 + fr) * 2^(ex - 15 - 10) */
+    }
+    return sign ? -v : v;
+}
+
+/* bfloat16: the upper 16 bits of an IEEE 754 binary32. */
+static double bfloat_bits_to_double(uint16_t h) {
+    int sign = (h >> 15) & 1;
+    int ex = (h >> 7) & 0xff;
+    int fr = h & 0x7f;
+    double v;
+    if (ex == 0) {
+        v = ldexp((double)fr, -133);                /* subnormal: fr * 2^(-126 - 7) */
+    } else if (ex == 255) {
+        v = fr ? NAN : INFINITY;
+    } else {
+        v = ldexp((double)(fr | 0x80), ex - 134);   /* (128 + fr) * 2^(ex - 127 - 7) */
+    }
+    return sign ? -v : v;
+}
+
+static double widen(const uint16_t* base, int64_t idx, int dtype) {
+    return dtype == 0 ? half_bits_to_double(base[idx]) : bfloat_bits_to_double(base[idx]);
+}
+
+/* element (b, h, n, c) of a tensor with `rows` tokens; layout 0 = [B,H,rows,d], 1 = [B,rows,H,d] */
+static int64_t at(int layout, int64_t H, int64_t rows, int64_t d, int64_t b, int64_t h, int64_t n, int64_t c) {
+    return layout == 0 ? ((b * H + h) * rows + n) * d + c : ((b * rows + n) * H + h) * d + c;
+}
+
+/* Neumaier's improvement of Kahan summation (A. Neumaier, ZAMM 54, 1974). */
+typedef struct { double s, c; } nsum;
+static void nsum_add(nsum* a, double x) {
+    double t = a->s + x;
+    if (fabs(a->s) >= fabs(x)) a->c += (a->s - t) + x;
+    else a->c += (x - t) + a->s;
+    a->s = t;
+}
+static double nsum_get(const nsum* a) { return a->s + a->c; }
+
+/*
+ * Attention rows of one chunk pair (the whole problem when q_off = kv_off = 0, Nq = Nkv = N).
+ * q: [B,H,Nq,d] (or [B,Nq,H,d]), k, v: [B,H,Nkv,d] (or [B,Nkv,H,d]) storage bits of `dtype`
+ * (0 fp16, 1 bf16). rows: nrows triples (b, h, i) with 0 <= i < Nq. out: nrows x d, lse: nrows.
+ * Returns 0, or -1 on a bad argument.
+ */
+int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int layout, int dtype,
+                     int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t d, int64_t q_off,
+                     int64_t kv_off, int causal, double scale, const int64_t* rows, int64_t nrows,
+                     double* out, double* lse) {
+    if (B < 1 || H < 1 || Nq < 0 || Nkv < 0 || d < 1 || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t* t = rows + 3 * r;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= Nq) return -1;
+    }
+    int bad = 0;
+#pragma omp parallel
+    {
+        double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
+        double* qi = (double*)malloc(sizeof(double) * (size_t)d);
+        nsum* acc = (nsum*)malloc(sizeof(nsum) * (size_t)d);
+        if (!s || !qi || !acc) {
+#pragma omp atomic write
+            bad = 1;
+        }
+#pragma omp for schedule(dynamic, 1)
+        for (int64_t r = 0; r < nrows; ++r) {
+            if (bad) continue;
+            int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
+            double* o = out + r * d;
+            for (int64_t c = 0; c < d; ++c) qi[c] = widen(q, at(layout, H, Nq, d, b, h, i, c), dtype);
+            /* allowed keys are j < jend (causal: kv_off + j <= q_off + i) */
+            int64_t jend = Nkv;
+            if (causal) {
+                int64_t lim = q_off + i - kv_off + 1;
+                if (lim < jend) jend = lim;
+                if (jend < 0) jend = 0;
+            }
+            if (jend == 0) {
+                for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+                lse[r] = -INFINITY;
+                continue;
+            }
+            double m = -INFINITY;
+            for (int64_t j = 0; j < jend; ++j) {
+                nsum dot = {0.0, 0.0};
+                for (int64_t c = 0; c < d; ++c) nsum_add(&dot, qi[c] * widen(k, at(layout, H, Nkv, d, b, h, j, c), dtype));
+                s[j] = scale * nsum_get(&dot);
+                if (s[j] > m) m = s[j];
+            }
+            nsum l = {0.0, 0.0};
+            for (int64_t c = 0; c < d; ++c) acc[c] = (nsum){0.0, 0.0};
+            for (int64_t j = 0; j < jend; ++j) {
+                double p = exp(s[j] - m);
+                nsum_add(&l, p);
+                for (int64_t c = 0; c < d; ++c) nsum_add(&acc[c], p * widen(v, at(layout, H, Nkv, d, b, h, j, c), dtype));
+            }
+            double lv = nsum_get(&l);
+            for (int64_t c = 0; c < d; ++c) o[c] = nsum_get(&acc[c]) / lv;
+            lse[r] = m + log(lv);
+        }
+        free(s);
+        free(qi);
+        free(acc);
+    }
+    return bad ? -1 : 0;
+}
+
+/*
+ * Exact merge of n partials. O_parts[k]: rows x d, LSE_parts[k]: rows (double). out: rows x d,
+ * lse: rows. Partials are combined in the order k = 0 .. n-1.
+ */
+int oracle_merge(const double* const* O_parts, const double* const* LSE_parts, int n, int64_t rows,
+                 int64_t d, double* out, double* lse) {
+    if (n < 1 || rows < 0 || d < 1) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        double m = -INFINITY;
+        for (int k = 0; k < n; ++k) if (LSE_parts[k][r] > m) m = LSE_parts[k][r];
+        double* o = out + r * d;
+        if (m == -INFINITY) {
+            for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+            lse[r] = -INFINITY;
+            continue;
+        }
+        nsum z = {0.0, 0.0};
+        for (int k = 0; k < n; ++k) nsum_add(&z, exp(LSE_parts[k][r] - m));
+        double L = m + log(nsum_get(&z));
+        for (int64_t c = 0; c < d; ++c) {
+            nsum a = {0.0, 0.0};
+            for (int k = 0; k < n; ++k) {
+                if (LSE_parts[k][r] == -INFINITY) continue;   /* an empty part has weight 0 */
+                nsum_add(&a, exp(LSE_parts[k][r] - L) * O_parts[k][r * d + c]);
+            }
+            o[c] = nsum_get(&a);
+        }
+        lse[r] = L;
+    }
+    return 0;
+}
+
+/*
+ * Brute force for tiny problems (scores must stay small: no max subtraction), in long double,
+ * [B,H,N,d] layout, whole problem (no offsets). out: B*H*N*d, lse: B*H*N.
+ */
+int oracle_attn_bruteforce_ld(const uint16_t* q, const uint16_t* k, const uint16_t* v, int dtype,
+                              int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                              double* out, double* lse) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || N > 4096) return -1;
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const int64_t base = bh * N * d;
+        for (int64_t i = 0; i < N; ++i) {
+            long double den = 0.0L;
+            long double num[512];
+            if (d > 512) return -1;
+            for (int64_t c = 0; c < d; ++c) num[c] = 0.0L;
+            for (int64_t j = 0; j < N; ++j) {
+                if (causal && j > i) break;
+                long double sc = 0.0L;
+                for (int64_t c = 0; c < d; ++c)
+                    sc += (long double)widen(q, base + i * d + c, dtype) * (long double)widen(k, base + j * d + c, dtype);
+                long double e = expl((long double)scale * sc);
+                den += e;
+                for (int64_t c = 0; c < d; ++c) num[c] += e * (long double)widen(v, base + j * d + c, dtype);
+            }
+            for (int64_t c = 0; c < d; ++c) out[(bh * N + i) * d + c] = (double)(num[c] / den);
+            lse[bh * N + i] = (double)logl(den);
+        }
+    }
+    return 0;
+}
+
+/* exact widening exposed for the tests (storage bits -> double) */
+void oracle_widen(const uint16_t* bits, int64_t n, int dtype, double* out) {
+    for (int64_t i = 0; i < n; ++i) out[i] = widen(bits, i, dtype);
+}
