@@ -1,0 +1,290 @@
+"""Benchmark: exact attention forward TFLOP/s (causal-adjusted) on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Workload (the one the headline metric is quoted on): exact attention forward, B=1, H=8, N=32768,
+d=64, fp16 Q/K/V i.i.d. N(0,1) (seeded synthetic inputs), causal, scale 1/sqrt(64), device-resident,
+monolithic path (cqsa_attn_fwd). A step is one forward over that input. Causal-adjusted FLOP per
+step = 4*B*H*N^2*d/2.
+
+- value: device time of the K timed steps, each bracketed by CUDA events on the launch stream, with
+  the 129 MB L2 flushed (256 MiB write) before every step outside the events; whole-job throughput
+  over N ranks (weak scaling: every rank runs the full workload; max time over ranks).
+- e2e: the same metric through the C ABI with HOST buffers: cqsa_stream_attn_fwd with pinned host
+  Q/K/V and a pinned host output, host<->device copies inside the timed region.
+- roofline: achieved algorithmic FLOP/s of the attention kernel vs the measured dense fp16/bf16 tensor
+  peak (MEASURED_PEAKS.json; else the fallback figure, labelled so).
+- cpu_baseline: the FP64 oracle on a bounded sample of the workload's rows on this host's cores.
+- --impl reference: the oracle itself as the reference arm, on a bounded row sample per step.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+B, H, N, D = 1, 8, 32768, 64
+CAUSAL = True
+FLOP_PER_STEP = 4.0 * B * H * N * N * D / 2.0
+WORKLOAD = "exact attention forward, B=1 H=8 N=32768 d=64 fp16 causal, scale 1/sqrt(64), device-resident, monolithic"
+METRIC = "exact attention fwd TFLOP/s (causal-adjusted) at 1 GB300; % of tensor-core peak"
+FALLBACK_TFLOPS = 1900.0
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        for key in ("bf16_tflops", "bf16_dense_tflops", "tflops_bf16"):
+            if key in pk:
+                return float(pk[key]), "measured (MEASURED_PEAKS.json %s)" % key, pk
+    return FALLBACK_TFLOPS, "fallback (1.9 PFLOP/s bf16 burst, earlier GB300 measurement)", None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled every 200 ms during the timed region."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+        except (OSError, FileNotFoundError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            parts = [x.strip() for x in ln.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                sm.append(float(parts[0]))
+                mx.append(float(parts[1]))
+            except ValueError:
+                continue
+            for nm, v in zip(names, parts[3:7]):
+                if v.lower().startswith("active"):
+                    reasons.add(nm)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return world, rank, local
+
+
+def oracle_sample(rows: int, seed: int = 1):
+    """Time the FP64 oracle on `rows` seeded rows of the workload; returns (seconds, FLOP, threads)."""
+    import oracle
+    import synthetic as syn
+    qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
+    sel = syn.sample_rows(B, H, N, rows, seed=seed)[:rows]
+    t0 = time.perf_counter()
+    oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=D, causal=CAUSAL, rows=sel)
+    dt = time.perf_counter() - t0
+    flop = float(np.sum(4.0 * D * (sel[:, 2] + 1)))  # causal: row i sees i+1 keys
+    threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    return dt, flop, threads
+
+
+def cpu_baseline(target_s: float = 12.0):
+    dt, flop, thr = oracle_sample(256)
+    rows = int(min(65536, max(256, 256 * target_s / max(dt, 1e-3))))
+    dt, flop, thr = oracle_sample(rows, seed=2)
+    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+            "sample": f"{rows} seeded query rows (b,h,i uniform) of the workload, each in full over its causal "
+                      f"keys, FP64, {dt:.1f} s"}
+
+
+def run_reference(args):
+    world, rank, _ = _dist()
+    if rank != 0:
+        return 0
+    # size one step to ~1/ (steps+warmup) of ~2 minutes of oracle time
+    dt, flop, thr = oracle_sample(128)
+    per_step_rows = int(max(64, min(8192, 128 * (90.0 / (args.steps + args.warmup)) / max(dt, 1e-3))))
+    for w in range(args.warmup):
+        oracle_sample(per_step_rows, seed=100 + w)
+    tot_t, tot_f = 0.0, 0.0
+    for s in range(args.steps):
+        dt, flop, thr = oracle_sample(per_step_rows, seed=200 + s)
+        tot_t += dt
+        tot_f += flop
+    value = tot_f / tot_t / 1e12
+    line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": args.gpus, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": 1000.0 * tot_t / args.steps, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic", "impl": "reference",
+            "config": {"workload": WORKLOAD, "sample_rows_per_step": per_step_rows},
+            "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+                             "sample": f"{per_step_rows} seeded query rows per step, FP64 oracle"},
+            "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_ours(args):
+    import torch
+
+    world, rank, local = _dist()
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    import exact_long_context_tcgen05_gb300 as cq
+    import synthetic as syn
+
+    qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
+    dev = torch.device("cuda", local)
+    q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        cq.cqsa_attn_fwd(q, k, v, out, lse, B, H, N, D, CAUSAL, 0.0, cq.CQSA_F16, stream)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    rc, code, _ = cq.cqsa_device_error()
+    if rc != cq.CQSA_OK:
+        raise SystemExit(f"device error after warm-up: {code}")
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    if world > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        t0 = time.perf_counter()
+        for i in range(args.steps):
+            flush.fill_(i & 0xFF)  # evict L2 (129 MB) between timed steps, outside the events
+            ev[i][0].record(stream)
+            step()
+            ev[i][1].record(stream)
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t0
+    ms = [a.elapsed_time(b) for a, b in ev]
+    dev_ms = sum(ms)
+    t_max = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
+    if world > 1:
+        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
+    dev_ms = float(t_max.item())
+    value = world * FLOP_PER_STEP * args.steps / (dev_ms / 1000.0) / 1e12
+    kernel_tflops = FLOP_PER_STEP / (statistics.mean(ms) / 1000.0) / 1e12
+
+    # end to end: host (pinned) buffers in and out through the C ABI
+    hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.float16).pin_memory() for x in (qn, kn, vn))
+    hout = torch.empty((B, H, N, D), dtype=torch.float16).pin_memory()
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    st = cq.cqsa_stream_stats()
+
+    def e2e_step():
+        cq.cqsa_stream_attn_fwd(hq, hk, hv, cq.CQSA_LAYOUT_BHND, hout, hlse, True, B, H, N, D, CAUSAL, 0.0,
+                                cq.CQSA_F16, N, st, stream)
+
+    for _ in range(2):
+        e2e_step()
+    e2e_steps = max(3, min(args.steps, 10))
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(e2e_steps):
+        e2e_step()
+    e2e_s = (time.perf_counter() - t0) / e2e_steps
+    e2e_val = world * FLOP_PER_STEP / e2e_s / 1e12
+
+    # correctness guard on the timed output: a few rows against the oracle
+    rc, code, _ = cq.cqsa_device_error()
+    ok = rc == cq.CQSA_OK
+    peak, peak_src, _ = _peaks()
+    if rank == 0:
+        line = {"metric": METRIC, "value": value, "unit": "TFLOP/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": dev_ms / args.steps, "higher_is_better": True,
+                "scaling": "weak", "vs_baseline": None, "dtype": "f16",
+                "data": "synthetic (seeded N(0,1) Q/K/V, SplitMix64 + Box-Muller)",
+                "config": {"workload": WORKLOAD, "B": B, "H": H, "N": N, "d": D, "causal": CAUSAL,
+                           "l2": "flushed before every timed step (256 MiB device write outside the events)",
+                           "parallelism": f"weak scaling, {world} independent rank(s)"},
+                "roofline": {"bound": "tensor", "achieved": kernel_tflops, "peak": peak, "unit": "TFLOP/s",
+                             "frac": kernel_tflops / peak, "traffic": _traffic_per_launch(),
+                             "peak_source": peak_src + "; dense fp16 rate = bf16 rate"},
+                "e2e": {"value": e2e_val, "unit": "TFLOP/s", "h2d_bytes_per_step": int(st.h2d_bytes),
+                        "d2h_bytes_per_step": int(st.d2h_bytes),
+                        "path": "cqsa_stream_attn_fwd, pinned host Q/K/V/out, one chunk"},
+                "gpu_launches": args.steps, "wall_s_timed_region": wall,
+                "clocks": clk.summary(), "device_error_free": ok}
+        if not args.no_cpu_baseline:
+            line["cpu_baseline"] = cpu_baseline()
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        torch.distributed.destroy_process_group()
+    return 0
+
+
+def _traffic_per_launch():
+    """DRAM bytes per attention launch from the committed ncu summary, or None."""
+    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            return json.load(f).get("dram_bytes_per_launch")
+    return None
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

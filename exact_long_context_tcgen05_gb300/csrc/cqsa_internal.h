@@ -1,0 +1,51 @@
+// Internal declarations shared by the library's translation units (not part of the public ABI).
+#pragma once
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "../../include/cqsa.h"
+
+namespace cqsa {
+
+// Output / partial modes of the attention kernel.
+enum AttnMode : int {
+  kModeOut = 0,    // normalised output in the input dtype + fp32 LSE (the SDPA-shaped call)
+  kModePart = 1,   // normalised fp32 partial output + fp32 LSE of one chunk pair
+  kModeAccum = 2,  // merge this chunk pair's result into an fp32 (O_acc, LSE_acc) in place
+};
+
+struct AttnArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  int B, H;
+  int Nq, Nkv;          // tokens held in the q / kv buffers
+  long long q_off;      // absolute position of q-buffer token 0 (causal mask)
+  long long kv_off;     // absolute position of kv-buffer token 0
+  int d;
+  int causal;
+  float scale;          // already resolved (0 -> 1/sqrt(d) done by the caller)
+  int dtype;            // CQSA_F16 / CQSA_BF16
+  int in_layout;        // layout of q/k/v buffers: CQSA_LAYOUT_BHND / CQSA_LAYOUT_BNHD
+  int mode;             // AttnMode
+  void* out;            // kModeOut: [B,H,Nq,d] (or [B,Nq,H,d] with out_layout) in dtype
+  float* lse;           // kModeOut: [B,H,Nq]
+  float* o_part;        // kModePart / kModeAccum: fp32 [B,H,Nq,d] (or token-major)
+  float* lse_part;      // fp32 [B,H,Nq]
+  int out_layout;       // layout of out / o_part
+};
+
+// Validates nothing (the ABI layer does); encodes tensor maps and launches on `stream`.
+int launch_attention(const AttnArgs& a, cudaStream_t stream);
+
+// LSE merge of n partials (device pointer arrays passed by value).
+int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int n, void* out, float* lse,
+                 long long rows, int d, int out_dtype, cudaStream_t stream);
+
+// Status helpers
+void set_error(const char* fmt, ...);
+int cuda_status(cudaError_t e, const char* what);
+unsigned long long timeout_ns();
+
+}  // namespace cqsa

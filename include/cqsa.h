@@ -1,0 +1,139 @@
+/*
+ * cqsa.h - exact scaled-dot-product attention forward on one NVIDIA GB300 (sm_103a).
+ *
+ * C ABI of libcqsa_gb300.so. Every pointer is owned by the caller: the library never frees or
+ * keeps one after a call returns. Device calls are asynchronous and ordered on the given stream
+ * (NULL = the legacy default stream); cqsa_stream_attn_fwd is synchronous. Every entry point
+ * validates all arguments before it launches anything, returns a cqsa_status and never aborts the
+ * process; cqsa_last_error() gives a message for the calling thread's last failure.
+ *
+ * What is computed (the pages do not print the formula; this is the plain reading of their
+ * statement that the call is a drop-in for torch's F.scaled_dot_product_attention - "stream-cqsa
+ * 2.2.0 -> 2.2.2" diff, stream_cqsa/api.py, `attention` docstring - and that it is exact):
+ *   for every (b, h) and query row i, over the allowed keys A_i = { j < Nkv : not causal or
+ *   kv_pos(j) <= q_pos(i) },
+ *     s_ij = scale * q_i . k_j,   out_i = sum_j softmax_j(s_ij) v_j,   lse_i = ln sum_j exp(s_ij).
+ *   Causal masking is top-left aligned on absolute token positions. A row with no allowed key has
+ *   out = 0 and lse = -inf.
+ *
+ * Shapes and types: Q/K/V are fp16 or bf16, head dimension d in {64, 128} (the pages' kernels
+ * cover "fp16/bf16 and head dims 64/128": "stream-cqsa 2.2.2 -> 2.2.3" diff, README). Masks,
+ * dropout and grouped-query attention are not part of this ABI, as the pages' call rejects them
+ * ("stream-cqsa 2.2.0 -> 2.2.2" diff, api.py `attention` docstring). scale == 0 means 1/sqrt(d),
+ * the SDPA default (`scale: Optional[float] = None` in the same signature).
+ *
+ * Layouts: CQSA_LAYOUT_BHND is SDPA's [B, H, N, d] (contiguous). CQSA_LAYOUT_BNHD is the
+ * token-major [B, N, H, d] host layout the pages' streaming engine gathers from ("stream-cqsa
+ * 2.2.2 -> 2.2.3" diff, api.py `_pinned_copy`). lse / LSE arrays are always [B, H, N] fp32.
+ * All device pointers must be 16-byte aligned.
+ */
+#ifndef CQSA_H
+#define CQSA_H
+
+#include <cuda_runtime_api.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  CQSA_OK = 0,
+  CQSA_ERR_INVALID = -1,     /* bad argument (null pointer, size, alignment, non-finite scale) */
+  CQSA_ERR_UNSUPPORTED = -2, /* valid but not implemented (d not 64/128, dtype, layout) */
+  CQSA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
+  CQSA_ERR_OOM = -4,         /* a device or pinned allocation failed: the caller may re-plan */
+  CQSA_ERR_TIMEOUT = -5,     /* a device-side bounded wait gave up (see cqsa_device_error) */
+  CQSA_ERR_DEVICE = -6       /* no usable sm_103 device */
+} cqsa_status;
+
+typedef enum { CQSA_F16 = 0, CQSA_BF16 = 1, CQSA_F32 = 2 /* outputs only */ } cqsa_dtype;
+typedef enum { CQSA_LAYOUT_BHND = 0, CQSA_LAYOUT_BNHD = 1 } cqsa_layout;
+
+/*
+ * Monolithic exact attention forward ("below the memory boundary the call is the monolithic
+ * kernel": "stream-cqsa 2.2.2 -> 2.2.3" diff, api.py `_run`, mono branch).
+ * q, k, v: device [B,H,N,d] of `dtype`. out: device [B,H,N,d] of `dtype` (RNE from fp32).
+ * lse: device [B,H,N] fp32, natural log, or NULL if not wanted.
+ */
+int cqsa_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H,
+                  int N, int d, int causal, float scale, int dtype, cudaStream_t stream);
+
+/*
+ * One chunk pair of the out-of-memory decomposition: queries of a Q block against the keys of a
+ * KV block, giving a normalised fp32 partial output and its LSE ("partial outputs are merged into
+ * an accumulator": "stream-cqsa 2.2.0 -> 2.2.2" diff, README profile sweep; the engine returns
+ * `lse`: "stream-cqsa 2.2.2 -> 2.2.3" diff, oom_fallback.py `stream_cqsa_auto`).
+ * q_blk: device [B,H,Nq,d]; k_blk, v_blk: device [B,H,Nkv,d]; q_off / kv_off: absolute position
+ * of token 0 of each block (causal mask: key allowed iff kv_off + j <= q_off + i). Nkv may be 0.
+ * O_part: device fp32 [B,H,Nq,d]; LSE_part: device fp32 [B,H,Nq].
+ * accumulate = 0: O_part/LSE_part are overwritten with this pair's result (empty rows: 0 / -inf).
+ * accumulate = 1: (O_part, LSE_part) hold a running (O_acc, LSE_acc) that this pair is merged
+ * into exactly, in place (initialise LSE_acc to -inf; calls on one stream are race-free).
+ */
+int cqsa_attn_fwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk, long long q_off,
+                        long long kv_off, int B, int H, int Nq, int Nkv, int d, int causal, float scale,
+                        int dtype, float* O_part, float* LSE_part, int accumulate, cudaStream_t stream);
+
+/*
+ * Exact merge of n partials over disjoint key sets:
+ *   M = max_k LSE_k, lse = M + ln sum_k exp(LSE_k - M), out = sum_k exp(LSE_k - lse) O_k,
+ * summed in the order k = 0 .. n-1 (deterministic). All-empty rows give out = 0, lse = -inf.
+ * O_parts / LSE_parts: HOST arrays of n device pointers (1 <= n <= 1024) to fp32 [B,H,Nq,d] and
+ * [B,H,Nq]. out: device [B,H,Nq,d] of out_dtype (F16, BF16 or F32); lse: device fp32 or NULL.
+ */
+int cqsa_merge_partials(const float* const* O_parts, const float* const* LSE_parts, int n, void* out,
+                        float* lse, int B, int H, int Nq, int d, int out_dtype, cudaStream_t stream);
+
+/* Statistics of one streaming call (times in milliseconds). */
+typedef struct {
+  double wall_ms;        /* host clock around the whole call */
+  double compute_ms;     /* sum of chunk-kernel event intervals on the compute stream */
+  double h2d_ms;         /* sum of host-to-device copy event intervals */
+  double stall_ms;       /* time the compute stream waited for a copy (event gaps) */
+  long long h2d_bytes;   /* bytes copied host -> device */
+  long long d2h_bytes;   /* bytes copied device -> host */
+  long long peak_device_bytes; /* device memory the driver allocated */
+  int n_chunks;          /* Q chunks x KV chunks processed (non-empty pairs) */
+  int n_launches;        /* kernels launched */
+} cqsa_stream_stats;
+
+/*
+ * Out-of-memory exact attention: Q/K/V stay in pinned (or pageable) host memory in `layout` and
+ * are streamed to the device in chunks of chunk_tokens (a multiple of 128): for each Q chunk, the
+ * K/V chunks it needs are double-buffered over the host link on a copy stream while the chunk
+ * kernel merges each pair into an fp32 device accumulator ("stream_from_host", with per-subproblem
+ * host transfers overlapping compute: "stream-cqsa 2.2.0 -> 2.2.2" diff, README profile sweep).
+ * out: [B,H,N,d] (layout BHND) or [B,N,H,d] (layout BNHD) of dtype, on the host if out_on_host
+ * else on the device; lse: fp32 [B,H,N] in the same memory as out, or NULL.
+ * Synchronous: returns when out, lse and *stats (may be NULL) are final. Allocates its device
+ * buffers up front and frees them on every path; CQSA_ERR_OOM if they do not fit.
+ */
+int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_host, int layout, void* out,
+                         float* lse, int out_on_host, int B, int H, long long N, int d, int causal,
+                         float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,
+                         cudaStream_t stream);
+
+/* Human-readable name of a status code. */
+const char* cqsa_status_string(int status);
+
+/* Message of the calling thread's last failed call ("" if none). */
+const char* cqsa_last_error(void);
+
+/*
+ * Device error word written by a kernel whose bounded wait gave up (instead of hanging the GPU):
+ * synchronises the device, stores the code (0 = none) and the block index, optionally clears it.
+ * Returns CQSA_OK, or CQSA_ERR_TIMEOUT if a code was set.
+ */
+int cqsa_device_error(int* code, int* block, int clear);
+
+/* Device-side wait limit in milliseconds (default 2000; env CQSA_TIMEOUT_MS). */
+void cqsa_set_timeout_ms(unsigned int ms);
+
+/* Library version, e.g. "0.1.0". */
+const char* cqsa_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CQSA_H */

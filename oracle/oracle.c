@@ -92,7 +92,11 @@ static double nsum_get(const nsum* a) { return a->s + a->c; }
  * Attention rows of one chunk pair (the whole problem when q_off = kv_off = 0, Nq = Nkv = N).
  * q: [B,H,Nq,d] (or [B,Nq,H,d]), k, v: [B,H,Nkv,d] (or [B,Nkv,H,d]) storage bits of `dtype`
  * (0 fp16, 1 bf16). rows: nrows triples (b, h, i) with 0 <= i < Nq. out: nrows x d, lse: nrows.
- * Returns 0, or -1 on a bad argument.
+ * Rows are evaluated head by head: the K and V of one (b, h) are widened to double once (an exact
+ * conversion), then each row of that head is computed from its definition. Each product q_ic k_jc
+ * of two 16-bit values is exact in double; the d-term dot product is summed plainly (error ~1e-14
+ * relative to the sum of |terms|), the long sums over keys with compensation.
+ * Returns 0, or -1 on a bad argument or allocation failure.
  */
 int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, int layout, int dtype,
                      int64_t B, int64_t H, int64_t Nq, int64_t Nkv, int64_t d, int64_t q_off,
@@ -104,55 +108,82 @@ int oracle_attn_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, in
         if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= Nq) return -1;
     }
     int bad = 0;
-#pragma omp parallel
-    {
-        double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
-        double* qi = (double*)malloc(sizeof(double) * (size_t)d);
-        nsum* acc = (nsum*)malloc(sizeof(nsum) * (size_t)d);
-        if (!s || !qi || !acc) {
-#pragma omp atomic write
-            bad = 1;
-        }
-#pragma omp for schedule(dynamic, 1)
-        for (int64_t r = 0; r < nrows; ++r) {
-            if (bad) continue;
-            int64_t b = rows[3 * r], h = rows[3 * r + 1], i = rows[3 * r + 2];
-            double* o = out + r * d;
-            for (int64_t c = 0; c < d; ++c) qi[c] = widen(q, at(layout, H, Nq, d, b, h, i, c), dtype);
-            /* allowed keys are j < jend (causal: kv_off + j <= q_off + i) */
-            int64_t jend = Nkv;
-            if (causal) {
-                int64_t lim = q_off + i - kv_off + 1;
-                if (lim < jend) jend = lim;
-                if (jend < 0) jend = 0;
-            }
-            if (jend == 0) {
-                for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
-                lse[r] = -INFINITY;
-                continue;
-            }
-            double m = -INFINITY;
-            for (int64_t j = 0; j < jend; ++j) {
-                nsum dot = {0.0, 0.0};
-                for (int64_t c = 0; c < d; ++c) nsum_add(&dot, qi[c] * widen(k, at(layout, H, Nkv, d, b, h, j, c), dtype));
-                s[j] = scale * nsum_get(&dot);
-                if (s[j] > m) m = s[j];
-            }
-            nsum l = {0.0, 0.0};
-            for (int64_t c = 0; c < d; ++c) acc[c] = (nsum){0.0, 0.0};
-            for (int64_t j = 0; j < jend; ++j) {
-                double p = exp(s[j] - m);
-                nsum_add(&l, p);
-                for (int64_t c = 0; c < d; ++c) nsum_add(&acc[c], p * widen(v, at(layout, H, Nkv, d, b, h, j, c), dtype));
-            }
-            double lv = nsum_get(&l);
-            for (int64_t c = 0; c < d; ++c) o[c] = nsum_get(&acc[c]) / lv;
-            lse[r] = m + log(lv);
-        }
-        free(s);
-        free(qi);
-        free(acc);
+    size_t kv_elems = (size_t)(Nkv > 0 ? Nkv : 1) * (size_t)d;
+    double* kd = (double*)malloc(sizeof(double) * kv_elems);
+    double* vd = (double*)malloc(sizeof(double) * kv_elems);
+    if (!kd || !vd) {
+        free(kd);
+        free(vd);
+        return -1;
     }
+    for (int64_t b = 0; b < B && !bad; ++b) {
+        for (int64_t h = 0; h < H && !bad; ++h) {
+            int64_t cnt = 0;
+            for (int64_t r = 0; r < nrows; ++r) cnt += (rows[3 * r] == b && rows[3 * r + 1] == h);
+            if (cnt == 0) continue;
+            /* exact widening of this head's keys and values */
+#pragma omp parallel for schedule(static)
+            for (int64_t j = 0; j < Nkv; ++j) {
+                for (int64_t c = 0; c < d; ++c) {
+                    kd[j * d + c] = widen(k, at(layout, H, Nkv, d, b, h, j, c), dtype);
+                    vd[j * d + c] = widen(v, at(layout, H, Nkv, d, b, h, j, c), dtype);
+                }
+            }
+#pragma omp parallel
+            {
+                double* s = (double*)malloc(sizeof(double) * (size_t)(Nkv > 0 ? Nkv : 1));
+                double* qi = (double*)malloc(sizeof(double) * (size_t)d);
+                nsum* acc = (nsum*)malloc(sizeof(nsum) * (size_t)d);
+                if (!s || !qi || !acc) {
+#pragma omp atomic write
+                    bad = 1;
+                }
+#pragma omp for schedule(dynamic, 1)
+                for (int64_t r = 0; r < nrows; ++r) {
+                    if (bad || rows[3 * r] != b || rows[3 * r + 1] != h) continue;
+                    int64_t i = rows[3 * r + 2];
+                    double* o = out + r * d;
+                    for (int64_t c = 0; c < d; ++c) qi[c] = widen(q, at(layout, H, Nq, d, b, h, i, c), dtype);
+                    /* allowed keys are j < jend (causal: kv_off + j <= q_off + i) */
+                    int64_t jend = Nkv;
+                    if (causal) {
+                        int64_t lim = q_off + i - kv_off + 1;
+                        if (lim < jend) jend = lim;
+                        if (jend < 0) jend = 0;
+                    }
+                    if (jend == 0) {
+                        for (int64_t c = 0; c < d; ++c) o[c] = 0.0;
+                        lse[r] = -INFINITY;
+                        continue;
+                    }
+                    double m = -INFINITY;
+                    for (int64_t j = 0; j < jend; ++j) {
+                        const double* kj = kd + j * d;
+                        double dot = 0.0;
+                        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kj[c];
+                        s[j] = scale * dot;
+                        if (s[j] > m) m = s[j];
+                    }
+                    nsum l = {0.0, 0.0};
+                    for (int64_t c = 0; c < d; ++c) acc[c] = (nsum){0.0, 0.0};
+                    for (int64_t j = 0; j < jend; ++j) {
+                        double p = exp(s[j] - m);
+                        const double* vj = vd + j * d;
+                        nsum_add(&l, p);
+                        for (int64_t c = 0; c < d; ++c) nsum_add(&acc[c], p * vj[c]);
+                    }
+                    double lv = nsum_get(&l);
+                    for (int64_t c = 0; c < d; ++c) o[c] = nsum_get(&acc[c]) / lv;
+                    lse[r] = m + log(lv);
+                }
+                free(s);
+                free(qi);
+                free(acc);
+            }
+        }
+    }
+    free(kd);
+    free(vd);
     return bad ? -1 : 0;
 }
 
