@@ -263,18 +263,29 @@ def run_ours(args):
 
 
 def _traffic_per_launch():
-    """DRAM bytes per attention launch from the committed ncu summary, or None."""
-    path = os.path.join(ROOT, "profiles", "attn_fwd_traffic.json")
-    if os.path.exists(path):
-        with open(path) as f:
-            return json.load(f).get("dram_bytes_per_launch")
-    return None
+    """DRAM bytes per attention launch from the committed ncu summary of this workload, or None when
+    the kernel source has changed since those counters were taken (the summary records its hash)."""
+    import hashlib
+    import re
+    path = os.path.join(ROOT, "profiles", "attn_fwd_f16_d64_causal_N32768.md")
+    src = os.path.join(ROOT, "exact_long_context_tcgen05_gb300", "csrc", "attn_fwd.cu")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        text = f.read()
+    with open(src, "rb") as f:
+        sha = hashlib.sha256(f.read()).hexdigest()[:16]
+    m_sha = re.search(r"sha256\[:16\] = `([0-9a-f]{16})`", text)
+    m_b = re.search(r"\| dram_bytes_per_launch \| (\d+) \|", text)
+    if not m_sha or not m_b or m_sha.group(1) != sha:
+        return None
+    return int(m_b.group(1))
 
 
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -66,7 +66,9 @@ def test_shapes_and_tails(cq, N, d, dtype, causal):
     assert_close(o32, ref_o, to_np64(L), ref_l, what="bf16 fp32 result")
     got = to_np64(out)
     assert np.array_equal(got, _bf16_rne(O.cpu().numpy())), "bf16 output is not RNE of the fp32 result"
-    assert np.all(np.abs(got - _bf16_rne(ref_o.astype(np.float32))) <= _bf16_ulp(ref_o) * 1.0001)
+    # hence |out - oracle| <= half a bf16 ulp of out + the fp32 result's own error (a plain "one ulp of
+    # the rounded oracle" cannot hold for outputs near zero, where the fp32 error exceeds a bf16 ulp)
+    assert np.all(np.abs(got - ref_o) <= 0.5 * _bf16_ulp(got) + np.abs(o32 - ref_o) + 1e-12)
     assert np.array_equal(to_np64(lse), to_np64(L))
 
 
