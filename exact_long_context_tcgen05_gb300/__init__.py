@@ -20,7 +20,9 @@ CQSA_F16, CQSA_BF16, CQSA_F32 = 0, 1, 2
 CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
-            "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms", "cqsa_version")
+            "cqsa_attn_fwd_chunked_static", "cqsa_status_string", "cqsa_last_error", "cqsa_device_error",
+            "cqsa_set_timeout_ms", "cqsa_version")
+CQSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
 class CqsaError(RuntimeError):
@@ -51,6 +53,7 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_merge_partials.argtypes = [_vp, _vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp]
     lib.cqsa_stream_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _ll,
                                          ctypes.POINTER(cqsa_stream_stats), _vp]
+    lib.cqsa_attn_fwd_chunked_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]
     lib.cqsa_status_string.argtypes = [_i]
     lib.cqsa_status_string.restype = ctypes.c_char_p
     lib.cqsa_last_error.argtypes = []
@@ -61,7 +64,7 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_version.argtypes = []
     lib.cqsa_version.restype = ctypes.c_char_p
     for name in ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
-                 "cqsa_device_error"):
+                 "cqsa_attn_fwd_chunked_static", "cqsa_device_error"):
         getattr(lib, name).restype = _i
     return lib
 
@@ -141,6 +144,14 @@ def cqsa_stream_attn_fwd(q_host, k_host, v_host, layout, out, lse, out_on_host, 
     return _check(lib.cqsa_stream_attn_fwd(_ptr(q_host), _ptr(k_host), _ptr(v_host), layout, _ptr(out), _ptr(lse),
                                            int(bool(out_on_host)), B, H, N, d, int(bool(causal)), float(scale), dtype,
                                            chunk_tokens, ctypes.byref(st), _stream(stream)))
+
+
+def cqsa_attn_fwd_chunked_static(q, k, v, out, lse, B, H, N, d, causal, scale, dtype, chunk_tokens,
+                                 stream=None) -> int:
+    """No-allocation chunked forward (scratch in the library's static device array)."""
+    return _check(lib.cqsa_attn_fwd_chunked_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
+                                                   int(bool(causal)), float(scale), dtype, chunk_tokens,
+                                                   _stream(stream)))
 
 
 def cqsa_device_error(clear: bool = True):

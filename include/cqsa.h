@@ -113,6 +113,31 @@ int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_h
                          float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,
                          cudaStream_t stream);
 
+/*
+ * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).
+ */
+#define CQSA_STATIC_SCRATCH_BYTES (32u << 20)
+
+/*
+ * Chunked exact attention over device-resident q, k, v ([B,H,N,d], fp16/bf16) into out ([B,H,N,d],
+ * same dtype) and lse ([B,H,N] fp32, or NULL) that ALLOCATES NOTHING. It is for callers that cannot
+ * let a library call cudaMalloc (code running under its own memory pool or a hard device-memory
+ * budget, where an allocation inside the call would fail, exceed the budget or synchronise the device
+ * at an unwanted point). The paper has no counterpart of this entry point: it is a library facility.
+ * The computation is the same as cqsa_stream_attn_fwd's (key chunks of chunk_tokens merged exactly
+ * into an fp32 accumulator, one query chunk and one (b, h) at a time), but the accumulator lives in
+ * a fixed file-scope device array of CQSA_STATIC_SCRATCH_BYTES, held by every device on which the
+ * library's module is loaded until the process exits. chunk_tokens must be a multiple of 128 with
+ * chunk_tokens * (d + 1) * 4 <= CQSA_STATIC_SCRATCH_BYTES, else CQSA_ERR_UNSUPPORTED.
+ * The first call on a device looks up the array's device address (cudaGetSymbolAddress) with that
+ * device current; make that first call before any stream capture. All calls share the array and it
+ * keeps the last call's contents: calls whose work overlaps on the GPU (different streams, or host
+ * threads without ordering between them) race on it. Asynchronous on `stream`.
+ */
+int cqsa_attn_fwd_chunked_static(const void* q, const void* k, const void* v, void* out, float* lse, int B,
+                                 int H, int N, int d, int causal, float scale, int dtype, int chunk_tokens,
+                                 cudaStream_t stream);
+
 /* Human-readable name of a status code. */
 const char* cqsa_status_string(int status);
 
