@@ -21,7 +21,7 @@ CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_status_string", "cqsa_last_error", "cqsa_device_error",
-            "cqsa_set_timeout_ms", "cqsa_version")
+            "cqsa_set_timeout_ms", "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -61,6 +61,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_device_error.argtypes = [ctypes.POINTER(_i), ctypes.POINTER(_i), _i]
     lib.cqsa_set_timeout_ms.argtypes = [ctypes.c_uint]
     lib.cqsa_set_timeout_ms.restype = None
+    lib.cqsa_debug_set_fault.argtypes = [_i]
+    lib.cqsa_debug_set_fault.restype = _i
     lib.cqsa_version.argtypes = []
     lib.cqsa_version.restype = ctypes.c_char_p
     for name in ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
@@ -163,6 +165,10 @@ def cqsa_device_error(clear: bool = True):
 
 def cqsa_set_timeout_ms(ms: int) -> None:
     lib.cqsa_set_timeout_ms(ms)
+
+
+def cqsa_debug_set_fault(kind: int) -> int:
+    return _check(lib.cqsa_debug_set_fault(kind))
 
 
 def cqsa_version() -> str:

@@ -15,6 +15,9 @@ int device_error_word(DevErr* out, int clear);  // attn_fwd.cu (owns the device 
 
 static thread_local char t_err[512];
 static unsigned int g_timeout_ms = 0;
+static int g_fault = 0;
+
+int debug_fault() { return g_fault; }
 
 void set_error(const char* fmt, ...) {
   va_list ap;
@@ -96,6 +99,15 @@ const char* cqsa_status_string(int status) {
 }
 
 void cqsa_set_timeout_ms(unsigned int ms) { g_timeout_ms = ms; }
+
+int cqsa_debug_set_fault(int kind) {
+  if (kind < 0 || kind > 1) {
+    set_error("unknown fault kind %d", kind);
+    return CQSA_ERR_INVALID;
+  }
+  g_fault = kind;
+  return CQSA_OK;
+}
 
 int cqsa_device_error(int* code, int* block, int clear) {
   t_err[0] = 0;

@@ -29,6 +29,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
+#include <stdlib.h>
 
 #include "cqsa_internal.h"
 #include "sm103_ptx.cuh"
@@ -42,7 +43,12 @@ namespace {
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
 constexpr int NTHREADS = 192;  // 6 warps
-constexpr float TAU = 8.0f;    // allowed growth of the row max over m_ref (log2 units) before a rescale
+// m_ref is raised (to ceil of the tile's row max) whenever a tile's row max exceeds it, so every
+// exponent argument is <= 0: ex2.approx is exactly covariant under integer shifts of its argument
+// only while the argument keeps its sign, and the chunked and monolithic paths (whose m_ref differ
+// by integers) must produce P values that differ by exact powers of two. Rescales stay rare: the
+// integer m_ref moves only when the running max crosses an integer.
+constexpr float TAU = 0.0f;
 constexpr uint32_t TILE_BYTES = 128 * 64 * 2;  // one 128 x 64 box of 16-bit elements
 constexpr uint32_t TMEM_COLS = 512;
 constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 384;
@@ -59,6 +65,7 @@ struct KParams {
   float* lse_part;
   int out_layout;
   unsigned long long timeout_ns;
+  int fault;  // test hook: 1 = block 0 never loads key tile 1 (its waits must time out cleanly)
 };
 
 template <int D>
@@ -118,6 +125,34 @@ __device__ __forceinline__ float exp2_int(float k) {
   int e = static_cast<int>(k);
   if (e < -126) return 0.0f;
   return __int_as_float((e + 127) << 23);
+}
+
+__device__ __forceinline__ float max3(float a, float b, float c) {
+  float r;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(r) : "f"(a), "f"(b), "f"(c));
+  return r;
+}
+
+// Row maximum of 128 scores: three-input max, four independent chains.
+__device__ __forceinline__ float row_max128(const float (&x)[128]) {
+  float m0 = x[0], m1 = x[1], m2 = x[2], m3 = x[3];
+#pragma unroll
+  for (int c = 4; c < 128; c += 8) {
+    m0 = max3(m0, x[c], x[c + 1]);
+    m1 = max3(m1, x[c + 2], x[c + 3]);
+    m2 = max3(m2, x[c + 4], x[c + 5]);
+    m3 = max3(m3, x[c + 6], x[c + 7]);
+  }
+  return fmaxf(fmaxf(m0, m1), fmaxf(m2, m3));
+}
+
+// p = exp2(fl(x * scale*log2e + 192) - (192 + m_ref)) for the pair (x0, x1), with packed fp32x2
+// arithmetic. The first rounding puts the argument on a grid fixed by x alone (2^-16 while the
+// sum stays in [128, 256)), so the subtraction of the integer-valued 192 + m_ref is exact.
+__device__ __forceinline__ float2 exp_pair(float x0, float x1, float2 sl2v, float2 ncm) {
+  const float2 t = __ffma2_rn(make_float2(x0, x1), sl2v, make_float2(192.0f, 192.0f));
+  const float2 r = __fadd2_rn(t, ncm);
+  return make_float2(fast_exp2(r.x), fast_exp2(r.y));
 }
 
 __device__ __forceinline__ long long out_row_index(int layout, int b, int h, int H, int N, int i) {
@@ -339,15 +374,7 @@ __global__ void __launch_bounds__(NTHREADS, 1)
         for (int c = 0; c < 128; ++c)
           if (c >= lim) x[c] = -INFINITY;
       }
-      float mx0 = x[0], mx1 = x[1], mx2 = x[2], mx3 = x[3];
-#pragma unroll
-      for (int c = 4; c < 128; c += 4) {
-        mx0 = fmaxf(mx0, x[c]);
-        mx1 = fmaxf(mx1, x[c + 1]);
-        mx2 = fmaxf(mx2, x[c + 2]);
-        mx3 = fmaxf(mx3, x[c + 3]);
-      }
-      const float tmax = fmaxf(fmaxf(mx0, mx1), fmaxf(mx2, mx3)) * sl2;
+      const float tmax = row_max128(x) * sl2;
       float alpha = 1.0f;
       bool rescale = false;
       if (tmax > m_ref + TAU) {
@@ -362,30 +389,31 @@ __global__ void __launch_bounds__(NTHREADS, 1)
       // for |t - 192| < 64), so t - (192 + m_ref) is exact and p for two different integer m_ref
       // differ by an exact power of two; the 16-bit rounding of P then commutes with that factor.
       const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
+      const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
+      float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
       const uint32_t pbuf = trow + COL_P + (j & 1) * 128;
-      float rs[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
       for (int c4 = 0; c4 < 4; ++c4) {
         uint32_t hi[16], lo[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const float p0 = fast_exp2(fmaf(x[c4 * 32 + 2 * e], sl2, 192.0f) - cm);
-          const float p1 = fast_exp2(fmaf(x[c4 * 32 + 2 * e + 1], sl2, 192.0f) - cm);
-          rs[e & 3] += p0 + p1;
+          const int c = c4 * 16 + e;  // pair index: keys 2c, 2c+1
+          const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
+          rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
           if (DT) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(p0, p1);
+            __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
             const float2 hf = __bfloat1622float2(h2);
-            __nv_bfloat162 l2 = __floats2bfloat162_rn(p0 - hf.x, p1 - hf.y);
+            __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
             hi[e] = *reinterpret_cast<uint32_t*>(&h2);
             lo[e] = *reinterpret_cast<uint32_t*>(&l2);
           } else {
-            hi[e] = pack2(p0, p1, 0);
+            hi[e] = pack2(pp.x, pp.y, 0);
           }
         }
         tmem_st16(pbuf + c4 * 16, hi);
         if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
       }
-      l = l * alpha + ((rs[0] + rs[1]) + (rs[2] + rs[3]));
+      l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
       if (__any_sync(0xffffffffu, rescale) && j > 0) {
         // O must hold the result of PV(j-1) before it is scaled (alpha is 1 on rows that keep m_ref).
         // Parity wait on phase j-1 is exact here: S_j complete implies PV(j-2) complete (S_j is
@@ -505,31 +533,600 @@ __global__ void __launch_bounds__(NTHREADS, 1)
   }
 }
 
-template <int D, int DT, bool CAUSAL, int MODE>
-int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const KParams& kp, int grid,
-             cudaStream_t stream) {
-  auto kern = attn_fwd_kernel<D, DT, CAUSAL, MODE>;
-  static bool attr_done = false;  // per instantiation; benign race (idempotent call)
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
-    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem)");
-    attr_done = true;
+// MMA issue from one elected lane of a converged warp, with descriptors prepared by the whole warp
+// and the accumulate flag as an immediate: measured on GB300 to issue at the tensor pipe's own rate
+// (a 128x64x16 MMA every 32 cycles), while issuing from a lone thread with register-held flags costs
+// ~150 cycles per MMA whatever its size.
+template <int ACC>
+__device__ __forceinline__ void mma_ss_i(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 1;" ::"r"(d), "l"(a), "l"(b), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, 0;" ::"r"(d), "l"(a), "l"(b), "r"(idesc)
+                 : "memory");
+}
+template <int ACC>
+__device__ __forceinline__ void mma_ts_i(uint32_t d, uint32_t a, uint64_t b, uint32_t idesc) {
+  if (ACC)
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 1;" ::"r"(d), "r"(a), "l"(b), "r"(idesc)
+                 : "memory");
+  else
+    asm volatile("tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, 0;" ::"r"(d), "r"(a), "l"(b), "r"(idesc)
+                 : "memory");
+}
+__device__ __forceinline__ bool elect_one() {
+  uint32_t p;
+  asm volatile("{\n\t.reg .pred e;\n\telect.sync _|e, 0xffffffff;\n\tselp.u32 %0, 1, 0, e;\n\t}" : "=r"(p));
+  return p != 0;
+}
+
+// S = Q K^T for one query tile: D/16 MMAs of 128x128x16 (K-major Q and K, 128-byte swizzle).
+template <int D>
+__device__ __forceinline__ void issue_qk(uint32_t dcol, uint64_t a0, uint64_t b0, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    const uint32_t off = static_cast<uint32_t>((ks >> 2) * (TILE_BYTES >> 4) + (ks & 3) * 2);
+    if (ks == 0) mma_ss_i<0>(dcol, a0 + off, b0 + off, idesc);
+    else mma_ss_i<1>(dcol, a0 + off, b0 + off, idesc);
   }
-  kern<<<grid, NTHREADS, Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, kp);
+}
+
+// O += P V for one query tile: 8 MMAs of 128 x D x 16 (P from tensor memory, V MN-major); bf16 adds
+// the P_lo half. FIRST: the first MMA overwrites O.
+template <int D, int DT, bool FIRST>
+__device__ __forceinline__ void issue_pv(uint32_t ocol, uint32_t pcol, uint64_t v0, uint32_t idesc) {
+#pragma unroll
+  for (int ks = 0; ks < BN / 16; ++ks) {
+    const uint64_t bd = v0 + static_cast<uint32_t>(ks * (2048 >> 4));
+    if (FIRST && ks == 0) mma_ts_i<0>(ocol, pcol + ks * 8, bd, idesc);
+    else mma_ts_i<1>(ocol, pcol + ks * 8, bd, idesc);
+    if (DT) mma_ts_i<1>(ocol, pcol + 64 + ks * 8, bd, idesc);
+  }
+}
+
+// ---------------------------------------------------------------------------------------------
+// Two query tiles per CTA (256 rows of one (batch, head)), two softmax warpgroups. While one
+// warpgroup computes its softmax, the tensor pipe runs the other tile's MMAs, and each SM sub-
+// partition has two softmax warps to interleave. K/V tiles are loaded once for both query tiles.
+//   warp 0      TMA producer          warp 1      TMEM allocation + MMA issue for query tile 0
+//   warp 2      MMA issue for tile 1  warp 3      idle (warpgroup 0 gives registers to the softmax)
+//   warps 4..7  softmax of tile 0     warps 8..11 softmax of tile 1
+// Tensor memory: S0, S1 at 0 / 128. fp16 with d = 64 keeps P apart (P0, P1 at 256 / 320, O0, O1 at
+// 384 / 448), so S_t(j+1) is computed as soon as S_t(j) has been read. Otherwise (d = 128, or bf16
+// whose P_hi|P_lo fills 128 columns) P_t is written over S_t and the MMA issuer waits for PV_t(j)
+// to finish reading it before S_t(j+1) overwrites the columns; O0, O1 then sit at 256 / 256 + d.
+// ---------------------------------------------------------------------------------------------
+constexpr int NTHREADS2 = 384;
+// Register split (setmaxnreg): the launch gives 384 x 168 registers; warpgroup 0 (producer, MMA issuer,
+// two idle warps) drops to 72 and the two softmax warpgroups rise to 216: 128*72 + 256*216 = 384*168.
+constexpr int REGS_LOW = 72, REGS_HIGH = 216;
+static_assert(128 * REGS_LOW + 256 * REGS_HIGH <= NTHREADS2 * 168, "register split exceeds the launch allocation");
+
+template <int D, int DT>
+struct Cfg2 {
+  static constexpr bool ALIAS = (D == 128) || (DT == 1);
+  static constexpr int KSUB = D / 64;
+  static constexpr int STAGES = (D == 64) ? 4 : 2;
+  static constexpr uint32_t QT_BYTES = KSUB * TILE_BYTES;
+  static constexpr uint32_t KV_BYTES = KSUB * TILE_BYTES;
+  static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
+  static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
+  static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
+  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
+  static constexpr uint32_t SMEM_BYTES = 1024 + 2 * QT_BYTES + 2 * STAGES * KV_BYTES + NBARS * 8 + 16;
+  static_assert(COL_O1 + D <= TMEM_COLS, "tensor memory layout exceeds 512 columns");
+};
+
+template <int D, int DT, bool CAUSAL, int MODE>
+__global__ void __launch_bounds__(NTHREADS2, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const KParams p) {
+  using C = Cfg2<D, DT>;
+  constexpr int STAGES = C::STAGES;
+  constexpr int KSUB = C::KSUB;
+  constexpr bool ALIAS = C::ALIAS;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  uint8_t* sQ = smem;  // tile t at sQ + t * QT_BYTES
+  uint8_t* sK = sQ + 2 * C::QT_BYTES;
+  uint8_t* sV = sK + STAGES * C::KV_BYTES;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES);
+  uint64_t* bar_q = bars;
+  uint64_t* bar_k_full = bar_q + 1;
+  uint64_t* bar_v_full = bar_k_full + STAGES;
+  uint64_t* bar_kv_empty = bar_v_full + STAGES;
+  uint64_t* bar_s_full = bar_kv_empty + STAGES;  // [2]
+  uint64_t* bar_s_free = bar_s_full + 2;         // [2] (P kept apart only)
+  uint64_t* bar_p_full = bar_s_free + 2;         // [2]
+  uint64_t* bar_pv_done = bar_p_full + 2;        // [2]
+  uint64_t* bar_o_final = bar_pv_done + 2;       // [2] single phase each
+  uint64_t* bar_mma_idle = bar_o_final + 2;     // [2] one per MMA warp
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_idle + 2);
+  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
+
+  const int warp = threadIdx.x >> 5;
+  const int lane = threadIdx.x & 31;
+
+  // Work unit: a pair of query tiles, heaviest (latest) first.
+  const int unit = blockIdx.x;
+  const int qp = p.n_q_tiles - 1 - unit / p.BH;
+  const int bh = unit % p.BH;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  int q0[2], n_kv[2];
+#pragma unroll
+  for (int t = 0; t < 2; ++t) {
+    q0[t] = qp * 2 * BM + t * BM;
+    const int rows = min(BM, p.Nq - q0[t]);
+    int n = (p.Nkv + BN - 1) / BN;
+    if (rows <= 0) {
+      n = 0;
+    } else if (CAUSAL) {
+      const long long last_key = p.q_off + q0[t] + rows - 1 - p.kv_off;
+      n = last_key < 0 ? 0 : (last_key / BN + 1 < n ? static_cast<int>(last_key / BN + 1) : n);
+    }
+    n_kv[t] = n;
+  }
+  const int n_max = max(n_kv[0], n_kv[1]);
+
+  if (threadIdx.x == 0) {
+    mbar_init(bar_q, 1);
+    for (int s = 0; s < STAGES; ++s) {
+      mbar_init(&bar_k_full[s], 1);
+      mbar_init(&bar_v_full[s], 1);
+      mbar_init(&bar_kv_empty[s], 2);  // one arrival per MMA warp
+    }
+    for (int t = 0; t < 2; ++t) {
+      mbar_init(&bar_s_full[t], 1);
+      mbar_init(&bar_s_free[t], 128);
+      mbar_init(&bar_p_full[t], 128);
+      mbar_init(&bar_pv_done[t], 1);
+      mbar_init(&bar_o_final[t], 1);
+      mbar_init(&bar_mma_idle[t], 1);
+    }
+    *abort_flag = 0;
+    fence_mbar_init();
+  }
+  if (warp == 1) {
+    __syncwarp();
+    tmem_alloc(tmem_slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const unsigned long long tmo = p.timeout_ns;
+  // Each warpgroup changes its register budget at the top of its own branch and leaves through its
+  // own copy of the teardown barrier, so no code runs under two different budgets.
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
+  if (warp == 0) {
+    // ------------------------------------------------------------------ TMA producer
+    if (lane == 0 && n_max > 0) {
+      mbar_arrive_expect_tx(bar_q, 2 * C::QT_BYTES);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sQ + t * C::QT_BYTES + s * TILE_BYTES, &tmQ, bar_q, s * 64, q0[t], h, b);
+      int issued = 0;
+      int skipped = -1;  // fault injection: the key/value tile never loaded
+      for (int j = 0; j < n_max; ++j) {
+        const int stage = j % STAGES;
+        const uint32_t round = j / STAGES;
+        if (!wait_or_abort(&bar_kv_empty[stage], (round & 1u) ^ 1u, tmo, abort_flag, kDevTimeoutKV, 10)) break;
+        if (p.fault == 1 && blockIdx.x == 0 && j == 1) {
+          skipped = j;
+          issued = j + 1;
+          continue;
+        }
+        mbar_arrive_expect_tx(&bar_k_full[stage], C::KV_BYTES);
+#pragma unroll
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sK + stage * C::KV_BYTES + s * TILE_BYTES, &tmK, &bar_k_full[stage], s * 64, j * BN, h, b);
+        mbar_arrive_expect_tx(&bar_v_full[stage], C::KV_BYTES);
+#pragma unroll
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sV + stage * C::KV_BYTES + s * TILE_BYTES, &tmV, &bar_v_full[stage], s * 64, j * BN, h, b);
+        issued = j + 1;
+      }
+      {
+        // Every load issued must land before the CTA exits (bounded waits, no abort check); on the
+        // normal path these phases are already complete.
+        for (int j = max(0, issued - STAGES); j < issued; ++j) {
+          if (j == skipped) continue;
+          const int stage = j % STAGES;
+          const uint32_t par = (j / STAGES) & 1u;
+          mbar_wait_bounded(&bar_k_full[stage], par, tmo);
+          mbar_wait_bounded(&bar_v_full[stage], par, tmo);
+        }
+        mbar_wait_bounded(bar_q, 0, tmo);
+      }
+    }
+  } else if (warp == 1 || warp == 2) {
+    // ------------------------------------------------------------------ MMA issuers
+    // Warp 1 issues every MMA of query tile 0 and warp 2 every MMA of tile 1, on different SM
+    // sub-partitions, each on its own schedule. Each warp runs its schedule and barrier waits
+    // converged (warp-uniform values); one elected lane issues each MMA group and commit.
+    const int t = warp - 1;
+    const bool leader = elect_one();
+    const int nkv = n_kv[t];
+    if (n_max > 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(DT, 0, 128, 128);
+      constexpr uint32_t IDESC_O = idesc_f16(DT, 1, 128, D);  // N = d: one MMA covers every feature
+      // Shared-memory descriptors are built once; each MMA adds a compile-time offset (16-byte units)
+      // to the start-address field, which cannot carry out of its 14 bits below 256 KiB. V is MN-major:
+      // 8 keys x 64 features per 1024-byte atom (SBO = 1024 along keys); the second 64-feature box of
+      // d = 128 starts TILE_BYTES further (LBO).
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ + t * C::QT_BYTES), 16, 1024);
+      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), D == 128 ? TILE_BYTES : 1024, 1024);
+      const uint32_t col_s = tmem + (t ? C::COL_S1 : C::COL_S0);
+      const uint32_t col_p = tmem + (t ? C::COL_P1 : C::COL_P0);
+      const uint32_t col_o = tmem + (t ? C::COL_O1 : C::COL_O0);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
+        const bool w = wait_or_abort(bar, parity, tmo, abort_flag, code, where);
+        return __all_sync(0xffffffffu, w);
+      };
+      auto do_s = [&](int j) {
+        const uint64_t b0 = dK + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
+        tc_fence_after();
+        if (leader) {
+          issue_qk<D>(col_s, dQ, b0, IDESC_S);
+          tc_commit(&bar_s_full[t]);
+        }
+        __syncwarp();
+      };
+      auto do_pv = [&](int j) {
+        const uint64_t v0 = dV + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
+        const bool first = (j == 0), last = (j == nkv - 1);
+        tc_fence_after();
+        if (leader) {
+          if (first) issue_pv<D, DT, true>(col_o, col_p, v0, IDESC_O);
+          else issue_pv<D, DT, false>(col_o, col_p, v0, IDESC_O);
+          tc_commit(&bar_pv_done[t]);
+          if (last) tc_commit(&bar_o_final[t]);
+        }
+        __syncwarp();
+      };
+      bool ok = wait_all(bar_q, 0, kDevTimeoutQ, 11);
+      if (ok && nkv > 0) {
+        ok = wait_all(&bar_k_full[0], 0, kDevTimeoutKV, 12);
+        if (ok) do_s(0);
+      }
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int stage = j % STAGES;
+        if (j < nkv) {
+          if (!ALIAS) {
+            if (j + 1 < nkv) {
+              ok = wait_all(&bar_k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
+              if (ok) ok = wait_all(&bar_s_free[t], j & 1u, kDevTimeoutSoftmax, 14);
+              if (ok) do_s(j + 1);
+            }
+            if (ok) ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 15);
+            if (ok) ok = wait_all(&bar_p_full[t], j & 1u, kDevTimeoutSoftmax, 16);
+            if (ok) do_pv(j);
+          } else {
+            ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 15);
+            if (ok) ok = wait_all(&bar_p_full[t], j & 1u, kDevTimeoutSoftmax, 16);
+            if (ok) do_pv(j);
+            if (ok && j + 1 < nkv) {
+              ok = wait_all(&bar_k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
+              // P_t(j) lives in S_t's columns: PV_t(j) must have read it before S_t(j+1) lands there.
+              if (ok) ok = wait_all(&bar_pv_done[t], j & 1u, kDevTimeoutMMA, 17);
+              if (ok) do_s(j + 1);
+            }
+          }
+          // This tile's use of the K/V stage ends when its MMAs complete.
+          if (ok && leader) tc_commit(&bar_kv_empty[stage]);
+        } else {
+          // Key tile beyond this query tile's range: it never reads the stage, but its release must
+          // count toward this load's phase only; waiting for the load first keeps this warp from
+          // arriving a phase early (with fewer stages than key tiles it would otherwise free a stage
+          // the other warp is still reading).
+          ok = wait_all(&bar_k_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 21);
+          if (ok) ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 22);
+          if (ok && leader) mbar_arrive(&bar_kv_empty[stage]);
+        }
+        __syncwarp();
+      }
+      // Every MMA of this warp must be complete before tensor memory is released.
+      if (leader) tc_commit(&bar_mma_idle[t]);
+      __syncwarp();
+      mbar_wait_bounded(&bar_mma_idle[t], 0, tmo);
+    }
+  }
+    // ------------------------------------------------------------------ teardown (warpgroup 0)
+    tc_fence_before();
+    asm volatile("bar.sync 0;" ::: "memory");
+    if (warp == 1) {
+      __syncwarp();
+      tc_fence_after();
+      tmem_dealloc(tmem, TMEM_COLS);
+    }
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(REGS_HIGH));
+    // ------------------------------------------------------------------ softmax warpgroups
+    const int wg = (warp - 4) >> 2;           // query tile of this warpgroup
+    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
+    const int r = quarter * 32 + lane;        // row within the tile
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const uint32_t colS = wg ? C::COL_S1 : C::COL_S0;
+    const uint32_t colP = wg ? C::COL_P1 : C::COL_P0;
+    const uint32_t colO = wg ? C::COL_O1 : C::COL_O0;
+    const int qt0 = q0[wg];
+    const int nkv = n_kv[wg];
+    const int qi = qt0 + r;
+    const long long qpos = p.q_off + qi;
+    const float sl2 = p.scale_log2;
+    float m_ref = -INFINITY;
+    float l = 0.0f;
+    bool ok = true;
+
+    for (int j = 0; j < nkv; ++j) {
+      ok = wait_or_abort(&bar_s_full[wg], j & 1u, tmo, abort_flag, kDevTimeoutMMA, 18);
+      if (!__all_sync(0xffffffffu, ok)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t sr[128];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) tmem_ld32(trow + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      tmem_wait_ld();
+#pragma unroll
+      for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+      if (!ALIAS) {
+        tc_fence_before();
+        mbar_arrive(&bar_s_free[wg]);  // S_t may now take S_t(j+1)
+      }
+
+      float x[128];
+#pragma unroll
+      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+      const int k0 = j * BN;
+      const bool tail = (k0 + BN > p.Nkv);
+      const bool diag = CAUSAL && (p.kv_off + k0 + BN - 1 > p.q_off + qt0);
+      if (tail || diag) {
+        long long lim = p.Nkv - k0;
+        if (CAUSAL) {
+          const long long lc = qpos - p.kv_off - k0 + 1;
+          lim = lc < lim ? lc : lim;
+        }
+#pragma unroll
+        for (int c = 0; c < 128; ++c)
+          if (c >= lim) x[c] = -INFINITY;
+      }
+      const float tmax = row_max128(x) * sl2;
+      float alpha = 1.0f;
+      bool rescale = false;
+      if (tmax > m_ref + TAU) {
+        const float m_new = ceilf(tmax);
+        if (m_ref != -INFINITY) {
+          alpha = exp2_int(m_ref - m_new);
+          rescale = true;
+        }
+        m_ref = m_new;
+      }
+      const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
+      const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
+      float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+      const uint32_t pbuf = trow + colP;
+      if (!ALIAS) {
+        // fp16, P kept apart and single-buffered: compute all of P in registers first, then wait for
+        // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
+        // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
+        uint32_t pk[64];
+#pragma unroll
+        for (int c = 0; c < 64; ++c) {
+          const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
+          rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
+          pk[c] = pack2(pp.x, pp.y, 0);
+        }
+        if (j > 0) {
+          ok = wait_or_abort(&bar_pv_done[wg], (j - 1) & 1u, tmo, abort_flag, kDevTimeoutMMA, 19);
+          if (!__all_sync(0xffffffffu, ok)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+        }
+        tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+        tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+      } else {
+        // P over S: S_t(j) was issued only after PV_t(j-1) completed, so P_t(j-1) and O_t are settled.
+#pragma unroll
+        for (int c4 = 0; c4 < 4; ++c4) {
+          uint32_t hi[16], lo[16];
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int c = c4 * 16 + e;
+            const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
+            rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
+            if (DT) {
+              __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
+              const float2 hf = __bfloat1622float2(h2);
+              __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
+              hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+              lo[e] = *reinterpret_cast<uint32_t*>(&l2);
+            } else {
+              hi[e] = pack2(pp.x, pp.y, 0);
+            }
+          }
+          tmem_st16(pbuf + c4 * 16, hi);
+          if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
+        }
+      }
+      l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
+      if (__any_sync(0xffffffffu, rescale) && j > 0) {
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(trow + colO + c * 32, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+          tmem_st32(trow + colO + c * 32, o);
+        }
+      }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(&bar_p_full[wg]);
+    }
+
+    // ---------------------------------------------------------------- epilogue
+    if (ok && nkv > 0) {
+      ok = wait_or_abort(&bar_o_final[wg], 0, tmo, abort_flag, kDevTimeoutMMA, 20);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    const bool has = (nkv > 0) && (l > 0.0f);
+    const float inv_l = has ? 1.0f / l : 0.0f;
+    const float lse_v = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    const bool store = ok && qi < p.Nq;
+    const long long row = out_row_index(p.out_layout, b, h, p.H, p.Nq, qi);
+    const long long lrow = static_cast<long long>(bh) * p.Nq + qi;
+    bool write = store;
+    bool fresh = true;
+    float wa = 0.0f, wn = 1.0f, lse_out = lse_v;
+    if (MODE == kModeAccum && store) {
+      if (!has) {
+        write = false;
+      } else {
+        const float la = p.lse_part[lrow];
+        if (la != -INFINITY) {
+          fresh = false;
+          const float M = fmaxf(la, lse_v);
+          const float L = M + logf(expf(la - M) + expf(lse_v - M));
+          wa = expf(la - L);
+          wn = expf(lse_v - L);
+          lse_out = L;
+        }
+      }
+    }
+#pragma unroll
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (ok && nkv > 0) {
+        tmem_ld32(trow + colO + c * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      float v[32];
+#pragma unroll
+      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
+      if (write) {
+        if (MODE == kModeOut) {
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 w;
+            w.x = pack2(v[8 * q8 + 0], v[8 * q8 + 1], DT);
+            w.y = pack2(v[8 * q8 + 2], v[8 * q8 + 3], DT);
+            w.z = pack2(v[8 * q8 + 4], v[8 * q8 + 5], DT);
+            w.w = pack2(v[8 * q8 + 6], v[8 * q8 + 7], DT);
+            dst[q8] = w;
+          }
+        } else {
+          float4* dst = reinterpret_cast<float4*>(p.o_part + row * D + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            if (MODE == kModeAccum && !fresh) {
+              const float4 a = dst[q4];
+              w.x = wa * a.x + wn * w.x;
+              w.y = wa * a.y + wn * w.y;
+              w.z = wa * a.z + wn * w.z;
+              w.w = wa * a.w + wn * w.w;
+            }
+            dst[q4] = w;
+          }
+        }
+      }
+    }
+    if (write) {
+      if (MODE == kModeOut) {
+        if (p.lse) p.lse[lrow] = lse_v;
+      } else {
+        p.lse_part[lrow] = lse_out;
+      }
+    }
+
+    // ------------------------------------------------------------------ teardown (softmax warpgroups)
+    tc_fence_before();
+    asm volatile("bar.sync 0;" ::: "memory");
+  }
+}
+
+// Single-tile kernel (one 128-row query tile per CTA), selected only by CQSA_ATTN_SINGLE_TILE=1 to
+// compare against the two-tile kernel (both compute every row with the same operation sequence).
+bool single_tile_kernel() {
+  const char* e = getenv("CQSA_ATTN_SINGLE_TILE");
+  return e && e[0] == '1';
+}
+
+template <int D, int DT, bool CAUSAL, int MODE>
+int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, KParams kp, int Nq, int BH,
+             cudaStream_t stream) {
+  if (single_tile_kernel()) {
+    auto kern = attn_fwd_kernel<D, DT, CAUSAL, MODE>;
+    static bool attr_done = false;  // per instantiation; idempotent
+    if (!attr_done) {
+      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
+      if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem)");
+      attr_done = true;
+    }
+    kp.n_q_tiles = (Nq + BM - 1) / BM;
+    const long long grid = static_cast<long long>(kp.n_q_tiles) * BH;
+    kern<<<static_cast<int>(grid), NTHREADS, Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, kp);
+    return cuda_status(cudaGetLastError(), "attention kernel launch");
+  }
+  auto kern = attn_fwd2_kernel<D, DT, CAUSAL, MODE>;
+  static bool attr2_done = false;
+  if (!attr2_done) {
+    // setmaxnreg.inc waits until its registers are free: the launch must hold at least the split,
+    // or the softmax warpgroups would wait forever. Refuse to launch otherwise.
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(attention)");
+    if (fa.numRegs * NTHREADS2 < 128 * REGS_LOW + 256 * REGS_HIGH) {
+      set_error("attention kernel built with %d registers/thread; the register split needs %d",
+                fa.numRegs, (128 * REGS_LOW + 256 * REGS_HIGH + NTHREADS2 - 1) / NTHREADS2);
+      return CQSA_ERR_UNSUPPORTED;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<D, DT>::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem)");
+    attr2_done = true;
+  }
+  kp.n_q_tiles = (Nq + 2 * BM - 1) / (2 * BM);  // pairs of query tiles
+  const long long grid = static_cast<long long>(kp.n_q_tiles) * BH;
+  kern<<<static_cast<int>(grid), NTHREADS2, Cfg2<D, DT>::SMEM_BYTES, stream>>>(mq, mk, mv, kp);
   return cuda_status(cudaGetLastError(), "attention kernel launch");
 }
 
 template <int D, int DT>
-int dispatch_mode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const KParams& kp, int grid,
-                  int causal, int mode, cudaStream_t s) {
+int dispatch_mode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const KParams& kp, int Nq,
+                  int BH, int causal, int mode, cudaStream_t s) {
   if (causal) {
-    if (mode == kModeOut) return launch_t<D, DT, true, kModeOut>(mq, mk, mv, kp, grid, s);
-    if (mode == kModePart) return launch_t<D, DT, true, kModePart>(mq, mk, mv, kp, grid, s);
-    return launch_t<D, DT, true, kModeAccum>(mq, mk, mv, kp, grid, s);
+    if (mode == kModeOut) return launch_t<D, DT, true, kModeOut>(mq, mk, mv, kp, Nq, BH, s);
+    if (mode == kModePart) return launch_t<D, DT, true, kModePart>(mq, mk, mv, kp, Nq, BH, s);
+    return launch_t<D, DT, true, kModeAccum>(mq, mk, mv, kp, Nq, BH, s);
   }
-  if (mode == kModeOut) return launch_t<D, DT, false, kModeOut>(mq, mk, mv, kp, grid, s);
-  if (mode == kModePart) return launch_t<D, DT, false, kModePart>(mq, mk, mv, kp, grid, s);
-  return launch_t<D, DT, false, kModeAccum>(mq, mk, mv, kp, grid, s);
+  if (mode == kModeOut) return launch_t<D, DT, false, kModeOut>(mq, mk, mv, kp, Nq, BH, s);
+  if (mode == kModePart) return launch_t<D, DT, false, kModePart>(mq, mk, mv, kp, Nq, BH, s);
+  return launch_t<D, DT, false, kModeAccum>(mq, mk, mv, kp, Nq, BH, s);
 }
 
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda dependency).
@@ -611,25 +1208,26 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   kp.q_off = a.q_off;
   kp.kv_off = a.kv_off;
   kp.scale_log2 = a.scale * 1.4426950408889634f;
-  kp.n_q_tiles = (a.Nq + BM - 1) / BM;
+  kp.n_q_tiles = 0;  // set per kernel variant at launch
   kp.out = a.out;
   kp.lse = a.lse;
   kp.o_part = a.o_part;
   kp.lse_part = a.lse_part;
   kp.out_layout = a.out_layout;
   kp.timeout_ns = timeout_ns();
-  const long long grid = static_cast<long long>(kp.n_q_tiles) * kp.BH;
+  kp.fault = debug_fault();
+  const long long grid = static_cast<long long>((a.Nq + BM - 1) / BM) * kp.BH;
   if (grid > 0x7fffffffLL) {
     set_error("problem too large for one launch (%lld tiles)", grid);
     return CQSA_ERR_UNSUPPORTED;
   }
   const bool c = a.causal != 0;
   if (a.d == 64) {
-    return a.dtype == CQSA_BF16 ? dispatch_mode<64, 1>(mq, mk, mv, kp, (int)grid, c, a.mode, stream)
-                                : dispatch_mode<64, 0>(mq, mk, mv, kp, (int)grid, c, a.mode, stream);
+    return a.dtype == CQSA_BF16 ? dispatch_mode<64, 1>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream)
+                                : dispatch_mode<64, 0>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream);
   }
-  return a.dtype == CQSA_BF16 ? dispatch_mode<128, 1>(mq, mk, mv, kp, (int)grid, c, a.mode, stream)
-                              : dispatch_mode<128, 0>(mq, mk, mv, kp, (int)grid, c, a.mode, stream);
+  return a.dtype == CQSA_BF16 ? dispatch_mode<128, 1>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream)
+                              : dispatch_mode<128, 0>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream);
 }
 
 }  // namespace cqsa

@@ -47,5 +47,6 @@ int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int
 void set_error(const char* fmt, ...);
 int cuda_status(cudaError_t e, const char* what);
 unsigned long long timeout_ns();
+int debug_fault();
 
 }  // namespace cqsa

@@ -154,6 +154,14 @@ int cqsa_device_error(int* code, int* block, int clear);
 /* Device-side wait limit in milliseconds (default 2000; env CQSA_TIMEOUT_MS). */
 void cqsa_set_timeout_ms(unsigned int ms);
 
+/*
+ * Test hook for the device-side bounded waits (not for production use): kind 1 makes the next
+ * attention launches skip the load of key/value tile 1 in their first CTA, so that CTA's waits run
+ * out after the timeout; the kernel then records CQSA_ERR_TIMEOUT in the device error word, drains
+ * its own copies and MMAs, frees tensor memory and returns (no trap, no hang). kind 0 turns it off.
+ */
+int cqsa_debug_set_fault(int kind);
+
 /* Library version, e.g. "0.1.0". */
 const char* cqsa_version(void);
 
