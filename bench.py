@@ -114,6 +114,22 @@ def _dist():
     return world, rank, local
 
 
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The largest value of x over all ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_tflops(flop_per_step: float, steps: int, world: int, max_ms: float) -> float:
+    """Weak scaling: every rank runs `steps` full steps; the job takes the slowest rank's time."""
+    return world * flop_per_step * steps / (max_ms / 1000.0) / 1e12
+
+
 def oracle_sample(rows: int, seed: int = 1):
     """Time the FP64 oracle on `rows` seeded rows of the workload; returns (seconds, FLOP, threads)."""
     import oracle
@@ -206,12 +222,8 @@ def run_ours(args):
         torch.cuda.synchronize()
         wall = time.perf_counter() - t0
     ms = [a.elapsed_time(b) for a, b in ev]
-    dev_ms = sum(ms)
-    t_max = torch.tensor([dev_ms], dtype=torch.float64, device=dev)
-    if world > 1:
-        torch.distributed.all_reduce(t_max, op=torch.distributed.ReduceOp.MAX)
-    dev_ms = float(t_max.item())
-    value = world * FLOP_PER_STEP * args.steps / (dev_ms / 1000.0) / 1e12
+    dev_ms = max_over_ranks(sum(ms), world, dev)
+    value = whole_job_tflops(FLOP_PER_STEP, args.steps, world, dev_ms)
     kernel_tflops = FLOP_PER_STEP / (statistics.mean(ms) / 1000.0) / 1e12
 
     # end to end: host (pinned) buffers in and out through the C ABI
