@@ -614,7 +614,14 @@ struct Cfg2 {
   static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
   static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
   static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
-  static constexpr uint32_t SMEM_BYTES = 1024 + 2 * QT_BYTES + 2 * STAGES * KV_BYTES + NBARS * 8 + 16;
+  // d = 64: every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running
+  // sum in shared memory ([tile][feature][row], conflict-free per row), so no tensor-core accumulation
+  // chain exceeds FLUSH * 8 MMAs. (The MMA's fp32 accumulation is biased toward zero: measured
+  // relative drift -1.6e-5 after 16K keys, -6.9e-5 after 65K; the running sum uses RNE adds.)
+  static constexpr int FLUSH = (D == 64) ? 128 : 0;
+  static constexpr uint32_t OSUM_BYTES = (D == 64) ? 2u * D * 128u * 4u : 0u;
+  static constexpr uint32_t SMEM_BYTES =
+      1024 + 2 * QT_BYTES + 2 * STAGES * KV_BYTES + OSUM_BYTES + NBARS * 8 + 16;
   static_assert(COL_O1 + D <= TMEM_COLS, "tensor memory layout exceeds 512 columns");
 };
 
@@ -632,7 +639,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   uint8_t* sQ = smem;  // tile t at sQ + t * QT_BYTES
   uint8_t* sK = sQ + 2 * C::QT_BYTES;
   uint8_t* sV = sK + STAGES * C::KV_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES);
+  float* sOsum = reinterpret_cast<float*>(sV + STAGES * C::KV_BYTES);  // d = 64 only
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES + C::OSUM_BYTES);
   uint64_t* bar_q = bars;
   uint64_t* bar_k_full = bar_q + 1;
   uint64_t* bar_v_full = bar_k_full + STAGES;
@@ -655,21 +663,21 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   const int bh = unit % p.BH;
   const int b = bh / p.H;
   const int h = bh % p.H;
-  int q0[2], n_kv[2];
-#pragma unroll
-  for (int t = 0; t < 2; ++t) {
-    q0[t] = qp * 2 * BM + t * BM;
-    const int rows = min(BM, p.Nq - q0[t]);
+  // Per query tile: first row and number of key tiles (scalars: no runtime-indexed local arrays).
+  auto tile_kv = [&](int qt0) -> int {
+    const int rows = min(BM, p.Nq - qt0);
     int n = (p.Nkv + BN - 1) / BN;
     if (rows <= 0) {
       n = 0;
     } else if (CAUSAL) {
-      const long long last_key = p.q_off + q0[t] + rows - 1 - p.kv_off;
+      const long long last_key = p.q_off + qt0 + rows - 1 - p.kv_off;
       n = last_key < 0 ? 0 : (last_key / BN + 1 < n ? static_cast<int>(last_key / BN + 1) : n);
     }
-    n_kv[t] = n;
-  }
-  const int n_max = max(n_kv[0], n_kv[1]);
+    return n;
+  };
+  const int q00 = qp * 2 * BM, q01 = q00 + BM;
+  const int nkv0 = tile_kv(q00), nkv1 = tile_kv(q01);
+  const int n_max = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
     mbar_init(bar_q, 1);
@@ -716,7 +724,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       for (int t = 0; t < 2; ++t)
 #pragma unroll
         for (int s = 0; s < KSUB; ++s)
-          tma_load_4d(sQ + t * C::QT_BYTES + s * TILE_BYTES, &tmQ, bar_q, s * 64, q0[t], h, b);
+          tma_load_4d(sQ + t * C::QT_BYTES + s * TILE_BYTES, &tmQ, bar_q, s * 64, t ? q01 : q00, h, b);
       int issued = 0;
       int skipped = -1;  // fault injection: the key/value tile never loaded
       for (int j = 0; j < n_max; ++j) {
@@ -758,7 +766,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     // converged (warp-uniform values); one elected lane issues each MMA group and commit.
     const int t = warp - 1;
     const bool leader = elect_one();
-    const int nkv = n_kv[t];
+    const int nkv = t ? nkv1 : nkv0;
     if (n_max > 0) {
       constexpr uint32_t IDESC_S = idesc_f16(DT, 0, 128, 128);
       constexpr uint32_t IDESC_O = idesc_f16(DT, 1, 128, D);  // N = d: one MMA covers every feature
@@ -787,7 +795,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       };
       auto do_pv = [&](int j) {
         const uint64_t v0 = dV + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
-        const bool first = (j == 0), last = (j == nkv - 1);
+        const bool first = (j == 0) || (C::FLUSH > 0 && j % C::FLUSH == 0), last = (j == nkv - 1);
         tc_fence_after();
         if (leader) {
           if (first) issue_pv<D, DT, true>(col_o, col_p, v0, IDESC_O);
@@ -862,8 +870,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     const uint32_t colS = wg ? C::COL_S1 : C::COL_S0;
     const uint32_t colP = wg ? C::COL_P1 : C::COL_P0;
     const uint32_t colO = wg ? C::COL_O1 : C::COL_O0;
-    const int qt0 = q0[wg];
-    const int nkv = n_kv[wg];
+    const int qt0 = wg ? q01 : q00;
+    const int nkv = wg ? nkv1 : nkv0;
     const int qi = qt0 + r;
     const long long qpos = p.q_off + qi;
     const float sl2 = p.scale_log2;
@@ -872,6 +880,30 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
+      if (C::FLUSH > 0 && j > 0 && j % C::FLUSH == 0) {
+        // Segment boundary: once PV_t(j-1) is complete, fold O into the running sum O_sum (RNE fp32
+        // adds); PV_t(j) restarts O. Both are in the current reference max at this point.
+        ok = wait_or_abort(&bar_pv_done[wg], (j - 1) & 1u, tmo, abort_flag, kDevTimeoutMMA, 23);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float* os = sOsum + (wg * D) * 128 + r;
+        const bool have = j > C::FLUSH;
+#pragma unroll
+        for (int c = 0; c < D / 32; ++c) {
+          uint32_t o[32];
+          tmem_ld32(trow + colO + c * 32, o);
+          tmem_wait_ld();
+          reg_fence32(o);
+#pragma unroll
+          for (int e = 0; e < 32; ++e) {
+            const float prev = have ? os[(c * 32 + e) * 128] : 0.0f;
+            os[(c * 32 + e) * 128] = prev + __uint_as_float(o[e]);
+          }
+        }
+      }
       ok = wait_or_abort(&bar_s_full[wg], j & 1u, tmo, abort_flag, kDevTimeoutMMA, 18);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
@@ -966,7 +998,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
       }
       l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
+      // PV_t(j-1) is complete here (waited for above, or implied by S_t(j) when P is over S).
       if (__any_sync(0xffffffffu, rescale) && j > 0) {
+        // O (and O_sum, once it holds a segment) take the new reference max.
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -976,6 +1010,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(trow + colO + c * 32, o);
+        }
+        if (C::FLUSH > 0 && rescale && j >= C::FLUSH) {
+          float* os = sOsum + (wg * D) * 128 + r;
+#pragma unroll 8
+          for (int e = 0; e < D; ++e) os[e * 128] *= alpha;
         }
       }
       tmem_wait_st();
@@ -1025,8 +1064,14 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
       float v[32];
+      if (C::FLUSH > 0 && nkv > C::FLUSH) {
+        const float* os = sOsum + (wg * D + c * 32) * 128 + r;
 #pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
+        for (int e = 0; e < 32; ++e) v[e] = (os[e * 128] + __uint_as_float(o[e])) * inv_l;
+      } else {
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
+      }
       if (write) {
         if (MODE == kModeOut) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
