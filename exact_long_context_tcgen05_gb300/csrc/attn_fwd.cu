@@ -65,6 +65,7 @@ struct KParams {
   float* lse_part;
   int out_layout;
   unsigned long long timeout_ns;
+  unsigned timeout_us;  // the same limit in microseconds (32-bit, for the two-tile kernel's loops)
   int fault;  // test hook: 1 = block 0 never loads key tile 1 (its waits must time out cleanly)
 };
 
@@ -100,6 +101,23 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, un
         *abort_flag = 1;
         return false;
       }
+    }
+  }
+}
+
+// wait_or_abort on 32-bit shared addresses with a microsecond limit; the waiting thread sleeps in
+// try_wait (woken when the phase completes) between checks of the abort flag and the clock.
+__device__ __forceinline__ bool wait_or_abort_a(uint32_t bar, uint32_t parity, uint32_t tmo_us, uint32_t abort_addr,
+                                                int code, int where) {
+  if (mbar_try_wait_a(bar, parity)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (true) {
+    if (mbar_try_wait_sleep_a(bar, parity, 1000000u)) return true;
+    if (ld_shared_volatile_u32(abort_addr)) return false;
+    if (globaltimer_ns() - t0 > static_cast<uint64_t>(tmo_us) * 1000ull) {
+      record_error(code, where);
+      st_shared_volatile_u32(abort_addr, 1u);
+      return false;
     }
   }
 }
@@ -712,6 +730,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
   const unsigned long long tmo = p.timeout_ns;
+  const uint32_t tmo_us = p.timeout_us;
+  const uint32_t a_abort = smem_u32(const_cast<int*>(abort_flag));
   // Each warpgroup changes its register budget at the top of its own branch and leaves through its
   // own copy of the teardown barrier, so no code runs under two different budgets.
   if (warp < 4) {
@@ -730,7 +750,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       for (int j = 0; j < n_max; ++j) {
         const int stage = j % STAGES;
         const uint32_t round = j / STAGES;
-        if (!wait_or_abort(&bar_kv_empty[stage], (round & 1u) ^ 1u, tmo, abort_flag, kDevTimeoutKV, 10)) break;
+        if (!wait_or_abort_a(smem_u32(&bar_kv_empty[stage]), (round & 1u) ^ 1u, tmo_us, a_abort, kDevTimeoutKV, 10)) break;
         if (p.fault == 1 && blockIdx.x == 0 && j == 1) {
           skipped = j;
           issued = j + 1;
@@ -781,7 +801,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       const uint32_t col_p = tmem + (t ? C::COL_P1 : C::COL_P0);
       const uint32_t col_o = tmem + (t ? C::COL_O1 : C::COL_O0);
       auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
-        const bool w = wait_or_abort(bar, parity, tmo, abort_flag, code, where);
+        const bool w = wait_or_abort_a(smem_u32(bar), parity, tmo_us, a_abort, code, where);
         return __all_sync(0xffffffffu, w);
       };
       auto do_s = [&](int j) {
@@ -871,6 +891,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     const uint32_t colP = wg ? C::COL_P1 : C::COL_P0;
     const uint32_t colO = wg ? C::COL_O1 : C::COL_O0;
     const int qt0 = wg ? q01 : q00;
+    const uint32_t a_s_full = smem_u32(&bar_s_full[wg]), a_s_free = smem_u32(&bar_s_free[wg]);
+    const uint32_t a_p_full = smem_u32(&bar_p_full[wg]), a_pv_done = smem_u32(&bar_pv_done[wg]);
     const int nkv = wg ? nkv1 : nkv0;
     const int qi = qt0 + r;
     const long long qpos = p.q_off + qi;
@@ -883,13 +905,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       if (C::FLUSH > 0 && j > 0 && j % C::FLUSH == 0) {
         // Segment boundary: once PV_t(j-1) is complete, fold O into the running sum O_sum (RNE fp32
         // adds); PV_t(j) restarts O. Both are in the current reference max at this point.
-        ok = wait_or_abort(&bar_pv_done[wg], (j - 1) & 1u, tmo, abort_flag, kDevTimeoutMMA, 23);
+        ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 23);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
           break;
         }
         tc_fence_after();
-        float* os = sOsum + (wg * D) * 128 + r;
+        const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
         const bool have = j > C::FLUSH;
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
@@ -899,12 +921,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           reg_fence32(o);
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
-            const float prev = have ? os[(c * 32 + e) * 128] : 0.0f;
-            os[(c * 32 + e) * 128] = prev + __uint_as_float(o[e]);
+            const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
+            const float prev = have ? ld_shared_f32(a) : 0.0f;
+            st_shared_f32(a, prev + __uint_as_float(o[e]));
           }
         }
       }
-      ok = wait_or_abort(&bar_s_full[wg], j & 1u, tmo, abort_flag, kDevTimeoutMMA, 18);
+      ok = wait_or_abort_a(a_s_full, j & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
       if (!__all_sync(0xffffffffu, ok)) {
         ok = false;
         break;
@@ -918,7 +941,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
       if (!ALIAS) {
         tc_fence_before();
-        mbar_arrive(&bar_s_free[wg]);  // S_t may now take S_t(j+1)
+        mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
       }
 
       float x[128];
@@ -964,7 +987,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           pk[c] = pack2(pp.x, pp.y, 0);
         }
         if (j > 0) {
-          ok = wait_or_abort(&bar_pv_done[wg], (j - 1) & 1u, tmo, abort_flag, kDevTimeoutMMA, 19);
+          ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
           if (!__all_sync(0xffffffffu, ok)) {
             ok = false;
             break;
@@ -1012,19 +1035,19 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           tmem_st32(trow + colO + c * 32, o);
         }
         if (C::FLUSH > 0 && rescale && j >= C::FLUSH) {
-          float* os = sOsum + (wg * D) * 128 + r;
+          const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
 #pragma unroll 8
-          for (int e = 0; e < D; ++e) os[e * 128] *= alpha;
+          for (int e = 0; e < D; ++e) st_shared_f32(os + e * 512, ld_shared_f32(os + e * 512) * alpha);
         }
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(&bar_p_full[wg]);
+      mbar_arrive_a(a_p_full);
     }
 
     // ---------------------------------------------------------------- epilogue
     if (ok && nkv > 0) {
-      ok = wait_or_abort(&bar_o_final[wg], 0, tmo, abort_flag, kDevTimeoutMMA, 20);
+      ok = wait_or_abort_a(smem_u32(&bar_o_final[wg]), 0, tmo_us, a_abort, kDevTimeoutMMA, 20);
       ok = __all_sync(0xffffffffu, ok);
       tc_fence_after();
     }
@@ -1260,6 +1283,8 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   kp.lse_part = a.lse_part;
   kp.out_layout = a.out_layout;
   kp.timeout_ns = timeout_ns();
+  kp.timeout_us = static_cast<unsigned>(kp.timeout_ns / 1000ull > 0xffffffffull ? 0xffffffffull
+                                                                                : kp.timeout_ns / 1000ull + 1ull);
   kp.fault = debug_fault();
   const long long grid = static_cast<long long>((a.Nq + BM - 1) / BM) * kp.BH;
   if (grid > 0x7fffffffLL) {
