@@ -899,12 +899,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     const float sl2 = p.scale_log2;
     float m_ref = -INFINITY;
     float l = 0.0f;
+    float m_sum = -INFINITY;  // reference max of O_sum (the m_ref of its last fold); O_sum holds
+                              // values scaled by 2^-m_sum and is only brought to m_ref when read
     bool ok = true;
 
     for (int j = 0; j < nkv; ++j) {
       if (C::FLUSH > 0 && j > 0 && j % C::FLUSH == 0) {
         // Segment boundary: once PV_t(j-1) is complete, fold O into the running sum O_sum (RNE fp32
-        // adds); PV_t(j) restarts O. Both are in the current reference max at this point.
+        // adds); PV_t(j) restarts O. O is in the current reference max; O_sum is brought from m_sum
+        // to it by an exact power of two.
         ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 23);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -913,6 +916,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         tc_fence_after();
         const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
         const bool have = j > C::FLUSH;
+        const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -922,10 +926,11 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) {
             const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
-            const float prev = have ? ld_shared_f32(a) : 0.0f;
+            const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
             st_shared_f32(a, prev + __uint_as_float(o[e]));
           }
         }
+        m_sum = m_ref;
       }
       ok = wait_or_abort_a(a_s_full, j & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
       if (!__all_sync(0xffffffffu, ok)) {
@@ -1023,7 +1028,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
       // PV_t(j-1) is complete here (waited for above, or implied by S_t(j) when P is over S).
       if (__any_sync(0xffffffffu, rescale) && j > 0) {
-        // O (and O_sum, once it holds a segment) take the new reference max.
+        // O takes the new reference max (O_sum keeps its own, m_sum).
 #pragma unroll
         for (int c = 0; c < D / 32; ++c) {
           uint32_t o[32];
@@ -1033,11 +1038,6 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
 #pragma unroll
           for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
           tmem_st32(trow + colO + c * 32, o);
-        }
-        if (C::FLUSH > 0 && rescale && j >= C::FLUSH) {
-          const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
-#pragma unroll 8
-          for (int e = 0; e < D; ++e) st_shared_f32(os + e * 512, ld_shared_f32(os + e * 512) * alpha);
         }
       }
       tmem_wait_st();
@@ -1089,8 +1089,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       float v[32];
       if (C::FLUSH > 0 && nkv > C::FLUSH) {
         const float* os = sOsum + (wg * D + c * 32) * 128 + r;
+        const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = (os[e * 128] + __uint_as_float(o[e])) * inv_l;
+        for (int e = 0; e < 32; ++e) v[e] = (os[e * 128] * sc + __uint_as_float(o[e])) * inv_l;
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
