@@ -16,6 +16,15 @@ step = 4*B*H*N^2*d/2.
   peak (MEASURED_PEAKS.json; else the fallback figure, labelled so).
 - cpu_baseline: the FP64 oracle on a bounded sample of the workload's rows on this host's cores.
 - --impl reference: the oracle itself as the reference arm, on a bounded row sample per step.
+
+Secondary measurements (one JSON line each, not the headline; `--measure NAME`):
+- merge: the LSE merge of the 131,072-token chunked workload (16,384-token chunks, Q chunk i merges
+  i+1 fp32 partials), achieved HBM GB/s of the algorithmic bytes vs the measured copy bandwidth.
+- link: pinned host <-> device copy probe (1 GiB cudaMemcpyAsync each way), the link roofline.
+- stream: the host-resident streaming driver (token-major pinned Q/K/V, 262,144-token chunks; N from
+  --n, default 4,000,000): TFLOP/s, copy rate while overlapped vs the link probe, stall time.
+- bf16: B=2 H=32 N=16384 d=128 bf16 non-causal monolithic forward (K scaled by 3), TFLOP/s and the
+  fraction of the tensor peak (algorithmic FLOP; the hi/lo split of P costs 1.5x the MMA work).
 """
 from __future__ import annotations
 
@@ -40,6 +49,7 @@ FLOP_PER_STEP = 4.0 * B * H * N * N * D / 2.0
 WORKLOAD = "exact attention forward, B=1 H=8 N=32768 d=64 fp16 causal, scale 1/sqrt(64), device-resident, monolithic"
 METRIC = "exact attention fwd TFLOP/s (causal-adjusted) at 1 GB300; % of tensor-core peak"
 FALLBACK_TFLOPS = 1900.0
+FALLBACK_HBM_GBS = 6800.0
 
 
 def _peaks():
@@ -294,6 +304,156 @@ def _traffic_per_launch():
     return int(m_b.group(1))
 
 
+def _hbm_peak():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as f:
+            pk = json.load(f)
+        for key in ("hbm_gbs", "hbm_GBps", "copy_gbs"):
+            if key in pk:
+                return float(pk[key]), "measured (MEASURED_PEAKS.json %s)" % key
+    return FALLBACK_HBM_GBS, "fallback (6.8 TB/s, earlier GB300 copy measurement)"
+
+
+def _time_events(fn, reps, stream):
+    import torch
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(reps)]
+    for a, b in ev:
+        a.record(stream)
+        fn()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in ev]
+
+
+def measure_merge(cq, dev, reps):
+    """LSE merge of the chunked 131,072-token workload: for Q chunk i (of 8), i+1 fp32 partials
+    [1,8,16384,64] + LSE are merged into fp16 out + fp32 LSE. Partials are seeded on the device (the
+    merge's speed does not depend on their values); 1.2 GB of partials, far above L2."""
+    import torch
+    Bm, Hm, C, Dm, nch = 1, 8, 16384, 64, 8
+    g = torch.Generator(device=dev)
+    g.manual_seed(0)
+    parts_o = [torch.randn((Bm, Hm, C, Dm), generator=g, device=dev) for _ in range(nch * (nch + 1) // 2)]
+    parts_l = [torch.randn((Bm, Hm, C), generator=g, device=dev) for _ in range(nch * (nch + 1) // 2)]
+    outs = [torch.empty((Bm, Hm, C, Dm), dtype=torch.float16, device=dev) for _ in range(nch)]
+    lses = [torch.empty((Bm, Hm, C), dtype=torch.float32, device=dev) for _ in range(nch)]
+    stream = torch.cuda.current_stream(dev)
+    offs = [i * (i + 1) // 2 for i in range(nch)]
+
+    def step():
+        for i in range(nch):
+            cq.cqsa_merge_partials(parts_o[offs[i]:offs[i] + i + 1], parts_l[offs[i]:offs[i] + i + 1], i + 1,
+                                   outs[i], lses[i], Bm, Hm, C, Dm, cq.CQSA_F16, stream)
+
+    for _ in range(3):
+        step()
+    ms = statistics.median(_time_events(step, reps, stream))
+    rows = Bm * Hm * C
+    nparts = nch * (nch + 1) // 2
+    algo = nparts * rows * (Dm * 4 + 4) + nch * rows * (Dm * 2 + 4)
+    peak, src = _hbm_peak()
+    gbs = algo / (ms / 1000.0) / 1e9
+    return {"measure": "merge", "workload": "LSE merge, 131,072 tokens in 16,384-token chunks (36 partials, 8 merges), "
+            "B=1 H=8 d=64, fp32 partials -> fp16 out + fp32 LSE", "ms_per_step": ms, "algorithmic_bytes": algo,
+            "launches_per_step": nch,
+            "roofline": {"bound": "hbm", "achieved": gbs, "peak": peak, "unit": "GB/s", "frac": gbs / peak,
+                         "peak_source": src}}
+
+
+def measure_link(dev, reps):
+    import torch
+    nbytes = 1 << 30
+    h = torch.empty(nbytes, dtype=torch.uint8).pin_memory()
+    d = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    h2d = _time_events(lambda: d.copy_(h, non_blocking=True), reps, stream)
+    d2h = _time_events(lambda: h.copy_(d, non_blocking=True), reps, stream)
+    return {"measure": "link", "bytes": nbytes, "h2d_gbs": nbytes / (statistics.median(h2d) / 1e3) / 1e9,
+            "d2h_gbs": nbytes / (statistics.median(d2h) / 1e3) / 1e9,
+            "method": "1 GiB pinned host buffer, cudaMemcpyAsync, CUDA events, median of %d" % reps}
+
+
+def measure_stream(cq, dev, n_tokens, link_h2d_gbs):
+    import torch
+    import synthetic as syn
+    Bs, Hs, Ds, C = 1, 8, 64, 262_144
+    shape = (Bs, n_tokens, Hs, Ds)
+    host = [torch.empty(shape, dtype=torch.float16).pin_memory() for _ in range(3)]
+    for tid, t in enumerate(host):
+        syn.normal(Bs, Hs, n_tokens, Ds, seed=0, tensor_id=tid, layout=syn.LAYOUT_BNHD, out=t.numpy().view(np.uint16))
+    out = torch.empty(shape, dtype=torch.float16).pin_memory()
+    lse = torch.empty((Bs, Hs, n_tokens), dtype=torch.float32).pin_memory()
+    st = cq.cqsa_stream_stats()
+    stream = torch.cuda.current_stream(dev)
+    t0 = time.perf_counter()
+    cq.cqsa_stream_attn_fwd(host[0], host[1], host[2], cq.CQSA_LAYOUT_BNHD, out, lse, True, Bs, Hs, n_tokens, Ds,
+                            True, 0.0, cq.CQSA_F16, C, st, stream)
+    wall = time.perf_counter() - t0
+    flop = 4.0 * Bs * Hs * n_tokens * n_tokens * Ds / 2.0
+    copy_gbs = st.h2d_bytes / (st.h2d_ms / 1e3) / 1e9 if st.h2d_ms > 0 else None
+    return {"measure": "stream", "workload": f"host-resident streaming, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
+            f"token-major pinned Q/K/V/out, {C}-token chunks", "wall_s": wall, "tflops": flop / wall / 1e12,
+            "compute_s": st.compute_ms / 1e3, "stall_ms": st.stall_ms, "h2d_bytes": st.h2d_bytes,
+            "d2h_bytes": st.d2h_bytes, "copy_gbs_overlapped": copy_gbs, "link_h2d_gbs": link_h2d_gbs,
+            "copy_frac_of_link": (copy_gbs / link_h2d_gbs) if (copy_gbs and link_h2d_gbs) else None,
+            "overlap_wall_over_compute": wall / (st.compute_ms / 1e3) if st.compute_ms > 0 else None,
+            "peak_device_bytes": st.peak_device_bytes, "n_chunk_pairs": st.n_chunks}
+
+
+def measure_bf16(cq, dev, reps):
+    import torch
+    import synthetic as syn
+    Bb, Hb, Nb, Db = 2, 32, 16384, 128
+    qn, kn, vn = syn.qkv(Bb, Hb, Nb, Db, seed=0, dtype=syn.BF16, k_mul=3.0)
+    q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).to(dev) for x in (qn, kn, vn))
+    out = torch.empty_like(q)
+    lse = torch.empty((Bb, Hb, Nb), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        cq.cqsa_attn_fwd(q, k, v, out, lse, Bb, Hb, Nb, Db, False, 0.0, cq.CQSA_BF16, stream)
+
+    for _ in range(3):
+        step()
+    ms = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        ms += _time_events(step, 1, stream)
+    flop = 4.0 * Bb * Hb * Nb * Nb * Db
+    tf = flop / (statistics.median(ms) / 1e3) / 1e12
+    peak, src, _ = _peaks()
+    return {"measure": "bf16", "workload": "B=2 H=32 N=16384 d=128 bf16 non-causal, K x3, monolithic",
+            "ms_per_step": statistics.median(ms), "tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_source": src, "note": "algorithmic FLOP; the P hi/lo split issues 1.5x the MMA work"}}
+
+
+def run_measure(args):
+    import torch
+    world, rank, local = _dist()
+    if rank != 0:
+        return 0
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    import exact_long_context_tcgen05_gb300 as cq
+    reps = max(5, min(args.steps, 20))
+    if args.measure == "merge":
+        line = measure_merge(cq, dev, reps)
+    elif args.measure == "link":
+        line = measure_link(dev, reps)
+    elif args.measure == "stream":
+        link = measure_link(dev, 5)
+        line = measure_stream(cq, dev, args.n, link["h2d_gbs"])
+    else:
+        line = measure_bf16(cq, dev, reps)
+    rc, code, _ = cq.cqsa_device_error()
+    line["device_error_free"] = rc == cq.CQSA_OK
+    print(json.dumps(line), flush=True)
+    return 0
+
+
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
@@ -301,9 +461,13 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16"), default=None)
+    ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
+    if args.measure:
+        return run_measure(args)
     if args.impl == "reference":
         return run_reference(args)
     return run_ours(args)

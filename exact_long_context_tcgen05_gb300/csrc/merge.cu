@@ -6,10 +6,11 @@
 // ("stream-cqsa 2.2.0 -> 2.2.2" diff, README profile sweep) without printing the formula; this is
 // the exact combination of softmax partials that carry their log-sum-exp.
 //
-// Layout of the work: a group of d/4 threads owns one row; each thread owns 4 consecutive features
-// and streams its float4 of every O_k (fully coalesced: a warp reads 512 contiguous bytes per part).
-// The LSE pass is spread over the group's threads and reduced with shuffles inside the group.
-// Grid-stride over row groups with a grid sized to the SM count.
+// Layout of the work: a group of d/4 threads owns four rows at a time; each thread owns 4 consecutive
+// features and streams its float4 of every O_k for the four rows (fully coalesced: a warp reads 512
+// contiguous bytes per part and row pair; four independent loads in flight per part). The LSE pass is
+// spread over the group's threads and reduced with shuffles inside the group. Grid-stride over row
+// groups with a grid sized to the SM count.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 #include <math.h>
@@ -47,6 +48,7 @@ template <int D, int MAXN>
 __global__ void __launch_bounds__(256) merge_kernel(const PartPtrs<MAXN> parts, int n, void* out, float* lse,
                                                     long long rows, int out_dtype) {
   constexpr int G = D / 4;  // threads per row (16 or 32)
+  constexpr int R = 4;      // rows per group per step: R independent loads in flight per part
   const int tid = blockIdx.x * blockDim.x + threadIdx.x;
   const int g = threadIdx.x % G;
   const long long group0 = tid / G;
@@ -54,32 +56,66 @@ __global__ void __launch_bounds__(256) merge_kernel(const PartPtrs<MAXN> parts, 
   const unsigned lane = threadIdx.x & 31;
   const unsigned gmask = (G == 32) ? 0xffffffffu : (0xffffu << (lane & 16u));
 
-  for (long long r = group0; r < rows; r += ngroups) {
-    float m = -INFINITY;
-    for (int k = g; k < n; k += G) m = fmaxf(m, __ldg(parts.l[k] + r));
+  for (long long r0 = group0 * R; r0 < rows; r0 += ngroups * R) {
+    long long rr[R];
 #pragma unroll
-    for (int o = G / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(gmask, m, o));
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    float L = -INFINITY;
-    if (m != -INFINITY) {
-      float z = 0.0f;
-      for (int k = g; k < n; k += G) z += expf(__ldg(parts.l[k] + r) - m);
+    for (int u = 0; u < R; ++u) rr[u] = (r0 + u < rows) ? r0 + u : rows - 1;  // clamped rows repeat a valid one
+    float m[R];
 #pragma unroll
-      for (int o = G / 2; o > 0; o >>= 1) z += __shfl_xor_sync(gmask, z, o);
-      L = m + logf(z);
-      for (int k = 0; k < n; ++k) {
-        const float lk = __ldg(parts.l[k] + r);
-        if (lk == -INFINITY) continue;  // an empty part has weight 0
-        const float w = expf(lk - L);
-        const float4 v = __ldg(reinterpret_cast<const float4*>(parts.o[k] + r * D) + g);
-        acc.x = fmaf(w, v.x, acc.x);
-        acc.y = fmaf(w, v.y, acc.y);
-        acc.z = fmaf(w, v.z, acc.z);
-        acc.w = fmaf(w, v.w, acc.w);
+    for (int u = 0; u < R; ++u) m[u] = -INFINITY;
+    for (int k = g; k < n; k += G) {
+#pragma unroll
+      for (int u = 0; u < R; ++u) m[u] = fmaxf(m[u], __ldg(parts.l[k] + rr[u]));
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < R; ++u) m[u] = fmaxf(m[u], __shfl_xor_sync(gmask, m[u], o));
+    }
+    float z[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) z[u] = 0.0f;
+    for (int k = g; k < n; k += G) {
+#pragma unroll
+      for (int u = 0; u < R; ++u)
+        if (m[u] != -INFINITY) z[u] += expf(__ldg(parts.l[k] + rr[u]) - m[u]);
+    }
+#pragma unroll
+    for (int o = G / 2; o > 0; o >>= 1) {
+#pragma unroll
+      for (int u = 0; u < R; ++u) z[u] += __shfl_xor_sync(gmask, z[u], o);
+    }
+    float L[R];
+    float4 acc[R];
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      L[u] = (m[u] != -INFINITY) ? m[u] + logf(z[u]) : -INFINITY;
+      acc[u] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    for (int k = 0; k < n; ++k) {
+      float lk[R];
+      float4 v[R];
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        lk[u] = __ldg(parts.l[k] + rr[u]);
+        v[u] = __ldg(reinterpret_cast<const float4*>(parts.o[k] + rr[u] * D) + g);
+      }
+#pragma unroll
+      for (int u = 0; u < R; ++u) {
+        if (lk[u] == -INFINITY) continue;  // an empty part has weight 0 (and every part of an empty row)
+        const float w = expf(lk[u] - L[u]);
+        acc[u].x = fmaf(w, v[u].x, acc[u].x);
+        acc[u].y = fmaf(w, v[u].y, acc[u].y);
+        acc[u].z = fmaf(w, v[u].z, acc[u].z);
+        acc[u].w = fmaf(w, v[u].w, acc[u].w);
       }
     }
-    store4(out, r * G + g, acc, out_dtype);
-    if (lse && g == 0) lse[r] = L;
+#pragma unroll
+    for (int u = 0; u < R; ++u) {
+      if (r0 + u >= rows) break;
+      store4(out, rr[u] * G + g, acc[u], out_dtype);
+      if (lse && g == 0) lse[rr[u]] = L[u];
+    }
   }
 }
 
@@ -102,8 +138,8 @@ int launch_n(const float* const* O_parts, const float* const* LSE_parts, int n, 
     pp.l[k] = k < n ? LSE_parts[k] : nullptr;
   }
   constexpr int G = D / 4;
-  const long long groups_per_block = 256 / G;
-  long long blocks = (rows + groups_per_block - 1) / groups_per_block;
+  const long long rows_per_block = 256 / G * 4;
+  long long blocks = (rows + rows_per_block - 1) / rows_per_block;
   const long long cap = static_cast<long long>(sm_count()) * 8;  // 8 x 256 threads resident per SM
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
