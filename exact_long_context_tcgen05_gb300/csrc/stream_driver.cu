@@ -4,9 +4,10 @@
 // per-subproblem host transfers with compute ("stream-cqsa 2.2.0 -> 2.2.2" diff, README profile
 // sweep); host copies are token-major ("stream-cqsa 2.2.2 -> 2.2.3" diff, api.py `_pinned_copy`).
 //
-// Schedule (Q-outer): for each Q chunk i, Q_i is copied once; the KV chunks j it needs (j <= i when
-// causal) are double-buffered on a copy stream: copy(j) waits for the kernel that last used its
-// slot, the kernel for (i, j) waits for copy(j). The first pair of a Q chunk writes the accumulator
+// Schedule (Q-outer): for each Q chunk i, Q_i is copied once into one of two Q buffers (the copy of
+// Q_{i+1} overlaps Q_i's kernels); the KV chunks j it needs (j <= i when causal) are double-buffered
+// on the same copy stream: copy(j) waits for the kernel that last used its slot, the kernel for
+// (i, j) waits for copy(j). Contiguous chunks (token-major, B = 1) travel as plain copies. The first pair of a Q chunk writes the accumulator
 // (partial mode), later pairs merge into it in place (accumulate mode). A finalize kernel converts
 // the accumulator to the output dtype and layout; host outputs leave on a second copy stream.
 // The KV order alternates direction between consecutive Q chunks (serpentine), so the chunk that
@@ -114,6 +115,10 @@ cudaError_t copy_chunk_h2d(void* dst, const void* src, int layout, int B, int H,
     base += static_cast<size_t>(t0) * H * d * es;
   }
   *bytes += static_cast<long long>(width * height);
+  // A chunk that is one contiguous host range (token-major with B = 1, or the whole sequence) goes
+  // as a plain copy; the strided form only for [B,H,N,d] chunks.
+  if (height == 1 || spitch == width)
+    return cudaMemcpyAsync(dst, base, width * height, cudaMemcpyHostToDevice, s);
   return cudaMemcpy2DAsync(dst, width, base, spitch, width, height, cudaMemcpyHostToDevice, s);
 }
 
@@ -170,9 +175,12 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   cx.res.compute = stream;
   cx.res.compute_set = true;
   int rc = CQSA_OK;
-  void *qbuf = nullptr, *kbuf[2] = {nullptr, nullptr}, *vbuf[2] = {nullptr, nullptr};
+  void *qbuf[2] = {nullptr, nullptr}, *kbuf[2] = {nullptr, nullptr}, *vbuf[2] = {nullptr, nullptr};
   void *acc = nullptr, *lacc = nullptr, *ostage = nullptr, *lstage = nullptr;
-  rc = cx.alloc(&qbuf, chunk_elems * es);
+  // Q is double-buffered too (when there is more than one Q chunk), so the next Q chunk's copy does
+  // not wait for the current chunk's last kernel.
+  const int nqbuf = nch > 1 ? 2 : 1;
+  for (int s = 0; rc == CQSA_OK && s < nqbuf; ++s) rc = cx.alloc(&qbuf[s], chunk_elems * es);
   for (int s = 0; rc == CQSA_OK && s < 2; ++s) {
     rc = cx.alloc(&kbuf[s], chunk_elems * es);
     if (rc == CQSA_OK) rc = cx.alloc(&vbuf[s], chunk_elems * es);
@@ -190,14 +198,14 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
     return rc;
 
   // Events: ordering (no timing) and per-operation timing pairs.
-  cudaEvent_t kv_ready[2], kv_free[2], q_ready, q_free, fin_done, d2h_done;
+  cudaEvent_t kv_ready[2], kv_free[2], q_ready[2], q_free[2], fin_done, d2h_done;
   for (int s = 0; s < 2; ++s) {
     if ((rc = cx.event(&kv_ready[s], false)) != CQSA_OK) return rc;
     if ((rc = cx.event(&kv_free[s], false)) != CQSA_OK) return rc;
+    if ((rc = cx.event(&q_ready[s], false)) != CQSA_OK) return rc;
+    if ((rc = cx.event(&q_free[s], false)) != CQSA_OK) return rc;
   }
-  if ((rc = cx.event(&q_ready, false)) != CQSA_OK || (rc = cx.event(&q_free, false)) != CQSA_OK ||
-      (rc = cx.event(&fin_done, false)) != CQSA_OK || (rc = cx.event(&d2h_done, false)) != CQSA_OK)
-    return rc;
+  if ((rc = cx.event(&fin_done, false)) != CQSA_OK || (rc = cx.event(&d2h_done, false)) != CQSA_OK) return rc;
   struct Span {
     cudaEvent_t a, b;
   };
@@ -217,7 +225,7 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   int launches = 0, pairs = 0;
   int slot_of_chunk[2] = {-1, -1};  // KV chunk index resident in each slot
   int next_slot = 0;
-  bool q_free_recorded = false, d2h_recorded = false;
+  bool q_free_recorded[2] = {false, false}, d2h_recorded = false;
 
 #define CK(call, what)                                 \
   do {                                                 \
@@ -231,17 +239,18 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   for (int i = 0; i < nch; ++i) {
     const long long qt0 = static_cast<long long>(i) * C;
     const int qn = static_cast<int>(N - qt0 < C ? N - qt0 : C);
-    // Q chunk i: the previous Q chunk's kernels must be done with the buffer.
-    if (q_free_recorded) CK(cudaStreamWaitEvent(cx.res.copy, q_free, 0), "wait q_free");
+    // Q chunk i goes to buffer i % 2: the kernels of Q chunk i-2 must be done with it.
+    const int qs = i % nqbuf;
+    if (q_free_recorded[qs]) CK(cudaStreamWaitEvent(cx.res.copy, q_free[qs], 0), "wait q_free");
     {
       Span sp;
       if ((rc = span(copies, &sp)) != CQSA_OK) return rc;
       CK(cudaEventRecord(sp.a, cx.res.copy), "record");
-      CK(copy_chunk_h2d(qbuf, q_host, layout, B, H, N, d, qt0, qn, cx.res.copy, &h2d_bytes), "copy Q chunk");
+      CK(copy_chunk_h2d(qbuf[qs], q_host, layout, B, H, N, d, qt0, qn, cx.res.copy, &h2d_bytes), "copy Q chunk");
       CK(cudaEventRecord(sp.b, cx.res.copy), "record");
     }
-    CK(cudaEventRecord(q_ready, cx.res.copy), "record q_ready");
-    CK(cudaStreamWaitEvent(stream, q_ready, 0), "wait q_ready");
+    CK(cudaEventRecord(q_ready[qs], cx.res.copy), "record q_ready");
+    CK(cudaStreamWaitEvent(stream, q_ready[qs], 0), "wait q_ready");
     // The accumulator is reused per Q chunk: the previous finalize must have read it (same stream),
     // and a host-side D2H of the previous staging buffer must be done before finalize overwrites it.
 
@@ -272,7 +281,7 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
       CK(cudaStreamWaitEvent(stream, kv_ready[slot], 0), "wait kv_ready");
       AttnArgs a;
       memset(&a, 0, sizeof(a));
-      a.q = qbuf;
+      a.q = qbuf[qs];
       a.k = kbuf[slot];
       a.v = vbuf[slot];
       a.B = B;
@@ -303,8 +312,8 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
       ++launches;
       ++pairs;
     }
-    CK(cudaEventRecord(q_free, stream), "record q_free");
-    q_free_recorded = true;
+    CK(cudaEventRecord(q_free[qs], stream), "record q_free");
+    q_free_recorded[qs] = true;
 
     // Finalize Q chunk i.
     if (out_on_host && d2h_recorded) CK(cudaStreamWaitEvent(stream, d2h_done, 0), "wait d2h_done");
@@ -337,7 +346,11 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
         dpitch = static_cast<size_t>(N) * H * d * es;
         obase += static_cast<size_t>(qt0) * H * d * es;
       }
-      CK(cudaMemcpy2DAsync(obase, dpitch, ostage, width, width, height, cudaMemcpyDeviceToHost, cx.res.d2h), "D2H out");
+      if (height == 1 || dpitch == width)
+        CK(cudaMemcpyAsync(obase, ostage, width * height, cudaMemcpyDeviceToHost, cx.res.d2h), "D2H out");
+      else
+        CK(cudaMemcpy2DAsync(obase, dpitch, ostage, width, width, height, cudaMemcpyDeviceToHost, cx.res.d2h),
+           "D2H out");
       d2h_bytes += static_cast<long long>(width * height);
       if (lse) {
         const size_t lw = static_cast<size_t>(qn) * 4;

@@ -99,7 +99,8 @@ typedef struct {
 
 /*
  * Out-of-memory exact attention: Q/K/V stay in pinned (or pageable) host memory in `layout` and
- * are streamed to the device in chunks of chunk_tokens (a multiple of 128): for each Q chunk, the
+ * are streamed to the device in chunks of chunk_tokens (a multiple of 128): for each Q chunk (two Q
+ * buffers, so the next Q chunk arrives during the current one), the
  * K/V chunks it needs are double-buffered over the host link on a copy stream while the chunk
  * kernel merges each pair into an fp32 device accumulator ("stream_from_host", with per-subproblem
  * host transfers overlapping compute: "stream-cqsa 2.2.0 -> 2.2.2" diff, README profile sweep).
