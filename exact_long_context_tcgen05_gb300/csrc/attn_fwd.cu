@@ -903,11 +903,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
                               // values scaled by 2^-m_sum and is only brought to m_ref when read
     bool ok = true;
 
-    for (int j = 0; j < nkv; ++j) {
-      if (C::FLUSH > 0 && j > 0 && j % C::FLUSH == 0) {
-        // Segment boundary: once PV_t(j-1) is complete, fold O into the running sum O_sum (RNE fp32
-        // adds); PV_t(j) restarts O. O is in the current reference max; O_sum is brought from m_sum
-        // to it by an exact power of two.
+    // Key tiles in segments of FLUSH (one segment when FLUSH = 0). Between segments, once PV_t of the
+    // segment's last tile is complete, O is folded into the fp32 running sum O_sum (RNE adds) and
+    // the next segment's first PV_t restarts O; O is in the current reference max, O_sum is brought
+    // from m_sum to it by an exact power of two. Keeping the fold out of the per-tile loop keeps that
+    // loop's code identical to the unsegmented one.
+    constexpr int SEG = C::FLUSH > 0 ? C::FLUSH : (1 << 30);
+    for (int j0 = 0; ok && j0 < nkv; j0 += SEG) {
+      if (j0 > 0) {
+        const int j = j0;
         ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 23);
         if (!__all_sync(0xffffffffu, ok)) {
           ok = false;
@@ -932,117 +936,120 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         }
         m_sum = m_ref;
       }
-      ok = wait_or_abort_a(a_s_full, j & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[128];
+      const int j1 = (nkv - j0 < SEG) ? nkv : j0 + SEG;
+      for (int j = j0; j < j1; ++j) {
+        ok = wait_or_abort_a(a_s_full, j & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[128];
 #pragma unroll
-      for (int c = 0; c < 4; ++c) tmem_ld32(trow + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_wait_ld();
+        for (int c = 0; c < 4; ++c) tmem_ld32(trow + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
 #pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      if (!ALIAS) {
-        tc_fence_before();
-        mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
-      }
+        for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        if (!ALIAS) {
+          tc_fence_before();
+          mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+        }
 
-      float x[128];
+        float x[128];
 #pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-      const int k0 = j * BN;
-      const bool tail = (k0 + BN > p.Nkv);
-      const bool diag = CAUSAL && (p.kv_off + k0 + BN - 1 > p.q_off + qt0);
-      if (tail || diag) {
-        long long lim = p.Nkv - k0;
-        if (CAUSAL) {
-          const long long lc = qpos - p.kv_off - k0 + 1;
-          lim = lc < lim ? lc : lim;
-        }
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) x[c] = -INFINITY;
-      }
-      const float tmax = row_max128(x) * sl2;
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (tmax > m_ref + TAU) {
-        const float m_new = ceilf(tmax);
-        if (m_ref != -INFINITY) {
-          alpha = exp2_int(m_ref - m_new);
-          rescale = true;
-        }
-        m_ref = m_new;
-      }
-      const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
-      const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
-      float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-      const uint32_t pbuf = trow + colP;
-      if (!ALIAS) {
-        // fp16, P kept apart and single-buffered: compute all of P in registers first, then wait for
-        // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
-        // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
-        uint32_t pk[64];
-#pragma unroll
-        for (int c = 0; c < 64; ++c) {
-          const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
-          rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
-          pk[c] = pack2(pp.x, pp.y, 0);
-        }
-        if (j > 0) {
-          ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+        const int k0 = j * BN;
+        const bool tail = (k0 + BN > p.Nkv);
+        const bool diag = CAUSAL && (p.kv_off + k0 + BN - 1 > p.q_off + qt0);
+        if (tail || diag) {
+          long long lim = p.Nkv - k0;
+          if (CAUSAL) {
+            const long long lc = qpos - p.kv_off - k0 + 1;
+            lim = lc < lim ? lc : lim;
           }
-          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) x[c] = -INFINITY;
         }
-        tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-        tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-      } else {
-        // P over S: S_t(j) was issued only after PV_t(j-1) completed, so P_t(j-1) and O_t are settled.
+        const float tmax = row_max128(x) * sl2;
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (tmax > m_ref + TAU) {
+          const float m_new = ceilf(tmax);
+          if (m_ref != -INFINITY) {
+            alpha = exp2_int(m_ref - m_new);
+            rescale = true;
+          }
+          m_ref = m_new;
+        }
+        const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
+        const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
+        float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        const uint32_t pbuf = trow + colP;
+        if (!ALIAS) {
+          // fp16, P kept apart and single-buffered: compute all of P in registers first, then wait for
+          // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
+          // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
+          uint32_t pk[64];
 #pragma unroll
-        for (int c4 = 0; c4 < 4; ++c4) {
-          uint32_t hi[16], lo[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int c = c4 * 16 + e;
+          for (int c = 0; c < 64; ++c) {
             const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
             rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
-            if (DT) {
-              __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
-              const float2 hf = __bfloat1622float2(h2);
-              __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
-              hi[e] = *reinterpret_cast<uint32_t*>(&h2);
-              lo[e] = *reinterpret_cast<uint32_t*>(&l2);
-            } else {
-              hi[e] = pack2(pp.x, pp.y, 0);
-            }
+            pk[c] = pack2(pp.x, pp.y, 0);
           }
-          tmem_st16(pbuf + c4 * 16, hi);
-          if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
-        }
-      }
-      l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
-      // PV_t(j-1) is complete here (waited for above, or implied by S_t(j) when P is over S).
-      if (__any_sync(0xffffffffu, rescale) && j > 0) {
-        // O takes the new reference max (O_sum keeps its own, m_sum).
+          if (j > 0) {
+            ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        } else {
+          // P over S: S_t(j) was issued only after PV_t(j-1) completed, so P_t(j-1) and O_t are settled.
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(trow + colO + c * 32, o);
-          tmem_wait_ld();
-          reg_fence32(o);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t hi[16], lo[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(trow + colO + c * 32, o);
+            for (int e = 0; e < 16; ++e) {
+              const int c = c4 * 16 + e;
+              const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
+              rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
+              if (DT) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
+                const float2 hf = __bfloat1622float2(h2);
+                __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
+                hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+                lo[e] = *reinterpret_cast<uint32_t*>(&l2);
+              } else {
+                hi[e] = pack2(pp.x, pp.y, 0);
+              }
+            }
+            tmem_st16(pbuf + c4 * 16, hi);
+            if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
+          }
         }
+        l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
+        // PV_t(j-1) is complete here (waited for above, or implied by S_t(j) when P is over S).
+        if (__any_sync(0xffffffffu, rescale) && j > 0) {
+          // O takes the new reference max (O_sum keeps its own, m_sum).
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(trow + colO + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive_a(a_p_full);
       }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive_a(a_p_full);
     }
 
     // ---------------------------------------------------------------- epilogue
