@@ -20,8 +20,9 @@ CQSA_F16, CQSA_BF16, CQSA_F32 = 0, 1, 2
 CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
-            "cqsa_attn_fwd_chunked_static", "cqsa_status_string", "cqsa_last_error", "cqsa_device_error",
-            "cqsa_set_timeout_ms", "cqsa_debug_set_fault", "cqsa_version")
+            "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
+            "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
+            "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -35,6 +36,16 @@ class cqsa_stream_stats(ctypes.Structure):
     _fields_ = [("wall_ms", ctypes.c_double), ("compute_ms", ctypes.c_double), ("h2d_ms", ctypes.c_double),
                 ("stall_ms", ctypes.c_double), ("h2d_bytes", ctypes.c_longlong), ("d2h_bytes", ctypes.c_longlong),
                 ("peak_device_bytes", ctypes.c_longlong), ("n_chunks", ctypes.c_int), ("n_launches", ctypes.c_int)]
+
+    def as_dict(self):
+        return {f: getattr(self, f) for f, _ in self._fields_}
+
+
+class cqsa_quorum_stats(ctypes.Structure):
+    _fields_ = [("wall_ms", ctypes.c_double), ("compute_ms", ctypes.c_double), ("copy_ms", ctypes.c_double),
+                ("copy_bytes", ctypes.c_longlong), ("peak_device_bytes", ctypes.c_longlong),
+                ("chunk_tokens", ctypes.c_longlong), ("n_subproblems", ctypes.c_int), ("n_pairs", ctypes.c_int),
+                ("n_chunk_loads", ctypes.c_int), ("n_launches", ctypes.c_int)]
 
     def as_dict(self):
         return {f: getattr(self, f) for f, _ in self._fields_}
@@ -54,6 +65,11 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_stream_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _ll,
                                          ctypes.POINTER(cqsa_stream_stats), _vp]
     lib.cqsa_attn_fwd_chunked_static.argtypes = [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _f, _i, _i, _vp]
+    lib.cqsa_quorum_check.argtypes = [_i, _vp, _i]
+    lib.cqsa_quorum_schedule.argtypes = [_i, _vp, _i, _i, _i, _i, _vp, _ll]
+    lib.cqsa_quorum_schedule.restype = _ll
+    lib.cqsa_quorum_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i, _vp,
+                                         _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
     lib.cqsa_status_string.argtypes = [_i]
     lib.cqsa_status_string.restype = ctypes.c_char_p
     lib.cqsa_last_error.argtypes = []
@@ -66,7 +82,7 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_version.argtypes = []
     lib.cqsa_version.restype = ctypes.c_char_p
     for name in ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
-                 "cqsa_attn_fwd_chunked_static", "cqsa_device_error"):
+                 "cqsa_attn_fwd_chunked_static", "cqsa_device_error", "cqsa_quorum_check", "cqsa_quorum_attn_fwd"):
         getattr(lib, name).restype = _i
     return lib
 
@@ -154,6 +170,41 @@ def cqsa_attn_fwd_chunked_static(q, k, v, out, lse, B, H, N, d, causal, scale, d
     return _check(lib.cqsa_attn_fwd_chunked_static(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(lse), B, H, N, d,
                                                    int(bool(causal)), float(scale), dtype, chunk_tokens,
                                                    _stream(stream)))
+
+
+def _int_array(values):
+    vals = [int(x) for x in values]
+    return (ctypes.c_int * max(len(vals), 1))(*vals), len(vals)
+
+
+def cqsa_quorum_check(c, interest_set) -> int:
+    """CQSA_OK if interest_set is a perfect difference set modulo c (raises CqsaError otherwise)."""
+    arr, l = _int_array(interest_set)
+    return _check(lib.cqsa_quorum_check(c, ctypes.cast(arr, _vp), l))
+
+
+def cqsa_quorum_schedule(c, interest_set, itr, n_chunks, causal):
+    """The quorum schedule as a list of (subproblem, query chunk, key chunk) triples (host only)."""
+    arr, l = _int_array(interest_set)
+    n = lib.cqsa_quorum_schedule(c, ctypes.cast(arr, _vp), l, itr, n_chunks, int(bool(causal)), None, 0)
+    if n < 0:
+        raise CqsaError(int(n), last_error())
+    buf = (ctypes.c_int * max(3 * n, 1))()
+    m = lib.cqsa_quorum_schedule(c, ctypes.cast(arr, _vp), l, itr, n_chunks, int(bool(causal)),
+                                 ctypes.cast(buf, _vp), n)
+    if m != n:
+        raise CqsaError(int(m) if m < 0 else CQSA_ERR_INVALID, last_error())
+    return [(buf[3 * i], buf[3 * i + 1], buf[3 * i + 2]) for i in range(n)]
+
+
+def cqsa_quorum_attn_fwd(q, k, v, layout, inputs_on_host, out, lse, out_on_host, B, H, N, d, causal, scale, dtype,
+                         c, interest_set, itr, stats=None, stream=None) -> int:
+    st = stats if stats is not None else cqsa_quorum_stats()
+    arr, l = _int_array(interest_set)
+    return _check(lib.cqsa_quorum_attn_fwd(_ptr(q), _ptr(k), _ptr(v), layout, int(bool(inputs_on_host)), _ptr(out),
+                                           _ptr(lse), int(bool(out_on_host)), B, H, N, d, int(bool(causal)),
+                                           float(scale), dtype, c, ctypes.cast(arr, _vp), l, itr, ctypes.byref(st),
+                                           _stream(stream)))
 
 
 def cqsa_device_error(clear: bool = True):

@@ -43,6 +43,15 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream);
 int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int n, void* out, float* lse,
                  long long rows, int d, int out_dtype, cudaStream_t stream);
 
+// Copy tokens [t0, t0+n) of a [B,H,N,d] / [B,N,H,d] tensor (host or device) into a packed chunk buffer.
+cudaError_t copy_chunk(void* dst, const void* src, int layout, int B, int H, long long N, int d, long long t0, int n,
+                       cudaMemcpyKind kind, cudaStream_t s, long long* bytes);
+
+// Normalised fp32 accumulator (acc [B,H,n,d], lse_acc [B,H,n]) -> out tokens [t0, t0+n) of an N-token
+// tensor in `layout` and `dtype`, plus lse_out (may be NULL).
+int launch_finalize(const float* acc, const float* lse_acc, void* out, float* lse_out, int B, int H, int n,
+                    long long N, long long t0, int d, int layout, int dtype, cudaStream_t stream);
+
 // Status helpers
 void set_error(const char* fmt, ...);
 int cuda_status(cudaError_t e, const char* what);

@@ -1,0 +1,452 @@
+// Cyclic quorum-set decomposition of exact attention ("stream-cqsa 2.2.0 -> 2.2.2" diff: README and
+// `autoconfig.plan`, where a configuration is (c, interest_set, itr) with c**itr subproblems and
+// cost (l^2/c)^itr, l = |interest_set|; the default set is (0, 1, 3) at c = 7).
+//
+// Reading used here (the pages name the parameters and the costs but not the construction):
+//   * the sequence is cut into T = c^itr chunks of C tokens (C a multiple of 128, the last chunk
+//     ragged); chunk t has base-c digits t_0 .. t_{itr-1};
+//   * subproblem s (digits s_e) owns the l^itr chunks t with t_e in s_e + D (mod c) for every e,
+//     D the interest set; each subproblem therefore holds l^itr of the T chunks, and running every
+//     subproblem in full would cost c^itr (l^itr C)^2 = (l^2/c)^itr N^2 score entries;
+//   * D must be a perfect difference set modulo c (its l(l-1) ordered differences cover every non-zero
+//     residue once, so c = l(l-1) + 1): then two chunks with digits q_e != k_e share exactly one
+//     s_e, and every (query chunk, key chunk) pair meets in at least one subproblem;
+//   * each needed pair (q, k) (k <= q when causal) is computed exactly once, in the subproblem whose
+//     digit e is the unique shared one where q_e != k_e and q_e - D[0] where q_e = k_e; its partial
+//     (O, LSE) is merged into query chunk q's fp32 accumulator, so the result is the exact attention
+//     whatever the order of the subproblems.
+// A subproblem needs only its own chunks on the device: the executor stages Q and K/V chunks through
+// two sets of l^itr slots (the previous subproblem's chunks stay while the next ones load) and keeps
+// one fp32 accumulator per query chunk.
+#include <algorithm>
+#include <chrono>
+#include <math.h>
+#include <string.h>
+#include <vector>
+
+#include "cqsa_internal.h"
+
+namespace cqsa {
+namespace {
+
+constexpr int kMaxQuorumChunks = 1 << 16;  // c^itr
+
+struct Triple {
+  int s, q, k;
+};
+
+bool ipow_bounded(int c, int itr, int limit, int* out) {
+  long long v = 1;
+  for (int e = 0; e < itr; ++e) {
+    v *= c;
+    if (v > limit) return false;
+  }
+  *out = static_cast<int>(v);
+  return true;
+}
+
+// CQSA_OK if D (l distinct residues in [0, c)) is a perfect difference set modulo c.
+int check_set(int c, const int* D, int l) {
+  if (c < 1 || l < 1 || !D) {
+    set_error("quorum set: c and l must be positive and interest_set non-null");
+    return CQSA_ERR_INVALID;
+  }
+  if (static_cast<long long>(l) * (l - 1) + 1 != c) {
+    set_error("quorum set: a perfect difference set of %d residues needs c = %d (got c = %d)", l, l * (l - 1) + 1, c);
+    return CQSA_ERR_INVALID;
+  }
+  std::vector<int> seen(c, 0);
+  for (int i = 0; i < l; ++i) {
+    if (D[i] < 0 || D[i] >= c) {
+      set_error("quorum set: element %d is outside [0, %d)", D[i], c);
+      return CQSA_ERR_INVALID;
+    }
+    for (int j = 0; j < l; ++j) {
+      if (i == j) continue;
+      const int delta = ((D[j] - D[i]) % c + c) % c;
+      if (delta == 0) {
+        set_error("quorum set: repeated element %d", D[i]);
+        return CQSA_ERR_INVALID;
+      }
+      if (++seen[delta] > 1) {
+        set_error("quorum set: difference %d occurs more than once (not a perfect difference set mod %d)", delta, c);
+        return CQSA_ERR_INVALID;
+      }
+    }
+  }
+  return CQSA_OK;
+}
+
+// Every needed (q, k) chunk pair with the subproblem that computes it, sorted by (s, q, k).
+int build_schedule(int c, const int* D, int l, int itr, int n_chunks, bool causal, std::vector<Triple>* out) {
+  int rc = check_set(c, D, l);
+  if (rc != CQSA_OK) return rc;
+  int T = 0;
+  if (itr < 1 || !ipow_bounded(c, itr, kMaxQuorumChunks, &T)) {
+    set_error("quorum depth: need itr >= 1 and c^itr <= %d", kMaxQuorumChunks);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (n_chunks < 0 || n_chunks > T) {
+    set_error("quorum schedule: %d non-empty chunks for %d chunk slots", n_chunks, T);
+    return CQSA_ERR_INVALID;
+  }
+  // For a non-zero digit difference delta = k_e - q_e, the index i of the set element that q_e
+  // stands at in the shared subproblem: D[j] - D[i] = delta for exactly one (i, j).
+  std::vector<int> first_of(c, -1);
+  for (int i = 0; i < l; ++i)
+    for (int j = 0; j < l; ++j)
+      if (i != j) first_of[((D[j] - D[i]) % c + c) % c] = i;
+  out->clear();
+  for (int q = 0; q < n_chunks; ++q) {
+    const int kmax = causal ? q : n_chunks - 1;
+    for (int k = 0; k <= kmax; ++k) {
+      int s = 0, place = 1, qq = q, kk = k;
+      for (int e = 0; e < itr; ++e) {
+        const int qe = qq % c, ke = kk % c;
+        qq /= c;
+        kk /= c;
+        const int base = (qe == ke) ? D[0] : D[first_of[((ke - qe) % c + c) % c]];
+        s += (((qe - base) % c + c) % c) * place;
+        place *= c;
+      }
+      out->push_back({s, q, k});
+    }
+  }
+  std::stable_sort(out->begin(), out->end(), [](const Triple& a, const Triple& b) { return a.s < b.s; });
+  return CQSA_OK;
+}
+
+struct Resources {
+  std::vector<void*> dev;
+  std::vector<cudaEvent_t> events;
+  cudaStream_t copy = nullptr;
+  cudaStream_t compute = nullptr;
+  ~Resources() {
+    if (compute) cudaStreamSynchronize(compute);
+    if (copy) cudaStreamSynchronize(copy);
+    for (void* p : dev) cudaFree(p);
+    for (cudaEvent_t e : events) cudaEventDestroy(e);
+    if (copy) cudaStreamDestroy(copy);
+  }
+};
+
+}  // namespace
+}  // namespace cqsa
+
+using namespace cqsa;
+
+extern "C" int cqsa_quorum_check(int c, const int* interest_set, int l) { return check_set(c, interest_set, l); }
+
+extern "C" long long cqsa_quorum_schedule(int c, const int* interest_set, int l, int itr, int n_chunks, int causal,
+                                          int* out, long long max_triples) {
+  std::vector<Triple> tr;
+  const int rc = build_schedule(c, interest_set, l, itr, n_chunks, causal != 0, &tr);
+  if (rc != CQSA_OK) return rc;
+  if (out) {
+    if (max_triples < static_cast<long long>(tr.size())) {
+      set_error("quorum schedule: %zu triples do not fit in %lld", tr.size(), max_triples);
+      return CQSA_ERR_INVALID;
+    }
+    for (size_t i = 0; i < tr.size(); ++i) {
+      out[3 * i + 0] = tr[i].s;
+      out[3 * i + 1] = tr[i].q;
+      out[3 * i + 2] = tr[i].k;
+    }
+  }
+  return static_cast<long long>(tr.size());
+}
+
+extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host,
+                                    void* out, float* lse, int out_on_host, int B, int H, long long N, int d,
+                                    int causal, float scale, int dtype, int c, const int* interest_set, int l,
+                                    int itr, cqsa_quorum_stats* stats, cudaStream_t stream) {
+  const auto t_start = std::chrono::steady_clock::now();
+  if (stats) memset(stats, 0, sizeof(*stats));
+  if (!q || !k || !v || !out) {
+    set_error("q, k, v and out must be non-null");
+    return CQSA_ERR_INVALID;
+  }
+  if (B < 1 || H < 1 || N < 1) {
+    set_error("sizes must be positive");
+    return CQSA_ERR_INVALID;
+  }
+  if (d != 64 && d != 128) {
+    set_error("head dim %d is not supported (64 or 128)", d);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (dtype != CQSA_F16 && dtype != CQSA_BF16) {
+    set_error("dtype %d is not supported", dtype);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (layout != CQSA_LAYOUT_BHND && layout != CQSA_LAYOUT_BNHD) {
+    set_error("layout %d is not supported", layout);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (!isfinite(scale) || scale < 0.0f) {
+    set_error("scale must be finite and >= 0 (0 selects 1/sqrt(d))");
+    return CQSA_ERR_INVALID;
+  }
+  int T = 0;
+  if (itr < 1 || c < 1 || !ipow_bounded(c, itr, kMaxQuorumChunks, &T)) {
+    set_error("quorum depth: need c >= 1, itr >= 1 and c^itr <= %d", kMaxQuorumChunks);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  const long long per = (N + T - 1) / T;
+  const long long C = ((per + 127) / 128) * 128;
+  const int nne = static_cast<int>((N + C - 1) / C);  // non-empty chunks
+  if (static_cast<long long>(B) * H * C > (1LL << 31) - 1) {
+    set_error("B*H*chunk too large for one chunk launch");
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  std::vector<Triple> sched;
+  int rc = build_schedule(c, interest_set, l, itr, nne, causal != 0, &sched);
+  if (rc != CQSA_OK) return rc;
+  int per_sub = 1;
+  for (int e = 0; e < itr; ++e) per_sub *= l;
+  const int nslots = std::min(2 * per_sub, nne);
+  const float sc = scale == 0.0f ? 1.0f / sqrtf(static_cast<float>(d)) : scale;
+  const size_t es = 2;
+  const size_t chunk_elems = static_cast<size_t>(B) * H * C * d;
+  const size_t rows = static_cast<size_t>(B) * H * C;
+  const cudaMemcpyKind kind = inputs_on_host ? cudaMemcpyHostToDevice : cudaMemcpyDeviceToDevice;
+
+  Resources res;
+  res.compute = stream;
+  long long dev_bytes = 0;
+  auto alloc = [&](void** p, size_t n) -> int {
+    cudaError_t e = cudaMalloc(p, n);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("device allocation of %zu bytes failed: %s", n, cudaGetErrorString(e));
+      return e == cudaErrorMemoryAllocation ? CQSA_ERR_OOM : CQSA_ERR_CUDA;
+    }
+    res.dev.push_back(*p);
+    dev_bytes += static_cast<long long>(n);
+    return CQSA_OK;
+  };
+  auto event = [&](cudaEvent_t* e, bool timing) -> int {
+    cudaError_t r = cudaEventCreateWithFlags(e, timing ? cudaEventDefault : cudaEventDisableTiming);
+    if (r != cudaSuccess) return cuda_status(r, "cudaEventCreate");
+    res.events.push_back(*e);
+    return CQSA_OK;
+  };
+  std::vector<void*> qs(nslots), ks(nslots), vs(nslots);
+  for (int s = 0; rc == CQSA_OK && s < nslots; ++s) {
+    rc = alloc(&qs[s], chunk_elems * es);
+    if (rc == CQSA_OK) rc = alloc(&ks[s], chunk_elems * es);
+    if (rc == CQSA_OK) rc = alloc(&vs[s], chunk_elems * es);
+  }
+  void *acc = nullptr, *lacc = nullptr, *ostage = nullptr, *lstage = nullptr;
+  if (rc == CQSA_OK) rc = alloc(&acc, static_cast<size_t>(nne) * chunk_elems * 4);
+  if (rc == CQSA_OK) rc = alloc(&lacc, static_cast<size_t>(nne) * rows * 4);
+  if (rc == CQSA_OK && out_on_host) {
+    rc = alloc(&ostage, chunk_elems * es);
+    if (rc == CQSA_OK && lse) rc = alloc(&lstage, rows * 4);
+  }
+  if (rc != CQSA_OK) return rc;
+  if ((rc = cuda_status(cudaStreamCreateWithFlags(&res.copy, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
+    return rc;
+  std::vector<cudaEvent_t> q_ready(nslots), q_free(nslots), kv_ready(nslots), kv_free(nslots);
+  for (int s = 0; s < nslots; ++s) {
+    if ((rc = event(&q_ready[s], false)) != CQSA_OK || (rc = event(&q_free[s], false)) != CQSA_OK ||
+        (rc = event(&kv_ready[s], false)) != CQSA_OK || (rc = event(&kv_free[s], false)) != CQSA_OK)
+      return rc;
+  }
+  struct Span {
+    cudaEvent_t a, b;
+  };
+  std::vector<Span> copies, kernels;
+  auto span = [&](std::vector<Span>& vv, Span* sp) -> int {
+    int r = event(&sp->a, true);
+    if (r == CQSA_OK) r = event(&sp->b, true);
+    if (r == CQSA_OK) vv.push_back(*sp);
+    return r;
+  };
+#define CK(call, what)                     \
+  do {                                     \
+    int _r = cuda_status((call), what);    \
+    if (_r != CQSA_OK) return _r;          \
+  } while (0)
+
+  auto ntok = [&](int chunk) -> int { return static_cast<int>(std::min(C, N - static_cast<long long>(chunk) * C)); };
+  struct Pool {
+    std::vector<int> chunk;     // chunk held by each slot (-1: none)
+    std::vector<int> last_use;  // subproblem group of the last use
+    std::vector<bool> used;     // a kernel has read the slot (its free event is recorded)
+  };
+  Pool qp{std::vector<int>(nslots, -1), std::vector<int>(nslots, -1), std::vector<bool>(nslots, false)};
+  Pool kp = qp;
+  long long copy_bytes = 0;
+  int loads = 0, groups = 0, launches = 0;
+  std::vector<bool> started(nne, false);
+
+  // Slot of `chunk` in `pool` (*slot), staging it on the copy stream (after the slot's previous reader)
+  // if absent. `keep` lists chunks the current subproblem needs, which are never evicted.
+  auto stage = [&](Pool& pool, bool is_q, int chunk, int group, const std::vector<int>& keep, int* slot) -> int {
+    for (int s = 0; s < nslots; ++s)
+      if (pool.chunk[s] == chunk) {
+        pool.last_use[s] = group;
+        *slot = s;
+        return CQSA_OK;
+      }
+    int victim = -1;
+    for (int s = 0; s < nslots; ++s) {
+      if (pool.chunk[s] >= 0 && std::find(keep.begin(), keep.end(), pool.chunk[s]) != keep.end()) continue;
+      if (victim < 0 || pool.chunk[s] < 0 ||
+          (pool.chunk[victim] >= 0 && pool.last_use[s] < pool.last_use[victim]))
+        victim = s;
+      if (pool.chunk[victim] < 0) break;
+    }
+    if (victim < 0) {  // cannot happen: a subproblem needs at most l^itr <= nslots chunks
+      set_error("quorum executor: no free chunk slot");
+      return CQSA_ERR_INVALID;
+    }
+    int r;
+    if (pool.used[victim] &&
+        (r = cuda_status(cudaStreamWaitEvent(res.copy, is_q ? q_free[victim] : kv_free[victim], 0), "wait slot")) !=
+            CQSA_OK)
+      return r;
+    Span sp;
+    if ((r = span(copies, &sp)) != CQSA_OK) return r;
+    const long long t0 = static_cast<long long>(chunk) * C;
+    const int n = ntok(chunk);
+    if ((r = cuda_status(cudaEventRecord(sp.a, res.copy), "record")) != CQSA_OK) return r;
+    if (is_q) {
+      r = cuda_status(copy_chunk(qs[victim], q, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy Q chunk");
+    } else {
+      r = cuda_status(copy_chunk(ks[victim], k, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy K chunk");
+      if (r == CQSA_OK)
+        r = cuda_status(copy_chunk(vs[victim], v, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes),
+                        "copy V chunk");
+    }
+    if (r != CQSA_OK) return r;
+    if ((r = cuda_status(cudaEventRecord(sp.b, res.copy), "record")) != CQSA_OK) return r;
+    if ((r = cuda_status(cudaEventRecord(is_q ? q_ready[victim] : kv_ready[victim], res.copy), "record ready")) !=
+        CQSA_OK)
+      return r;
+    pool.chunk[victim] = chunk;
+    pool.last_use[victim] = group;
+    ++loads;
+    *slot = victim;
+    return CQSA_OK;
+  };
+
+  size_t i0 = 0;
+  while (i0 < sched.size()) {
+    size_t i1 = i0;
+    while (i1 < sched.size() && sched[i1].s == sched[i0].s) ++i1;
+    std::vector<int> needq, needk;
+    for (size_t i = i0; i < i1; ++i) {
+      if (std::find(needq.begin(), needq.end(), sched[i].q) == needq.end()) needq.push_back(sched[i].q);
+      if (std::find(needk.begin(), needk.end(), sched[i].k) == needk.end()) needk.push_back(sched[i].k);
+    }
+    for (size_t i = i0; i < i1; ++i) {
+      const Triple& t = sched[i];
+      int sq = -1, sk = -1;
+      if ((rc = stage(qp, true, t.q, groups, needq, &sq)) != CQSA_OK) return rc;
+      if ((rc = stage(kp, false, t.k, groups, needk, &sk)) != CQSA_OK) return rc;
+      CK(cudaStreamWaitEvent(stream, q_ready[sq], 0), "wait q_ready");
+      CK(cudaStreamWaitEvent(stream, kv_ready[sk], 0), "wait kv_ready");
+      AttnArgs a;
+      memset(&a, 0, sizeof(a));
+      a.q = qs[sq];
+      a.k = ks[sk];
+      a.v = vs[sk];
+      a.B = B;
+      a.H = H;
+      a.Nq = ntok(t.q);
+      a.Nkv = ntok(t.k);
+      a.q_off = static_cast<long long>(t.q) * C;
+      a.kv_off = static_cast<long long>(t.k) * C;
+      a.d = d;
+      a.causal = causal != 0;
+      a.scale = sc;
+      a.dtype = dtype;
+      a.in_layout = layout;
+      a.mode = started[t.q] ? kModeAccum : kModePart;
+      a.o_part = static_cast<float*>(acc) + static_cast<size_t>(t.q) * chunk_elems;
+      a.lse_part = static_cast<float*>(lacc) + static_cast<size_t>(t.q) * rows;
+      a.out_layout = CQSA_LAYOUT_BHND;
+      Span sp;
+      if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
+      CK(cudaEventRecord(sp.a, stream), "record");
+      if ((rc = launch_attention(a, stream)) != CQSA_OK) return rc;
+      CK(cudaEventRecord(sp.b, stream), "record");
+      CK(cudaEventRecord(q_free[sq], stream), "record q_free");
+      CK(cudaEventRecord(kv_free[sk], stream), "record kv_free");
+      qp.used[sq] = true;
+      kp.used[sk] = true;
+      started[t.q] = true;
+      ++launches;
+    }
+    ++groups;
+    i0 = i1;
+  }
+
+  // Finalize every query chunk into the output (device), or through a staging buffer to the host.
+  for (int qc = 0; qc < nne; ++qc) {
+    const int n = ntok(qc);
+    const long long t0 = static_cast<long long>(qc) * C;
+    const float* accq = static_cast<float*>(acc) + static_cast<size_t>(qc) * chunk_elems;
+    const float* laccq = static_cast<float*>(lacc) + static_cast<size_t>(qc) * rows;
+    if (!out_on_host) {
+      if ((rc = launch_finalize(accq, laccq, out, lse, B, H, n, N, t0, d, layout, dtype, stream)) != CQSA_OK) return rc;
+    } else {
+      if ((rc = launch_finalize(accq, laccq, ostage, static_cast<float*>(lstage), B, H, n, n, 0, d, layout, dtype,
+                                stream)) != CQSA_OK)
+        return rc;
+      size_t width, height, dpitch;
+      char* obase = static_cast<char*>(out);
+      if (layout == CQSA_LAYOUT_BHND) {
+        width = static_cast<size_t>(n) * d * es;
+        height = static_cast<size_t>(B) * H;
+        dpitch = static_cast<size_t>(N) * d * es;
+        obase += static_cast<size_t>(t0) * d * es;
+      } else {
+        width = static_cast<size_t>(n) * H * d * es;
+        height = static_cast<size_t>(B);
+        dpitch = static_cast<size_t>(N) * H * d * es;
+        obase += static_cast<size_t>(t0) * H * d * es;
+      }
+      if (height == 1 || dpitch == width)
+        CK(cudaMemcpyAsync(obase, ostage, width * height, cudaMemcpyDeviceToHost, stream), "D2H out");
+      else
+        CK(cudaMemcpy2DAsync(obase, dpitch, ostage, width, width, height, cudaMemcpyDeviceToHost, stream), "D2H out");
+      if (lse) {
+        const size_t lw = static_cast<size_t>(n) * 4;
+        CK(cudaMemcpy2DAsync(lse + t0, static_cast<size_t>(N) * 4, lstage, lw, lw, static_cast<size_t>(B) * H,
+                             cudaMemcpyDeviceToHost, stream),
+           "D2H lse");
+      }
+    }
+    ++launches;
+  }
+  CK(cudaStreamSynchronize(stream), "synchronize compute stream");
+  CK(cudaStreamSynchronize(res.copy), "synchronize copy stream");
+  {
+    int code = 0;
+    int r = cqsa_device_error(&code, nullptr, 1);
+    if (r != CQSA_OK) return r;
+  }
+#undef CK
+  if (stats) {
+    double cp = 0.0, comp = 0.0;
+    float ms = 0.0f;
+    for (const Span& s : copies)
+      if (cudaEventElapsedTime(&ms, s.a, s.b) == cudaSuccess) cp += ms;
+    for (const Span& s : kernels)
+      if (cudaEventElapsedTime(&ms, s.a, s.b) == cudaSuccess) comp += ms;
+    stats->copy_ms = cp;
+    stats->compute_ms = comp;
+    stats->copy_bytes = copy_bytes;
+    stats->peak_device_bytes = dev_bytes;
+    stats->n_subproblems = groups;
+    stats->n_pairs = static_cast<int>(sched.size());
+    stats->n_chunk_loads = loads;
+    stats->n_launches = launches;
+    stats->chunk_tokens = C;
+    stats->wall_ms =
+        std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  }
+  return CQSA_OK;
+}

@@ -96,10 +96,12 @@ struct Ctx {
   }
 };
 
-// Copy tokens [t0, t0+n) of a host tensor (layout, N tokens) into a packed device chunk buffer of the
-// same layout ([B,H,n,d] or [B,n,H,d]).
-cudaError_t copy_chunk_h2d(void* dst, const void* src, int layout, int B, int H, long long N, int d, long long t0,
-                           int n, cudaStream_t s, long long* bytes) {
+}  // namespace
+
+// Copy tokens [t0, t0+n) of a tensor (layout, N tokens; host or device memory) into a packed device
+// chunk buffer of the same layout ([B,H,n,d] or [B,n,H,d]).
+cudaError_t copy_chunk(void* dst, const void* src, int layout, int B, int H, long long N, int d, long long t0, int n,
+                       cudaMemcpyKind kind, cudaStream_t s, long long* bytes) {
   const size_t es = 2;
   size_t width, height, spitch;
   const char* base = static_cast<const char*>(src);
@@ -115,14 +117,23 @@ cudaError_t copy_chunk_h2d(void* dst, const void* src, int layout, int B, int H,
     base += static_cast<size_t>(t0) * H * d * es;
   }
   *bytes += static_cast<long long>(width * height);
-  // A chunk that is one contiguous host range (token-major with B = 1, or the whole sequence) goes
-  // as a plain copy; the strided form only for [B,H,N,d] chunks.
-  if (height == 1 || spitch == width)
-    return cudaMemcpyAsync(dst, base, width * height, cudaMemcpyHostToDevice, s);
-  return cudaMemcpy2DAsync(dst, width, base, spitch, width, height, cudaMemcpyHostToDevice, s);
+  // A chunk that is one contiguous range (token-major with B = 1, or the whole sequence) goes as a
+  // plain copy; the strided form only for [B,H,N,d] chunks.
+  if (height == 1 || spitch == width) return cudaMemcpyAsync(dst, base, width * height, kind, s);
+  return cudaMemcpy2DAsync(dst, width, base, spitch, width, height, kind, s);
 }
 
-}  // namespace
+int launch_finalize(const float* acc, const float* lse_acc, void* out, float* lse_out, int B, int H, int n,
+                    long long N, long long t0, int d, int layout, int dtype, cudaStream_t stream) {
+  const long long total4 = static_cast<long long>(B) * H * n * d / 4;
+  long long blocks = (total4 + 255) / 256;
+  if (blocks > 152 * 16) blocks = 152 * 16;
+  if (blocks < 1) blocks = 1;
+  finalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(acc, lse_acc, out, lse_out, B, H, n, N, t0, d,
+                                                               layout, dtype);
+  return cuda_status(cudaGetLastError(), "finalize launch");
+}
+
 }  // namespace cqsa
 
 using namespace cqsa;
@@ -246,7 +257,7 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
       Span sp;
       if ((rc = span(copies, &sp)) != CQSA_OK) return rc;
       CK(cudaEventRecord(sp.a, cx.res.copy), "record");
-      CK(copy_chunk_h2d(qbuf[qs], q_host, layout, B, H, N, d, qt0, qn, cx.res.copy, &h2d_bytes), "copy Q chunk");
+      CK(copy_chunk(qbuf[qs], q_host, layout, B, H, N, d, qt0, qn, cudaMemcpyHostToDevice, cx.res.copy, &h2d_bytes), "copy Q chunk");
       CK(cudaEventRecord(sp.b, cx.res.copy), "record");
     }
     CK(cudaEventRecord(q_ready[qs], cx.res.copy), "record q_ready");
@@ -270,8 +281,8 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
         Span sp;
         if ((rc = span(copies, &sp)) != CQSA_OK) return rc;
         CK(cudaEventRecord(sp.a, cx.res.copy), "record");
-        CK(copy_chunk_h2d(kbuf[slot], k_host, layout, B, H, N, d, kt0, kn, cx.res.copy, &h2d_bytes), "copy K chunk");
-        CK(copy_chunk_h2d(vbuf[slot], v_host, layout, B, H, N, d, kt0, kn, cx.res.copy, &h2d_bytes), "copy V chunk");
+        CK(copy_chunk(kbuf[slot], k_host, layout, B, H, N, d, kt0, kn, cudaMemcpyHostToDevice, cx.res.copy, &h2d_bytes), "copy K chunk");
+        CK(copy_chunk(vbuf[slot], v_host, layout, B, H, N, d, kt0, kn, cudaMemcpyHostToDevice, cx.res.copy, &h2d_bytes), "copy V chunk");
         CK(cudaEventRecord(sp.b, cx.res.copy), "record");
         CK(cudaEventRecord(kv_ready[slot], cx.res.copy), "record kv_ready");
         slot_of_chunk[slot] = j;
@@ -322,12 +333,12 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
       float* ldst = out_on_host ? static_cast<float*>(lstage) : lse;
       const long long Nd = out_on_host ? qn : N;
       const long long td = out_on_host ? 0 : qt0;
-      const long long total4 = static_cast<long long>(B) * H * qn * d / 4;
-      long long blocks = (total4 + 255) / 256;
-      if (blocks > 152 * 16) blocks = 152 * 16;
-      finalize_kernel<<<static_cast<int>(blocks), 256, 0, stream>>>(static_cast<float*>(acc), static_cast<float*>(lacc), dst,
-                                                                   ldst, B, H, qn, Nd, td, d, layout, dtype);
-      CK(cudaGetLastError(), "finalize launch");
+      rc = launch_finalize(static_cast<float*>(acc), static_cast<float*>(lacc), dst, ldst, B, H, qn, Nd, td, d, layout,
+                           dtype, stream);
+      if (rc != CQSA_OK) {
+        cudaStreamSynchronize(stream);
+        return rc;
+      }
       ++launches;
     }
     if (out_on_host) {

@@ -114,6 +114,55 @@ int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_h
                          float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,
                          cudaStream_t stream);
 
+/* ------------------------------------------------------------------------------------------------
+ * Cyclic quorum-set decomposition ("stream-cqsa 2.2.0 -> 2.2.2" diff, README and autoconfig.plan: a
+ * configuration is (c, interest_set, itr) with c**itr subproblems and cost (l^2/c)^itr, l the size of
+ * the interest set; the default set is (0, 1, 3) at c = 7). The pages name the parameters, not the
+ * construction; the reading implemented: the sequence is cut into T = c^itr chunks (a multiple of 128
+ * tokens each, the last ragged); subproblem s owns the chunks whose base-c digits t_e lie in
+ * s_e + interest_set (mod c) for every digit e; interest_set must be a perfect difference set mod c;
+ * every needed (query chunk, key chunk) pair (key <= query when causal) is computed in exactly one
+ * subproblem containing both and merged exactly into the query chunk's accumulator.
+ * ------------------------------------------------------------------------------------------------ */
+
+/* CQSA_OK if interest_set (l residues) is a perfect difference set modulo c (its l(l-1) ordered
+ * differences are the non-zero residues, each once); CQSA_ERR_INVALID (with a message) otherwise. */
+int cqsa_quorum_check(int c, const int* interest_set, int l);
+
+/* The schedule of a quorum decomposition with n_chunks non-empty chunks (<= c^itr): writes the
+ * triples (subproblem, query chunk, key chunk), sorted by subproblem, into out[3*i .. 3*i+2] and
+ * returns their number; out == NULL returns the number only. Host-only (no GPU). Negative status on
+ * an invalid set, itr < 1, c^itr > 65536, or max_triples too small. */
+long long cqsa_quorum_schedule(int c, const int* interest_set, int l, int itr, int n_chunks, int causal, int* out,
+                               long long max_triples);
+
+typedef struct {
+  double wall_ms;              /* host wall time of the call */
+  double compute_ms;           /* sum of attention-kernel event intervals */
+  double copy_ms;              /* sum of chunk-staging copy intervals (copy stream) */
+  long long copy_bytes;        /* bytes staged (host->device or device->device) */
+  long long peak_device_bytes; /* device memory the executor allocated */
+  long long chunk_tokens;      /* C */
+  int n_subproblems;           /* subproblems with at least one pair */
+  int n_pairs;                 /* chunk pairs computed (= kernels of attention) */
+  int n_chunk_loads;           /* chunk stagings (Q and K/V counted separately) */
+  int n_launches;              /* kernels launched (attention + finalize) */
+} cqsa_quorum_stats;
+
+/*
+ * Exact attention through the quorum decomposition. q, k, v: [B,H,N,d] (layout BHND) or [B,N,H,d]
+ * (layout BNHD), fp16/bf16, in host memory (inputs_on_host, pinned for speed) or device memory. Each
+ * subproblem's chunks are staged into two sets of l^itr device slots; one fp32 accumulator per query
+ * chunk lives on the device. out/lse as in cqsa_stream_attn_fwd (host if out_on_host). Synchronous;
+ * allocates its device buffers up front and frees them on every path (CQSA_ERR_OOM if they do not
+ * fit). The result equals the chunked-and-merged attention with chunk size C up to fp32 rounding of
+ * the merge order.
+ */
+int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host, void* out,
+                         float* lse, int out_on_host, int B, int H, long long N, int d, int causal, float scale,
+                         int dtype, int c, const int* interest_set, int l, int itr, cqsa_quorum_stats* stats,
+                         cudaStream_t stream);
+
 /*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).
  */

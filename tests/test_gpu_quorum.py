@@ -1,0 +1,113 @@
+"""GPU parity of the quorum executor (cqsa_quorum_attn_fwd).
+
+Every needed chunk pair is computed once and merged exactly, so the result must match the FP64
+oracle within the stated tolerances, and match the streaming driver with the same chunk size (the same
+chunk-pair partials merged in another order) to fp32 merge-order rounding.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests._gpu import assert_close, to_dev, to_np64
+
+pytestmark = pytest.mark.gpu
+
+SETS = {3: (0, 1), 7: (0, 1, 3), 13: (0, 1, 3, 9)}
+
+
+@pytest.fixture(scope="module")
+def cq():
+    import exact_long_context_tcgen05_gb300 as m
+    return m
+
+
+def _host(x, dtype):
+    t = torch.from_numpy(x.view(np.int16))
+    t = t.view(torch.float16 if dtype == syn.F16 else torch.bfloat16)
+    return t.pin_memory()
+
+
+def _oracle(qn, kn, vn, B, H, N, d, causal, dtype, layout):
+    out, lse, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=causal, dtype=dtype, layout=layout)
+    return out.reshape(B, H, N, d), lse.reshape(B, H, N)
+
+
+def _chunk_tokens(N, T):
+    per = -(-N // T)
+    return -(-per // 128) * 128
+
+
+@pytest.mark.parametrize("c,itr,N,d,dtype,causal,layout,on_host", [
+    (7, 1, 3000, 64, syn.F16, True, syn.LAYOUT_BHND, True),
+    (7, 1, 3000, 64, syn.F16, False, syn.LAYOUT_BNHD, False),
+    (3, 2, 2300, 64, syn.F16, True, syn.LAYOUT_BNHD, True),
+    (13, 1, 4000, 128, syn.BF16, True, syn.LAYOUT_BHND, False),
+    (3, 1, 1000, 128, syn.F16, False, syn.LAYOUT_BHND, True),
+])
+def test_quorum_vs_oracle_and_stream(cq, c, itr, N, d, dtype, causal, layout, on_host):
+    B, H = 1, 2
+    D = SETS[c]
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=c + itr, dtype=dtype, layout=layout)
+    shape = (B, H, N, d) if layout == syn.LAYOUT_BHND else (B, N, H, d)
+    tdt = torch.float16 if dtype == syn.F16 else torch.bfloat16
+    if on_host:
+        q, k, v = (_host(x, dtype) for x in (qn, kn, vn))
+    else:
+        q, k, v = (to_dev(x, dtype) for x in (qn, kn, vn))
+    out = torch.empty(shape, dtype=tdt, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    st = cq.cqsa_quorum_stats()
+    cq.cqsa_quorum_attn_fwd(q, k, v, layout, on_host, out, lse, False, B, H, N, d, causal, 0.0, dtype, c, D, itr, st)
+    T = c ** itr
+    C = _chunk_tokens(N, T)
+    nne = -(-N // C)
+    assert st.chunk_tokens == C
+    assert st.n_pairs == (nne * (nne + 1) // 2 if causal else nne * nne)
+    ro, rl = _oracle(qn, kn, vn, B, H, N, d, causal, dtype, layout)
+    o64 = to_np64(out)
+    if layout == syn.LAYOUT_BNHD:
+        o64 = o64.transpose(0, 2, 1, 3)
+    if dtype == syn.F16:
+        assert_close(o64, ro, to_np64(lse), rl, what=f"quorum c={c} itr={itr}")
+    else:
+        # bf16 output: within half an ulp plus the fp32 tolerance (bf16 reading of the tolerance)
+        err = np.abs(o64 - ro)
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(o64), 2.0 ** -126))) - 7)
+        assert np.all(err <= 0.5 * ulp + 4e-3)
+        assert np.abs(to_np64(lse) - rl).max() <= 1e-3
+    # the streaming driver with the same chunk size: same pair partials, merged in key order
+    hq, hk, hv = (_host(x, dtype) for x in (qn, kn, vn))
+    out2 = torch.empty(shape, dtype=tdt, device="cuda")
+    lse2 = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    cq.cqsa_stream_attn_fwd(hq, hk, hv, layout, out2, lse2, False, B, H, N, d, causal, 0.0, dtype, C)
+    lrel = ((lse - lse2).abs() / lse2.abs().clamp_min(1.0)).max().item()
+    assert lrel <= 1e-6, lrel
+    diff = (out.float() - out2.float()).abs()
+    tol = (out2.float().abs() * (2.0 ** -10 if dtype == syn.F16 else 2.0 ** -7)).clamp_min(2.0 ** -24)
+    assert bool((diff <= tol).all()), "outputs differ by more than one ulp"
+
+
+def test_quorum_host_output_and_itr_cost(cq):
+    """Host output buffers; itr = 2 at c = 3: 9 subproblems, chunks staged once per subproblem need."""
+    B, H, N, d = 1, 3, 2200, 64
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=5, layout=syn.LAYOUT_BNHD)
+    q, k, v = (_host(x, syn.F16) for x in (qn, kn, vn))
+    out = torch.empty((B, N, H, d), dtype=torch.float16).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    st = cq.cqsa_quorum_stats()
+    cq.cqsa_quorum_attn_fwd(q, k, v, syn.LAYOUT_BNHD, True, out, lse, True, B, H, N, d, True, 0.0, syn.F16, 3, (0, 1),
+                            2, st)
+    assert st.n_subproblems <= 9 and st.n_pairs == 45
+    ro, rl = _oracle(qn, kn, vn, B, H, N, d, True, syn.F16, syn.LAYOUT_BNHD)
+    assert_close(to_np64(out).transpose(0, 2, 1, 3), ro, to_np64(lse), rl, what="quorum host output")
+
+
+def test_quorum_rejects_bad_set(cq):
+    B, H, N, d = 1, 1, 256, 64
+    x = torch.zeros((B, H, N, d), dtype=torch.float16, device="cuda")
+    out = torch.empty_like(x)
+    with pytest.raises(cq.CqsaError):
+        cq.cqsa_quorum_attn_fwd(x, x, x, syn.LAYOUT_BHND, False, out, None, False, B, H, N, d, True, 0.0, syn.F16, 7,
+                                (0, 1, 2), 1)
