@@ -25,6 +25,9 @@ Secondary measurements (one JSON line each, not the headline; `--measure NAME`):
   --n, default 4,000,000): TFLOP/s, copy rate while overlapped vs the link probe, stall time.
 - bf16: B=2 H=32 N=16384 d=128 bf16 non-causal monolithic forward (K scaled by 3), TFLOP/s and the
   fraction of the tensor peak (algorithmic FLOP; the hi/lo split of P costs 1.5x the MMA work).
+- quorum: the cyclic quorum-set decomposition on the pages' 4,000,000-token example (B=1 H=8 d=64
+  fp16 causal, c=31, interest set (0,1,3,8,12,18), itr=1: 31 subproblems), token-major pinned host
+  Q/K/V/out (N from --n); TFLOP/s, kernel time, staging copies.
 """
 from __future__ import annotations
 
@@ -376,12 +379,9 @@ def measure_link(dev, reps):
 
 def measure_stream(cq, dev, n_tokens, link_h2d_gbs):
     import torch
-    import synthetic as syn
     Bs, Hs, Ds, C = 1, 8, 64, 262_144
     shape = (Bs, n_tokens, Hs, Ds)
-    host = [torch.empty(shape, dtype=torch.float16).pin_memory() for _ in range(3)]
-    for tid, t in enumerate(host):
-        syn.normal(Bs, Hs, n_tokens, Ds, seed=0, tensor_id=tid, layout=syn.LAYOUT_BNHD, out=t.numpy().view(np.uint16))
+    host = _host_qkv_token_major(n_tokens, Hs, Ds)
     out = torch.empty(shape, dtype=torch.float16).pin_memory()
     lse = torch.empty((Bs, Hs, n_tokens), dtype=torch.float32).pin_memory()
     st = cq.cqsa_stream_stats()
@@ -399,6 +399,37 @@ def measure_stream(cq, dev, n_tokens, link_h2d_gbs):
             "copy_frac_of_link": (copy_gbs / link_h2d_gbs) if (copy_gbs and link_h2d_gbs) else None,
             "overlap_wall_over_compute": wall / (st.compute_ms / 1e3) if st.compute_ms > 0 else None,
             "peak_device_bytes": st.peak_device_bytes, "n_chunk_pairs": st.n_chunks}
+
+
+def _host_qkv_token_major(n_tokens, Hs=8, Ds=64):
+    import torch
+    import synthetic as syn
+    shape = (1, n_tokens, Hs, Ds)
+    host = [torch.empty(shape, dtype=torch.float16).pin_memory() for _ in range(3)]
+    for tid, t in enumerate(host):
+        syn.normal(1, Hs, n_tokens, Ds, seed=0, tensor_id=tid, layout=syn.LAYOUT_BNHD, out=t.numpy().view(np.uint16))
+    return host
+
+
+def measure_quorum(cq, dev, n_tokens):
+    import torch
+    Hs, Ds, c, D, itr = 8, 64, 31, (0, 1, 3, 8, 12, 18), 1
+    host = _host_qkv_token_major(n_tokens, Hs, Ds)
+    out = torch.empty((1, n_tokens, Hs, Ds), dtype=torch.float16).pin_memory()
+    lse = torch.empty((1, Hs, n_tokens), dtype=torch.float32).pin_memory()
+    st = cq.cqsa_quorum_stats()
+    stream = torch.cuda.current_stream(dev)
+    t0 = time.perf_counter()
+    cq.cqsa_quorum_attn_fwd(host[0], host[1], host[2], cq.CQSA_LAYOUT_BNHD, True, out, lse, True, 1, Hs, n_tokens, Ds,
+                            True, 0.0, cq.CQSA_F16, c, D, itr, st, stream)
+    wall = time.perf_counter() - t0
+    flop = 4.0 * Hs * n_tokens * n_tokens * Ds / 2.0
+    return {"measure": "quorum", "workload": f"cyclic quorum decomposition, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
+            f"c={c} interest_set={D} itr={itr}, token-major pinned host Q/K/V/out", "wall_s": wall,
+            "tflops": flop / wall / 1e12, "compute_s": st.compute_ms / 1e3, "copy_s": st.copy_ms / 1e3,
+            "copy_bytes": st.copy_bytes, "chunk_tokens": st.chunk_tokens, "subproblems": st.n_subproblems,
+            "pairs": st.n_pairs, "chunk_loads": st.n_chunk_loads, "peak_device_bytes": st.peak_device_bytes,
+            "context": "the pages' own run of this example (unnamed GPU): 2 min 06 s, 31 subproblems"}
 
 
 def measure_bf16(cq, dev, reps):
@@ -446,6 +477,8 @@ def run_measure(args):
     elif args.measure == "stream":
         link = measure_link(dev, 5)
         line = measure_stream(cq, dev, args.n, link["h2d_gbs"])
+    elif args.measure == "quorum":
+        line = measure_quorum(cq, dev, args.n)
     else:
         line = measure_bf16(cq, dev, reps)
     rc, code, _ = cq.cqsa_device_error()
@@ -461,7 +494,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16"), default=None)
+    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum"), default=None)
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream")
     args = ap.parse_args()
     if args.warmup < 3:
