@@ -17,7 +17,10 @@
 //     whatever the order of the subproblems.
 // A subproblem needs only its own chunks on the device: the executor stages Q and K/V chunks through
 // two sets of l^itr slots (the previous subproblem's chunks stay while the next ones load) and keeps
-// one fp32 accumulator per query chunk.
+// one fp32 accumulator per query chunk on the device, or, with the host accumulator (the pages'
+// `accumulate_on_gpu=False`), in pinned host memory: a query chunk's accumulator then travels with
+// its Q slot (copied in when the chunk is staged, written back when the slot is reused), so device
+// memory stays at the slots whatever the sequence length.
 #include <algorithm>
 #include <chrono>
 #include <math.h>
@@ -118,6 +121,7 @@ int build_schedule(int c, const int* D, int l, int itr, int n_chunks, bool causa
 
 struct Resources {
   std::vector<void*> dev;
+  std::vector<void*> host;  // pinned host allocations (cudaHostAlloc)
   std::vector<cudaEvent_t> events;
   cudaStream_t copy = nullptr;
   cudaStream_t compute = nullptr;
@@ -125,6 +129,7 @@ struct Resources {
     if (compute) cudaStreamSynchronize(compute);
     if (copy) cudaStreamSynchronize(copy);
     for (void* p : dev) cudaFree(p);
+    for (void* p : host) cudaFreeHost(p);
     for (cudaEvent_t e : events) cudaEventDestroy(e);
     if (copy) cudaStreamDestroy(copy);
   }
@@ -159,7 +164,7 @@ extern "C" long long cqsa_quorum_schedule(int c, const int* interest_set, int l,
 extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host,
                                     void* out, float* lse, int out_on_host, int B, int H, long long N, int d,
                                     int causal, float scale, int dtype, int c, const int* interest_set, int l,
-                                    int itr, cqsa_quorum_stats* stats, cudaStream_t stream) {
+                                    int itr, int acc_on_host, cqsa_quorum_stats* stats, cudaStream_t stream) {
   const auto t_start = std::chrono::steady_clock::now();
   if (stats) memset(stats, 0, sizeof(*stats));
   if (!q || !k || !v || !out) {
@@ -236,9 +241,25 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     if (rc == CQSA_OK) rc = alloc(&ks[s], chunk_elems * es);
     if (rc == CQSA_OK) rc = alloc(&vs[s], chunk_elems * es);
   }
+  // Accumulators: one per query chunk on the device, or one per Q slot on the device backed by one
+  // per query chunk in pinned host memory.
+  const int nacc = acc_on_host ? nslots : nne;
   void *acc = nullptr, *lacc = nullptr, *ostage = nullptr, *lstage = nullptr;
-  if (rc == CQSA_OK) rc = alloc(&acc, static_cast<size_t>(nne) * chunk_elems * 4);
-  if (rc == CQSA_OK) rc = alloc(&lacc, static_cast<size_t>(nne) * rows * 4);
+  float *hacc = nullptr, *hlacc = nullptr;
+  if (rc == CQSA_OK) rc = alloc(&acc, static_cast<size_t>(nacc) * chunk_elems * 4);
+  if (rc == CQSA_OK) rc = alloc(&lacc, static_cast<size_t>(nacc) * rows * 4);
+  if (rc == CQSA_OK && acc_on_host) {
+    void* p = nullptr;
+    cudaError_t e = cudaHostAlloc(&p, static_cast<size_t>(nne) * (chunk_elems + rows) * 4, cudaHostAllocDefault);
+    if (e != cudaSuccess) {
+      cudaGetLastError();
+      set_error("pinned host allocation of the accumulator failed: %s", cudaGetErrorString(e));
+      return e == cudaErrorMemoryAllocation ? CQSA_ERR_OOM : CQSA_ERR_CUDA;
+    }
+    res.host.push_back(p);
+    hacc = static_cast<float*>(p);
+    hlacc = hacc + static_cast<size_t>(nne) * chunk_elems;
+  }
   if (rc == CQSA_OK && out_on_host) {
     rc = alloc(&ostage, chunk_elems * es);
     if (rc == CQSA_OK && lse) rc = alloc(&lstage, rows * 4);
@@ -279,6 +300,31 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   long long copy_bytes = 0;
   int loads = 0, groups = 0, launches = 0;
   std::vector<bool> started(nne, false);
+  long long acc_bytes = 0;
+  // Device accumulator of query chunk qc in Q slot sq.
+  auto dacc = [&](int qc, int sq) -> float* {
+    return static_cast<float*>(acc) + static_cast<size_t>(acc_on_host ? sq : qc) * chunk_elems;
+  };
+  auto dlacc = [&](int qc, int sq) -> float* {
+    return static_cast<float*>(lacc) + static_cast<size_t>(acc_on_host ? sq : qc) * rows;
+  };
+  // Host accumulator: copy a chunk's accumulator between its host home and a device slot.
+  auto acc_copy = [&](int qc, int sq, bool to_host, cudaStream_t s) -> int {
+    float* h = hacc + static_cast<size_t>(qc) * chunk_elems;
+    float* hl = hlacc + static_cast<size_t>(qc) * rows;
+    const size_t n = static_cast<size_t>(B) * H * ntok(qc);
+    int r = cuda_status(cudaMemcpyAsync(to_host ? static_cast<void*>(h) : static_cast<void*>(dacc(qc, sq)),
+                                        to_host ? static_cast<void*>(dacc(qc, sq)) : static_cast<void*>(h),
+                                        n * d * 4, to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, s),
+                        "accumulator copy");
+    if (r == CQSA_OK)
+      r = cuda_status(cudaMemcpyAsync(to_host ? static_cast<void*>(hl) : static_cast<void*>(dlacc(qc, sq)),
+                                      to_host ? static_cast<void*>(dlacc(qc, sq)) : static_cast<void*>(hl), n * 4,
+                                      to_host ? cudaMemcpyDeviceToHost : cudaMemcpyHostToDevice, s),
+                      "accumulator copy");
+    acc_bytes += static_cast<long long>(n) * (d + 1) * 4;
+    return r;
+  };
 
   // Slot of `chunk` in `pool` (*slot), staging it on the copy stream (after the slot's previous reader)
   // if absent. `keep` lists chunks the current subproblem needs, which are never evicted.
@@ -312,7 +358,11 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     const int n = ntok(chunk);
     if ((r = cuda_status(cudaEventRecord(sp.a, res.copy), "record")) != CQSA_OK) return r;
     if (is_q) {
+      if (acc_on_host && pool.chunk[victim] >= 0 && started[pool.chunk[victim]] &&
+          (r = acc_copy(pool.chunk[victim], victim, true, res.copy)) != CQSA_OK)
+        return r;
       r = cuda_status(copy_chunk(qs[victim], q, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy Q chunk");
+      if (r == CQSA_OK && acc_on_host && started[chunk]) r = acc_copy(chunk, victim, false, res.copy);
     } else {
       r = cuda_status(copy_chunk(ks[victim], k, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy K chunk");
       if (r == CQSA_OK)
@@ -364,8 +414,8 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       a.dtype = dtype;
       a.in_layout = layout;
       a.mode = started[t.q] ? kModeAccum : kModePart;
-      a.o_part = static_cast<float*>(acc) + static_cast<size_t>(t.q) * chunk_elems;
-      a.lse_part = static_cast<float*>(lacc) + static_cast<size_t>(t.q) * rows;
+      a.o_part = dacc(t.q, sq);
+      a.lse_part = dlacc(t.q, sq);
       a.out_layout = CQSA_LAYOUT_BHND;
       Span sp;
       if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
@@ -384,11 +434,30 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   }
 
   // Finalize every query chunk into the output (device), or through a staging buffer to the host.
-  for (int qc = 0; qc < nne; ++qc) {
+  // With the host accumulator, chunks still in a Q slot are finalized from it first; every other
+  // chunk's accumulator is then copied into slot 0 (stream-ordered after the previous finalize).
+  std::vector<int> order, slot_of(nne, -1);
+  if (acc_on_host) {
+    CK(cudaStreamSynchronize(res.copy), "synchronize copy stream");
+    for (int s = 0; s < nslots; ++s)
+      if (qp.chunk[s] >= 0) slot_of[qp.chunk[s]] = s;
+    for (int qc = 0; qc < nne; ++qc)
+      if (slot_of[qc] >= 0) order.push_back(qc);
+    for (int qc = 0; qc < nne; ++qc)
+      if (slot_of[qc] < 0) order.push_back(qc);
+  } else {
+    for (int qc = 0; qc < nne; ++qc) order.push_back(qc);
+  }
+  for (int qc : order) {
     const int n = ntok(qc);
     const long long t0 = static_cast<long long>(qc) * C;
-    const float* accq = static_cast<float*>(acc) + static_cast<size_t>(qc) * chunk_elems;
-    const float* laccq = static_cast<float*>(lacc) + static_cast<size_t>(qc) * rows;
+    int sq = slot_of[qc];
+    if (acc_on_host && sq < 0) {
+      sq = 0;
+      if ((rc = acc_copy(qc, sq, false, stream)) != CQSA_OK) return rc;
+    }
+    const float* accq = dacc(qc, sq);
+    const float* laccq = dlacc(qc, sq);
     if (!out_on_host) {
       if ((rc = launch_finalize(accq, laccq, out, lse, B, H, n, N, t0, d, layout, dtype, stream)) != CQSA_OK) return rc;
     } else {
@@ -439,6 +508,7 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     stats->copy_ms = cp;
     stats->compute_ms = comp;
     stats->copy_bytes = copy_bytes;
+    stats->acc_host_bytes = acc_bytes;
     stats->peak_device_bytes = dev_bytes;
     stats->n_subproblems = groups;
     stats->n_pairs = static_cast<int>(sched.size());

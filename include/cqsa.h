@@ -143,6 +143,7 @@ typedef struct {
   long long copy_bytes;        /* bytes staged (host->device or device->device) */
   long long peak_device_bytes; /* device memory the executor allocated */
   long long chunk_tokens;      /* C */
+  long long acc_host_bytes;    /* accumulator bytes moved between host and device (host accumulator) */
   int n_subproblems;           /* subproblems with at least one pair */
   int n_pairs;                 /* chunk pairs computed (= kernels of attention) */
   int n_chunk_loads;           /* chunk stagings (Q and K/V counted separately) */
@@ -152,16 +153,19 @@ typedef struct {
 /*
  * Exact attention through the quorum decomposition. q, k, v: [B,H,N,d] (layout BHND) or [B,N,H,d]
  * (layout BNHD), fp16/bf16, in host memory (inputs_on_host, pinned for speed) or device memory. Each
- * subproblem's chunks are staged into two sets of l^itr device slots; one fp32 accumulator per query
- * chunk lives on the device. out/lse as in cqsa_stream_attn_fwd (host if out_on_host). Synchronous;
- * allocates its device buffers up front and frees them on every path (CQSA_ERR_OOM if they do not
- * fit). The result equals the chunked-and-merged attention with chunk size C up to fp32 rounding of
- * the merge order.
+ * subproblem's chunks are staged into two sets of l^itr device slots. acc_on_host = 0: one fp32
+ * accumulator per query chunk on the device; acc_on_host = 1 (the pages' accumulate_on_gpu=False,
+ * "stream-cqsa 2.2.0 -> 2.2.2" README): the accumulators live in pinned host memory allocated by the
+ * call and travel with their Q slot, so device memory is bounded by the slots. out/lse as in
+ * cqsa_stream_attn_fwd (host if out_on_host). Synchronous; allocates its buffers up front and frees
+ * them on every path (CQSA_ERR_OOM if they do not fit). The result equals the chunked-and-merged
+ * attention with chunk size C up to fp32 rounding of the merge order (bit-identical with and without
+ * the host accumulator).
  */
 int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host, void* out,
                          float* lse, int out_on_host, int B, int H, long long N, int d, int causal, float scale,
-                         int dtype, int c, const int* interest_set, int l, int itr, cqsa_quorum_stats* stats,
-                         cudaStream_t stream);
+                         int dtype, int c, const int* interest_set, int l, int itr, int acc_on_host,
+                         cqsa_quorum_stats* stats, cudaStream_t stream);
 
 /*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).

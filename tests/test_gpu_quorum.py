@@ -59,7 +59,8 @@ def test_quorum_vs_oracle_and_stream(cq, c, itr, N, d, dtype, causal, layout, on
     out = torch.empty(shape, dtype=tdt, device="cuda")
     lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     st = cq.cqsa_quorum_stats()
-    cq.cqsa_quorum_attn_fwd(q, k, v, layout, on_host, out, lse, False, B, H, N, d, causal, 0.0, dtype, c, D, itr, st)
+    cq.cqsa_quorum_attn_fwd(q, k, v, layout, on_host, out, lse, False, B, H, N, d, causal, 0.0, dtype, c, D, itr,
+                            stats=st)
     T = c ** itr
     C = _chunk_tokens(N, T)
     nne = -(-N // C)
@@ -98,7 +99,7 @@ def test_quorum_host_output_and_itr_cost(cq):
     lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
     st = cq.cqsa_quorum_stats()
     cq.cqsa_quorum_attn_fwd(q, k, v, syn.LAYOUT_BNHD, True, out, lse, True, B, H, N, d, True, 0.0, syn.F16, 3, (0, 1),
-                            2, st)
+                            2, stats=st)
     assert st.n_subproblems <= 9 and st.n_pairs == 45
     ro, rl = _oracle(qn, kn, vn, B, H, N, d, True, syn.F16, syn.LAYOUT_BNHD)
     assert_close(to_np64(out).transpose(0, 2, 1, 3), ro, to_np64(lse), rl, what="quorum host output")
@@ -111,3 +112,26 @@ def test_quorum_rejects_bad_set(cq):
     with pytest.raises(cq.CqsaError):
         cq.cqsa_quorum_attn_fwd(x, x, x, syn.LAYOUT_BHND, False, out, None, False, B, H, N, d, True, 0.0, syn.F16, 7,
                                 (0, 1, 2), 1)
+
+
+@pytest.mark.parametrize("c,itr,N,causal", [(7, 1, 5000, True), (3, 2, 2300, False), (13, 1, 6000, True)])
+def test_host_accumulator_bitwise_equal(cq, c, itr, N, causal):
+    """The host accumulator moves fp32 accumulators through pinned host memory unchanged, so the result
+    equals the device-accumulator run bit for bit; it must actually spill (fewer slots than chunks)."""
+    B, H, d = 1, 2, 64
+    D = SETS[c]
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=17, layout=syn.LAYOUT_BNHD)
+    q, k, v = (_host(x, syn.F16) for x in (qn, kn, vn))
+    res = []
+    for acc_on_host in (False, True):
+        out = torch.empty((B, N, H, d), dtype=torch.float16, device="cuda")
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        st = cq.cqsa_quorum_stats()
+        cq.cqsa_quorum_attn_fwd(q, k, v, syn.LAYOUT_BNHD, True, out, lse, False, B, H, N, d, causal, 0.0, syn.F16, c,
+                                D, itr, acc_on_host=acc_on_host, stats=st)
+        res.append((out, lse, st.acc_host_bytes, st.peak_device_bytes))
+    assert torch.equal(res[0][0], res[1][0]) and torch.equal(res[0][1], res[1][1])
+    assert res[0][2] == 0 and res[1][2] > 0
+    assert res[1][3] < res[0][3]
+    ro, rl = _oracle(qn, kn, vn, B, H, N, d, causal, syn.F16, syn.LAYOUT_BNHD)
+    assert_close(to_np64(res[1][0]).transpose(0, 2, 1, 3), ro, to_np64(res[1][1]), rl, what="host accumulator")
