@@ -411,7 +411,7 @@ def _host_qkv_token_major(n_tokens, Hs=8, Ds=64):
     return host
 
 
-def measure_quorum(cq, dev, n_tokens, acc_on_host=False):
+def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1):
     import torch
     Hs, Ds, c, D, itr = 8, 64, 31, (0, 1, 3, 8, 12, 18), 1
     host = _host_qkv_token_major(n_tokens, Hs, Ds)
@@ -421,7 +421,8 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False):
     stream = torch.cuda.current_stream(dev)
     t0 = time.perf_counter()
     cq.cqsa_quorum_attn_fwd(host[0], host[1], host[2], cq.CQSA_LAYOUT_BNHD, True, out, lse, True, 1, Hs, n_tokens, Ds,
-                            True, 0.0, cq.CQSA_F16, c, D, itr, acc_on_host=acc_on_host, stats=st, stream=stream)
+                            True, 0.0, cq.CQSA_F16, c, D, itr, acc_on_host=acc_on_host, max_parallel=npar, stats=st,
+                            stream=stream)
     wall = time.perf_counter() - t0
     flop = 4.0 * Hs * n_tokens * n_tokens * Ds / 2.0
     return {"measure": "quorum", "workload": f"cyclic quorum decomposition, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
@@ -430,6 +431,7 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False):
             "copy_bytes": st.copy_bytes, "chunk_tokens": st.chunk_tokens, "subproblems": st.n_subproblems,
             "pairs": st.n_pairs, "chunk_loads": st.n_chunk_loads, "peak_device_bytes": st.peak_device_bytes,
             "accumulator": "host (pinned)" if acc_on_host else "device", "acc_host_bytes": st.acc_host_bytes,
+            "max_parallel": npar,
             "context": "the pages' own run of this example (unnamed GPU): 2 min 06 s, 31 subproblems"}
 
 
@@ -479,7 +481,7 @@ def run_measure(args):
         link = measure_link(dev, 5)
         line = measure_stream(cq, dev, args.n, link["h2d_gbs"])
     elif args.measure == "quorum":
-        line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host)
+        line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel)
     else:
         line = measure_bf16(cq, dev, reps)
     rc, code, _ = cq.cqsa_device_error()
@@ -498,6 +500,7 @@ def main():
     ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum"), default=None)
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream / quorum")
     ap.add_argument("--acc-on-host", action="store_true", help="--measure quorum with the host accumulator")
+    ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -70,7 +70,7 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_quorum_schedule.argtypes = [_i, _vp, _i, _i, _i, _i, _vp, _ll]
     lib.cqsa_quorum_schedule.restype = _ll
     lib.cqsa_quorum_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i, _vp,
-                                         _i, _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
+                                         _i, _i, _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
     lib.cqsa_status_string.argtypes = [_i]
     lib.cqsa_status_string.restype = ctypes.c_char_p
     lib.cqsa_last_error.argtypes = []
@@ -199,13 +199,14 @@ def cqsa_quorum_schedule(c, interest_set, itr, n_chunks, causal):
 
 
 def cqsa_quorum_attn_fwd(q, k, v, layout, inputs_on_host, out, lse, out_on_host, B, H, N, d, causal, scale, dtype,
-                         c, interest_set, itr, acc_on_host=False, stats=None, stream=None) -> int:
+                         c, interest_set, itr, acc_on_host=False, max_parallel=1, stats=None, stream=None) -> int:
     st = stats if stats is not None else cqsa_quorum_stats()
     arr, l = _int_array(interest_set)
     return _check(lib.cqsa_quorum_attn_fwd(_ptr(q), _ptr(k), _ptr(v), layout, int(bool(inputs_on_host)), _ptr(out),
                                            _ptr(lse), int(bool(out_on_host)), B, H, N, d, int(bool(causal)),
                                            float(scale), dtype, c, ctypes.cast(arr, _vp), l, itr,
-                                           int(bool(acc_on_host)), ctypes.byref(st), _stream(stream)))
+                                           int(bool(acc_on_host)), int(max_parallel), ctypes.byref(st),
+                                           _stream(stream)))
 
 
 def cqsa_device_error(clear: bool = True):

@@ -21,6 +21,10 @@
 // `accumulate_on_gpu=False`), in pinned host memory: a query chunk's accumulator then travels with
 // its Q slot (copied in when the chunk is staged, written back when the slot is reused), so device
 // memory stays at the slots whatever the sequence length.
+// Parallel subproblem lanes (the pages' `max_parallel`): chunk pairs of different query chunks are
+// independent, so pair (q, k) runs on compute stream q mod n_par; pairs of one query chunk stay in
+// one stream, in schedule order, so the accumulation order (and the result, bit for bit) does not
+// depend on n_par. Small chunk pairs, whose grids do not fill the GPU, then run side by side.
 #include <algorithm>
 #include <chrono>
 #include <math.h>
@@ -123,14 +127,17 @@ struct Resources {
   std::vector<void*> dev;
   std::vector<void*> host;  // pinned host allocations (cudaHostAlloc)
   std::vector<cudaEvent_t> events;
+  std::vector<cudaStream_t> lanes;  // extra compute streams (parallel subproblem lanes)
   cudaStream_t copy = nullptr;
   cudaStream_t compute = nullptr;
   ~Resources() {
     if (compute) cudaStreamSynchronize(compute);
+    for (cudaStream_t s : lanes) cudaStreamSynchronize(s);
     if (copy) cudaStreamSynchronize(copy);
     for (void* p : dev) cudaFree(p);
     for (void* p : host) cudaFreeHost(p);
     for (cudaEvent_t e : events) cudaEventDestroy(e);
+    for (cudaStream_t s : lanes) cudaStreamDestroy(s);
     if (copy) cudaStreamDestroy(copy);
   }
 };
@@ -164,7 +171,8 @@ extern "C" long long cqsa_quorum_schedule(int c, const int* interest_set, int l,
 extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host,
                                     void* out, float* lse, int out_on_host, int B, int H, long long N, int d,
                                     int causal, float scale, int dtype, int c, const int* interest_set, int l,
-                                    int itr, int acc_on_host, cqsa_quorum_stats* stats, cudaStream_t stream) {
+                                    int itr, int acc_on_host, int max_parallel, cqsa_quorum_stats* stats,
+                                    cudaStream_t stream) {
   const auto t_start = std::chrono::steady_clock::now();
   if (stats) memset(stats, 0, sizeof(*stats));
   if (!q || !k || !v || !out) {
@@ -189,6 +197,10 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   }
   if (!isfinite(scale) || scale < 0.0f) {
     set_error("scale must be finite and >= 0 (0 selects 1/sqrt(d))");
+    return CQSA_ERR_INVALID;
+  }
+  if (max_parallel < 1 || max_parallel > 16) {
+    set_error("max_parallel must be in [1, 16] (got %d)", max_parallel);
     return CQSA_ERR_INVALID;
   }
   int T = 0;
@@ -267,12 +279,25 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   if (rc != CQSA_OK) return rc;
   if ((rc = cuda_status(cudaStreamCreateWithFlags(&res.copy, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
     return rc;
-  std::vector<cudaEvent_t> q_ready(nslots), q_free(nslots), kv_ready(nslots), kv_free(nslots);
-  for (int s = 0; s < nslots; ++s) {
-    if ((rc = event(&q_ready[s], false)) != CQSA_OK || (rc = event(&q_free[s], false)) != CQSA_OK ||
-        (rc = event(&kv_ready[s], false)) != CQSA_OK || (rc = event(&kv_free[s], false)) != CQSA_OK)
+  const int npar = max_parallel;
+  std::vector<cudaStream_t> lane(npar, stream);
+  for (int j = 1; j < npar; ++j) {
+    cudaStream_t sj = nullptr;
+    if ((rc = cuda_status(cudaStreamCreateWithFlags(&sj, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
       return rc;
+    res.lanes.push_back(sj);
+    lane[j] = sj;
   }
+  // ready: the slot's staging copy is done; free[slot * npar + j]: lane j's last kernel reading the slot.
+  std::vector<cudaEvent_t> q_ready(nslots), kv_ready(nslots), q_free(nslots * npar), kv_free(nslots * npar);
+  for (int s = 0; s < nslots; ++s) {
+    if ((rc = event(&q_ready[s], false)) != CQSA_OK || (rc = event(&kv_ready[s], false)) != CQSA_OK) return rc;
+    for (int j = 0; j < npar; ++j)
+      if ((rc = event(&q_free[s * npar + j], false)) != CQSA_OK || (rc = event(&kv_free[s * npar + j], false)) != CQSA_OK)
+        return rc;
+  }
+  cudaEvent_t joined = nullptr;
+  if ((rc = event(&joined, false)) != CQSA_OK) return rc;
   struct Span {
     cudaEvent_t a, b;
   };
@@ -293,9 +318,9 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   struct Pool {
     std::vector<int> chunk;     // chunk held by each slot (-1: none)
     std::vector<int> last_use;  // subproblem group of the last use
-    std::vector<bool> used;     // a kernel has read the slot (its free event is recorded)
+    std::vector<bool> used;     // [slot * npar + lane]: a kernel of that lane has read the slot
   };
-  Pool qp{std::vector<int>(nslots, -1), std::vector<int>(nslots, -1), std::vector<bool>(nslots, false)};
+  Pool qp{std::vector<int>(nslots, -1), std::vector<int>(nslots, -1), std::vector<bool>(nslots * npar, false)};
   Pool kp = qp;
   long long copy_bytes = 0;
   int loads = 0, groups = 0, launches = 0;
@@ -348,10 +373,11 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       return CQSA_ERR_INVALID;
     }
     int r;
-    if (pool.used[victim] &&
-        (r = cuda_status(cudaStreamWaitEvent(res.copy, is_q ? q_free[victim] : kv_free[victim], 0), "wait slot")) !=
-            CQSA_OK)
-      return r;
+    for (int j = 0; j < npar; ++j)
+      if (pool.used[victim * npar + j] &&
+          (r = cuda_status(cudaStreamWaitEvent(res.copy, is_q ? q_free[victim * npar + j] : kv_free[victim * npar + j], 0),
+                           "wait slot")) != CQSA_OK)
+        return r;
     Span sp;
     if ((r = span(copies, &sp)) != CQSA_OK) return r;
     const long long t0 = static_cast<long long>(chunk) * C;
@@ -395,8 +421,10 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       int sq = -1, sk = -1;
       if ((rc = stage(qp, true, t.q, groups, needq, &sq)) != CQSA_OK) return rc;
       if ((rc = stage(kp, false, t.k, groups, needk, &sk)) != CQSA_OK) return rc;
-      CK(cudaStreamWaitEvent(stream, q_ready[sq], 0), "wait q_ready");
-      CK(cudaStreamWaitEvent(stream, kv_ready[sk], 0), "wait kv_ready");
+      const int j = t.q % npar;
+      cudaStream_t ls = lane[j];
+      CK(cudaStreamWaitEvent(ls, q_ready[sq], 0), "wait q_ready");
+      CK(cudaStreamWaitEvent(ls, kv_ready[sk], 0), "wait kv_ready");
       AttnArgs a;
       memset(&a, 0, sizeof(a));
       a.q = qs[sq];
@@ -419,18 +447,24 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       a.out_layout = CQSA_LAYOUT_BHND;
       Span sp;
       if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
-      CK(cudaEventRecord(sp.a, stream), "record");
-      if ((rc = launch_attention(a, stream)) != CQSA_OK) return rc;
-      CK(cudaEventRecord(sp.b, stream), "record");
-      CK(cudaEventRecord(q_free[sq], stream), "record q_free");
-      CK(cudaEventRecord(kv_free[sk], stream), "record kv_free");
-      qp.used[sq] = true;
-      kp.used[sk] = true;
+      CK(cudaEventRecord(sp.a, ls), "record");
+      if ((rc = launch_attention(a, ls)) != CQSA_OK) return rc;
+      CK(cudaEventRecord(sp.b, ls), "record");
+      CK(cudaEventRecord(q_free[sq * npar + j], ls), "record q_free");
+      CK(cudaEventRecord(kv_free[sk * npar + j], ls), "record kv_free");
+      qp.used[sq * npar + j] = true;
+      kp.used[sk * npar + j] = true;
       started[t.q] = true;
       ++launches;
     }
     ++groups;
     i0 = i1;
+  }
+
+  // Every lane's kernels finish before the caller's stream finalizes.
+  for (int j = 1; j < npar; ++j) {
+    CK(cudaEventRecord(joined, lane[j]), "record join");
+    CK(cudaStreamWaitEvent(stream, joined, 0), "wait join");
   }
 
   // Finalize every query chunk into the output (device), or through a staging buffer to the host.

@@ -138,7 +138,8 @@ long long cqsa_quorum_schedule(int c, const int* interest_set, int l, int itr, i
 
 typedef struct {
   double wall_ms;              /* host wall time of the call */
-  double compute_ms;           /* sum of attention-kernel event intervals */
+  double compute_ms;           /* sum of attention-kernel event intervals (lanes overlap, so with
+                                  max_parallel > 1 this can exceed the wall time) */
   double copy_ms;              /* sum of chunk-staging copy intervals (copy stream) */
   long long copy_bytes;        /* bytes staged (host->device or device->device) */
   long long peak_device_bytes; /* device memory the executor allocated */
@@ -158,14 +159,16 @@ typedef struct {
  * "stream-cqsa 2.2.0 -> 2.2.2" README): the accumulators live in pinned host memory allocated by the
  * call and travel with their Q slot, so device memory is bounded by the slots. out/lse as in
  * cqsa_stream_attn_fwd (host if out_on_host). Synchronous; allocates its buffers up front and frees
- * them on every path (CQSA_ERR_OOM if they do not fit). The result equals the chunked-and-merged
- * attention with chunk size C up to fp32 rounding of the merge order (bit-identical with and without
- * the host accumulator).
+ * them on every path (CQSA_ERR_OOM if they do not fit). max_parallel (1..16, the pages' max_parallel):
+ * chunk pairs of different query chunks run on that many compute streams (pair (q, k) on stream
+ * q mod max_parallel; stream 0 is `stream`), so small pairs fill the GPU side by side. The result
+ * equals the chunked-and-merged attention with chunk size C up to fp32 rounding of the merge order,
+ * and is bit-identical for every acc_on_host and max_parallel.
  */
 int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout, int inputs_on_host, void* out,
                          float* lse, int out_on_host, int B, int H, long long N, int d, int causal, float scale,
                          int dtype, int c, const int* interest_set, int l, int itr, int acc_on_host,
-                         cqsa_quorum_stats* stats, cudaStream_t stream);
+                         int max_parallel, cqsa_quorum_stats* stats, cudaStream_t stream);
 
 /*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).

@@ -135,3 +135,24 @@ def test_host_accumulator_bitwise_equal(cq, c, itr, N, causal):
     assert res[1][3] < res[0][3]
     ro, rl = _oracle(qn, kn, vn, B, H, N, d, causal, syn.F16, syn.LAYOUT_BNHD)
     assert_close(to_np64(res[1][0]).transpose(0, 2, 1, 3), ro, to_np64(res[1][1]), rl, what="host accumulator")
+
+
+@pytest.mark.parametrize("npar", [2, 4])
+def test_parallel_lanes_bitwise_equal(cq, npar):
+    """Pairs of one query chunk stay in one lane in schedule order, so lanes change nothing bitwise."""
+    B, H, N, d, c, D = 1, 2, 9000, 64, 13, (0, 1, 3, 9)
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=23)
+    q, k, v = (to_dev(x, syn.F16) for x in (qn, kn, vn))
+    res = []
+    for p, acc_host in ((1, False), (npar, False), (npar, True)):
+        out = torch.empty((B, H, N, d), dtype=torch.float16, device="cuda")
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        cq.cqsa_quorum_attn_fwd(q, k, v, syn.LAYOUT_BHND, False, out, lse, False, B, H, N, d, True, 0.0, syn.F16, c, D,
+                                1, acc_on_host=acc_host, max_parallel=p)
+        res.append((out, lse))
+    for o, l in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(l, res[0][1])
+    rows = syn.sample_rows(B, H, N, 256)
+    ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=True, rows=rows)
+    b, h, i = (torch.as_tensor(rows[:, j], device="cuda") for j in range(3))
+    assert_close(to_np64(res[1][0][b, h, i]), ro, to_np64(res[1][1][b, h, i]), rl, what="parallel lanes")
