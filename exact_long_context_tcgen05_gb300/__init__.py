@@ -21,6 +21,7 @@ CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
+            "cqsa_release_cache",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
             "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
@@ -71,6 +72,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_quorum_schedule.restype = _ll
     lib.cqsa_quorum_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i, _vp,
                                          _i, _i, _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
+    lib.cqsa_release_cache.argtypes = []
+    lib.cqsa_release_cache.restype = _i
     lib.cqsa_status_string.argtypes = [_i]
     lib.cqsa_status_string.restype = ctypes.c_char_p
     lib.cqsa_last_error.argtypes = []
@@ -207,6 +210,11 @@ def cqsa_quorum_attn_fwd(q, k, v, layout, inputs_on_host, out, lse, out_on_host,
                                            float(scale), dtype, c, ctypes.cast(arr, _vp), l, itr,
                                            int(bool(acc_on_host)), int(max_parallel), ctypes.byref(st),
                                            _stream(stream)))
+
+
+def cqsa_release_cache() -> int:
+    """Free the device buffers, events and streams the host-driven entry points keep between calls."""
+    return _check(lib.cqsa_release_cache())
 
 
 def cqsa_device_error(clear: bool = True):

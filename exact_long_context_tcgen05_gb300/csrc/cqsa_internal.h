@@ -52,6 +52,15 @@ cudaError_t copy_chunk(void* dst, const void* src, int layout, int B, int H, lon
 int launch_finalize(const float* acc, const float* lse_acc, void* out, float* lse_out, int B, int H, int n,
                     long long N, long long t0, int d, int layout, int dtype, cudaStream_t stream);
 
+// Reusable device buffers, events and non-blocking streams (per device; csrc/pool.cu). A caller
+// returns them only after all work using them has completed.
+int pool_alloc(void** p, size_t n);
+void pool_free(void* p);
+int pool_event(cudaEvent_t* e, bool timing);
+void pool_event_free(cudaEvent_t e, bool timing);
+int pool_stream(cudaStream_t* s);
+void pool_stream_free(cudaStream_t s);
+
 // Status helpers
 void set_error(const char* fmt, ...);
 int cuda_status(cudaError_t e, const char* what);

@@ -123,10 +123,12 @@ int build_schedule(int c, const int* D, int l, int itr, int n_chunks, bool causa
   return CQSA_OK;
 }
 
+// Device buffers, events and streams come from the library's pool and go back once the streams
+// that use them have drained; the pinned host accumulator is allocated per call.
 struct Resources {
   std::vector<void*> dev;
   std::vector<void*> host;  // pinned host allocations (cudaHostAlloc)
-  std::vector<cudaEvent_t> events;
+  std::vector<std::pair<cudaEvent_t, bool>> events;
   std::vector<cudaStream_t> lanes;  // extra compute streams (parallel subproblem lanes)
   cudaStream_t copy = nullptr;
   cudaStream_t compute = nullptr;
@@ -134,11 +136,11 @@ struct Resources {
     if (compute) cudaStreamSynchronize(compute);
     for (cudaStream_t s : lanes) cudaStreamSynchronize(s);
     if (copy) cudaStreamSynchronize(copy);
-    for (void* p : dev) cudaFree(p);
+    for (void* p : dev) pool_free(p);
     for (void* p : host) cudaFreeHost(p);
-    for (cudaEvent_t e : events) cudaEventDestroy(e);
-    for (cudaStream_t s : lanes) cudaStreamDestroy(s);
-    if (copy) cudaStreamDestroy(copy);
+    for (const auto& e : events) pool_event_free(e.first, e.second);
+    for (cudaStream_t s : lanes) pool_stream_free(s);
+    pool_stream_free(copy);
   }
 };
 
@@ -231,20 +233,16 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   res.compute = stream;
   long long dev_bytes = 0;
   auto alloc = [&](void** p, size_t n) -> int {
-    cudaError_t e = cudaMalloc(p, n);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      set_error("device allocation of %zu bytes failed: %s", n, cudaGetErrorString(e));
-      return e == cudaErrorMemoryAllocation ? CQSA_ERR_OOM : CQSA_ERR_CUDA;
-    }
+    const int r = pool_alloc(p, n);
+    if (r != CQSA_OK) return r;
     res.dev.push_back(*p);
     dev_bytes += static_cast<long long>(n);
     return CQSA_OK;
   };
   auto event = [&](cudaEvent_t* e, bool timing) -> int {
-    cudaError_t r = cudaEventCreateWithFlags(e, timing ? cudaEventDefault : cudaEventDisableTiming);
-    if (r != cudaSuccess) return cuda_status(r, "cudaEventCreate");
-    res.events.push_back(*e);
+    const int r = pool_event(e, timing);
+    if (r != CQSA_OK) return r;
+    res.events.push_back({*e, timing});
     return CQSA_OK;
   };
   std::vector<void*> qs(nslots), ks(nslots), vs(nslots);
@@ -277,14 +275,12 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     if (rc == CQSA_OK && lse) rc = alloc(&lstage, rows * 4);
   }
   if (rc != CQSA_OK) return rc;
-  if ((rc = cuda_status(cudaStreamCreateWithFlags(&res.copy, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
-    return rc;
+  if ((rc = pool_stream(&res.copy)) != CQSA_OK) return rc;
   const int npar = max_parallel;
   std::vector<cudaStream_t> lane(npar, stream);
   for (int j = 1; j < npar; ++j) {
     cudaStream_t sj = nullptr;
-    if ((rc = cuda_status(cudaStreamCreateWithFlags(&sj, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
-      return rc;
+    if ((rc = pool_stream(&sj)) != CQSA_OK) return rc;
     res.lanes.push_back(sj);
     lane[j] = sj;
   }

@@ -57,20 +57,22 @@ __global__ void finalize_kernel(const float* __restrict__ acc, const float* __re
   }
 }
 
+// Buffers, events and streams come from the library's pool and go back to it once the streams that
+// use them have drained.
 struct Resources {
   std::vector<void*> dev;
-  std::vector<cudaEvent_t> events;
+  std::vector<std::pair<cudaEvent_t, bool>> events;
   cudaStream_t copy = nullptr, d2h = nullptr;
-  cudaStream_t compute = nullptr;  // caller's stream: drained before buffers are freed
+  cudaStream_t compute = nullptr;  // caller's stream: drained before buffers are returned
   bool compute_set = false;
   ~Resources() {
     if (compute_set) cudaStreamSynchronize(compute);
     if (copy) cudaStreamSynchronize(copy);
     if (d2h) cudaStreamSynchronize(d2h);
-    for (void* p : dev) cudaFree(p);
-    for (cudaEvent_t e : events) cudaEventDestroy(e);
-    if (copy) cudaStreamDestroy(copy);
-    if (d2h) cudaStreamDestroy(d2h);
+    for (void* p : dev) pool_free(p);
+    for (const auto& e : events) pool_event_free(e.first, e.second);
+    pool_stream_free(copy);
+    pool_stream_free(d2h);
   }
 };
 
@@ -78,20 +80,16 @@ struct Ctx {
   Resources res;
   long long bytes = 0;
   int alloc(void** p, size_t n) {
-    cudaError_t e = cudaMalloc(p, n);
-    if (e != cudaSuccess) {
-      cudaGetLastError();
-      set_error("device allocation of %zu bytes failed: %s", n, cudaGetErrorString(e));
-      return e == cudaErrorMemoryAllocation ? CQSA_ERR_OOM : CQSA_ERR_CUDA;
-    }
+    const int r = pool_alloc(p, n);
+    if (r != CQSA_OK) return r;
     res.dev.push_back(*p);
     bytes += static_cast<long long>(n);
     return CQSA_OK;
   }
   int event(cudaEvent_t* e, bool timing) {
-    cudaError_t r = cudaEventCreateWithFlags(e, timing ? cudaEventDefault : cudaEventDisableTiming);
-    if (r != cudaSuccess) return cuda_status(r, "cudaEventCreate");
-    res.events.push_back(*e);
+    const int r = pool_event(e, timing);
+    if (r != CQSA_OK) return r;
+    res.events.push_back({*e, timing});
     return CQSA_OK;
   }
 };
@@ -203,10 +201,8 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
     if (rc == CQSA_OK && lse) rc = cx.alloc(&lstage, static_cast<size_t>(B) * H * C * 4);
   }
   if (rc != CQSA_OK) return rc;
-  if ((rc = cuda_status(cudaStreamCreateWithFlags(&cx.res.copy, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
-    return rc;
-  if ((rc = cuda_status(cudaStreamCreateWithFlags(&cx.res.d2h, cudaStreamNonBlocking), "cudaStreamCreate")) != CQSA_OK)
-    return rc;
+  if ((rc = pool_stream(&cx.res.copy)) != CQSA_OK) return rc;
+  if ((rc = pool_stream(&cx.res.d2h)) != CQSA_OK) return rc;
 
   // Events: ordering (no timing) and per-operation timing pairs.
   cudaEvent_t kv_ready[2], kv_free[2], q_ready[2], q_free[2], fin_done, d2h_done;

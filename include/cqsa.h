@@ -171,6 +171,16 @@ int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout
                          int max_parallel, cqsa_quorum_stats* stats, cudaStream_t stream);
 
 /*
+ * The host-driven entry points (cqsa_stream_attn_fwd, cqsa_quorum_attn_fwd) take their device buffers,
+ * events and copy streams from a per-device cache that persists across calls (allocation, stream and
+ * event creation and cudaFree's device synchronisation would otherwise cost a large share of a short
+ * call). Cached device memory stays allocated until this call frees everything idle (all devices);
+ * an allocation that fails frees the idle buffers of its device and retries once. Returns CQSA_OK.
+ * Not to be called while one of those entry points runs on another thread.
+ */
+int cqsa_release_cache(void);
+
+/*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).
  */
 #define CQSA_STATIC_SCRATCH_BYTES (32u << 20)
