@@ -815,7 +815,9 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       };
       auto do_pv = [&](int j) {
         const uint64_t v0 = dV + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
-        const bool first = (j == 0) || (C::FLUSH > 0 && j % C::FLUSH == 0), last = (j == nkv - 1);
+        // O restarts at every segment start of the softmax loop (key tiles 0, FLUSH, 2 FLUSH, ...)
+        const bool first = (j == 0) || (C::FLUSH > 0 && j % (C::FLUSH > 0 ? C::FLUSH : 1) == 0);
+        const bool last = (j == nkv - 1);
         tc_fence_after();
         if (leader) {
           if (first) issue_pv<D, DT, true>(col_o, col_p, v0, IDESC_O);
