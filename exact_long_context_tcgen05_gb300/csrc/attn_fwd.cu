@@ -1,18 +1,24 @@
 // Exact attention forward for sm_103a: TMA-fed, tcgen05 MMAs accumulating in tensor memory, and a
 // warp-specialised online softmax between the two contractions.
 //
-// One CTA computes one 128-row query tile of one (batch, head) against every key tile it may see.
-//   warp 0      TMA producer: the Q tile once, then K and V tiles through a ring of STAGES
-//               shared-memory stages (mbarrier full/empty pairs, byte-counted completion).
-//   warp 1      allocates tensor memory; one thread issues S = Q K^T (A and B from shared memory)
-//               and O += P V (P read from tensor memory, V from shared memory), committing each
-//               group to an mbarrier.
-//   warps 2..5  softmax warpgroup, one thread per query row: tcgen05.ld of the row of S, masking,
-//               row max, p = exp2(s * scale * log2 e - m_ref) with one FFMA and ex2.approx, row sum,
-//               P packed to 16 bits and stored back with tcgen05.st; rare O rescales; epilogue.
-// Tensor memory (512 columns): S at 0 (128 fp32 columns), P double buffer at 128 and 256 (128 columns
-// each: 16-bit pairs of P, for bf16 P_hi in the first 64 and P_lo in the second 64), O at 384 (d fp32
-// columns). S_{j+1} is computed while the softmax works on tile j (it has read S_j by then).
+// attn_fwd2_kernel (the one every entry point launches): one CTA computes two 128-row query tiles of
+// one (batch, head) against every key tile either may see, loading each K/V tile once for both.
+//   warp 0        TMA producer (one lane): both Q tiles once, then K and V tiles through a ring of
+//                 STAGES shared-memory stages (mbarrier full/empty pairs, byte-counted completion).
+//   warps 1, 2    MMA issuers for query tiles 0 and 1 (warp 1 also owns the tensor memory): one
+//                 elected lane issues S = Q K^T (A and B from shared memory) and O += P V (P from
+//                 tensor memory, V from shared memory) and commits each group to mbarriers.
+//   warps 4..7,   softmax warpgroups of tiles 0 and 1, one thread per query row: tcgen05.ld of the
+//   8..11         row of S, masking, row max, p = exp2(s * scale * log2 e - m_ref), row sum, P packed
+//                 to 16 bits and stored with tcgen05.st; rare exact rescales of O; the fold of O into
+//                 an fp32 running sum between 128-key-tile segments (d = 64); the epilogue.
+//   setmaxnreg moves registers from warpgroup 0 (72 per thread) to the softmax warpgroups (216).
+// Tensor memory (512 columns), fp16 d = 64: S0 | S1 | P0 | P1 | O0 | O1 at 0, 128, 256, 320, 384, 448,
+// so S_t(j+1) is computed while the softmax still stores P_t(j); d = 128 and bf16 write P over S.
+//
+// attn_fwd_kernel (kept as an independent structure that a test compares bit for bit): one 128-row
+// query tile per CTA, warp 0 TMA, warp 1 MMA, warps 2..5 softmax; S at 0, a P double buffer at 128 and
+// 256 (bf16: P_hi in the first 64 columns, P_lo in the second 64), O at 384.
 //
 // bf16: P rounded to bf16 alone (8-bit significand) costs ~2^-9 relative per weight; P is split into
 // P_hi = bf16(p) and P_lo = bf16(p - P_hi) and both are multiplied into O (as the hi/lo operand split

@@ -39,6 +39,23 @@ def test_status_strings(cq):
     assert cq.cqsa_version() == "0.1.0"
 
 
+def test_release_cache_without_device(cq):
+    """Freeing the (empty) resource cache is a no-op that succeeds on a machine without a GPU."""
+    assert cq.cqsa_release_cache() == cq.CQSA_OK
+
+
+def test_quorum_validation(cq):
+    st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 64, True,
+                                                  0.0, cq.CQSA_F16, 7, (0, 1, 3), 1, max_parallel=0, stream=0))
+    assert st == cq.CQSA_ERR_INVALID and "max_parallel" in msg
+    st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 96, True,
+                                                  0.0, cq.CQSA_F16, 7, (0, 1, 3), 1, stream=0))
+    assert st == cq.CQSA_ERR_UNSUPPORTED
+    st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 64, True,
+                                                  0.0, cq.CQSA_F16, 7, (0, 1, 2), 1, stream=0))
+    assert st == cq.CQSA_ERR_INVALID and "difference" in msg
+
+
 def _rc(fn):
     try:
         fn()
