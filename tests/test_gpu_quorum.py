@@ -156,3 +156,24 @@ def test_parallel_lanes_bitwise_equal(cq, npar):
     ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=True, rows=rows)
     b, h, i = (torch.as_tensor(rows[:, j], device="cuda") for j in range(3))
     assert_close(to_np64(res[1][0][b, h, i]), ro, to_np64(res[1][1][b, h, i]), rl, what="parallel lanes")
+
+
+@pytest.mark.parametrize("layout,on_host", [(syn.LAYOUT_BHND, False), (syn.LAYOUT_BHND, True), (syn.LAYOUT_BNHD, True)])
+def test_quorum_batched_heads(cq, layout, on_host):
+    """B = 2: chunk staging of strided [B,H,N,d] chunks (2-D copies) and of token-major chunks with B > 1."""
+    B, H, N, d, c, D = 2, 3, 1800, 64, 7, (0, 1, 3)
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=29, layout=layout)
+    shape = (B, H, N, d) if layout == syn.LAYOUT_BHND else (B, N, H, d)
+    if on_host:
+        q, k, v = (_host(x, syn.F16) for x in (qn, kn, vn))
+    else:
+        q, k, v = (to_dev(x, syn.F16) for x in (qn, kn, vn))
+    out = torch.empty(shape, dtype=torch.float16).pin_memory()
+    lse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    cq.cqsa_quorum_attn_fwd(q, k, v, layout, on_host, out, lse, True, B, H, N, d, True, 0.0, syn.F16, c, D, 1,
+                            acc_on_host=True, max_parallel=3)
+    ro, rl = _oracle(qn, kn, vn, B, H, N, d, True, syn.F16, layout)
+    o64 = to_np64(out)
+    if layout == syn.LAYOUT_BNHD:
+        o64 = o64.transpose(0, 2, 1, 3)
+    assert_close(o64, ro, to_np64(lse), rl, what="quorum B=2")
