@@ -158,13 +158,31 @@ def oracle_sample(rows: int, seed: int = 1):
     return dt, flop, threads
 
 
+def _cpu_model() -> str:
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                key = line.split(":")[0].strip().lower()
+                if key in ("model name", "cpu model", "hardware"):
+                    return line.split(":", 1)[1].strip()
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.lower().startswith("model name"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return "unknown"
+
+
 def cpu_baseline(target_s: float = 12.0):
     dt, flop, thr = oracle_sample(256)
     rows = int(min(65536, max(256, 256 * target_s / max(dt, 1e-3))))
     dt, flop, thr = oracle_sample(rows, seed=2)
     return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
             "sample": f"{rows} seeded query rows (b,h,i uniform) of the workload, each in full over its causal "
-                      f"keys, FP64, {dt:.1f} s"}
+                      f"keys, FP64, {dt:.1f} s",
+            "cpu_model": _cpu_model(), "rows_per_s": rows / dt,
+            "extrapolated_full_s": FLOP_PER_STEP / (flop / dt)}
 
 
 def run_reference(args):
