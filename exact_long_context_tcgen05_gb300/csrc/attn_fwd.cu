@@ -856,8 +856,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
             if (ok) do_pv(j);
             if (ok && j + 1 < nkv) {
               ok = wait_all(&bar_k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
-              // P_t(j) lives in S_t's columns: PV_t(j) must have read it before S_t(j+1) lands there.
-              if (ok) ok = wait_all(&bar_pv_done[t], j & 1u, kDevTimeoutMMA, 17);
+              // P_t(j) lives in S_t's columns: S_t(j+1) is issued by this thread after PV_t(j), and MMAs
+              // of one issuing thread run in issue order, so PV_t(j) reads P_t(j) before it is overwritten.
               if (ok) do_s(j + 1);
             }
           }
@@ -1016,7 +1016,8 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
           tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
         } else {
-          // P over S: S_t(j) was issued only after PV_t(j-1) completed, so P_t(j-1) and O_t are settled.
+          // P over S: S_t(j) is complete, and its commit covers every earlier MMA of the issuing
+          // thread, PV_t(j-1) included, so P_t(j-1) has been read and O_t is settled.
 #pragma unroll
           for (int c4 = 0; c4 < 4; ++c4) {
             uint32_t hi[16], lo[16];
