@@ -5,6 +5,11 @@ leg may import this package; the library in ``exact_long_context_tcgen05_gb300``
 shares no code with it. The arithmetic is in ``oracle.c`` (plain C, double precision, OpenMP over
 rows), which states the definition it follows and where the pages state the problem.
 
+The backward (``attn_bwd``, ``attn_bwd_f64``) is the chain rule through the softmax, pinned in
+``tests/test_oracle_bwd.py`` by central finite differences of the loss sum(dO * O), by the forward
+part agreeing with ``attn_full``, by the key-shift invariance sum_j dK_j = 0 and by the uniform-score
+closed form of dV.
+
 Pins (``tests/test_oracle.py``): normalisation (V = 1 gives O = 1), causal row 0 (O_0 = v_0,
 LSE_0 = s_00), uniform scores (Q = 0 gives the mean of the allowed V rows and LSE = ln|A_i|),
 affinity in V, permutation equivariance, the two-key closed form, hand-derived fixtures under
@@ -59,6 +64,9 @@ def _load():
                                                       ctypes.c_int, ctypes.c_double, _p, _p]
             lib.oracle_widen.restype = None
             lib.oracle_widen.argtypes = [_p, _i64, ctypes.c_int, _p]
+            lib.oracle_attn_bwd.restype = ctypes.c_int
+            lib.oracle_attn_bwd.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_double,
+                                            _p, _p, _p, _p, _p]
             _lib = lib
     return _lib
 
@@ -148,3 +156,28 @@ def widen(bits, dtype=F16) -> np.ndarray:
     out = np.empty(bits.shape, dtype=np.float64)
     _load().oracle_widen(bits.ctypes.data, bits.size, dtype, out.ctypes.data)
     return out
+
+
+def attn_bwd_f64(q, k, v, dout, *, causal, scale):
+    """Backward from double inputs [B,H,N,d]: returns dict(out, lse, dq, dk, dv) in float64."""
+    q, k, v, dout = (np.ascontiguousarray(x, dtype=np.float64) for x in (q, k, v, dout))
+    if q.ndim != 4 or any(x.shape != q.shape for x in (k, v, dout)):
+        raise ValueError("q, k, v, dout must share one [B,H,N,d] shape")
+    B, H, N, d = q.shape
+    res = {n: np.empty(q.shape, dtype=np.float64) for n in ("out", "dq", "dk", "dv")}
+    res["lse"] = np.empty((B, H, N), dtype=np.float64)
+    rc = _load().oracle_attn_bwd(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, B, H, N, d,
+                                 int(bool(causal)), float(scale), res["out"].ctypes.data, res["lse"].ctypes.data,
+                                 res["dq"].ctypes.data, res["dk"].ctypes.data, res["dv"].ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd rejected its arguments")
+    return res
+
+
+def attn_bwd(q, k, v, dout, *, B, H, N, d, causal, scale=None, dtype=F16):
+    """Backward of [B,H,N,d] fp16/bf16 storage bits (q, k, v, dout), widened exactly; scale defaults to
+    the fp32 1/sqrt(d). Returns dict(out, lse, dq, dk, dv) in float64."""
+    scale = default_scale(d) if scale is None else float(np.float32(scale))
+    shape = (B, H, N, d)
+    ws = [widen(x, dtype).reshape(shape) for x in (q, k, v, dout)]
+    return attn_bwd_f64(*ws, causal=causal, scale=scale)

@@ -30,6 +30,8 @@
  *
  * A second routine, written separately, evaluates tiny problems in long double without the max
  * subtraction (p_ij = exp(s_ij) directly), as a brute-force cross-check of the first.
+ *
+ * The backward (gradients of q, k, v from an upstream dO) is defined at `oracle_attn_bwd` below.
  */
 #include <math.h>
 #include <stdint.h>
@@ -254,4 +256,98 @@ int oracle_attn_bruteforce_ld(const uint16_t* q, const uint16_t* k, const uint16
 /* exact widening exposed for the tests (storage bits -> double) */
 void oracle_widen(const uint16_t* bits, int64_t n, int dtype, double* out) {
     for (int64_t i = 0; i < n; ++i) out[i] = widen(bits, i, dtype);
+}
+
+/*
+ * Backward of the same attention: the gradients of a scalar loss with respect to q, k and v, given
+ * its gradient dO with respect to the output. The pages name the call (`stream_cqsa_backward`,
+ * "stream-cqsa 2.2.0 -> 2.2.2" diff, README list of explicit entry points) and say it consumes the
+ * forward's per-row log-sum-exp ("2.2.2 -> 2.2.3" diff, stream_cqsa/oom_fallback.py,
+ * `stream_cqsa_auto` docstring), but print no formula; this is the chain rule through
+ * O_i = sum_j P_ij v_j and the row softmax P_i = softmax(s_i), s_ij = scale q_i . k_j:
+ *   dV_j  = sum_i P_ij dO_i
+ *   dP_ij = dO_i . v_j
+ *   dS_ij = P_ij (dP_ij - sum_m P_im dP_im)        (softmax Jacobian applied to dP_i)
+ *   dQ_i  = scale sum_j dS_ij k_j,     dK_j = scale sum_i dS_ij q_i
+ * with P_ij = 0 outside A_i (causal: j <= i). Inputs and outputs are doubles in [B,H,N,d] (the
+ * Python wrapper widens 16-bit storage exactly); the forward's O and LSE come back as well. Per
+ * head the whole P and dS matrices are materialised (N*N doubles each): rows in parallel, then the
+ * key-side sums column by column. Returns 0, or -1 on a bad argument or allocation failure.
+ */
+int oracle_attn_bwd(const double* q, const double* k, const double* v, const double* dout, int64_t B,
+                    int64_t H, int64_t N, int64_t d, int causal, double scale, double* out, double* lse,
+                    double* dq, double* dk, double* dv) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || N > 8192) return -1;
+    double* P = (double*)malloc(sizeof(double) * (size_t)N * (size_t)N);
+    double* dS = (double*)malloc(sizeof(double) * (size_t)N * (size_t)N);
+    if (!P || !dS) {
+        free(P);
+        free(dS);
+        return -1;
+    }
+    for (int64_t bh = 0; bh < B * H; ++bh) {
+        const double* qh = q + bh * N * d;
+        const double* kh = k + bh * N * d;
+        const double* vh = v + bh * N * d;
+        const double* gh = dout + bh * N * d;
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t i = 0; i < N; ++i) {
+            const int64_t jend = causal ? i + 1 : N;
+            double* Pi = P + i * N;
+            double* dSi = dS + i * N;
+            double m = -INFINITY;
+            for (int64_t j = 0; j < jend; ++j) {
+                double dot = 0.0;
+                for (int64_t c = 0; c < d; ++c) dot += qh[i * d + c] * kh[j * d + c];
+                Pi[j] = scale * dot;
+                if (Pi[j] > m) m = Pi[j];
+            }
+            nsum l = {0.0, 0.0};
+            for (int64_t j = 0; j < jend; ++j) {
+                Pi[j] = exp(Pi[j] - m);
+                nsum_add(&l, Pi[j]);
+            }
+            const double lv = nsum_get(&l);
+            for (int64_t j = 0; j < jend; ++j) Pi[j] /= lv;
+            for (int64_t j = jend; j < N; ++j) Pi[j] = 0.0;
+            lse[bh * N + i] = m + log(lv);
+            for (int64_t c = 0; c < d; ++c) {
+                nsum a = {0.0, 0.0};
+                for (int64_t j = 0; j < jend; ++j) nsum_add(&a, Pi[j] * vh[j * d + c]);
+                out[(bh * N + i) * d + c] = nsum_get(&a);
+            }
+            /* dP_ij, then its P-weighted row mean, then dS_ij */
+            nsum D = {0.0, 0.0};
+            for (int64_t j = 0; j < jend; ++j) {
+                double dp = 0.0;
+                for (int64_t c = 0; c < d; ++c) dp += gh[i * d + c] * vh[j * d + c];
+                dSi[j] = dp;
+                nsum_add(&D, Pi[j] * dp);
+            }
+            const double Dv = nsum_get(&D);
+            for (int64_t j = 0; j < jend; ++j) dSi[j] = Pi[j] * (dSi[j] - Dv);
+            for (int64_t j = jend; j < N; ++j) dSi[j] = 0.0;
+            for (int64_t c = 0; c < d; ++c) {
+                nsum a = {0.0, 0.0};
+                for (int64_t j = 0; j < jend; ++j) nsum_add(&a, dSi[j] * kh[j * d + c]);
+                dq[(bh * N + i) * d + c] = scale * nsum_get(&a);
+            }
+        }
+#pragma omp parallel for schedule(dynamic, 8)
+        for (int64_t j = 0; j < N; ++j) {
+            const int64_t i0 = causal ? j : 0;
+            for (int64_t c = 0; c < d; ++c) {
+                nsum a = {0.0, 0.0}, g = {0.0, 0.0};
+                for (int64_t i = i0; i < N; ++i) {
+                    nsum_add(&a, P[i * N + j] * gh[i * d + c]);
+                    nsum_add(&g, dS[i * N + j] * qh[i * d + c]);
+                }
+                dv[(bh * N + j) * d + c] = nsum_get(&a);
+                dk[(bh * N + j) * d + c] = scale * nsum_get(&g);
+            }
+        }
+    }
+    free(P);
+    free(dS);
+    return 0;
 }

@@ -22,8 +22,8 @@ _lib = None
 
 F16, BF16, F32 = 0, 1, 2
 LAYOUT_BHND, LAYOUT_BNHD = 0, 1
-# tensor ids of the Q/K/V streams
-TID_Q, TID_K, TID_V = 0, 1, 2
+# tensor ids of the Q/K/V streams and of the upstream output gradient dO of the backward
+TID_Q, TID_K, TID_V, TID_DO = 0, 1, 2, 3
 
 
 def build(force: bool = False) -> str:

@@ -1,0 +1,76 @@
+"""Pins of the oracle's attention backward (CPU, no GPU): its gradients against central finite
+differences of the loss sum(dO * O), its forward part against the forward oracle, the key-shift
+invariance sum_j dK_j = 0, and the uniform-score closed forms of dV and dK."""
+import numpy as np
+import pytest
+
+import oracle
+import synthetic as syn
+
+
+def _loss(q, k, v, g, causal, scale):
+    return float(np.sum(g * oracle.attn_bwd_f64(q, k, v, g, causal=causal, scale=scale)["out"]))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_gradients_match_central_differences(causal):
+    """dq, dk, dv are the derivatives of L = sum(dO * O): a dropped softmax term, a wrong sign or a
+    transposed operand in any of them moves it far beyond the difference quotient's error (~1e-9)."""
+    rng = np.random.default_rng(11 + int(causal))
+    B, H, N, d = 1, 2, 7, 3
+    q, k, v, g = (rng.standard_normal((B, H, N, d)) for _ in range(4))
+    scale = 0.7
+    res = oracle.attn_bwd_f64(q, k, v, g, causal=causal, scale=scale)
+    h = 1e-5
+    for name, pos in (("dq", 0), ("dk", 1), ("dv", 2)):
+        base = [q, k, v]
+        fd = np.empty_like(q)
+        for idx in np.ndindex(q.shape):
+            plus = [x.copy() for x in base]
+            minus = [x.copy() for x in base]
+            plus[pos][idx] += h
+            minus[pos][idx] -= h
+            fd[idx] = (_loss(*plus, g, causal, scale) - _loss(*minus, g, causal, scale)) / (2 * h)
+        np.testing.assert_allclose(res[name], fd, rtol=1e-6, atol=1e-8, err_msg=name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_forward_part_matches_forward_oracle(causal):
+    B, H, N, d = 1, 2, 40, 16
+    q, k, v = syn.qkv(B, H, N, d, seed=3)
+    g = syn.normal(B, H, N, d, seed=3, tensor_id=syn.TID_DO)
+    res = oracle.attn_bwd(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal)
+    o, lse = oracle.attn_full(q, k, v, B=B, H=H, N=N, d=d, causal=causal)
+    np.testing.assert_allclose(res["out"], o, rtol=0, atol=1e-13)
+    np.testing.assert_allclose(res["lse"], lse, rtol=0, atol=1e-12)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_key_shift_invariance(causal):
+    """Adding one vector to every key adds the same amount to each score of a row, which the
+    softmax ignores: the loss is flat along that direction, so the key gradients sum to zero."""
+    B, H, N, d = 2, 1, 33, 8
+    q, k, v = syn.qkv(B, H, N, d, seed=5)
+    g = syn.normal(B, H, N, d, seed=5, tensor_id=syn.TID_DO)
+    res = oracle.attn_bwd(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal)
+    tot = np.abs(res["dk"]).sum(axis=2)
+    assert np.all(np.abs(res["dk"].sum(axis=2)) <= 1e-13 * np.maximum(tot, 1.0))
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_uniform_scores_closed_form(causal):
+    """q = 0 makes every allowed score 0: P_ij = 1/|A_i|, so dV_j = sum over the rows i that see key
+    j of dO_i / |A_i|, and dK = scale * sum_i dS_ij q_i vanishes exactly."""
+    B, H, N, d = 1, 2, 24, 8
+    _, k, v = syn.qkv(B, H, N, d, seed=9)
+    q = np.zeros_like(k)
+    g = syn.normal(B, H, N, d, seed=9, tensor_id=syn.TID_DO)
+    res = oracle.attn_bwd(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal)
+    gd = oracle.widen(g).reshape(B, H, N, d)
+    want = np.zeros((B, H, N, d))
+    for j in range(N):
+        for i in range(N):
+            if not causal or j <= i:
+                want[:, :, j] += gd[:, :, i] / ((i + 1) if causal else N)
+    np.testing.assert_allclose(res["dv"], want, rtol=1e-13, atol=1e-14)
+    assert np.all(res["dk"] == 0.0)
