@@ -25,6 +25,8 @@ Secondary measurements (one JSON line each, not the headline; `--measure NAME`):
   --n, default 4,000,000): TFLOP/s, copy rate while overlapped vs the link probe, stall time.
 - bf16: B=2 H=32 N=16384 d=128 bf16 non-causal monolithic forward (K scaled by 3), TFLOP/s and the
   fraction of the tensor peak (algorithmic FLOP; the hi/lo split of P costs 1.5x the MMA work).
+- bwd: the attention backward (dq, dk, dv from the saved LSE) on the headline shape, TFLOP/s of the
+  five products vs the tensor peak.
 - quorum: the cyclic quorum-set decomposition on the pages' 4,000,000-token example (B=1 H=8 d=64
   fp16 causal, c=31, interest set (0,1,3,8,12,18), itr=1: 31 subproblems), token-major pinned host
   Q/K/V/out (N from --n); TFLOP/s, kernel time, staging copies.
@@ -497,6 +499,44 @@ def measure_bf16(cq, dev, reps):
                          "peak_source": src, "note": "algorithmic FLOP; the P hi/lo split issues 1.5x the MMA work"}}
 
 
+def measure_bwd(cq, dev, reps):
+    """Attention backward on the headline shape (B=1 H=8 N=32768 d=64 fp16 causal): the whole
+    cqsa_attn_bwd call (D = rowsum(dO * O), zeroing the dQ accumulator, the tcgen05 kernel, the dQ
+    conversion) timed with CUDA events, inputs and forward outputs resident. Algorithmic FLOP: five
+    products of 2*N*N*d per head (S, dP, dV, dK, dQ), halved by the causal mask = 2.5x the forward."""
+    import torch
+    import synthetic as syn
+    B, H, N, D = 1, 8, 32768, 64
+    qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
+    gn = syn.normal(B, H, N, D, seed=0, tensor_id=syn.TID_DO)
+    q, k, v, g = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn, gn))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cq.cqsa_attn_fwd(q, k, v, out, lse, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = cq.cqsa_attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
+
+    def step():
+        cq.cqsa_attn_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+
+    for _ in range(3):
+        step()
+    ms = []
+    for i in range(reps):
+        flush.fill_(i & 0xFF)
+        ms += _time_events(step, 1, stream)
+    flop = 2.5 * 4.0 * B * H * N * N * D / 2
+    tf = flop / (statistics.median(ms) / 1e3) / 1e12
+    peak, src, _ = _peaks()
+    return {"measure": "bwd", "workload": "B=1 H=8 N=32768 d=64 fp16 causal backward (dq, dk, dv)",
+            "ms_per_step": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
+            "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
+                         "peak_source": src, "note": "algorithmic FLOP of the five products, whole call"}}
+
+
 def run_measure(args):
     import torch
     world, rank, local = _dist()
@@ -515,6 +555,8 @@ def run_measure(args):
         line = measure_stream(cq, dev, args.n, link["h2d_gbs"])
     elif args.measure == "quorum":
         line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel)
+    elif args.measure == "bwd":
+        line = measure_bwd(cq, dev, reps)
     else:
         line = measure_bf16(cq, dev, reps)
     rc, code, _ = cq.cqsa_device_error()
@@ -530,7 +572,7 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum"), default=None)
+    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum", "bwd"), default=None)
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream / quorum")
     ap.add_argument("--acc-on-host", action="store_true", help="--measure quorum with the host accumulator")
     ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")

@@ -21,7 +21,7 @@ CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
-            "cqsa_release_cache",
+            "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
             "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
@@ -72,6 +72,10 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_quorum_schedule.restype = _ll
     lib.cqsa_quorum_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i, _vp,
                                          _i, _i, _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
+    lib.cqsa_attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
+    lib.cqsa_attn_bwd_workspace_size.restype = ctypes.c_size_t
+    lib.cqsa_attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i,
+                                  _i, _f, _i, _vp]
     lib.cqsa_release_cache.argtypes = []
     lib.cqsa_release_cache.restype = _i
     lib.cqsa_status_string.argtypes = [_i]
@@ -212,6 +216,17 @@ def cqsa_quorum_attn_fwd(q, k, v, layout, inputs_on_host, out, lse, out_on_host,
                                            _stream(stream)))
 
 
+def cqsa_attn_bwd_workspace_size(B, H, N, d) -> int:
+    return int(lib.cqsa_attn_bwd_workspace_size(B, H, N, d))
+
+
+def cqsa_attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, workspace, workspace_bytes, B, H, N, d, causal, scale, dtype,
+                  stream=None) -> int:
+    return _check(lib.cqsa_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq), _ptr(dk),
+                                    _ptr(dv), _ptr(workspace), int(workspace_bytes), B, H, N, d, int(bool(causal)),
+                                    float(scale), dtype, _stream(stream)))
+
+
 def cqsa_release_cache() -> int:
     """Free the device buffers, events and streams the host-driven entry points keep between calls."""
     return _check(lib.cqsa_release_cache())
@@ -250,3 +265,22 @@ def attention(q, k, v, *, causal=False, scale=None, return_lse=False, stream=Non
     cqsa_attn_fwd(q, k, v, out, lse, B, H, N, d, causal, 0.0 if scale is None else scale, dtype_code(q.dtype),
                   stream)
     return (out, lse) if return_lse else out
+
+
+def attention_backward(q, k, v, out, dout, lse, *, causal=False, scale=None, stream=None):
+    """Gradients (dq, dk, dv) of attention on device tensors [B,H,N,64] (fp16/bf16), from the forward's
+    out and lse ([B,H,N] fp32) and the upstream gradient dout."""
+    import torch
+    B, H, N, d = q.shape
+    for t in (k, v, out, dout):
+        if t.shape != q.shape or t.dtype != q.dtype or not t.is_cuda:
+            raise ValueError("q, k, v, out, dout must be CUDA tensors of one shape and dtype [B,H,N,d]")
+    if lse.shape != (B, H, N) or lse.dtype != torch.float32:
+        raise ValueError("lse must be a float32 tensor [B,H,N]")
+    q, k, v, out, dout, lse = (t.contiguous() for t in (q, k, v, out, dout, lse))
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = cqsa_attn_bwd_workspace_size(B, H, N, d)
+    ws = torch.empty(max(ws_bytes, 16), dtype=torch.uint8, device=q.device)
+    cqsa_attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, ws, ws.numel(), B, H, N, d, causal,
+                  0.0 if scale is None else scale, dtype_code(q.dtype), stream)
+    return dq, dk, dv

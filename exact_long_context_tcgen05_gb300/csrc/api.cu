@@ -1,5 +1,5 @@
 // C ABI: argument validation, status reporting and dispatch to the kernels. Nothing here computes
-// attention; every step of the path runs in the kernels of attn_fwd.cu and merge.cu.
+// attention; every step of the path runs in the kernels of attn_fwd.cu, attn_bwd.cu and merge.cu.
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -11,7 +11,8 @@
 
 namespace cqsa {
 
-int device_error_word(DevErr* out, int clear);  // attn_fwd.cu (owns the device word)
+int device_error_word(DevErr* out, int clear);  // attn_fwd.cu (owns the forward's device word)
+int bwd_error_word(DevErr* out, int clear);     // attn_bwd.cu (the backward's)
 
 static thread_local char t_err[512];
 static unsigned int g_timeout_ms = 0;
@@ -116,6 +117,10 @@ int cqsa_device_error(int* code, int* block, int clear) {
   if (rc != CQSA_OK) return rc;
   rc = device_error_word(&e, clear);
   if (rc != CQSA_OK) return rc;
+  if (e.code == 0) {
+    rc = bwd_error_word(&e, clear);
+    if (rc != CQSA_OK) return rc;
+  }
   if (code) *code = e.code;
   if (block) *block = e.block;
   if (e.code != 0) {
@@ -237,6 +242,58 @@ int cqsa_merge_partials(const float* const* O_parts, const float* const* LSE_par
     return CQSA_ERR_INVALID;
   }
   return launch_merge(O_parts, LSE_parts, n, out, lse, static_cast<long long>(B) * H * Nq, d, out_dtype, stream);
+}
+
+size_t cqsa_attn_bwd_workspace_size(int B, int H, int N, int d) {
+  if (B < 1 || H < 1 || N < 1 || d < 1) return 0;
+  return attention_bwd_workspace(B, H, N, d);
+}
+
+int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                  int causal, float scale, int dtype, cudaStream_t stream) {
+  t_err[0] = 0;
+  int rc = check_problem(B, H, N, N, d, scale, dtype, false);
+  if (rc != CQSA_OK) return rc;
+  if (d != 64) {
+    set_error("the backward supports head dim 64 (got %d)", d);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace) {
+    set_error("q, k, v, out, dout, lse, dq, dk, dv and workspace must be non-null device pointers");
+    return CQSA_ERR_INVALID;
+  }
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out) || !aligned16(dout) || !aligned16(dq) ||
+      !aligned16(dk) || !aligned16(dv) || !aligned16(workspace) || (reinterpret_cast<uintptr_t>(lse) & 3u)) {
+    set_error("q, k, v, out, dout, dq, dk, dv and workspace must be 16-byte aligned (lse 4-byte)");
+    return CQSA_ERR_INVALID;
+  }
+  const size_t need = attention_bwd_workspace(B, H, N, d);
+  if (workspace_bytes < need) {
+    set_error("workspace of %zu bytes is smaller than the %zu bytes cqsa_attn_bwd_workspace_size reports",
+              workspace_bytes, need);
+    return CQSA_ERR_INVALID;
+  }
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q;
+  a.k = k;
+  a.v = v;
+  a.out = out;
+  a.dout = dout;
+  a.lse = lse;
+  a.dq = dq;
+  a.dk = dk;
+  a.dv = dv;
+  a.workspace = workspace;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.d = d;
+  a.causal = causal != 0;
+  a.scale = resolve_scale(scale, d);
+  a.dtype = dtype;
+  return launch_attention_bwd(a, stream);
 }
 
 }  // extern "C"

@@ -39,6 +39,27 @@ struct AttnArgs {
 // Validates nothing (the ABI layer does); encodes tensor maps and launches on `stream`.
 int launch_attention(const AttnArgs& a, cudaStream_t stream);
 
+// Attention backward (attn_bwd.cu): dQ, dK, dV of [B,H,N,64] q, k, v from out, dout and the forward's
+// LSE. `workspace` holds the fp32 dQ accumulator and D_i (attention_bwd_workspace bytes).
+struct BwdArgs {
+  const void* q;
+  const void* k;
+  const void* v;
+  const void* out;
+  const void* dout;
+  const float* lse;
+  void* dq;
+  void* dk;
+  void* dv;
+  void* workspace;
+  int B, H, N, d;
+  int causal;
+  float scale;  // resolved
+  int dtype;
+};
+size_t attention_bwd_workspace(int B, int H, int N, int d);
+int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream);
+
 // LSE merge of n partials (device pointer arrays passed by value).
 int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int n, void* out, float* lse,
                  long long rows, int d, int out_dtype, cudaStream_t stream);

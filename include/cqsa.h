@@ -1,5 +1,5 @@
 /*
- * cqsa.h - exact scaled-dot-product attention forward on one NVIDIA GB300 (sm_103a).
+ * cqsa.h - exact scaled-dot-product attention forward (and its backward) on one NVIDIA GB300 (sm_103a).
  *
  * C ABI of libcqsa_gb300.so. Every pointer is owned by the caller: the library never frees or
  * keeps one after a call returns. Device calls are asynchronous and ordered on the given stream
@@ -179,6 +179,31 @@ int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout
  * Not to be called while one of those entry points runs on another thread.
  */
 int cqsa_release_cache(void);
+
+/*
+ * Attention backward: the gradients of a scalar loss with respect to q, k and v, given its gradient
+ * dout with respect to the forward output. The pages name a backward that works from the forward's
+ * saved per-row log-sum-exp (`stream_cqsa_backward`, "stream-cqsa 2.2.0 -> 2.2.2" diff, README list of
+ * explicit entry points; "2.2.2 -> 2.2.3" diff, stream_cqsa/oom_fallback.py, `stream_cqsa_auto`
+ * docstring: info["lse"] is what it needs) but print no formula; this is the chain rule through the
+ * row softmax of the forward above, with P recomputed from lse:
+ *   P_ij = exp(s_ij - lse_i) on A_i (0 elsewhere),  D_i = dout_i . out_i,  dP_ij = dout_i . v_j,
+ *   dS_ij = P_ij (dP_ij - D_i),  dv_j = sum_i P_ij dout_i,  dk_j = scale sum_i dS_ij q_i,
+ *   dq_i = scale sum_j dS_ij k_j.
+ * q, k, v, out (the forward's output), dout: device [B,H,N,64], fp16 or bf16 (dtype), contiguous
+ * (layout BHND); lse: device [B,H,N] fp32 as cqsa_attn_fwd wrote it (natural log). dq, dk, dv:
+ * device [B,H,N,64] in dtype, written in full. P and dS enter the tensor-core products rounded to
+ * dtype; all sums are fp32. workspace: caller-owned device memory of at least
+ * cqsa_attn_bwd_workspace_size(B, H, N, d) bytes (the fp32 dq accumulator and D), 16-byte aligned;
+ * its contents on entry do not matter. Head dimension 64 only (CQSA_ERR_UNSUPPORTED otherwise).
+ * Asynchronous on `stream`; allocates nothing. Runs are bitwise reproducible except dq, whose fp32
+ * accumulation order across key tiles follows the atomic adds (differences of a few fp32 ulps
+ * before the final rounding to dtype).
+ */
+size_t cqsa_attn_bwd_workspace_size(int B, int H, int N, int d);
+int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout, const float* lse,
+                  void* dq, void* dk, void* dv, void* workspace, size_t workspace_bytes, int B, int H, int N, int d,
+                  int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).

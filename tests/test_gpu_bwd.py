@@ -1,0 +1,107 @@
+"""GPU parity of the attention backward (cqsa_attn_bwd) against the FP64 oracle backward.
+
+The GPU forward supplies out and lse, as a caller's forward would; the oracle recomputes everything
+from q, k, v and dout in double. Tolerance, per gradient tensor, from the arithmetic: the result is
+rounded to the input dtype (relative half-ulp u = 2^-11 for fp16, 2^-8 for bf16), and P and dS enter
+the tensor-core products rounded to the same dtype (one more relative error <= u per term, mostly
+averaging out over the sums); D uses the rounded forward output. So the largest error is held to
+8u of the tensor's largest |value| and the mean error to u of its mean |value|.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synthetic as syn
+from tests._gpu import mono, to_dev, to_np64
+
+pytestmark = pytest.mark.gpu
+
+U = {syn.F16: 2.0 ** -11, syn.BF16: 2.0 ** -8}
+
+
+@pytest.fixture(scope="module")
+def cq():
+    import exact_long_context_tcgen05_gb300 as m
+    return m
+
+
+def _run(cq, B, H, N, d, causal, dtype, seed=0, q_zero=False):
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=seed, dtype=dtype)
+    if q_zero:
+        qn = np.zeros_like(qn)
+    gn = syn.normal(B, H, N, d, seed=seed, tensor_id=syn.TID_DO, dtype=dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
+    dq, dk, dv = cq.attention_backward(q, k, v, out, g, lse, causal=causal)
+    torch.cuda.synchronize()
+    rc, code, _ = cq.cqsa_device_error()
+    assert rc == cq.CQSA_OK and code == 0
+    return (qn, kn, vn, gn), (dq, dk, dv)
+
+
+def _check(got: np.ndarray, ref: np.ndarray, dtype, what):
+    u = U[dtype]
+    e = np.abs(got - ref)
+    mx, mn = float(e.max()), float(e.mean())
+    ref_max, ref_mean = float(np.abs(ref).max()), float(np.abs(ref).mean())
+    assert mx <= 8 * u * ref_max, f"{what}: max abs {mx:.3e} > {8 * u * ref_max:.3e} (8u of max |ref| {ref_max:.3e})"
+    assert mn <= u * ref_mean, f"{what}: mean abs {mn:.3e} > {u * ref_mean:.3e} (u of mean |ref| {ref_mean:.3e})"
+    return mx / ref_max, mn / ref_mean
+
+
+@pytest.mark.parametrize("B,H,N,causal,dtype", [
+    (1, 2, 1024, True, syn.F16),     # several tiles, diagonal masking
+    (1, 2, 640, False, syn.F16),
+    (2, 3, 333, True, syn.F16),      # ragged last tile, several heads and batches
+    (1, 2, 200, False, syn.F16),
+    (1, 1, 77, True, syn.F16),       # one partial tile
+    (1, 2, 512, True, syn.BF16),
+    (1, 1, 384, False, syn.BF16),
+])
+def test_backward_matches_oracle(cq, B, H, N, causal, dtype):
+    d = 64
+    (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, B, H, N, d, causal, dtype)
+    ref = oracle.attn_bwd(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=causal, dtype=dtype)
+    rel = {}
+    for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
+        rel[name] = _check(to_np64(t), ref[name], dtype, f"{name} N={N} causal={causal}")
+    print(f"\nbwd N={N} causal={causal} dtype={dtype}: " +
+          ", ".join(f"{n} max/maxref {a:.2e} mean/meanref {b:.2e}" for n, (a, b) in rel.items()))
+
+
+def test_single_token(cq):
+    """N = 1: P = 1, so dv = dout exactly (P rounds to 1.0) and dS = dP - D, which is zero up to the
+    fp32 rounding of two orders of the same dot product, so dq and dk are ~1e-6 instead of O(1)."""
+    (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, 1, 2, 1, 64, True, syn.F16)
+    assert float(dq.float().abs().max()) <= 1e-4 and float(dk.float().abs().max()) <= 1e-4
+    np.testing.assert_array_equal(to_np64(dv), oracle.widen(gn).reshape(1, 2, 1, 64))
+
+
+def test_uniform_scores_give_zero_dk(cq):
+    """q = 0: dk = scale * sum_i dS_ij q_i is exactly zero on any hardware."""
+    _, (dq, dk, dv) = _run(cq, 1, 2, 384, 64, True, syn.F16, q_zero=True)
+    assert torch.count_nonzero(dk).item() == 0
+
+
+def test_dk_dv_bitwise_reproducible(cq):
+    """dk and dv are accumulated in a fixed order (one CTA per key tile); dq's atomic order may vary."""
+    _, (dq1, dk1, dv1) = _run(cq, 1, 2, 768, 64, True, syn.F16, seed=4)
+    _, (dq2, dk2, dv2) = _run(cq, 1, 2, 768, 64, True, syn.F16, seed=4)
+    assert torch.equal(dk1, dk2) and torch.equal(dv1, dv2)
+    assert float((dq1.float() - dq2.float()).abs().max()) <= 2.0 ** -10 * float(dq1.float().abs().max())
+
+
+@pytest.mark.parametrize("causal", [True, False])
+def test_sum_identities_large(cq, causal):
+    """At a size the oracle cannot evaluate in full (8 heads x 8,192 tokens), two identities that hold
+    for any inputs: sum_j dk_j = 0 (keys shifted together leave the softmax unchanged) and
+    sum_j dv_j = sum_i dout_i (every P row sums to one)."""
+    B, H, N, d = 1, 8, 8192, 64
+    (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, B, H, N, d, causal, syn.F16, seed=2)
+    dk64, dv64 = to_np64(dk), to_np64(dv)
+    g64 = oracle.widen(gn).reshape(B, H, N, d)
+    u = U[syn.F16]
+    # each summed element carries a rounding error <= u |x|; the sums are checked against that budget
+    assert np.all(np.abs(dk64.sum(axis=2)) <= 4 * u * np.abs(dk64).sum(axis=2) + 1e-6)
+    assert np.all(np.abs(dv64.sum(axis=2) - g64.sum(axis=2)) <= 4 * u * np.abs(dv64).sum(axis=2) + 1e-6)
