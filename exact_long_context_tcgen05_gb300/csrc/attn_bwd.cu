@@ -45,7 +45,9 @@ constexpr int BT = 128;                         // keys per CTA tile, queries pe
 constexpr int HD = 64;                          // head dimension
 constexpr uint32_t BOX = BT * HD * 2;           // one 128 x 64 tile of 16-bit elements (16 KiB)
 constexpr uint32_t OFF_K = 0, OFF_V = BOX, OFF_Q = 2 * BOX, OFF_G = 4 * BOX, OFF_DS = 6 * BOX;
-constexpr uint32_t OFF_ROW = 8 * BOX;           // float lse2[2][128], dd[2][128]
+constexpr uint32_t OFF_DQ = 8 * BOX;            // dQ staging: 2 slots of 128 x 64 fp32
+constexpr uint32_t DQ_SLOT = BT * HD * 4;
+constexpr uint32_t OFF_ROW = OFF_DQ + 2 * DQ_SLOT;  // float lse2[2][128], dd[2][128]
 constexpr uint32_t OFF_BAR = OFF_ROW + 4 * BT * 4;
 constexpr int NBAR = 6;                         // kv, q[2], mma1, mma2, idle
 constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
@@ -53,6 +55,7 @@ constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 
 constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
+constexpr int NTHR = 256;  // eight warps: two per tensor-memory lane quarter, each on half the columns
 
 enum : int { kBwdTimeoutLoad = 1, kBwdTimeoutMMA = 3 };
 
@@ -128,6 +131,20 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d) : "memory");
 }
 
+// Bulk tensor reduction: the shared-memory box at `src` is added (fp32) into the global tensor at
+// (x, y, z); rows outside the tensor are skipped. Completion is tracked by bulk groups.
+__device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMap* map, int x, int y, int z) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.3d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(x), "r"(y), "r"(z)
+      : "memory");
+}
+__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
+// at most one bulk group still reading shared memory
+__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
 __device__ __forceinline__ float ex2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -176,10 +193,10 @@ __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t
 }
 
 template <int DT, bool CAUSAL>
-__global__ void __launch_bounds__(128, 1)
+__global__ void __launch_bounds__(NTHR, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
-                    const BwdParams p) {
+                    const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = sm + OFF_K;
@@ -187,6 +204,7 @@ __global__ void __launch_bounds__(128, 1)
   uint8_t* sQ = sm + OFF_Q;  // [2][BOX]
   uint8_t* sG = sm + OFF_G;  // [2][BOX] (dO)
   uint8_t* sdS = sm + OFF_DS;
+  uint8_t* sdQ = sm + OFF_DQ;  // [2][128 x 64 fp32], two 32-float boxes each, 128-byte swizzle
   float* sLse = reinterpret_cast<float*>(sm + OFF_ROW);  // [2][128], base-2 LSE
   float* sDd = sLse + 2 * BT;                            // [2][128], D_i
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
@@ -198,7 +216,9 @@ __global__ void __launch_bounds__(128, 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int quarter = warp & 3;  // tensor-memory lane quarter of this warp
+  const int half = warp >> 2;    // query columns [64 half, 64 half + 64) / feature columns [32 half, +32)
   const int bh = blockIdx.x % p.BH, jt = blockIdx.x / p.BH;
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = jt * BT;
@@ -214,15 +234,16 @@ __global__ void __launch_bounds__(128, 1)
     prefetch_tensormap(&tmK);
     prefetch_tensormap(&tmV);
     prefetch_tensormap(&tmG);
+    prefetch_tensormap(&tmDQ);
   }
   if (warp == 0) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
   }
-  // row values (base-2 LSE, D) of the first query tile; later tiles are fetched one step ahead
+  // row values (base-2 LSE, D) of a query tile, one thread per row (threads < 128); fetched one step ahead
   auto row_vals = [&](int it, float& l2, float& dd) {
     const long long i = static_cast<long long>(it0 + it) * BT + tid;
-    if (it < nit && i < p.N) {
+    if (tid < BT && it < nit && i < p.N) {
       l2 = p.lse[static_cast<long long>(bh) * p.N + i] * LOG2E;
       dd = p.dvec[static_cast<long long>(bh) * p.N + i];
     } else {
@@ -233,8 +254,10 @@ __global__ void __launch_bounds__(128, 1)
   {
     float l2, dd;
     row_vals(0, l2, dd);
-    sLse[tid] = l2;
-    sDd[tid] = dd;
+    if (tid < BT) {
+      sLse[tid] = l2;
+      sDd[tid] = dd;
+    }
   }
   __syncthreads();
   tc_fence_after();
@@ -289,12 +312,14 @@ __global__ void __launch_bounds__(128, 1)
   };
   if (warp == 0) ok = issue_m1(0);
 
-  const int r = tid;  // key row (tensor-memory lane) of this thread
-  const uint32_t trow = tmem + (static_cast<uint32_t>(warp * 32) << 16);
+  const int r = quarter * 32 + lane;  // key row (tensor-memory lane) in the elementwise step, query row in the dQ step
+  const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
   const bool key_ok = k0 + r < p.N;
   const float sl2 = p.scale_log2;
-  const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(r * 128);
+  const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(half * BOX + r * 128);
+  const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>(half * (BT * 128) + r * 128);
   const int sw = r & 7;
+  int dq_groups = 0;  // bulk reductions issued (thread 0)
 
   for (int it = 0; it < nit; ++it) {
     const int slot = it & 1;
@@ -302,58 +327,69 @@ __global__ void __launch_bounds__(128, 1)
     float nl2, ndd;
     row_vals(it + 1, nl2, ndd);  // next tile's row values, consumed at the end of this step
     if (ok) ok = wait_abort(bar_m1, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 3);
-    ok = __all_sync(0xffffffffu, ok);  // the warp-collective tensor-memory loads below run warp-uniformly
+    ok = __all_sync(0xffffffffu, ok);  // the warp-collective tensor-memory accesses below run warp-uniformly
+    // S^T and dP^T of this warp's 64 query columns, all read before any P^T / dS^T is written over them
+    uint32_t s[64], g[64];
     if (ok) {
       tc_fence_after();
+      tmem_ld32(trow + COL_S + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      tmem_ld32(trow + COL_S + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      tmem_ld32(trow + COL_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+      tmem_ld32(trow + COL_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+      tmem_wait_ld();
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&g[0]));
+      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&g[32]));
+    }
+    ok = __syncthreads_and(ok) != 0;
+    if (!ok) break;
+    {
       const bool diag = CAUSAL && (i0 == k0);
-      const float* lrow = sLse + slot * BT;
-      const float* drow = sDd + slot * BT;
+      const float* lrow = sLse + slot * BT + half * 64;
+      const float* drow = sDd + slot * BT + half * 64;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
-        uint32_t s[32], g[32];
-        tmem_ld32(trow + COL_S + c * 32, s);
-        tmem_ld32(trow + COL_DP + c * 32, g);
-        tmem_wait_ld();
-        reg_fence32(s);
-        reg_fence32(g);
+      for (int c2 = 0; c2 < 2; ++c2) {  // 32-query chunk c = 2 half + c2
         uint32_t pw[16], dw[16];
 #pragma unroll
         for (int e = 0; e < 16; ++e) {
-          const int q0 = c * 32 + 2 * e;
-          const float2 l2 = *reinterpret_cast<const float2*>(lrow + q0);
-          const float2 dd = *reinterpret_cast<const float2*>(drow + q0);
-          float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -l2.x));
-          float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -l2.y));
+          const int ql = c2 * 32 + 2 * e;  // query within this half
+          const int q0 = half * 64 + ql;   // query within the tile
+          const float2 l2 = *reinterpret_cast<const float2*>(lrow + ql);
+          const float2 dd = *reinterpret_cast<const float2*>(drow + ql);
+          float p0 = ex2(fmaf(__uint_as_float(s[ql]), sl2, -l2.x));
+          float p1 = ex2(fmaf(__uint_as_float(s[ql + 1]), sl2, -l2.y));
           if (!key_ok) p0 = p1 = 0.0f;
           if (diag) {
             if (r > q0) p0 = 0.0f;
             if (r > q0 + 1) p1 = 0.0f;
           }
-          const float d0 = p0 * (__uint_as_float(g[2 * e]) - dd.x);
-          const float d1 = p1 * (__uint_as_float(g[2 * e + 1]) - dd.y);
+          const float d0 = p0 * (__uint_as_float(g[ql]) - dd.x);
+          const float d1 = p1 * (__uint_as_float(g[ql + 1]) - dd.y);
           pw[e] = pack_pair(p0, p1, DT);
           dw[e] = pack_pair(d0, d1, DT);
         }
-        // P^T over S^T columns [16c, 16c+16) and dS^T over dP^T's: those columns were read above
+        const int c = 2 * half + c2;
         tmem_st16(trow + COL_S + c * 16, pw);
         tmem_st16(trow + COL_DP + c * 16, dw);
-        // dS^T row r, queries [32c, 32c+32): box c/2, 16-byte chunks (c%2)*4 .. +3, 128-byte swizzle
-        const uint32_t base = ds_row + static_cast<uint32_t>((c >> 1) * BOX);
+        // dS^T row r, queries [32c, 32c+32): box `half`, 16-byte chunks c2*4 .. +3, 128-byte swizzle
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
-          const int cc = (c & 1) * 4 + u;
-          st_shared_v4(base + static_cast<uint32_t>((cc ^ sw) * 16), dw[4 * u], dw[4 * u + 1], dw[4 * u + 2],
+          const int cc = c2 * 4 + u;
+          st_shared_v4(ds_row + static_cast<uint32_t>((cc ^ sw) * 16), dw[4 * u], dw[4 * u + 1], dw[4 * u + 2],
                        dw[4 * u + 3]);
         }
       }
       tmem_wait_st();
       fence_proxy_async_smem();
     }
+    // the dQ staging slot written below was last read by the reduction issued two steps ago
+    if (tid == 0 && dq_groups > 0) bulk_wait_read_le1();
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
 
-    // gradients of this step, then (tensor pipe permitting) S^T and dP^T of the next one
+    // gradients of this step, then S^T and dP^T of the next one (the tensor pipe runs them in order)
     if (warp == 0) {
       bool w = true;
       if (elect_lane()) {
@@ -374,66 +410,70 @@ __global__ void __launch_bounds__(128, 1)
       tc_fence_after();
       // this slot's Q and dO are no longer read: fetch the tile two steps ahead into it
       if (tid == 0 && it + 2 < nit) load_q(it + 2);
-      // dQ tile (query row = tensor-memory lane) into the fp32 accumulator
-      const long long qi = static_cast<long long>(i0) + r;
+      // dQ tile rows (query = tensor-memory lane), feature columns [32 half, 32 half + 32), scaled,
+      // into the staging slot in the reduction's 128-byte-swizzled box layout
+      uint32_t o[32];
+      tmem_ld32(trow + COL_DQ + half * 32, o);
+      tmem_wait_ld();
+      reg_fence32(o);
+      const uint32_t dst = dq_row + static_cast<uint32_t>(slot * DQ_SLOT);
 #pragma unroll
-      for (int c = 0; c < HD / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(trow + COL_DQ + c * 32, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-        if (qi < p.N) {
-          float4* dst = reinterpret_cast<float4*>(p.dq_acc + (static_cast<long long>(bh) * p.N + qi) * HD + c * 32);
-#pragma unroll
-          for (int u = 0; u < 8; ++u)
-            atomicAdd(dst + u, make_float4(__uint_as_float(o[4 * u]) * p.scale, __uint_as_float(o[4 * u + 1]) * p.scale,
-                                           __uint_as_float(o[4 * u + 2]) * p.scale,
-                                           __uint_as_float(o[4 * u + 3]) * p.scale));
-        }
+      for (int u = 0; u < 8; ++u)
+        st_shared_v4(dst + static_cast<uint32_t>((u ^ sw) * 16), __float_as_uint(__uint_as_float(o[4 * u]) * p.scale),
+                     __float_as_uint(__uint_as_float(o[4 * u + 1]) * p.scale),
+                     __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
+                     __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
+      fence_proxy_async_smem();
+      if (tid < BT) {
+        sLse[(slot ^ 1) * BT + tid] = nl2;
+        sDd[(slot ^ 1) * BT + tid] = ndd;
       }
-      sLse[(slot ^ 1) * BT + tid] = nl2;
-      sDd[(slot ^ 1) * BT + tid] = ndd;
     }
     tc_fence_before();
     ok = __syncthreads_and(ok) != 0;
     if (!ok) break;
+    // add the staged dQ tile into the fp32 accumulator (rows past N are clipped by the tensor map)
+    if (tid == 0) {
+      const uint32_t src = smem_u32(sdQ) + static_cast<uint32_t>(slot * DQ_SLOT);
+      tma_reduce_add_3d(src, &tmDQ, 0, i0, bh);
+      tma_reduce_add_3d(src + BT * 128, &tmDQ, 32, i0, bh);
+      bulk_commit();
+      ++dq_groups;
+    }
   }
 
   if (ok) {
-    // dV_j and dK_j rows (key row = tensor-memory lane), written once
+    // dV_j and dK_j rows (key row = tensor-memory lane), feature columns [32 half, +32), written once
     tc_fence_after();
+    uint32_t a[32], g[32];
+    tmem_ld32(trow + COL_DV + half * 32, a);
+    tmem_ld32(trow + COL_DK + half * 32, g);
+    tmem_wait_ld();
+    reg_fence32(a);
+    reg_fence32(g);
+    if (key_ok) {
+      const long long row = static_cast<long long>(bh) * p.N + k0 + r;
+      uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + half * 32);
+      uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + half * 32);
 #pragma unroll
-    for (int c = 0; c < HD / 32; ++c) {
-      uint32_t a[32], g[32];
-      tmem_ld32(trow + COL_DV + c * 32, a);
-      tmem_ld32(trow + COL_DK + c * 32, g);
-      tmem_wait_ld();
-      reg_fence32(a);
-      reg_fence32(g);
-      if (key_ok) {
-        const long long row = static_cast<long long>(bh) * p.N + k0 + r;
-        uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + c * 32);
-        uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + c * 32);
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          uint4 wv, wk;
-          wv.x = pack_pair(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1]), DT);
-          wv.y = pack_pair(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]), DT);
-          wv.z = pack_pair(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]), DT);
-          wv.w = pack_pair(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]), DT);
-          wk.x = pack_pair(__uint_as_float(g[8 * u]) * p.scale, __uint_as_float(g[8 * u + 1]) * p.scale, DT);
-          wk.y = pack_pair(__uint_as_float(g[8 * u + 2]) * p.scale, __uint_as_float(g[8 * u + 3]) * p.scale, DT);
-          wk.z = pack_pair(__uint_as_float(g[8 * u + 4]) * p.scale, __uint_as_float(g[8 * u + 5]) * p.scale, DT);
-          wk.w = pack_pair(__uint_as_float(g[8 * u + 6]) * p.scale, __uint_as_float(g[8 * u + 7]) * p.scale, DT);
-          dv[u] = wv;
-          dk[u] = wk;
-        }
+      for (int u = 0; u < 4; ++u) {
+        uint4 wv, wk;
+        wv.x = pack_pair(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1]), DT);
+        wv.y = pack_pair(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]), DT);
+        wv.z = pack_pair(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]), DT);
+        wv.w = pack_pair(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]), DT);
+        wk.x = pack_pair(__uint_as_float(g[8 * u]) * p.scale, __uint_as_float(g[8 * u + 1]) * p.scale, DT);
+        wk.y = pack_pair(__uint_as_float(g[8 * u + 2]) * p.scale, __uint_as_float(g[8 * u + 3]) * p.scale, DT);
+        wk.z = pack_pair(__uint_as_float(g[8 * u + 4]) * p.scale, __uint_as_float(g[8 * u + 5]) * p.scale, DT);
+        wk.w = pack_pair(__uint_as_float(g[8 * u + 6]) * p.scale, __uint_as_float(g[8 * u + 7]) * p.scale, DT);
+        dv[u] = wv;
+        dk[u] = wk;
       }
     }
   }
 
-  // Drain: every issued MMA and TMA load completes before tensor memory is released and the CTA
-  // exits (bounded waits; on the normal path these phases are already complete).
+  // Drain: every issued MMA, TMA load and dQ reduction completes before tensor memory is released and
+  // the CTA exits (bounded waits; on the normal path these phases are already complete).
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
@@ -445,8 +485,9 @@ __global__ void __launch_bounds__(128, 1)
   }
   if (tid == 0) {
     mbar_wait_bounded(bar_kv, 0, tmo);
-    for (int s = 0; s < 2; ++s)
-      if (issued_q[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued_q[s] - 1) & 1), tmo);
+    for (int s2 = 0; s2 < 2; ++s2)
+      if (issued_q[s2] > 0) mbar_wait_bounded(&bar_q[s2], static_cast<uint32_t>((issued_q[s2] - 1) & 1), tmo);
+    bulk_wait_all();
   }
   __syncthreads();
   if (warp == 0) {
@@ -487,12 +528,12 @@ __global__ void __launch_bounds__(256) bwd_dq_kernel(const float4* acc, uint2* d
   }
 }
 
-// 4-D map over a [B,H,N,64] tensor: dims (64, N, H, B), box (64, 128, 1, 1), 128-byte swizzle, zero fill.
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
                                   CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
 
-int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N) {
+int encode_map(CUtensorMap* m, CUtensorMapDataType type, cuuint32_t rank, const void* base, const cuuint64_t* dims,
+               const cuuint64_t* strides, const cuuint32_t* box) {
   static EncodeTiledFn enc = nullptr;
   if (!enc) {
     void* ptr = nullptr;
@@ -506,13 +547,8 @@ int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int
     set_error("cuTensorMapEncodeTiled is not available from the driver");
     return CQSA_ERR_CUDA;
   }
-  const cuuint64_t es = 2;
-  cuuint64_t dims[4] = {HD, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
-  cuuint64_t strides[3] = {HD * es, static_cast<cuuint64_t>(N) * HD * es, static_cast<cuuint64_t>(H) * N * HD * es};
-  cuuint32_t box[4] = {64, BT, 1, 1};
-  cuuint32_t estr[4] = {1, 1, 1, 1};
-  CUresult r = enc(m, dtype == CQSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
-                   const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+  const cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = enc(m, type, rank, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
                    CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   if (r != CUDA_SUCCESS) {
     set_error("cuTensorMapEncodeTiled failed (CUresult %d)", static_cast<int>(r));
@@ -521,9 +557,28 @@ int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int
   return CQSA_OK;
 }
 
+// [B,H,N,64] 16-bit tensor: dims (64, N, H, B), box (64, 128, 1, 1), 128-byte swizzle, zero fill.
+int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N) {
+  const cuuint64_t es = 2;
+  const cuuint64_t dims[4] = {HD, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {HD * es, static_cast<cuuint64_t>(N) * HD * es,
+                                 static_cast<cuuint64_t>(H) * N * HD * es};
+  const cuuint32_t box[4] = {64, BT, 1, 1};
+  return encode_map(m, dtype == CQSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
+                    base, dims, strides, box);
+}
+
+// fp32 dQ accumulator [BH, N, 64]: dims (64, N, BH), box (32, 128, 1) (128-byte rows), 128-byte swizzle.
+int make_dq_map(CUtensorMap* m, float* base, int BH, int N) {
+  const cuuint64_t dims[3] = {HD, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {HD * 4, static_cast<cuuint64_t>(N) * HD * 4};
+  const cuuint32_t box[3] = {32, BT, 1};
+  return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box);
+}
+
 template <int DT, bool CAUSAL>
 int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
-                const BwdParams& p, cudaStream_t s) {
+                const CUtensorMap& mdq, const BwdParams& p, cudaStream_t s) {
   auto kern = attn_bwd_kernel<DT, CAUSAL>;
   static bool attr_done = false;
   if (!attr_done) {
@@ -532,7 +587,7 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     attr_done = true;
   }
   const long long grid = static_cast<long long>(p.n_tiles) * p.BH;
-  kern<<<static_cast<unsigned>(grid), 128, SMEM_BYTES, s>>>(mq, mk, mv, mg, p);
+  kern<<<static_cast<unsigned>(grid), NTHR, SMEM_BYTES, s>>>(mq, mk, mv, mg, mdq, p);
   return cuda_status(cudaGetLastError(), "attention backward kernel launch");
 }
 
@@ -554,11 +609,12 @@ int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream) {
   float* dq_acc = static_cast<float*>(a.workspace);
   float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
                                          ((static_cast<size_t>(rows) * HD * sizeof(float) + 255) & ~size_t(255)));
-  CUtensorMap mq, mk, mv, mg;
+  CUtensorMap mq, mk, mv, mg, mdq;
   int rc = make_bhnd_map(&mq, a.q, a.dtype, a.B, a.H, a.N);
   if (rc == CQSA_OK) rc = make_bhnd_map(&mk, a.k, a.dtype, a.B, a.H, a.N);
   if (rc == CQSA_OK) rc = make_bhnd_map(&mv, a.v, a.dtype, a.B, a.H, a.N);
   if (rc == CQSA_OK) rc = make_bhnd_map(&mg, a.dout, a.dtype, a.B, a.H, a.N);
+  if (rc == CQSA_OK) rc = make_dq_map(&mdq, dq_acc, a.B * a.H, a.N);
   if (rc != CQSA_OK) return rc;
 
   // D_i, then the zeroed dQ accumulator, the main kernel and the dQ conversion
@@ -590,9 +646,11 @@ int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream) {
   p.scale_log2 = a.scale * LOG2E;
   p.timeout_ns = timeout_ns();
   if (a.dtype == CQSA_BF16)
-    rc = a.causal ? launch_main<1, true>(mq, mk, mv, mg, p, stream) : launch_main<1, false>(mq, mk, mv, mg, p, stream);
+    rc = a.causal ? launch_main<1, true>(mq, mk, mv, mg, mdq, p, stream)
+                  : launch_main<1, false>(mq, mk, mv, mg, mdq, p, stream);
   else
-    rc = a.causal ? launch_main<0, true>(mq, mk, mv, mg, p, stream) : launch_main<0, false>(mq, mk, mv, mg, p, stream);
+    rc = a.causal ? launch_main<0, true>(mq, mk, mv, mg, mdq, p, stream)
+                  : launch_main<0, false>(mq, mk, mv, mg, mdq, p, stream);
   if (rc != CQSA_OK) return rc;
 
   const long long n4 = rows * HD / 4;
