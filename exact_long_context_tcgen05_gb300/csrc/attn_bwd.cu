@@ -47,17 +47,23 @@ constexpr uint32_t BOX = BT * HD * 2;           // one 128 x 64 tile of 16-bit e
 constexpr uint32_t OFF_K = 0, OFF_V = BOX, OFF_Q = 2 * BOX, OFF_G = 4 * BOX, OFF_DS = 6 * BOX;
 constexpr uint32_t OFF_DQ = 8 * BOX;            // dQ staging: 2 slots of 128 x 64 fp32
 constexpr uint32_t DQ_SLOT = BT * HD * 4;
-constexpr uint32_t OFF_ROW = OFF_DQ + 2 * DQ_SLOT;  // float lse2[2][128], dd[2][128]
+constexpr uint32_t OFF_ROW = OFF_DQ + 2 * DQ_SLOT;  // per elementwise warpgroup and slot: lse2[64], D[64]
 constexpr uint32_t OFF_BAR = OFF_ROW + 4 * BT * 4;
-constexpr int NBAR = 6;                         // kv, q[2], mma1, mma2, idle
+constexpr int NBAR = 14;
 constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
-// Tensor memory: S^T (P^T over its first 64 columns), dP^T (dS^T over its first 64), dV, dK, dQ.
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384;
+// Tensor memory: S^T, dP^T, the dV, dK and dQ accumulators, and P^T (16-bit pairs) as the A operand of dV.
+constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384, COL_PT = 448;
 constexpr uint32_t TMEM_COLS = 512;
 constexpr float LOG2E = 1.4426950408889634f;
-constexpr int NTHR = 256;  // eight warps: two per tensor-memory lane quarter, each on half the columns
+// Twelve warps: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
+// reductions (warp 2), one idle warp; warpgroups 1 and 2 = the elementwise step, each on half the query
+// columns (two warps per tensor-memory lane quarter). setmaxnreg moves registers from warpgroup 0 (96 per
+// thread) to the elementwise warpgroups (200): 128 * 96 + 256 * 200 <= 384 * 168.
+constexpr int NTHR = 384;
+constexpr int BWD_REGS_LOW = 96, BWD_REGS_HIGH = 200;
+static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= NTHR * 168, "register split exceeds the launch allocation");
 
-enum : int { kBwdTimeoutLoad = 1, kBwdTimeoutMMA = 3 };
+enum : int { kBwdTimeoutLoad = 1, kBwdTimeoutMMA = 3, kBwdTimeoutSoftmax = 4 };
 
 struct BwdParams {
   const float* lse;       // [BH, N] natural-log LSE of the forward
@@ -141,9 +147,19 @@ __device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMa
       : "memory");
 }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-// at most one bulk group still reading shared memory
-__device__ __forceinline__ void bulk_wait_read_le1() { asm volatile("cp.async.bulk.wait_group.read 1;" ::: "memory"); }
+__device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
+
+// AND of `v` over the 128 threads of elementwise warpgroup wg (named barrier wg + 1).
+__device__ __forceinline__ bool wg_bar_and(int wg, bool v) {
+  uint32_t r;
+  asm volatile(
+      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(v)), "r"(wg + 1)
+      : "memory");
+  return r != 0;
+}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -172,23 +188,25 @@ __device__ __forceinline__ void issue_t(uint32_t dcol, uint64_t a0, uint64_t b0,
   for (int ks = 1; ks < HD / 16; ++ks) mma_ss_imm<1>(dcol, a0 + ks * 2, b0 + ks * 2, idesc);
 }
 
-// dV += P^T dO, dK += dS^T Q (A from tensor memory, B MN-major) and dQ = dS K (A = dS^T staged
-// MN-major in shared memory, B = K MN-major): 8 key/query steps of 16.
+// dV += P^T dO (A = P^T from tensor memory), dK += dS^T Q (A = dS^T K-major in shared memory) and
+// dQ = dS K (A = the same dS^T tile read MN-major): 8 steps of 16 queries (dV, dK) or keys (dQ); the
+// B operands dO, Q and K are MN-major.
 template <int FIRST>
-__device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t dQm, uint64_t dS, uint64_t dK,
-                                            uint32_t idesc_g, uint32_t idesc_q) {
+__device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t dQm, uint64_t dS_k, uint64_t dS_mn,
+                                            uint64_t dK, uint32_t idesc_g, uint32_t idesc_q) {
 #pragma unroll
   for (int ks = 0; ks < BT / 16; ++ks) {
-    const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));  // 16 rows of 128 bytes
+    const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));                        // 16 rows of 128 bytes
+    const uint32_t koff = static_cast<uint32_t>((ks >> 2) * (BOX >> 4) + (ks & 3) * 2);  // 16 columns, K-major
     if (FIRST && ks == 0) {
-      mma_ts_imm<0>(tmem + COL_DV, tmem + COL_S + ks * 8, dG + off, idesc_g);
-      mma_ts_imm<0>(tmem + COL_DK, tmem + COL_DP + ks * 8, dQm + off, idesc_g);
+      mma_ts_imm<0>(tmem + COL_DV, tmem + COL_PT + ks * 8, dG + off, idesc_g);
+      mma_ss_imm<0>(tmem + COL_DK, dS_k + koff, dQm + off, idesc_g);
     } else {
-      mma_ts_imm<1>(tmem + COL_DV, tmem + COL_S + ks * 8, dG + off, idesc_g);
-      mma_ts_imm<1>(tmem + COL_DK, tmem + COL_DP + ks * 8, dQm + off, idesc_g);
+      mma_ts_imm<1>(tmem + COL_DV, tmem + COL_PT + ks * 8, dG + off, idesc_g);
+      mma_ss_imm<1>(tmem + COL_DK, dS_k + koff, dQm + off, idesc_g);
     }
-    if (ks == 0) mma_ss_imm<0>(tmem + COL_DQ, dS + off, dK + off, idesc_q);
-    else mma_ss_imm<1>(tmem + COL_DQ, dS + off, dK + off, idesc_q);
+    if (ks == 0) mma_ss_imm<0>(tmem + COL_DQ, dS_mn + off, dK + off, idesc_q);
+    else mma_ss_imm<1>(tmem + COL_DQ, dS_mn + off, dK + off, idesc_q);
   }
 }
 
@@ -201,24 +219,26 @@ __global__ void __launch_bounds__(NTHR, 1)
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   uint8_t* sK = sm + OFF_K;
   uint8_t* sV = sm + OFF_V;
-  uint8_t* sQ = sm + OFF_Q;  // [2][BOX]
-  uint8_t* sG = sm + OFF_G;  // [2][BOX] (dO)
-  uint8_t* sdS = sm + OFF_DS;
-  uint8_t* sdQ = sm + OFF_DQ;  // [2][128 x 64 fp32], two 32-float boxes each, 128-byte swizzle
-  float* sLse = reinterpret_cast<float*>(sm + OFF_ROW);  // [2][128], base-2 LSE
-  float* sDd = sLse + 2 * BT;                            // [2][128], D_i
+  uint8_t* sQ = sm + OFF_Q;    // [2][BOX]
+  uint8_t* sG = sm + OFF_G;    // [2][BOX] (dO)
+  uint8_t* sdS = sm + OFF_DS;  // dS^T [128 keys][128 queries], two 64-query boxes
+  uint8_t* sdQ = sm + OFF_DQ;  // [2][128 x 64 fp32], two 32-float boxes each
+  float* sRow = reinterpret_cast<float*>(sm + OFF_ROW);  // [wg 2][slot 2][lse2 64 | D 64]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
-  uint64_t* bar_kv = bars;
-  uint64_t* bar_q = bars + 1;  // [2]
-  uint64_t* bar_m1 = bars + 3;
-  uint64_t* bar_m2 = bars + 4;
-  uint64_t* bar_idle = bars + 5;
+  uint64_t* bar_kv = bars + 0;
+  uint64_t* bar_q = bars + 1;       // [2] Q/dO slot loaded
+  uint64_t* bar_qfree = bars + 3;   // [2] Q/dO slot read by every MMA (commit)
+  uint64_t* bar_m1 = bars + 5;      // S^T, dP^T ready (commit)
+  uint64_t* bar_m2 = bars + 6;      // dV, dK, dQ products done (commit)
+  uint64_t* bar_sfree = bars + 7;   // S^T, dP^T read into registers (256 elementwise threads)
+  uint64_t* bar_ready = bars + 8;   // P^T and dS^T written, previous dQ read out (256 threads)
+  uint64_t* bar_staged = bars + 9;  // [2] dQ staging slot written (256 threads)
+  uint64_t* bar_dqfree = bars + 11; // [2] dQ staging slot read by its reduction
+  uint64_t* bar_idle = bars + 13;   // every MMA done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int quarter = warp & 3;  // tensor-memory lane quarter of this warp
-  const int half = warp >> 2;    // query columns [64 half, 64 half + 64) / feature columns [32 half, +32)
   const int bh = blockIdx.x % p.BH, jt = blockIdx.x / p.BH;
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = jt * BT;
@@ -227,193 +247,167 @@ __global__ void __launch_bounds__(NTHR, 1)
   const unsigned long long tmo = p.timeout_ns;
 
   if (tid == 0) {
-    for (int i = 0; i < NBAR; ++i) mbar_init(&bars[i], 1);
+    mbar_init(bar_kv, 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(&bar_q[s], 1);
+      mbar_init(&bar_qfree[s], 1);
+      mbar_init(&bar_staged[s], 256);
+      mbar_init(&bar_dqfree[s], 1);
+    }
+    mbar_init(bar_m1, 1);
+    mbar_init(bar_m2, 1);
+    mbar_init(bar_sfree, 256);
+    mbar_init(bar_ready, 256);
+    mbar_init(bar_idle, 1);
     *abort_flag = 0;
     fence_mbar_init();
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-    prefetch_tensormap(&tmG);
-    prefetch_tensormap(&tmDQ);
   }
-  if (warp == 0) {
+  if (warp == 1) {
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
-  }
-  // row values (base-2 LSE, D) of a query tile, one thread per row (threads < 128); fetched one step ahead
-  auto row_vals = [&](int it, float& l2, float& dd) {
-    const long long i = static_cast<long long>(it0 + it) * BT + tid;
-    if (tid < BT && it < nit && i < p.N) {
-      l2 = p.lse[static_cast<long long>(bh) * p.N + i] * LOG2E;
-      dd = p.dvec[static_cast<long long>(bh) * p.N + i];
-    } else {
-      l2 = INFINITY;  // P = 0 for query rows past the end
-      dd = 0.0f;
-    }
-  };
-  {
-    float l2, dd;
-    row_vals(0, l2, dd);
-    if (tid < BT) {
-      sLse[tid] = l2;
-      sDd[tid] = dd;
-    }
   }
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  int issued_q[2] = {0, 0};  // loads issued per slot (thread 0)
-  auto load_q = [&](int it) {
-    const int slot = it & 1;
-    const int i0 = (it0 + it) * BT;
-    mbar_arrive_expect_tx(&bar_q[slot], 2 * BOX);
-    tma_load_4d(sQ + slot * BOX, &tmQ, &bar_q[slot], 0, i0, h, b);
-    tma_load_4d(sG + slot * BOX, &tmG, &bar_q[slot], 0, i0, h, b);
-    ++issued_q[slot];
-  };
-  if (tid == 0) {
-    mbar_arrive_expect_tx(bar_kv, 2 * BOX);
-    tma_load_4d(sK, &tmK, bar_kv, 0, k0, h, b);
-    tma_load_4d(sV, &tmV, bar_kv, 0, k0, h, b);
-    load_q(0);
-    if (nit > 1) load_q(1);
-  }
-
-  constexpr uint32_t IDESC_T = idesc_f16(DT, 0, 128, 128);              // S^T, dP^T
-  constexpr uint32_t IDESC_G = idesc_f16(DT, 1, 128, HD);               // dV, dK
-  constexpr uint32_t IDESC_Q = idesc_f16(DT, 1, 128, HD) | (1u << 15);  // dQ: A MN-major too
-  const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024);
-  const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);
-  const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 1024, 1024);
-  const uint64_t dS_mn = smem_desc_sw128(smem_u32(sdS), BOX, 1024);  // two 64-query boxes along M
-  auto dQ_k = [&](int slot) { return smem_desc_sw128(smem_u32(sQ + slot * BOX), 16, 1024); };
-  auto dG_k = [&](int slot) { return smem_desc_sw128(smem_u32(sG + slot * BOX), 16, 1024); };
-  auto dQ_mn = [&](int slot) { return smem_desc_sw128(smem_u32(sQ + slot * BOX), 1024, 1024); };
-  auto dG_mn = [&](int slot) { return smem_desc_sw128(smem_u32(sG + slot * BOX), 1024, 1024); };
-
-  bool ok = true;
-  // MMA warp (warp 0, one elected lane): S^T(it) and dP^T(it)
-  auto issue_m1 = [&](int it) -> bool {
-    bool w = true;
-    if (elect_lane()) {
-      const int slot = it & 1;
-      if (it == 0) w = wait_abort(bar_kv, 0, tmo, abort_flag, kBwdTimeoutLoad, 1);
-      if (w) w = wait_abort(&bar_q[slot], static_cast<uint32_t>((it >> 1) & 1), tmo, abort_flag, kBwdTimeoutLoad, 2);
-      if (w) {
-        tc_fence_after();
-        issue_t(tmem + COL_S, dK_k, dQ_k(slot), IDESC_T);
-        issue_t(tmem + COL_DP, dV_k, dG_k(slot), IDESC_T);
-        tc_commit(bar_m1);
+  if (warp < 4) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_REGS_LOW));
+    if (warp == 0 && lane == 0) {
+      // ---------------------------------------------------------------- TMA producer
+      prefetch_tensormap(&tmQ);
+      prefetch_tensormap(&tmK);
+      prefetch_tensormap(&tmV);
+      prefetch_tensormap(&tmG);
+      int issued[2] = {0, 0};
+      auto load_q = [&](int it) {
+        const int slot = it & 1;
+        mbar_arrive_expect_tx(&bar_q[slot], 2 * BOX);
+        tma_load_4d(sQ + slot * BOX, &tmQ, &bar_q[slot], 0, (it0 + it) * BT, h, b);
+        tma_load_4d(sG + slot * BOX, &tmG, &bar_q[slot], 0, (it0 + it) * BT, h, b);
+        ++issued[slot];
+      };
+      mbar_arrive_expect_tx(bar_kv, 2 * BOX);
+      tma_load_4d(sK, &tmK, bar_kv, 0, k0, h, b);
+      tma_load_4d(sV, &tmV, bar_kv, 0, k0, h, b);
+      load_q(0);
+      if (nit > 1) load_q(1);
+      for (int it = 0; it + 2 < nit; ++it) {
+        // slot it&1 is free once every MMA of step it has read it
+        if (!wait_abort(&bar_qfree[it & 1], static_cast<uint32_t>((it >> 1) & 1), tmo, abort_flag, kBwdTimeoutLoad, 5))
+          break;
+        load_q(it + 2);
       }
-    }
-    __syncwarp();
-    return __all_sync(0xffffffffu, w);
-  };
-  if (warp == 0) ok = issue_m1(0);
-
-  const int r = quarter * 32 + lane;  // key row (tensor-memory lane) in the elementwise step, query row in the dQ step
-  const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-  const bool key_ok = k0 + r < p.N;
-  const float sl2 = p.scale_log2;
-  const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(half * BOX + r * 128);
-  const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>(half * (BT * 128) + r * 128);
-  const int sw = r & 7;
-  int dq_groups = 0;  // bulk reductions issued (thread 0)
-
-  for (int it = 0; it < nit; ++it) {
-    const int slot = it & 1;
-    const int i0 = (it0 + it) * BT;
-    float nl2, ndd;
-    row_vals(it + 1, nl2, ndd);  // next tile's row values, consumed at the end of this step
-    if (ok) ok = wait_abort(bar_m1, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 3);
-    ok = __all_sync(0xffffffffu, ok);  // the warp-collective tensor-memory accesses below run warp-uniformly
-    // S^T and dP^T of this warp's 64 query columns, all read before any P^T / dS^T is written over them
-    uint32_t s[64], g[64];
-    if (ok) {
-      tc_fence_after();
-      tmem_ld32(trow + COL_S + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      tmem_ld32(trow + COL_S + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      tmem_ld32(trow + COL_DP + half * 64, *reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-      tmem_ld32(trow + COL_DP + half * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&g[32]));
-      tmem_wait_ld();
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[0]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&s[32]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&g[0]));
-      reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&g[32]));
-    }
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    {
-      const bool diag = CAUSAL && (i0 == k0);
-      const float* lrow = sLse + slot * BT + half * 64;
-      const float* drow = sDd + slot * BT + half * 64;
-#pragma unroll
-      for (int c2 = 0; c2 < 2; ++c2) {  // 32-query chunk c = 2 half + c2
-        uint32_t pw[16], dw[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int ql = c2 * 32 + 2 * e;  // query within this half
-          const int q0 = half * 64 + ql;   // query within the tile
-          const float2 l2 = *reinterpret_cast<const float2*>(lrow + ql);
-          const float2 dd = *reinterpret_cast<const float2*>(drow + ql);
-          float p0 = ex2(fmaf(__uint_as_float(s[ql]), sl2, -l2.x));
-          float p1 = ex2(fmaf(__uint_as_float(s[ql + 1]), sl2, -l2.y));
-          if (!key_ok) p0 = p1 = 0.0f;
-          if (diag) {
-            if (r > q0) p0 = 0.0f;
-            if (r > q0 + 1) p1 = 0.0f;
+      mbar_wait_bounded(bar_kv, 0, tmo);
+      for (int s = 0; s < 2; ++s)
+        if (issued[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued[s] - 1) & 1), tmo);
+    } else if (warp == 1) {
+      // ---------------------------------------------------------------- MMA issuer
+      constexpr uint32_t IDESC_T = idesc_f16(DT, 0, 128, 128);              // S^T, dP^T
+      constexpr uint32_t IDESC_V = idesc_f16(DT, 1, 128, HD);               // dV: A (P^T) in TMEM, B MN-major
+      constexpr uint32_t IDESC_Q = idesc_f16(DT, 1, 128, HD) | (1u << 15);  // dQ: A (dS) MN-major
+      const bool leader = elect_lane();
+      // descriptors, prepared by the whole warp before any issue
+      const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 1024, 1024);
+      const uint64_t dS_k = smem_desc_sw128(smem_u32(sdS), 16, 1024);     // dS^T as K-major A (M = keys)
+      const uint64_t dS_mn = smem_desc_sw128(smem_u32(sdS), BOX, 1024);   // dS^T as MN-major A (M = queries)
+      const uint64_t dQ0_k = smem_desc_sw128(smem_u32(sQ), 16, 1024);
+      const uint64_t dG0_k = smem_desc_sw128(smem_u32(sG), 16, 1024);
+      const uint64_t dQ0_mn = smem_desc_sw128(smem_u32(sQ), 1024, 1024);
+      const uint64_t dG0_mn = smem_desc_sw128(smem_u32(sG), 1024, 1024);
+      constexpr uint32_t SLOT16 = BOX >> 4;  // one slot in descriptor address units
+      auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
+        const bool w = wait_abort(bar, parity, tmo, abort_flag, code, where);
+        return __all_sync(0xffffffffu, w);
+      };
+      auto issue_m1 = [&](int it) {
+        const uint32_t so = static_cast<uint32_t>(it & 1) * SLOT16;
+        tc_fence_after();
+        if (leader) {
+          issue_t(tmem + COL_S, dK_k, dQ0_k + so, IDESC_T);
+          issue_t(tmem + COL_DP, dV_k, dG0_k + so, IDESC_T);
+          tc_commit(bar_m1);
+        }
+        __syncwarp();
+      };
+      bool ok = wait_all(bar_kv, 0, kBwdTimeoutLoad, 1);
+      if (ok) ok = wait_all(&bar_q[0], 0, kBwdTimeoutLoad, 2);
+      if (ok) issue_m1(0);
+      for (int it = 0; ok && it < nit; ++it) {
+        const int slot = it & 1;
+        if (it + 1 < nit) {
+          // S^T / dP^T of step it are in registers: the next step's products may overwrite them
+          ok = wait_all(bar_sfree, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 6);
+          if (ok) ok = wait_all(&bar_q[(it + 1) & 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), kBwdTimeoutLoad, 2);
+          if (ok) issue_m1(it + 1);
+        }
+        if (ok) ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
+        if (ok) {
+          const uint32_t so = static_cast<uint32_t>(slot) * SLOT16;
+          tc_fence_after();
+          if (leader) {
+            if (it == 0) issue_grads<1>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+            else issue_grads<0>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+            tc_commit(bar_m2);
+            tc_commit(&bar_qfree[slot]);
           }
-          const float d0 = p0 * (__uint_as_float(g[ql]) - dd.x);
-          const float d1 = p1 * (__uint_as_float(g[ql + 1]) - dd.y);
-          pw[e] = pack_pair(p0, p1, DT);
-          dw[e] = pack_pair(d0, d1, DT);
-        }
-        const int c = 2 * half + c2;
-        tmem_st16(trow + COL_S + c * 16, pw);
-        tmem_st16(trow + COL_DP + c * 16, dw);
-        // dS^T row r, queries [32c, 32c+32): box `half`, 16-byte chunks c2*4 .. +3, 128-byte swizzle
-#pragma unroll
-        for (int u = 0; u < 4; ++u) {
-          const int cc = c2 * 4 + u;
-          st_shared_v4(ds_row + static_cast<uint32_t>((cc ^ sw) * 16), dw[4 * u], dw[4 * u + 1], dw[4 * u + 2],
-                       dw[4 * u + 3]);
+          __syncwarp();
         }
       }
-      tmem_wait_st();
-      fence_proxy_async_smem();
-    }
-    // the dQ staging slot written below was last read by the reduction issued two steps ago
-    if (tid == 0 && dq_groups > 0) bulk_wait_read_le1();
-    tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-
-    // gradients of this step, then S^T and dP^T of the next one (the tensor pipe runs them in order)
-    if (warp == 0) {
-      bool w = true;
-      if (elect_lane()) {
-        tc_fence_after();
-        if (it == 0)
-          issue_grads<1>(tmem, dG_mn(slot), dQ_mn(slot), dS_mn, dK_mn, IDESC_G, IDESC_Q);
-        else
-          issue_grads<0>(tmem, dG_mn(slot), dQ_mn(slot), dS_mn, dK_mn, IDESC_G, IDESC_Q);
-        tc_commit(bar_m2);
-      }
+      if (leader) tc_commit(bar_idle);
       __syncwarp();
-      if (it + 1 < nit) w = issue_m1(it + 1);
-      ok = w;
+      mbar_wait_bounded(bar_idle, 0, tmo);
+    } else if (warp == 2 && lane == 0) {
+      // ---------------------------------------------------------------- dQ reductions
+      for (int it = 0; it < nit; ++it) {
+        const int slot = it & 1;
+        if (!wait_abort(&bar_staged[slot], static_cast<uint32_t>((it >> 1) & 1), tmo, abort_flag, kBwdTimeoutSoftmax, 8))
+          break;
+        const uint32_t src = smem_u32(sdQ) + static_cast<uint32_t>(slot * DQ_SLOT);
+        tma_reduce_add_3d(src, &tmDQ, 0, (it0 + it) * BT, bh);
+        tma_reduce_add_3d(src + BT * 128, &tmDQ, 32, (it0 + it) * BT, bh);
+        bulk_commit();
+        bulk_wait_read_all();
+        mbar_arrive(&bar_dqfree[slot]);
+      }
+      bulk_wait_all();
     }
-    if (ok) ok = wait_abort(bar_m2, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
-    ok = __all_sync(0xffffffffu, ok);
-    if (ok) {
-      tc_fence_after();
-      // this slot's Q and dO are no longer read: fetch the tile two steps ahead into it
-      if (tid == 0 && it + 2 < nit) load_q(it + 2);
-      // dQ tile rows (query = tensor-memory lane), feature columns [32 half, 32 half + 32), scaled,
-      // into the staging slot in the reduction's 128-byte-swizzled box layout
+  } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BWD_REGS_HIGH));
+    // ------------------------------------------------------------------ elementwise warpgroups
+    // warpgroup wg owns query columns [64 wg, 64 wg + 64) of each step, and feature columns
+    // [32 wg, 32 wg + 32) of the dQ, dK and dV read-outs; its warp q owns tensor-memory lanes [32q, 32q + 32)
+    const int wg = (warp >> 2) - 1;
+    const int quarter = warp & 3;
+    const int t128 = tid & 127;
+    const int r = quarter * 32 + lane;  // key row (tensor-memory lane) of P^T / dS^T; query row of dQ
+    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
+    const bool key_ok = k0 + r < p.N;
+    const float sl2 = p.scale_log2;
+    const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(wg * BOX + r * 128);
+    const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>(wg * (BT * 128) + r * 128);
+    const int sw = r & 7;
+    float* rows = sRow + wg * 256;  // [slot][lse2 64 | D 64]
+    // one value per thread: lse2 (t128 < 64) or D (t128 >= 64) of query 64 wg + (t128 & 63) of step it
+    auto row_val = [&](int it) -> float {
+      const long long i = static_cast<long long>(it0 + it) * BT + wg * 64 + (t128 & 63);
+      if (it >= nit || i >= p.N) return t128 < 64 ? INFINITY : 0.0f;  // P = 0 for rows past the end
+      const long long at = static_cast<long long>(bh) * p.N + i;
+      return t128 < 64 ? p.lse[at] * LOG2E : p.dvec[at];
+    };
+    rows[t128] = row_val(0);
+    bool ok = wg_bar_and(wg, true);
+    // dQ of step it (after its products completed): scaled rows into the staging slot, then hand-off
+    auto stage_dq = [&](int it) -> bool {
+      const int slot = it & 1;
+      bool w = true;
+      if (it >= 2) w = wait_abort(&bar_dqfree[slot], static_cast<uint32_t>(((it - 2) >> 1) & 1), tmo, abort_flag,
+                                  kBwdTimeoutSoftmax, 9);
+      w = __all_sync(0xffffffffu, w);
+      if (!w) return false;
       uint32_t o[32];
-      tmem_ld32(trow + COL_DQ + half * 32, o);
+      tmem_ld32(trow + COL_DQ + wg * 32, o);
       tmem_wait_ld();
       reg_fence32(o);
       const uint32_t dst = dq_row + static_cast<uint32_t>(slot * DQ_SLOT);
@@ -424,73 +418,120 @@ __global__ void __launch_bounds__(NTHR, 1)
                      __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
                      __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
       fence_proxy_async_smem();
-      if (tid < BT) {
-        sLse[(slot ^ 1) * BT + tid] = nl2;
-        sDd[(slot ^ 1) * BT + tid] = ndd;
-      }
-    }
-    tc_fence_before();
-    ok = __syncthreads_and(ok) != 0;
-    if (!ok) break;
-    // add the staged dQ tile into the fp32 accumulator (rows past N are clipped by the tensor map)
-    if (tid == 0) {
-      const uint32_t src = smem_u32(sdQ) + static_cast<uint32_t>(slot * DQ_SLOT);
-      tma_reduce_add_3d(src, &tmDQ, 0, i0, bh);
-      tma_reduce_add_3d(src + BT * 128, &tmDQ, 32, i0, bh);
-      bulk_commit();
-      ++dq_groups;
-    }
-  }
+      mbar_arrive(&bar_staged[slot]);
+      return true;
+    };
 
-  if (ok) {
-    // dV_j and dK_j rows (key row = tensor-memory lane), feature columns [32 half, +32), written once
-    tc_fence_after();
-    uint32_t a[32], g[32];
-    tmem_ld32(trow + COL_DV + half * 32, a);
-    tmem_ld32(trow + COL_DK + half * 32, g);
-    tmem_wait_ld();
-    reg_fence32(a);
-    reg_fence32(g);
-    if (key_ok) {
-      const long long row = static_cast<long long>(bh) * p.N + k0 + r;
-      uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + half * 32);
-      uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + half * 32);
+    for (int it = 0; ok && it < nit; ++it) {
+      const int slot = it & 1;
+      const float nrow = row_val(it + 1);  // next step's row value, stored at the end of this one
+      ok = wait_abort(bar_m1, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 3);
+      ok = __all_sync(0xffffffffu, ok);
+      uint32_t pw[32], dw[32];
+      if (ok) {
+        tc_fence_after();
+        const bool diag = CAUSAL && ((it0 + it) * BT == k0);
+        const float* lrow = rows + slot * 128;
+        const float* drow = lrow + 64;
+        // two 32-query chunks: S^T and dP^T columns in registers, then P and dS packed to 16-bit pairs;
+        // S^T / dP^T are released to the next step's products once both chunks are read
 #pragma unroll
-      for (int u = 0; u < 4; ++u) {
-        uint4 wv, wk;
-        wv.x = pack_pair(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1]), DT);
-        wv.y = pack_pair(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]), DT);
-        wv.z = pack_pair(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]), DT);
-        wv.w = pack_pair(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]), DT);
-        wk.x = pack_pair(__uint_as_float(g[8 * u]) * p.scale, __uint_as_float(g[8 * u + 1]) * p.scale, DT);
-        wk.y = pack_pair(__uint_as_float(g[8 * u + 2]) * p.scale, __uint_as_float(g[8 * u + 3]) * p.scale, DT);
-        wk.z = pack_pair(__uint_as_float(g[8 * u + 4]) * p.scale, __uint_as_float(g[8 * u + 5]) * p.scale, DT);
-        wk.w = pack_pair(__uint_as_float(g[8 * u + 6]) * p.scale, __uint_as_float(g[8 * u + 7]) * p.scale, DT);
-        dv[u] = wv;
-        dk[u] = wk;
+        for (int c2 = 0; c2 < 2; ++c2) {
+          uint32_t s[32], g[32];
+          tmem_ld32(trow + COL_S + wg * 64 + c2 * 32, s);
+          tmem_ld32(trow + COL_DP + wg * 64 + c2 * 32, g);
+          tmem_wait_ld();
+          reg_fence32(s);
+          reg_fence32(g);
+          if (c2 == 1) {
+            tc_fence_before();
+            mbar_arrive(bar_sfree);
+          }
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const int ql = c2 * 32 + 2 * e;  // query within this warpgroup's 64
+            const int q0 = wg * 64 + ql;     // query within the tile
+            const float2 l2 = *reinterpret_cast<const float2*>(lrow + ql);
+            const float2 dd = *reinterpret_cast<const float2*>(drow + ql);
+            float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -l2.x));
+            float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -l2.y));
+            if (!key_ok) p0 = p1 = 0.0f;
+            if (diag) {
+              if (r > q0) p0 = 0.0f;
+              if (r > q0 + 1) p1 = 0.0f;
+            }
+            pw[c2 * 16 + e] = pack_pair(p0, p1, DT);
+            dw[c2 * 16 + e] = pack_pair(p0 * (__uint_as_float(g[2 * e]) - dd.x),
+                                        p1 * (__uint_as_float(g[2 * e + 1]) - dd.y), DT);
+          }
+        }
+      }
+      // P^T and dS^T of the previous step are consumed once its products are done; its dQ is then read out
+      if (ok && it > 0) {
+        ok = wait_abort(bar_m2, static_cast<uint32_t>((it - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
+        ok = __all_sync(0xffffffffu, ok);
+        if (ok) {
+          tc_fence_after();
+          ok = stage_dq(it - 1);
+        }
+      }
+      if (ok) {
+        tmem_st16(trow + COL_PT + wg * 32, &pw[0]);
+        tmem_st16(trow + COL_PT + wg * 32 + 16, &pw[16]);
+        // dS^T row r, queries [64 wg, 64 wg + 64): box wg, all eight 16-byte chunks, 128-byte swizzle
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(ds_row + static_cast<uint32_t>((u ^ sw) * 16), dw[4 * u], dw[4 * u + 1], dw[4 * u + 2],
+                       dw[4 * u + 3]);
+        tmem_wait_st();
+        fence_proxy_async_smem();
+        tc_fence_before();
+        mbar_arrive(bar_ready);
+        rows[(slot ^ 1) * 128 + t128] = nrow;
+      }
+      ok = wg_bar_and(wg, ok);
+    }
+    if (ok) {
+      // last step: dQ, then dV_j and dK_j rows (key row = tensor-memory lane), written once
+      ok = wait_abort(bar_m2, static_cast<uint32_t>((nit - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
+      ok = __all_sync(0xffffffffu, ok);
+      if (ok) {
+        tc_fence_after();
+        ok = stage_dq(nit - 1);
+      }
+    }
+    if (ok) {
+      uint32_t a[32], g[32];
+      tmem_ld32(trow + COL_DV + wg * 32, a);
+      tmem_ld32(trow + COL_DK + wg * 32, g);
+      tmem_wait_ld();
+      reg_fence32(a);
+      reg_fence32(g);
+      if (key_ok) {
+        const long long row = static_cast<long long>(bh) * p.N + k0 + r;
+        uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + wg * 32);
+        uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + wg * 32);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          uint4 wv, wk;
+          wv.x = pack_pair(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1]), DT);
+          wv.y = pack_pair(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]), DT);
+          wv.z = pack_pair(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]), DT);
+          wv.w = pack_pair(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]), DT);
+          wk.x = pack_pair(__uint_as_float(g[8 * u]) * p.scale, __uint_as_float(g[8 * u + 1]) * p.scale, DT);
+          wk.y = pack_pair(__uint_as_float(g[8 * u + 2]) * p.scale, __uint_as_float(g[8 * u + 3]) * p.scale, DT);
+          wk.z = pack_pair(__uint_as_float(g[8 * u + 4]) * p.scale, __uint_as_float(g[8 * u + 5]) * p.scale, DT);
+          wk.w = pack_pair(__uint_as_float(g[8 * u + 6]) * p.scale, __uint_as_float(g[8 * u + 7]) * p.scale, DT);
+          dv[u] = wv;
+          dk[u] = wk;
+        }
       }
     }
   }
-
-  // Drain: every issued MMA, TMA load and dQ reduction completes before tensor memory is released and
-  // the CTA exits (bounded waits; on the normal path these phases are already complete).
+  // teardown: every role has drained its own asynchronous work (bounded waits) before this barrier
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
-    if (elect_lane()) {
-      tc_commit(bar_idle);
-      mbar_wait_bounded(bar_idle, 0, tmo);
-    }
-    __syncwarp();
-  }
-  if (tid == 0) {
-    mbar_wait_bounded(bar_kv, 0, tmo);
-    for (int s2 = 0; s2 < 2; ++s2)
-      if (issued_q[s2] > 0) mbar_wait_bounded(&bar_q[s2], static_cast<uint32_t>((issued_q[s2] - 1) & 1), tmo);
-    bulk_wait_all();
-  }
-  __syncthreads();
-  if (warp == 0) {
+  if (warp == 1) {
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -582,7 +623,16 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   auto kern = attn_bwd_kernel<DT, CAUSAL>;
   static bool attr_done = false;
   if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
+    // setmaxnreg.inc waits until its registers are free: refuse to launch unless the launch holds the split
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(attention backward)");
+    if (fa.numRegs * NTHR < 128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH) {
+      set_error("attention backward kernel built with %d registers/thread; the register split needs %d", fa.numRegs,
+                (128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH + NTHR - 1) / NTHR);
+      return CQSA_ERR_UNSUPPORTED;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention backward smem)");
     attr_done = true;
   }
