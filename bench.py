@@ -499,14 +499,14 @@ def measure_bf16(cq, dev, reps):
                          "peak_source": src, "note": "algorithmic FLOP; the P hi/lo split issues 1.5x the MMA work"}}
 
 
-def measure_bwd(cq, dev, reps):
-    """Attention backward on the headline shape (B=1 H=8 N=32768 d=64 fp16 causal): the whole
+def measure_bwd(cq, dev, reps, N=32768, H=8):
+    """Attention backward, by default on the headline shape (B=1 H=8 N=32768 d=64 fp16 causal): the whole
     cqsa_attn_bwd call (D = rowsum(dO * O), zeroing the dQ accumulator, the tcgen05 kernel, the dQ
     conversion) timed with CUDA events, inputs and forward outputs resident. Algorithmic FLOP: five
     products of 2*N*N*d per head (S, dP, dV, dK, dQ), halved by the causal mask = 2.5x the forward."""
     import torch
     import synthetic as syn
-    B, H, N, D = 1, 8, 32768, 64
+    B, D = 1, 64
     qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
     gn = syn.normal(B, H, N, D, seed=0, tensor_id=syn.TID_DO)
     q, k, v, g = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn, gn))
@@ -531,7 +531,7 @@ def measure_bwd(cq, dev, reps):
     flop = 2.5 * 4.0 * B * H * N * N * D / 2
     tf = flop / (statistics.median(ms) / 1e3) / 1e12
     peak, src, _ = _peaks()
-    return {"measure": "bwd", "workload": "B=1 H=8 N=32768 d=64 fp16 causal backward (dq, dk, dv)",
+    return {"measure": "bwd", "workload": f"B=1 H={H} N={N} d=64 fp16 causal backward (dq, dk, dv)",
             "ms_per_step": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                          "peak_source": src, "note": "algorithmic FLOP of the five products, whole call"}}
@@ -556,7 +556,7 @@ def run_measure(args):
     elif args.measure == "quorum":
         line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel)
     elif args.measure == "bwd":
-        line = measure_bwd(cq, dev, reps)
+        line = measure_bwd(cq, dev, reps, N=args.bwd_n, H=args.bwd_h)
     else:
         line = measure_bf16(cq, dev, reps)
     rc, code, _ = cq.cqsa_device_error()
@@ -576,6 +576,8 @@ def main():
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream / quorum")
     ap.add_argument("--acc-on-host", action="store_true", help="--measure quorum with the host accumulator")
     ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")
+    ap.add_argument("--bwd-n", type=int, default=32768, help="--measure bwd: tokens")
+    ap.add_argument("--bwd-h", type=int, default=8, help="--measure bwd: heads")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
