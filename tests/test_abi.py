@@ -122,3 +122,21 @@ def test_stream_validation(cq):
     assert f(layout=5) == cq.CQSA_ERR_UNSUPPORTED
     assert f(q=None) == cq.CQSA_ERR_INVALID
     assert f(N=0) == cq.CQSA_ERR_INVALID
+
+
+def test_bwd_validation(cq):
+    """The backward validates before launching: head dim, workspace size, pointers, alignment."""
+    L = cq.lib
+    need = cq.cqsa_attn_bwd_workspace_size(1, 2, 256, 64)
+    assert need == ((2 * 256 * 64 * 4 + 255) // 256) * 256 + 2 * 256 * 4
+    assert cq.cqsa_attn_bwd_workspace_size(0, 2, 256, 64) == 0
+
+    def call(d=64, ws_bytes=need, q=FAKE, lse=FAKE, dtype=cq.CQSA_F16):
+        return L.cqsa_attn_bwd(q, FAKE, FAKE, FAKE, FAKE, lse, FAKE, FAKE, FAKE, FAKE, ws_bytes, 1, 2, 256, d, 1, 0.0,
+                               dtype, None)
+    assert call(d=128) == cq.CQSA_ERR_UNSUPPORTED and "head dim 64" in cq.last_error()
+    assert call(ws_bytes=need - 16) == cq.CQSA_ERR_INVALID and "workspace" in cq.last_error()
+    assert call(q=None) == cq.CQSA_ERR_INVALID
+    assert call(q=FAKE + 8) == cq.CQSA_ERR_INVALID and "aligned" in cq.last_error()
+    assert call(lse=FAKE + 2) == cq.CQSA_ERR_INVALID
+    assert call(dtype=cq.CQSA_F32) == cq.CQSA_ERR_UNSUPPORTED
