@@ -17,12 +17,15 @@
 //                    tile j (every i, or i >= j when causal) stream through a two-slot TMA ring.
 //                    Per query tile, with the key dimension on the 128 tensor-memory lanes:
 //                      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (tcgen05, fp32 in tensor memory)
-//                      P^T and dS^T: one thread per key row, in registers
-//                      dV_j += P^T dO_i, dK_j += dS^T Q_i         (A operand from tensor memory)
-//                      dQ_i  = dS K_j                             (dS^T staged MN-major in shared memory)
-//                    and the dQ tile is added into an fp32 accumulator with 16-byte atomic adds while
-//                    the tensor pipe already computes the next S^T and dP^T. dK_j, dV_j are written
-//                    once, after the last query tile.
+//                      P^T and dS^T: one thread per key row and 64 queries, in registers; P^T goes
+//                                    to tensor memory, dS^T to a 128-byte-swizzled shared tile
+//                      dV_j += P^T dO_i                           (A operand from tensor memory)
+//                      dK_j += dS^T Q_i, dQ_i = dS K_j            (the dS^T tile read K-major / MN-major)
+//                    The dQ tile is scaled, staged in shared memory and added into an fp32
+//                    accumulator by TMA bulk reduce-add. S^T and dP^T of the next tile are computed
+//                    while the elementwise warps work on the current one. Roles: a TMA producer warp,
+//                    an MMA issuer warp, a dQ reduction warp and two elementwise warpgroups, joined by
+//                    mbarriers. dK_j, dV_j are written once, after the last query tile.
 //   bwd_dq_kernel    fp32 dQ accumulator -> dQ in the input dtype
 // P and dS enter the MMAs rounded to the input dtype; everything else is fp32. Head dimension 64.
 #include <cuda.h>
