@@ -288,12 +288,96 @@ int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, 
   a.workspace = workspace;
   a.B = B;
   a.H = H;
-  a.N = N;
+  a.Nq = N;
+  a.Nkv = N;
   a.d = d;
   a.causal = causal != 0;
   a.scale = resolve_scale(scale, d);
   a.dtype = dtype;
   return launch_attention_bwd(a, stream);
+}
+
+int cqsa_attn_bwd_dvec(const void* out_blk, const void* dout_blk, float* dvec_blk, int B, int H, int Nq, int d,
+                       int dtype, cudaStream_t stream) {
+  t_err[0] = 0;
+  int rc = check_problem(B, H, Nq, Nq, d, 0.0f, dtype, false);
+  if (rc != CQSA_OK) return rc;
+  if (d != 64) {
+    set_error("the backward supports head dim 64 (got %d)", d);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (!out_blk || !dout_blk || !dvec_blk || !aligned16(out_blk) || !aligned16(dout_blk) ||
+      (reinterpret_cast<uintptr_t>(dvec_blk) & 3u)) {
+    set_error("out_blk and dout_blk must be non-null 16-byte aligned device pointers, dvec_blk 4-byte aligned");
+    return CQSA_ERR_INVALID;
+  }
+  return launch_bwd_dvec(out_blk, dout_blk, dvec_blk, static_cast<long long>(B) * H * Nq, dtype, stream);
+}
+
+int cqsa_attn_bwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk, const void* dout_blk,
+                        const float* lse_blk, const float* dvec_blk, long long q_off, long long kv_off, int B, int H,
+                        int Nq, int Nkv, int d, int causal, float scale, int dtype, float* dq_acc, float* dk_acc,
+                        float* dv_acc, cudaStream_t stream) {
+  t_err[0] = 0;
+  int rc = check_problem(B, H, Nq, Nkv, d, scale, dtype, false);
+  if (rc != CQSA_OK) return rc;
+  if (d != 64) {
+    set_error("the backward supports head dim 64 (got %d)", d);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (q_off < 0 || kv_off < 0) {
+    set_error("q_off and kv_off must be >= 0");
+    return CQSA_ERR_INVALID;
+  }
+  if (!q_blk || !k_blk || !v_blk || !dout_blk || !lse_blk || !dvec_blk || !dq_acc || !dk_acc || !dv_acc) {
+    set_error("every block and accumulator pointer must be a non-null device pointer");
+    return CQSA_ERR_INVALID;
+  }
+  if (!aligned16(q_blk) || !aligned16(k_blk) || !aligned16(v_blk) || !aligned16(dout_blk) || !aligned16(dq_acc) ||
+      !aligned16(dk_acc) || !aligned16(dv_acc) || (reinterpret_cast<uintptr_t>(lse_blk) & 3u) ||
+      (reinterpret_cast<uintptr_t>(dvec_blk) & 3u)) {
+    set_error("blocks and accumulators must be 16-byte aligned (lse_blk, dvec_blk 4-byte)");
+    return CQSA_ERR_INVALID;
+  }
+  BwdArgs a;
+  memset(&a, 0, sizeof(a));
+  a.q = q_blk;
+  a.k = k_blk;
+  a.v = v_blk;
+  a.dout = dout_blk;
+  a.lse = lse_blk;
+  a.dvec = dvec_blk;
+  a.dq_acc = dq_acc;
+  a.dk_acc = dk_acc;
+  a.dv_acc = dv_acc;
+  a.B = B;
+  a.H = H;
+  a.Nq = Nq;
+  a.Nkv = Nkv;
+  a.d = d;
+  a.q_off = q_off;
+  a.kv_off = kv_off;
+  a.causal = causal != 0;
+  a.scale = resolve_scale(scale, d);
+  a.dtype = dtype;
+  return launch_attention_bwd_chunk(a, stream);
+}
+
+int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream) {
+  t_err[0] = 0;
+  if (n < 0 || (n & 3)) {
+    set_error("n must be a non-negative multiple of 4 (got %lld)", n);
+    return CQSA_ERR_INVALID;
+  }
+  if (dtype != CQSA_F16 && dtype != CQSA_BF16) {
+    set_error("dtype %d is not supported (fp16 or bf16)", dtype);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (n > 0 && (!acc || !out || !aligned16(acc) || (reinterpret_cast<uintptr_t>(out) & 7u))) {
+    set_error("acc must be a 16-byte aligned device pointer and out 8-byte aligned");
+    return CQSA_ERR_INVALID;
+  }
+  return launch_bwd_cast(acc, out, n, dtype, stream);
 }
 
 }  // extern "C"

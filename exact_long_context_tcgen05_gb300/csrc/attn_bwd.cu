@@ -69,12 +69,15 @@ static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= NTHR * 168, "register 
 enum : int { kBwdTimeoutLoad = 1, kBwdTimeoutMMA = 3, kBwdTimeoutSoftmax = 4 };
 
 struct BwdParams {
-  const float* lse;       // [BH, N] natural-log LSE of the forward
-  const float* dvec;      // [BH, N] D_i
-  float* dq_acc;          // [BH, N, 64] fp32, zeroed; receives scale * dS K
-  uint16_t* dk;           // [BH, N, 64] input dtype
+  const float* lse;       // [BH, Nq] natural-log LSE of the forward (over every key of the row)
+  const float* dvec;      // [BH, Nq] D_i
+  float* dq_acc;          // [BH, Nq, 64] fp32; receives scale * dS K (added)
+  uint16_t* dk;           // [BH, Nkv, 64] input dtype (monolithic mode: written)
   uint16_t* dv;
-  int H, BH, N, n_tiles;
+  float* dk_acc;          // [BH, Nkv, 64] fp32 (chunk-pair mode: scale * dS^T Q added)
+  float* dv_acc;          // [BH, Nkv, 64] fp32 (chunk-pair mode: P^T dO added)
+  int H, BH, Nq, Nkv, n_q_tiles;
+  long long q_off, kv_off;  // absolute positions of the chunks' first query / key (causal mask)
   float scale, scale_log2;
   unsigned long long timeout_ns;
 };
@@ -213,7 +216,9 @@ __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t
   }
 }
 
-template <int DT, bool CAUSAL>
+// ACCUM = 0: monolithic (dK, dV written in the input dtype); ACCUM = 1: one chunk pair, dK and dV
+// added into fp32 accumulators.
+template <int DT, bool CAUSAL, int ACCUM>
 __global__ void __launch_bounds__(NTHR, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
@@ -245,9 +250,22 @@ __global__ void __launch_bounds__(NTHR, 1)
   const int bh = blockIdx.x % p.BH, jt = blockIdx.x / p.BH;
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = jt * BT;
-  const int it0 = CAUSAL ? jt : 0;
-  const int nit = p.n_tiles - it0;  // >= 1
+  const int Nkv = ACCUM ? p.Nkv : p.Nq;
+  // first query tile with a query at or after this key tile's first key (causal; absolute positions)
+  int it0 = 0;
+  if constexpr (ACCUM) {
+    if (CAUSAL) {
+      const long long first = p.kv_off + k0 - p.q_off - (BT - 1);
+      it0 = first <= 0 ? 0 : static_cast<int>(first / BT + (first % BT != 0));
+    }
+  } else {
+    it0 = CAUSAL ? jt : 0;
+  }
+  const int nit = p.n_q_tiles - it0;  // >= 1 for the monolithic call
   const unsigned long long tmo = p.timeout_ns;
+  if constexpr (ACCUM) {
+    if (nit <= 0) return;  // every key of this tile lies after every query of the chunk: nothing to add
+  }
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
@@ -386,7 +404,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     const int t128 = tid & 127;
     const int r = quarter * 32 + lane;  // key row (tensor-memory lane) of P^T / dS^T; query row of dQ
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const bool key_ok = k0 + r < p.N;
+    const bool key_ok = k0 + r < Nkv;
     const float sl2 = p.scale_log2;
     const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(wg * BOX + r * 128);
     const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>(wg * (BT * 128) + r * 128);
@@ -395,8 +413,8 @@ __global__ void __launch_bounds__(NTHR, 1)
     // one value per thread: lse2 (t128 < 64) or D (t128 >= 64) of query 64 wg + (t128 & 63) of step it
     auto row_val = [&](int it) -> float {
       const long long i = static_cast<long long>(it0 + it) * BT + wg * 64 + (t128 & 63);
-      if (it >= nit || i >= p.N) return t128 < 64 ? INFINITY : 0.0f;  // P = 0 for rows past the end
-      const long long at = static_cast<long long>(bh) * p.N + i;
+      if (it >= nit || i >= p.Nq) return t128 < 64 ? INFINITY : 0.0f;  // P = 0 for rows past the end
+      const long long at = static_cast<long long>(bh) * p.Nq + i;
       return t128 < 64 ? p.lse[at] * LOG2E : p.dvec[at];
     };
     rows[t128] = row_val(0);
@@ -433,7 +451,17 @@ __global__ void __launch_bounds__(NTHR, 1)
       uint32_t pw[32], dw[32];
       if (ok) {
         tc_fence_after();
-        const bool diag = CAUSAL && ((it0 + it) * BT == k0);
+        // causal: key k0 + r hides from query i0 + q when r - q > dlt (absolute positions; |dlt| < 2^31
+        // as N is an int); only tiles with dlt < 127 contain such pairs. The monolithic call has dlt = 0
+        // on its diagonal tile and no other masked tile.
+        int dlt = 0;
+        bool diag;
+        if constexpr (ACCUM) {
+          dlt = static_cast<int>(p.q_off - p.kv_off) + (it0 + it) * BT - k0;
+          diag = CAUSAL && dlt < BT - 1;
+        } else {
+          diag = CAUSAL && ((it0 + it) * BT == k0);
+        }
         const float* lrow = rows + slot * 128;
         const float* drow = lrow + 64;
         // two 32-query chunks: S^T and dP^T columns in registers, then P and dS packed to 16-bit pairs;
@@ -460,8 +488,13 @@ __global__ void __launch_bounds__(NTHR, 1)
             float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -l2.y));
             if (!key_ok) p0 = p1 = 0.0f;
             if (diag) {
-              if (r > q0) p0 = 0.0f;
-              if (r > q0 + 1) p1 = 0.0f;
+              if constexpr (ACCUM) {
+                if (r - q0 > dlt) p0 = 0.0f;
+                if (r - q0 - 1 > dlt) p1 = 0.0f;
+              } else {
+                if (r > q0) p0 = 0.0f;
+                if (r > q0 + 1) p1 = 0.0f;
+              }
             }
             pw[c2 * 16 + e] = pack_pair(p0, p1, DT);
             dw[c2 * 16 + e] = pack_pair(p0 * (__uint_as_float(g[2 * e]) - dd.x),
@@ -510,8 +543,20 @@ __global__ void __launch_bounds__(NTHR, 1)
       tmem_wait_ld();
       reg_fence32(a);
       reg_fence32(g);
-      if (key_ok) {
-        const long long row = static_cast<long long>(bh) * p.N + k0 + r;
+      if (ACCUM && key_ok) {
+        const long long row = static_cast<long long>(bh) * Nkv + k0 + r;
+        float4* dv = reinterpret_cast<float4*>(p.dv_acc + row * HD + wg * 32);
+        float4* dk = reinterpret_cast<float4*>(p.dk_acc + row * HD + wg * 32);
+#pragma unroll
+        for (int u = 0; u < 8; ++u) {
+          atomicAdd(dv + u, make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
+                                        __uint_as_float(a[4 * u + 2]), __uint_as_float(a[4 * u + 3])));
+          atomicAdd(dk + u, make_float4(__uint_as_float(g[4 * u]) * p.scale, __uint_as_float(g[4 * u + 1]) * p.scale,
+                                        __uint_as_float(g[4 * u + 2]) * p.scale,
+                                        __uint_as_float(g[4 * u + 3]) * p.scale));
+        }
+      } else if (!ACCUM && key_ok) {
+        const long long row = static_cast<long long>(bh) * Nkv + k0 + r;
         uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + wg * 32);
         uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + wg * 32);
 #pragma unroll
@@ -620,10 +665,10 @@ int make_dq_map(CUtensorMap* m, float* base, int BH, int N) {
   return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box);
 }
 
-template <int DT, bool CAUSAL>
+template <int DT, bool CAUSAL, int ACCUM>
 int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
-                const CUtensorMap& mdq, const BwdParams& p, cudaStream_t s) {
-  auto kern = attn_bwd_kernel<DT, CAUSAL>;
+                const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, cudaStream_t s) {
+  auto kern = attn_bwd_kernel<DT, CAUSAL, ACCUM>;
   static bool attr_done = false;
   if (!attr_done) {
     // setmaxnreg.inc waits until its registers are free: refuse to launch unless the launch holds the split
@@ -639,9 +684,55 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention backward smem)");
     attr_done = true;
   }
-  const long long grid = static_cast<long long>(p.n_tiles) * p.BH;
+  const long long grid = static_cast<long long>(n_kv_tiles) * p.BH;
   kern<<<static_cast<unsigned>(grid), NTHR, SMEM_BYTES, s>>>(mq, mk, mv, mg, mdq, p);
   return cuda_status(cudaGetLastError(), "attention backward kernel launch");
+}
+
+template <int ACCUM>
+int dispatch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
+                  const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, int dtype, int causal, cudaStream_t s) {
+  if (dtype == CQSA_BF16)
+    return causal ? launch_main<1, true, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
+                  : launch_main<1, false, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
+  return causal ? launch_main<0, true, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
+                : launch_main<0, false, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
+}
+
+// Maps and parameters of one launch of the main kernel (the monolithic call or one chunk pair).
+int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cudaStream_t stream) {
+  const long long n_q_tiles = (a.Nq + BT - 1) / BT, n_kv_tiles = (a.Nkv + BT - 1) / BT;
+  if (n_kv_tiles * a.B * a.H > 0x7fffffffLL) {
+    set_error("problem too large for one launch");
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  CUtensorMap mq, mk, mv, mg, mdq;
+  int rc = make_bhnd_map(&mq, a.q, a.dtype, a.B, a.H, a.Nq);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mk, a.k, a.dtype, a.B, a.H, a.Nkv);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mv, a.v, a.dtype, a.B, a.H, a.Nkv);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mg, a.dout, a.dtype, a.B, a.H, a.Nq);
+  if (rc == CQSA_OK) rc = make_dq_map(&mdq, dq_acc, a.B * a.H, a.Nq);
+  if (rc != CQSA_OK) return rc;
+  BwdParams p;
+  p.lse = a.lse;
+  p.dvec = dvec;
+  p.dq_acc = dq_acc;
+  p.dk = static_cast<uint16_t*>(a.dk);
+  p.dv = static_cast<uint16_t*>(a.dv);
+  p.dk_acc = a.dk_acc;
+  p.dv_acc = a.dv_acc;
+  p.H = a.H;
+  p.BH = a.B * a.H;
+  p.Nq = a.Nq;
+  p.Nkv = a.Nkv;
+  p.n_q_tiles = static_cast<int>(n_q_tiles);
+  p.q_off = a.q_off;
+  p.kv_off = a.kv_off;
+  p.scale = a.scale;
+  p.scale_log2 = a.scale * LOG2E;
+  p.timeout_ns = timeout_ns();
+  return accum ? dispatch_main<1>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream)
+               : dispatch_main<0>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream);
 }
 
 }  // namespace
@@ -652,67 +743,48 @@ size_t attention_bwd_workspace(int B, int H, int N, int d) {
   return dq + rows * sizeof(float);
 }
 
+int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int dtype, cudaStream_t stream) {
+  if (rows <= 0) return CQSA_OK;
+  const long long dot_threads = rows * 8;
+  const unsigned dot_blocks = static_cast<unsigned>((dot_threads + 255) / 256);
+  if (dtype == CQSA_BF16)
+    bwd_dot_kernel<1><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
+                                                      dvec, rows);
+  else
+    bwd_dot_kernel<0><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
+                                                      dvec, rows);
+  return cuda_status(cudaGetLastError(), "attention backward dot kernel launch");
+}
+
+int launch_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream) {
+  const long long n4 = n / 4;
+  if (n4 <= 0) return CQSA_OK;
+  const unsigned cblocks = static_cast<unsigned>(std::min<long long>((n4 + 255) / 256, 152LL * 16));
+  if (dtype == CQSA_BF16)
+    bwd_dq_kernel<1><<<cblocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc), static_cast<uint2*>(out), n4);
+  else
+    bwd_dq_kernel<0><<<cblocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(acc), static_cast<uint2*>(out), n4);
+  return cuda_status(cudaGetLastError(), "attention backward cast kernel launch");
+}
+
 int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream) {
-  const long long rows = static_cast<long long>(a.B) * a.H * a.N;
-  const long long n_tiles = (a.N + BT - 1) / BT;
-  if (n_tiles * a.B * a.H > 0x7fffffffLL) {
-    set_error("problem too large for one launch");
-    return CQSA_ERR_UNSUPPORTED;
-  }
+  const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
   float* dq_acc = static_cast<float*>(a.workspace);
   float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
                                          ((static_cast<size_t>(rows) * HD * sizeof(float) + 255) & ~size_t(255)));
-  CUtensorMap mq, mk, mv, mg, mdq;
-  int rc = make_bhnd_map(&mq, a.q, a.dtype, a.B, a.H, a.N);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mk, a.k, a.dtype, a.B, a.H, a.N);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mv, a.v, a.dtype, a.B, a.H, a.N);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mg, a.dout, a.dtype, a.B, a.H, a.N);
-  if (rc == CQSA_OK) rc = make_dq_map(&mdq, dq_acc, a.B * a.H, a.N);
-  if (rc != CQSA_OK) return rc;
-
   // D_i, then the zeroed dQ accumulator, the main kernel and the dQ conversion
-  const long long dot_threads = rows * 8;
-  const unsigned dot_blocks = static_cast<unsigned>((dot_threads + 255) / 256);
-  if (a.dtype == CQSA_BF16)
-    bwd_dot_kernel<1><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(a.out),
-                                                      static_cast<const uint4*>(a.dout), dvec, rows);
-  else
-    bwd_dot_kernel<0><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(a.out),
-                                                      static_cast<const uint4*>(a.dout), dvec, rows);
-  rc = cuda_status(cudaGetLastError(), "attention backward dot kernel launch");
+  int rc = launch_bwd_dvec(a.out, a.dout, dvec, rows, a.dtype, stream);
   if (rc != CQSA_OK) return rc;
   rc = cuda_status(cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * HD * sizeof(float), stream),
                    "zero dQ accumulator");
   if (rc != CQSA_OK) return rc;
-
-  BwdParams p;
-  p.lse = a.lse;
-  p.dvec = dvec;
-  p.dq_acc = dq_acc;
-  p.dk = static_cast<uint16_t*>(a.dk);
-  p.dv = static_cast<uint16_t*>(a.dv);
-  p.H = a.H;
-  p.BH = a.B * a.H;
-  p.N = a.N;
-  p.n_tiles = static_cast<int>(n_tiles);
-  p.scale = a.scale;
-  p.scale_log2 = a.scale * LOG2E;
-  p.timeout_ns = timeout_ns();
-  if (a.dtype == CQSA_BF16)
-    rc = a.causal ? launch_main<1, true>(mq, mk, mv, mg, mdq, p, stream)
-                  : launch_main<1, false>(mq, mk, mv, mg, mdq, p, stream);
-  else
-    rc = a.causal ? launch_main<0, true>(mq, mk, mv, mg, mdq, p, stream)
-                  : launch_main<0, false>(mq, mk, mv, mg, mdq, p, stream);
+  rc = run_main(a, dq_acc, dvec, 0, stream);
   if (rc != CQSA_OK) return rc;
+  return launch_bwd_cast(dq_acc, a.dq, rows * HD, a.dtype, stream);
+}
 
-  const long long n4 = rows * HD / 4;
-  const unsigned cblocks = static_cast<unsigned>(std::min<long long>((n4 + 255) / 256, 152LL * 16));
-  if (a.dtype == CQSA_BF16)
-    bwd_dq_kernel<1><<<cblocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(a.dq), n4);
-  else
-    bwd_dq_kernel<0><<<cblocks, 256, 0, stream>>>(reinterpret_cast<const float4*>(dq_acc), static_cast<uint2*>(a.dq), n4);
-  return cuda_status(cudaGetLastError(), "attention backward dQ kernel launch");
+int launch_attention_bwd_chunk(const BwdArgs& a, cudaStream_t stream) {
+  return run_main(a, a.dq_acc, a.dvec, 1, stream);
 }
 
 int bwd_error_word(DevErr* out, int clear) {

@@ -39,8 +39,12 @@ struct AttnArgs {
 // Validates nothing (the ABI layer does); encodes tensor maps and launches on `stream`.
 int launch_attention(const AttnArgs& a, cudaStream_t stream);
 
-// Attention backward (attn_bwd.cu): dQ, dK, dV of [B,H,N,64] q, k, v from out, dout and the forward's
-// LSE. `workspace` holds the fp32 dQ accumulator and D_i (attention_bwd_workspace bytes).
+// Attention backward (attn_bwd.cu), head dimension 64. The monolithic call (launch_attention_bwd) takes
+// q, k, v, out, dout [B,H,N,64] with Nq = Nkv = N and offsets 0, writes dq, dk, dv, and uses
+// `workspace` (attention_bwd_workspace bytes) for the fp32 dQ accumulator and D. One chunk pair
+// (launch_attention_bwd_chunk) takes a query chunk (q, dout, lse, dvec: Nq rows at absolute position
+// q_off) and a key chunk (k, v: Nkv rows at kv_off) and adds into dq_acc [B,H,Nq,64], dk_acc and
+// dv_acc [B,H,Nkv,64] (fp32, scale applied).
 struct BwdArgs {
   const void* q;
   const void* k;
@@ -48,17 +52,26 @@ struct BwdArgs {
   const void* out;
   const void* dout;
   const float* lse;
+  const float* dvec;
   void* dq;
   void* dk;
   void* dv;
+  float* dq_acc;
+  float* dk_acc;
+  float* dv_acc;
   void* workspace;
-  int B, H, N, d;
+  int B, H, Nq, Nkv, d;
+  long long q_off, kv_off;
   int causal;
   float scale;  // resolved
   int dtype;
 };
 size_t attention_bwd_workspace(int B, int H, int N, int d);
 int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream);
+int launch_attention_bwd_chunk(const BwdArgs& a, cudaStream_t stream);
+// D_i = dout_i . out_i (fp32) for `rows` rows of 64 features; fp32 -> dtype for n elements (n % 4 == 0).
+int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int dtype, cudaStream_t stream);
+int launch_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream);
 
 // LSE merge of n partials (device pointer arrays passed by value).
 int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int n, void* out, float* lse,

@@ -206,6 +206,33 @@ int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, 
                   int causal, float scale, int dtype, cudaStream_t stream);
 
 /*
+ * The backward over chunk pairs, for problems cut the way the forward's chunk pairs cut them (the
+ * pages' streamed backward, `stream_cqsa_backward`, works subproblem by subproblem). The gradient is a
+ * sum over key chunks (dq) and over query chunks (dk, dv) of the same chain-rule terms, with P taken
+ * against the full-row lse, so accumulating every needed pair gives the monolithic gradient up to the
+ * fp32 summation order.
+ *
+ * cqsa_attn_bwd_dvec: D_i = dout_i . out_i (fp32) of a query chunk: out_blk, dout_blk [B,H,Nq,64]
+ *   (dtype), dvec_blk [B,H,Nq] fp32. out is the forward's full output for those rows.
+ * cqsa_attn_bwd_chunk: one pair. q_blk, dout_blk [B,H,Nq,64] with lse_blk (the forward's full-row lse)
+ *   and dvec_blk [B,H,Nq] of the query chunk at absolute position q_off; k_blk, v_blk [B,H,Nkv,64] of
+ *   the key chunk at kv_off (causal masking on absolute positions; a pair with every key after every
+ *   query adds nothing). Adds scale * dS K into dq_acc [B,H,Nq,64], scale * dS^T Q into dk_acc and
+ *   P^T dout into dv_acc [B,H,Nkv,64], all fp32, which the caller zeroes before its first pair and
+ *   keeps until its last; pairs on one stream may share accumulators. Head dim 64; asynchronous;
+ *   allocates nothing.
+ * cqsa_attn_bwd_cast: n fp32 values (n a multiple of 4) rounded to dtype (RNE), e.g. the accumulators
+ *   into dq, dk, dv.
+ */
+int cqsa_attn_bwd_dvec(const void* out_blk, const void* dout_blk, float* dvec_blk, int B, int H, int Nq, int d,
+                       int dtype, cudaStream_t stream);
+int cqsa_attn_bwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk, const void* dout_blk,
+                        const float* lse_blk, const float* dvec_blk, long long q_off, long long kv_off, int B, int H,
+                        int Nq, int Nkv, int d, int causal, float scale, int dtype, float* dq_acc, float* dk_acc,
+                        float* dv_acc, cudaStream_t stream);
+int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream);
+
+/*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).
  */
 #define CQSA_STATIC_SCRATCH_BYTES (32u << 20)

@@ -140,3 +140,25 @@ def test_bwd_validation(cq):
     assert call(q=FAKE + 8) == cq.CQSA_ERR_INVALID and "aligned" in cq.last_error()
     assert call(lse=FAKE + 2) == cq.CQSA_ERR_INVALID
     assert call(dtype=cq.CQSA_F32) == cq.CQSA_ERR_UNSUPPORTED
+
+
+def test_bwd_chunk_validation(cq):
+    L = cq.lib
+    args = dict(q=FAKE, k=FAKE, v=FAKE, g=FAKE, lse=FAKE, dvec=FAKE, qo=0, ko=0, B=1, H=1, Nq=256, Nkv=256, d=64, c=1,
+                s=0.0, dt=cq.CQSA_F16, dq=FAKE, dk=FAKE, dv=FAKE)
+
+    def call(**kw):
+        a = {**args, **kw}
+        return L.cqsa_attn_bwd_chunk(a["q"], a["k"], a["v"], a["g"], a["lse"], a["dvec"], a["qo"], a["ko"], a["B"],
+                                     a["H"], a["Nq"], a["Nkv"], a["d"], a["c"], a["s"], a["dt"], a["dq"], a["dk"],
+                                     a["dv"], None)
+    assert call(d=128) == cq.CQSA_ERR_UNSUPPORTED
+    assert call(qo=-1) == cq.CQSA_ERR_INVALID
+    assert call(dk=None) == cq.CQSA_ERR_INVALID
+    assert call(dv=FAKE + 4) == cq.CQSA_ERR_INVALID
+    assert call(Nkv=0) == cq.CQSA_ERR_INVALID
+    assert L.cqsa_attn_bwd_dvec(FAKE, FAKE, FAKE, 1, 1, 128, 128, cq.CQSA_F16, None) == cq.CQSA_ERR_UNSUPPORTED
+    assert L.cqsa_attn_bwd_dvec(FAKE, FAKE + 8, FAKE, 1, 1, 128, 64, cq.CQSA_F16, None) == cq.CQSA_ERR_INVALID
+    assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 6, cq.CQSA_F16, None) == cq.CQSA_ERR_INVALID
+    assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 8, cq.CQSA_F32, None) == cq.CQSA_ERR_UNSUPPORTED
+    assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 0, cq.CQSA_F16, None) == cq.CQSA_OK

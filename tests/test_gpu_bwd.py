@@ -105,3 +105,75 @@ def test_sum_identities_large(cq, causal):
     # each summed element carries a rounding error <= u |x|; the sums are checked against that budget
     assert np.all(np.abs(dk64.sum(axis=2)) <= 4 * u * np.abs(dk64).sum(axis=2) + 1e-6)
     assert np.all(np.abs(dv64.sum(axis=2) - g64.sum(axis=2)) <= 4 * u * np.abs(dv64).sum(axis=2) + 1e-6)
+
+
+def _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype, skip_masked=True):
+    """The backward over (query chunk, key chunk) pairs of C tokens through cqsa_attn_bwd_chunk, with
+    per-chunk fp32 accumulators cast to dtype at the end."""
+    dev = q.device
+    starts = list(range(0, N, C))
+    sz = {s0: min(C, N - s0) for s0 in starts}
+    dq_acc = {s0: torch.zeros((B, H, sz[s0], d), dtype=torch.float32, device=dev) for s0 in starts}
+    dk_acc = {s0: torch.zeros((B, H, sz[s0], d), dtype=torch.float32, device=dev) for s0 in starts}
+    dv_acc = {s0: torch.zeros((B, H, sz[s0], d), dtype=torch.float32, device=dev) for s0 in starts}
+    sl = lambda t, s0: t[:, :, s0:s0 + sz[s0]].contiguous()  # noqa: E731
+    for qs in starts:
+        nq = sz[qs]
+        qb, gb, ob, lb = sl(q, qs), sl(g, qs), sl(out, qs), sl(lse, qs)
+        db = torch.empty((B, H, nq), dtype=torch.float32, device=dev)
+        cq.cqsa_attn_bwd_dvec(ob, gb, db, B, H, nq, d, dtype)
+        for ks in starts:
+            if skip_masked and causal and ks > qs + nq - 1:
+                continue
+            cq.cqsa_attn_bwd_chunk(qb, sl(k, ks), sl(v, ks), gb, lb, db, qs, ks, B, H, nq, sz[ks], d, causal, 0.0,
+                                   dtype, dq_acc[qs], dk_acc[ks], dv_acc[ks])
+    res = []
+    for acc in (dq_acc, dk_acc, dv_acc):
+        parts = []
+        for s0 in starts:
+            o = torch.empty((B, H, sz[s0], d), dtype=q.dtype, device=dev)
+            cq.cqsa_attn_bwd_cast(acc[s0], o, acc[s0].numel(), dtype)
+            parts.append(o)
+        res.append(torch.cat(parts, dim=2))
+    torch.cuda.synchronize()
+    return res
+
+
+@pytest.mark.parametrize("N,C,causal,dtype", [
+    (768, 256, True, syn.F16),    # 3 x 3 chunks of two tiles, 6 causal pairs
+    (640, 200, True, syn.F16),    # chunks not aligned to the 128-token tiles, ragged last chunk
+    (512, 192, False, syn.BF16),  # every pair
+])
+def test_chunked_backward(cq, N, C, causal, dtype):
+    """Accumulating every chunk pair gives the oracle's gradients (same tolerance as the monolithic
+    call) and the monolithic call's, within a few ulps of dtype (fp32 summation order differs)."""
+    B, H, d = 1, 2, 64
+    (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, causal, dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
+    grads = _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype)
+    rc, code, _ = cq.cqsa_device_error()
+    assert rc == cq.CQSA_OK and code == 0
+    ref = oracle.attn_bwd(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=causal, dtype=dtype)
+    u = U[dtype]
+    for name, t, m in zip(("dq", "dk", "dv"), grads, mono_grads):
+        _check(to_np64(t), ref[name], dtype, f"chunked {name} N={N} C={C}")
+        diff = float((t.float() - m.float()).abs().max())
+        assert diff <= 4 * u * float(m.float().abs().max()), (name, diff)
+
+
+def test_chunk_pair_above_diagonal_adds_nothing(cq):
+    """A causal pair whose keys all follow every query leaves the accumulators untouched."""
+    B, H, N, d, C = 1, 2, 512, 64, 256
+    (qn, kn, vn, gn), _ = _run(cq, B, H, N, d, True, syn.F16)
+    q, k, v, g = (to_dev(x, syn.F16) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, True, syn.F16)
+    dev = q.device
+    qb, gb, ob, lb = (t[:, :, :C].contiguous() for t in (q, g, out, lse))
+    kb, vb = (t[:, :, C:].contiguous() for t in (k, v))
+    db = torch.empty((B, H, C), dtype=torch.float32, device=dev)
+    cq.cqsa_attn_bwd_dvec(ob, gb, db, B, H, C, d, syn.F16)
+    accs = [torch.full((B, H, C, d), 0.5, dtype=torch.float32, device=dev) for _ in range(3)]
+    cq.cqsa_attn_bwd_chunk(qb, kb, vb, gb, lb, db, 0, C, B, H, C, N - C, d, True, 0.0, syn.F16, *accs)
+    torch.cuda.synchronize()
+    assert all(bool((a == 0.5).all()) for a in accs)
