@@ -6,7 +6,8 @@ shares no code with it. The arithmetic is in ``oracle.c`` (plain C, double preci
 rows), which states the definition it follows and where the pages state the problem.
 
 The backward (``attn_bwd``, ``attn_bwd_f64``) is the chain rule through the softmax, pinned in
-``tests/test_oracle_bwd.py`` by central finite differences of the loss sum(dO * O), by the forward
+``tests/test_oracle_bwd.py`` by central finite differences of the loss sum(dO * O), by sympy's symbolic
+gradient of the written-out loss on a 3-token problem, by the forward
 part agreeing with ``attn_full``, by the key-shift invariance sum_j dK_j = 0 and by the uniform-score
 closed form of dV.
 

@@ -74,3 +74,29 @@ def test_uniform_scores_closed_form(causal):
                 want[:, :, j] += gd[:, :, i] / ((i + 1) if causal else N)
     np.testing.assert_allclose(res["dv"], want, rtol=1e-13, atol=1e-14)
     assert np.all(res["dk"] == 0.0)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+def test_symbolic_gradient_tiny(causal):
+    """N = 3, d = 2: the loss sum(dO * O) written out with sympy from the definition of attention
+    and differentiated symbolically; its gradients, evaluated at the same point, pin every element
+    of dq, dk and dv independently of the oracle's formulas."""
+    sp = pytest.importorskip("sympy")
+    N, d, scale = 3, 2, 0.6
+    rng = np.random.default_rng(21 + int(causal))
+    vals = {n: rng.standard_normal((N, d)) for n in ("q", "k", "v", "g")}
+    sym = {n: sp.Matrix(N, d, lambda i, c, n=n: sp.Symbol(f"{n}{i}{c}")) for n in ("q", "k", "v")}
+    loss = 0
+    for i in range(N):
+        keys = range(i + 1) if causal else range(N)
+        e = {j: sp.exp(scale * sum(sym["q"][i, c] * sym["k"][j, c] for c in range(d))) for j in keys}
+        z = sum(e.values())
+        for c in range(d):
+            o_ic = sum(e[j] * sym["v"][j, c] for j in keys) / z
+            loss += vals["g"][i, c] * o_ic
+    subs = {sym[n][i, c]: vals[n][i, c] for n in ("q", "k", "v") for i in range(N) for c in range(d)}
+    res = oracle.attn_bwd_f64(*(vals[n][None, None] for n in ("q", "k", "v", "g")), causal=causal, scale=scale)
+    for n, name in (("q", "dq"), ("k", "dk"), ("v", "dv")):
+        want = np.array([[float(sp.diff(loss, sym[n][i, c]).evalf(subs=subs, n=30)) for c in range(d)]
+                         for i in range(N)])
+        np.testing.assert_allclose(res[name][0, 0], want, rtol=1e-12, atol=1e-13, err_msg=name)
