@@ -22,7 +22,7 @@ CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
             "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd", "cqsa_attn_bwd_dvec",
-            "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast",
+            "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast", "cqsa_stream_attn_bwd",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
             "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
@@ -81,6 +81,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_attn_bwd_chunk.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _ll, _ll, _i, _i, _i, _i, _i, _i, _f, _i, _vp,
                                         _vp, _vp, _vp]
     lib.cqsa_attn_bwd_cast.argtypes = [_vp, _vp, _ll, _i, _vp]
+    lib.cqsa_stream_attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _ll, _i, _i, _f, _i,
+                                         _ll, _vp]
     lib.cqsa_release_cache.argtypes = []
     lib.cqsa_release_cache.restype = _i
     lib.cqsa_status_string.argtypes = [_i]
@@ -247,6 +249,14 @@ def cqsa_attn_bwd_chunk(q_blk, k_blk, v_blk, dout_blk, lse_blk, dvec_blk, q_off,
 
 def cqsa_attn_bwd_cast(acc, out, n, dtype, stream=None) -> int:
     return _check(lib.cqsa_attn_bwd_cast(_ptr(acc), _ptr(out), n, dtype, _stream(stream)))
+
+
+def cqsa_stream_attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, dtype, chunk_tokens,
+                         stream=None) -> int:
+    """Host-resident backward (all tensors in host memory, pinned for speed)."""
+    return _check(lib.cqsa_stream_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                                           _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), dtype,
+                                           chunk_tokens, _stream(stream)))
 
 
 def cqsa_release_cache() -> int:

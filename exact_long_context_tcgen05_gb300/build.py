@@ -15,7 +15,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libcqsa_gb300.so")
-SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "merge.cu", "api.cu", "stream_driver.cu", "chunked_static.cu", "quorum.cu", "pool.cu"]
+SOURCES = ["attn_fwd.cu", "attn_bwd.cu", "merge.cu", "api.cu", "stream_driver.cu", "chunked_static.cu", "quorum.cu", "pool.cu", "stream_bwd.cu"]
 HEADERS = ["sm103_ptx.cuh", "cqsa_internal.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

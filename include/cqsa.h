@@ -233,6 +233,21 @@ int cqsa_attn_bwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk,
 int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream);
 
 /*
+ * Host-resident backward over chunk pairs (the pages' streamed backward, `stream_cqsa_backward`): q, k,
+ * v, out, dout [B,H,N,64] (fp16/bf16, layout BHND) and lse [B,H,N] fp32 in host memory (pinned for
+ * speed); dq, dk, dv [B,H,N,64] written to host memory. Query-outer over chunks of chunk_tokens (a
+ * positive multiple of 128): each query chunk's q/out/dout/lse and each needed key chunk's k/v are
+ * copied to the device, the pair runs cqsa_attn_bwd_chunk's kernel, dq leaves after its query chunk,
+ * dk and dv after the last one. Device memory: 2 * B*H*N*64*4 bytes of dk/dv accumulators plus one
+ * chunk of each input, D, lse, the dq accumulator and an output buffer (from the library's pool;
+ * CQSA_ERR_OOM if they do not fit). Synchronous; the result equals cqsa_attn_bwd's up to the fp32
+ * summation order.
+ */
+int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                         const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d, int causal,
+                         float scale, int dtype, long long chunk_tokens, cudaStream_t stream);
+
+/*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).
  */
 #define CQSA_STATIC_SCRATCH_BYTES (32u << 20)

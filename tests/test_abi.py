@@ -162,3 +162,14 @@ def test_bwd_chunk_validation(cq):
     assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 6, cq.CQSA_F16, None) == cq.CQSA_ERR_INVALID
     assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 8, cq.CQSA_F32, None) == cq.CQSA_ERR_UNSUPPORTED
     assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 0, cq.CQSA_F16, None) == cq.CQSA_OK
+
+
+def test_stream_bwd_validation(cq):
+    L = cq.lib
+    f = lambda **kw: L.cqsa_stream_attn_bwd(  # noqa: E731
+        kw.get("q", FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, kw.get("N", 1000), kw.get("d", 64), 1,
+        0.0, cq.CQSA_F16, kw.get("C", 256), None)
+    assert f(C=100) == cq.CQSA_ERR_INVALID
+    assert f(d=128) == cq.CQSA_ERR_UNSUPPORTED
+    assert f(q=None) == cq.CQSA_ERR_INVALID
+    assert f(N=0) == cq.CQSA_ERR_INVALID

@@ -177,3 +177,21 @@ def test_chunk_pair_above_diagonal_adds_nothing(cq):
     cq.cqsa_attn_bwd_chunk(qb, kb, vb, gb, lb, db, 0, C, B, H, C, N - C, d, True, 0.0, syn.F16, *accs)
     torch.cuda.synchronize()
     assert all(bool((a == 0.5).all()) for a in accs)
+
+
+@pytest.mark.parametrize("B,H,N,C,causal", [(2, 2, 640, 256, True), (1, 2, 384, 128, False)])
+def test_stream_backward(cq, B, H, N, C, causal):
+    """Host-resident backward over chunks (ragged last chunk, several batches and heads): equal to the
+    monolithic device call within a few ulps (fp32 summation order differs)."""
+    d, dtype = 64, syn.F16
+    (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, causal, dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
+    host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
+    grads = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+    cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, d, causal, 0.0, dtype, C)
+    u = U[dtype]
+    for name, t, m in zip(("dq", "dk", "dv"), grads, mono_grads):
+        m = m.float().cpu()
+        diff = float((t.float() - m).abs().max())
+        assert diff <= 4 * u * float(m.abs().max()), (name, diff)
