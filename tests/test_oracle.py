@@ -107,21 +107,68 @@ def test_two_key_closed_form():
             assert abs(lse[0, h, i] - (s0 + np.log1p(np.exp(s1 - s0)))) < 1e-13
 
 
+def _bf16_exact(x):
+    """bfloat16 storage bits of values that bf16 represents exactly (the upper half of the fp32 bits)."""
+    b = np.asarray(x, dtype=np.float32).view(np.uint32)
+    assert np.all((b & 0xFFFF) == 0), "value not exactly representable in bf16"
+    return (b >> 16).astype(np.uint16)
+
+
 def test_golden_closed_forms():
     import sympy
     with open(GOLDEN) as f:
         cases = json.load(f)["cases"]
     ns = {"E": sympy.E, "exp": sympy.exp, "log": sympy.log, "Rational": sympy.Rational}
+    assert any(c.get("dtype") == "bf16" for c in cases)
     for c in cases:
         B, H, N, d = c["B"], c["H"], c["N"], c["d"]
-        q, k, v = (_f16(np.array(c[t]).reshape(B, H, N, d)) for t in ("q", "k", "v"))
-        out, lse = oracle.attn_full(q, k, v, B=B, H=H, N=N, d=d, causal=c["causal"], scale=c["scale"])
+        bf = c.get("dtype", "f16") == "bf16"
+        enc = _bf16_exact if bf else _f16
+        q, k, v = (enc(np.array(c[t]).reshape(B, H, N, d)) for t in ("q", "k", "v"))
+        if not bf:
+            assert np.array_equal(q.view(np.float16).astype(np.float64), np.array(c["q"]).reshape(B, H, N, d))
+        out, lse = oracle.attn_full(q, k, v, B=B, H=H, N=N, d=d, causal=c["causal"], scale=c["scale"],
+                                    dtype=syn.BF16 if bf else syn.F16)
         for i in range(N):
             for j in range(d):
                 ref = float(sympy.N(sympy.sympify(c["out"][i][j], locals=ns), 30))
                 assert abs(out[0, 0, i, j] - ref) < 1e-14 * max(1.0, abs(ref)), (c["name"], i, j)
             ref = float(sympy.N(sympy.sympify(c["lse"][i], locals=ns), 30))
             assert abs(lse[0, 0, i] - ref) < 1e-14 * max(1.0, abs(ref)), (c["name"], i)
+
+
+def _same_values(a, b):
+    """Equal as float64 values, NaN matching NaN, and zeros matching in sign."""
+    nan = np.isnan(a)
+    if not np.array_equal(nan, np.isnan(b)):
+        return False
+    a, b = a[~nan], b[~nan]
+    return np.array_equal(a, b) and np.array_equal(np.signbit(a), np.signbit(b))
+
+
+def test_widening_every_fp16_pattern():
+    # all 65,536 binary16 patterns (normals, subnormals, +-0, +-inf, NaNs) against numpy's float16
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    ref = bits.view(np.float16).astype(np.float64)
+    assert _same_values(oracle.widen(bits, syn.F16), ref)
+
+
+def test_widening_every_bf16_pattern():
+    # all 65,536 bfloat16 patterns against two independent routes: the pattern placed in the upper half
+    # of a binary32 (bfloat16's definition), and torch's bfloat16 dtype
+    import torch
+    bits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    with np.errstate(invalid="ignore"):  # signalling-NaN patterns widen to NaN
+        via_f32 = (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+    via_torch = torch.from_numpy(bits.view(np.int16)).view(torch.bfloat16).to(torch.float64).numpy()
+    got = oracle.widen(bits, syn.BF16)
+    assert _same_values(got, via_f32)
+    assert _same_values(got, via_torch)
+    # spot values: smallest subnormal, largest subnormal, 1 + 2^-7, -(1/2 + 2^-7), largest finite
+    spots = {0x0001: 2.0 ** -133, 0x007F: 127 * 2.0 ** -133, 0x3F81: 1 + 2.0 ** -7, 0xBF02: -(0.5 + 2.0 ** -7),
+             0x7F7F: (2 - 2.0 ** -7) * 2.0 ** 127}
+    for b, val in spots.items():
+        assert got[b] == val, hex(b)
 
 
 @pytest.mark.parametrize("dtype", [syn.F16, syn.BF16])
