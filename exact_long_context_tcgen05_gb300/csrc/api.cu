@@ -13,6 +13,8 @@ namespace cqsa {
 
 int device_error_word(DevErr* out, int clear);  // attn_fwd.cu (owns the forward's device word)
 int bwd_error_word(DevErr* out, int clear);     // attn_bwd.cu (the backward's)
+int device_error_word_on(DevErr* out, cudaStream_t s);  // read on one stream; cleared when set
+int bwd_error_word_on(DevErr* out, cudaStream_t s);
 
 static thread_local char t_err[512];
 static unsigned int g_timeout_ms = 0;
@@ -45,6 +47,21 @@ unsigned long long timeout_ns() {
     if (ms == 0) ms = 2000;
   }
   return static_cast<unsigned long long>(ms) * 1000000ull;
+}
+
+int check_device_error_on(cudaStream_t s) {
+  DevErr e = {0, 0, 0, 0};
+  int rc = device_error_word_on(&e, s);
+  if (rc != CQSA_OK) return rc;
+  if (e.code == 0) {
+    rc = bwd_error_word_on(&e, s);
+    if (rc != CQSA_OK) return rc;
+  }
+  if (e.code != 0) {
+    set_error("device wait gave up (code %d, block %d, site %d)", e.code, e.block, e.where);
+    return CQSA_ERR_TIMEOUT;
+  }
+  return CQSA_OK;
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }

@@ -669,8 +669,9 @@ template <int DT, bool CAUSAL, int ACCUM>
 int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
                 const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, cudaStream_t s) {
   auto kern = attn_bwd_kernel<DT, CAUSAL, ACCUM>;
-  static bool attr_done = false;
-  if (!attr_done) {
+  static PerDeviceOnce attr;  // the attributes belong to each device's context
+  int dev = 0;
+  if (!attr.done(&dev)) {
     // setmaxnreg.inc waits until its registers are free: refuse to launch unless the launch holds the split
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
@@ -682,7 +683,7 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention backward smem)");
-    attr_done = true;
+    attr.mark(dev);
   }
   const long long grid = static_cast<long long>(n_kv_tiles) * p.BH;
   kern<<<static_cast<unsigned>(grid), NTHR, SMEM_BYTES, s>>>(mq, mk, mv, mg, mdq, p);
@@ -792,6 +793,18 @@ int bwd_error_word(DevErr* out, int clear) {
   if (rc != CQSA_OK || !clear || out->code == 0) return rc;
   DevErr z = {0, 0, 0, 0};
   return cuda_status(cudaMemcpyToSymbol(g_bwd_err, &z, sizeof(z)), "clear backward error word");
+}
+
+int bwd_error_word_on(DevErr* out, cudaStream_t s) {
+  int rc = cuda_status(cudaMemcpyFromSymbolAsync(out, g_bwd_err, sizeof(DevErr), 0, cudaMemcpyDeviceToHost, s),
+                       "read backward error word");
+  if (rc == CQSA_OK) rc = cuda_status(cudaStreamSynchronize(s), "read backward error word");
+  if (rc != CQSA_OK || out->code == 0) return rc;
+  static const DevErr z = {0, 0, 0, 0};
+  rc = cuda_status(cudaMemcpyToSymbolAsync(g_bwd_err, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s),
+                   "clear backward error word");
+  if (rc == CQSA_OK) rc = cuda_status(cudaStreamSynchronize(s), "clear backward error word");
+  return rc;
 }
 
 }  // namespace cqsa

@@ -16,10 +16,6 @@
 // Tensor memory (512 columns), fp16 d = 64: S0 | S1 | P0 | P1 | O0 | O1 at 0, 128, 256, 320, 384, 448,
 // so S_t(j+1) is computed while the softmax still stores P_t(j); d = 128 and bf16 write P over S.
 //
-// attn_fwd_kernel (kept as an independent structure that a test compares bit for bit): one 128-row
-// query tile per CTA, warp 0 TMA, warp 1 MMA, warps 2..5 softmax; S at 0, a P double buffer at 128 and
-// 256 (bf16: P_hi in the first 64 columns, P_lo in the second 64), O at 384.
-//
 // bf16: P rounded to bf16 alone (8-bit significand) costs ~2^-9 relative per weight; P is split into
 // P_hi = bf16(p) and P_lo = bf16(p - P_hi) and both are multiplied into O (as the hi/lo operand split
 // of the prompt-attention kernel in the "Strata" pull request #800 does for fp16), ~2^-17 overall.
@@ -48,7 +44,6 @@ namespace {
 
 constexpr int BM = 128;        // query rows per tile
 constexpr int BN = 128;        // keys per tile
-constexpr int NTHREADS = 192;  // 6 warps
 // m_ref is raised (to ceil of the tile's row max) whenever a tile's row max exceeds it, so every
 // exponent argument is <= 0: ex2.approx is exactly covariant under integer shifts of its argument
 // only while the argument keeps its sign, and the chunked and monolithic paths (whose m_ref differ
@@ -57,7 +52,6 @@ constexpr int NTHREADS = 192;  // 6 warps
 constexpr float TAU = 0.0f;
 constexpr uint32_t TILE_BYTES = 128 * 64 * 2;  // one 128 x 64 box of 16-bit elements
 constexpr uint32_t TMEM_COLS = 512;
-constexpr uint32_t COL_S = 0, COL_P = 128, COL_O = 384;
 
 struct KParams {
   int H, BH;
@@ -75,15 +69,6 @@ struct KParams {
   int fault;  // test hook: 1 = block 0 never loads key tile 1 (its waits must time out cleanly)
 };
 
-template <int D>
-struct Cfg {
-  static constexpr int KSUB = D / 64;
-  static constexpr int STAGES = (D == 64) ? 4 : 2;
-  static constexpr uint32_t Q_BYTES = KSUB * TILE_BYTES;
-  static constexpr uint32_t KV_BYTES = KSUB * TILE_BYTES;
-  static constexpr int NBARS = 1 + 3 * STAGES + 1 + 1 + 2 + 1 + 1 + 1;
-  static constexpr uint32_t SMEM_BYTES = 1024 + Q_BYTES + 2 * STAGES * KV_BYTES + NBARS * 8 + 16;
-};
 
 __device__ __forceinline__ void record_error(int code, int where) {
   if (atomicCAS(&g_dev_err.code, 0, code) == 0) {
@@ -92,27 +77,9 @@ __device__ __forceinline__ void record_error(int code, int where) {
   }
 }
 
-// Bounded wait that also gives up as soon as another role of this CTA has aborted.
-__device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, unsigned long long tmo,
-                                              volatile int* abort_flag, int code, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  uint32_t spins = 0;
-  while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
-    if ((++spins & 31u) == 0) {
-      if (*abort_flag) return false;
-      if (globaltimer_ns() - t0 > tmo) {
-        record_error(code, where);
-        *abort_flag = 1;
-        return false;
-      }
-    }
-  }
-}
-
-// wait_or_abort on 32-bit shared addresses with a microsecond limit; the waiting thread sleeps in
-// try_wait (woken when the phase completes) between checks of the abort flag and the clock.
+// Bounded wait on a 32-bit shared address with a microsecond limit that also gives up as soon as another
+// role of this CTA has aborted; the waiting thread sleeps in try_wait (woken when the phase completes)
+// between checks of the abort flag and the clock.
 __device__ __forceinline__ bool wait_or_abort_a(uint32_t bar, uint32_t parity, uint32_t tmo_us, uint32_t abort_addr,
                                                 int code, int where) {
   if (mbar_try_wait_a(bar, parity)) return true;
@@ -182,379 +149,6 @@ __device__ __forceinline__ float2 exp_pair(float x0, float x1, float2 sl2v, floa
 __device__ __forceinline__ long long out_row_index(int layout, int b, int h, int H, int N, int i) {
   return layout == CQSA_LAYOUT_BHND ? (static_cast<long long>(b) * H + h) * N + i
                                     : (static_cast<long long>(b) * N + i) * H + h;
-}
-
-template <int D, int DT, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(NTHREADS, 1)
-    attn_fwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                    const __grid_constant__ CUtensorMap tmV, const KParams p) {
-  using C = Cfg<D>;
-  constexpr int STAGES = C::STAGES;
-  constexpr int KSUB = C::KSUB;
-
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sQ = smem;
-  uint8_t* sK = sQ + C::Q_BYTES;
-  uint8_t* sV = sK + STAGES * C::KV_BYTES;
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES);
-  uint64_t* bar_q = bars;
-  uint64_t* bar_k_full = bar_q + 1;
-  uint64_t* bar_v_full = bar_k_full + STAGES;
-  uint64_t* bar_kv_empty = bar_v_full + STAGES;
-  uint64_t* bar_s_full = bar_kv_empty + STAGES;
-  uint64_t* bar_s_free = bar_s_full + 1;
-  uint64_t* bar_p_full = bar_s_free + 1;
-  uint64_t* bar_o_done = bar_p_full + 2;
-  uint64_t* bar_mma_idle = bar_o_done + 1;
-  uint64_t* bar_o_final = bar_mma_idle + 1;  // single phase: every PV of this tile is complete
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_o_final + 1);
-  volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
-
-  const int warp = threadIdx.x >> 5;
-  const int lane = threadIdx.x & 31;
-
-  // Work unit: heaviest (latest) query tiles first so causal load imbalance drains early.
-  const int unit = blockIdx.x;
-  const int qt = p.n_q_tiles - 1 - unit / p.BH;
-  const int bh = unit % p.BH;
-  const int b = bh / p.H;
-  const int h = bh % p.H;
-  const int q0 = qt * BM;
-  const int q_rows = min(BM, p.Nq - q0);
-
-  int n_kv = (p.Nkv + BN - 1) / BN;
-  if (CAUSAL) {
-    const long long last_key = p.q_off + q0 + q_rows - 1 - p.kv_off;  // largest allowed key index
-    n_kv = last_key < 0 ? 0 : (last_key / BN + 1 < n_kv ? static_cast<int>(last_key / BN + 1) : n_kv);
-  }
-
-  if (threadIdx.x == 0) {
-    mbar_init(bar_q, 1);
-    for (int s = 0; s < STAGES; ++s) {
-      mbar_init(&bar_k_full[s], 1);
-      mbar_init(&bar_v_full[s], 1);
-      mbar_init(&bar_kv_empty[s], 1);
-    }
-    mbar_init(bar_s_full, 1);
-    mbar_init(bar_s_free, 128);
-    mbar_init(&bar_p_full[0], 128);
-    mbar_init(&bar_p_full[1], 128);
-    mbar_init(bar_o_done, 1);
-    mbar_init(bar_mma_idle, 1);
-    mbar_init(bar_o_final, 1);
-    *abort_flag = 0;
-    fence_mbar_init();
-  }
-  if (warp == 1) {
-    __syncwarp();
-    tmem_alloc(tmem_slot, TMEM_COLS);
-    tmem_relinquish();
-  }
-  if (warp == 0 && lane == 0) {
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
-  }
-  tc_fence_before();
-  __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const unsigned long long tmo = p.timeout_ns;
-
-  if (warp == 0) {
-    // ------------------------------------------------------------------ TMA producer
-    if (lane == 0 && n_kv > 0) {
-      mbar_arrive_expect_tx(bar_q, C::Q_BYTES);
-#pragma unroll
-      for (int s = 0; s < KSUB; ++s) tma_load_4d(sQ + s * TILE_BYTES, &tmQ, bar_q, s * 64, q0, h, b);
-      int issued = 0;
-      for (int j = 0; j < n_kv; ++j) {
-        const int stage = j % STAGES;
-        const uint32_t round = j / STAGES;
-        if (!wait_or_abort(&bar_kv_empty[stage], (round & 1u) ^ 1u, tmo, abort_flag, kDevTimeoutKV, 0)) break;
-        mbar_arrive_expect_tx(&bar_k_full[stage], C::KV_BYTES);
-#pragma unroll
-        for (int s = 0; s < KSUB; ++s)
-          tma_load_4d(sK + stage * C::KV_BYTES + s * TILE_BYTES, &tmK, &bar_k_full[stage], s * 64, j * BN, h, b);
-        mbar_arrive_expect_tx(&bar_v_full[stage], C::KV_BYTES);
-#pragma unroll
-        for (int s = 0; s < KSUB; ++s)
-          tma_load_4d(sV + stage * C::KV_BYTES + s * TILE_BYTES, &tmV, &bar_v_full[stage], s * 64, j * BN, h, b);
-        issued = j + 1;
-      }
-      if (*abort_flag) {
-        // Drain: every load issued must land before the CTA may exit (bounded; no abort check).
-        for (int j = max(0, issued - STAGES); j < issued; ++j) {
-          const int stage = j % STAGES;
-          const uint32_t par = (j / STAGES) & 1u;
-          mbar_wait_bounded(&bar_k_full[stage], par, tmo);
-          mbar_wait_bounded(&bar_v_full[stage], par, tmo);
-        }
-        mbar_wait_bounded(bar_q, 0, tmo);
-      }
-    }
-  } else if (warp == 1) {
-    // ------------------------------------------------------------------ MMA issuer
-    if (lane == 0 && n_kv > 0) {
-      constexpr uint32_t IDESC_S = idesc_f16(DT, 0, 128, 128);  // Q, K both K-major
-      constexpr uint32_t IDESC_O = idesc_f16(DT, 1, 128, 64);   // V is MN-major (d contiguous)
-      const uint32_t sQa = smem_u32(sQ), sKa = smem_u32(sK), sVa = smem_u32(sV);
-      bool ok = wait_or_abort(bar_q, 0, tmo, abort_flag, kDevTimeoutQ, 1);
-      // S_j = Q K_j^T into the single S buffer. For j >= 1 the softmax must have read S_{j-1}.
-      auto issue_s = [&](int j) -> bool {
-        const int stage = j % STAGES;
-        if (!wait_or_abort(&bar_k_full[stage], (j / STAGES) & 1u, tmo, abort_flag, kDevTimeoutKV, 2)) return false;
-        if (j >= 1 && !wait_or_abort(bar_s_free, (j - 1) & 1u, tmo, abort_flag, kDevTimeoutSoftmax, 3)) return false;
-        tc_fence_after();
-#pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * TILE_BYTES + (ks & 3) * 32;
-          const uint64_t a = smem_desc_sw128(sQa + off, 16, 1024);
-          const uint64_t bd = smem_desc_sw128(sKa + stage * C::KV_BYTES + off, 16, 1024);
-          mma_ss(tmem + COL_S, a, bd, IDESC_S, ks > 0 ? 1u : 0u);
-        }
-        tc_commit(bar_s_full);
-        return true;
-      };
-      // O += P_j V_j; for bf16, P = P_hi + P_lo and both halves are multiplied into O.
-      auto issue_pv = [&](int j) -> bool {
-        const int stage = j % STAGES;
-        if (!wait_or_abort(&bar_p_full[j & 1], (j >> 1) & 1u, tmo, abort_flag, kDevTimeoutSoftmax, 4)) return false;
-        if (!wait_or_abort(&bar_v_full[stage], (j / STAGES) & 1u, tmo, abort_flag, kDevTimeoutKV, 5)) return false;
-        tc_fence_after();
-        const uint32_t pbase = tmem + COL_P + (j & 1) * 128;
-#pragma unroll
-        for (int ks = 0; ks < BN / 16; ++ks) {
-#pragma unroll
-          for (int s = 0; s < KSUB; ++s) {
-            // 16 keys x 64 features per descriptor: 2 swizzle atoms of 8 keys along K (1024 B apart);
-            // the feature extent is exactly one 128-byte atom, so both offsets are set to 1024.
-            const uint64_t bd = smem_desc_sw128(sVa + stage * C::KV_BYTES + s * TILE_BYTES + ks * 2048, 1024, 1024);
-            mma_ts(tmem + COL_O + s * 64, pbase + ks * 8, bd, IDESC_O, (j > 0 || ks > 0) ? 1u : 0u);
-            if (DT) mma_ts(tmem + COL_O + s * 64, pbase + 64 + ks * 8, bd, IDESC_O, 1u);
-          }
-        }
-        tc_commit(&bar_kv_empty[stage]);
-        tc_commit(bar_o_done);
-        return true;
-      };
-      if (ok) ok = issue_s(0);
-      for (int j = 0; ok && j < n_kv; ++j) {
-        if (j + 1 < n_kv) ok = issue_s(j + 1);
-        if (ok) ok = issue_pv(j);
-      }
-      // The epilogue waits on its own barrier: o_done phases are only safe to wait on one tile
-      // behind (S_{j+1} is issued before PV_j, so o_done may trail the softmax by two phases).
-      if (ok) tc_commit(bar_o_final);
-      // Every MMA of this thread must be complete before tensor memory is released.
-      tc_commit(bar_mma_idle);
-      mbar_wait_bounded(bar_mma_idle, 0, tmo);
-    }
-  } else {
-    // ------------------------------------------------------------------ softmax warpgroup
-    const int quarter = warp & 3;             // TMEM lane quarter this warp may access
-    const int r = quarter * 32 + lane;        // row within the tile
-    const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
-    const int qi = q0 + r;
-    const long long qpos = p.q_off + qi;
-    const float sl2 = p.scale_log2;
-    float m_ref = -INFINITY;
-    float l = 0.0f;
-    bool ok = true;
-
-    for (int j = 0; j < n_kv; ++j) {
-      // tcgen05.ld/st are warp-collective (.sync.aligned): every exit decision is made warp-uniform.
-      ok = wait_or_abort(bar_s_full, j & 1u, tmo, abort_flag, kDevTimeoutMMA, 6);
-      if (!__all_sync(0xffffffffu, ok)) {
-        ok = false;
-        break;
-      }
-      tc_fence_after();
-      uint32_t sr[128];
-#pragma unroll
-      for (int c = 0; c < 4; ++c)
-        tmem_ld32(trow + COL_S + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tmem_wait_ld();
-#pragma unroll
-      for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-      tc_fence_before();
-      mbar_arrive(bar_s_free);  // the S buffer may now take S_{j+1}
-
-      float x[128];
-#pragma unroll
-      for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-      const int k0 = j * BN;
-      const bool tail = (k0 + BN > p.Nkv);
-      const bool diag = CAUSAL && (p.kv_off + k0 + BN - 1 > p.q_off + q0);
-      if (tail || diag) {
-        // valid keys of this row in this tile: c < lim
-        long long lim = p.Nkv - k0;
-        if (CAUSAL) {
-          const long long lc = qpos - p.kv_off - k0 + 1;
-          lim = lc < lim ? lc : lim;
-        }
-#pragma unroll
-        for (int c = 0; c < 128; ++c)
-          if (c >= lim) x[c] = -INFINITY;
-      }
-      const float tmax = row_max128(x) * sl2;
-      float alpha = 1.0f;
-      bool rescale = false;
-      if (tmax > m_ref + TAU) {
-        const float m_new = ceilf(tmax);
-        if (m_ref != -INFINITY) {
-          alpha = exp2_int(m_ref - m_new);
-          rescale = true;
-        }
-        m_ref = m_new;
-      }
-      // Exponent argument: t = fl(x * scale * log2 e + 192) lies on a grid fixed by x alone (2^-16
-      // for |t - 192| < 64), so t - (192 + m_ref) is exact and p for two different integer m_ref
-      // differ by an exact power of two; the 16-bit rounding of P then commutes with that factor.
-      const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
-      const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
-      float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-      const uint32_t pbuf = trow + COL_P + (j & 1) * 128;
-#pragma unroll
-      for (int c4 = 0; c4 < 4; ++c4) {
-        uint32_t hi[16], lo[16];
-#pragma unroll
-        for (int e = 0; e < 16; ++e) {
-          const int c = c4 * 16 + e;  // pair index: keys 2c, 2c+1
-          const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
-          rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
-          if (DT) {
-            __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
-            const float2 hf = __bfloat1622float2(h2);
-            __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
-            hi[e] = *reinterpret_cast<uint32_t*>(&h2);
-            lo[e] = *reinterpret_cast<uint32_t*>(&l2);
-          } else {
-            hi[e] = pack2(pp.x, pp.y, 0);
-          }
-        }
-        tmem_st16(pbuf + c4 * 16, hi);
-        if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
-      }
-      l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
-      if (__any_sync(0xffffffffu, rescale) && j > 0) {
-        // O must hold the result of PV(j-1) before it is scaled (alpha is 1 on rows that keep m_ref).
-        // Parity wait on phase j-1 is exact here: S_j complete implies PV(j-2) complete (S_j is
-        // issued after it), and PV(j) cannot start before this thread's p_full arrival.
-        ok = wait_or_abort(bar_o_done, (j - 1) & 1u, tmo, abort_flag, kDevTimeoutMMA, 7);
-        if (!__all_sync(0xffffffffu, ok)) {
-          ok = false;
-          break;
-        }
-        tc_fence_after();
-#pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(trow + COL_O + c * 32, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-#pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-          tmem_st32(trow + COL_O + c * 32, o);
-        }
-      }
-      tmem_wait_st();
-      tc_fence_before();
-      mbar_arrive(&bar_p_full[j & 1]);
-    }
-
-    // ---------------------------------------------------------------- epilogue
-    if (ok && n_kv > 0) {
-      ok = wait_or_abort(bar_o_final, 0, tmo, abort_flag, kDevTimeoutMMA, 8);
-      ok = __all_sync(0xffffffffu, ok);
-      tc_fence_after();
-    }
-    const bool has = (n_kv > 0) && (l > 0.0f);
-    const float inv_l = has ? 1.0f / l : 0.0f;
-    const float lse_v = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-    const bool store = ok && qi < p.Nq;
-    const long long row = out_row_index(p.out_layout, b, h, p.H, p.Nq, qi);
-    const long long lrow = static_cast<long long>(bh) * p.Nq + qi;
-    // Accumulate mode: weights of the running accumulator (wa) and of this pair (wn).
-    bool write = store;
-    bool fresh = true;  // accumulator empty: this pair's result is written as is
-    float wa = 0.0f, wn = 1.0f, lse_out = lse_v;
-    if (MODE == kModeAccum && store) {
-      if (!has) {
-        write = false;  // nothing allowed in this pair: the accumulator stays as it is
-      } else {
-        const float la = p.lse_part[lrow];
-        if (la != -INFINITY) {
-          fresh = false;
-          const float M = fmaxf(la, lse_v);
-          const float L = M + logf(expf(la - M) + expf(lse_v - M));
-          wa = expf(la - L);
-          wn = expf(lse_v - L);
-          lse_out = L;
-        }
-      }
-    }
-#pragma unroll
-    for (int c = 0; c < D / 32; ++c) {
-      uint32_t o[32];
-      if (ok && n_kv > 0) {
-        tmem_ld32(trow + COL_O + c * 32, o);
-        tmem_wait_ld();
-        reg_fence32(o);
-      } else {
-#pragma unroll
-        for (int e = 0; e < 32; ++e) o[e] = 0u;
-      }
-      float v[32];
-#pragma unroll
-      for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
-      if (write) {
-        if (MODE == kModeOut) {
-          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
-#pragma unroll
-          for (int q8 = 0; q8 < 4; ++q8) {
-            uint4 w;
-            w.x = pack2(v[8 * q8 + 0], v[8 * q8 + 1], DT);
-            w.y = pack2(v[8 * q8 + 2], v[8 * q8 + 3], DT);
-            w.z = pack2(v[8 * q8 + 4], v[8 * q8 + 5], DT);
-            w.w = pack2(v[8 * q8 + 6], v[8 * q8 + 7], DT);
-            dst[q8] = w;
-          }
-        } else {
-          float4* dst = reinterpret_cast<float4*>(p.o_part + row * D + c * 32);
-#pragma unroll
-          for (int q4 = 0; q4 < 8; ++q4) {
-            float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            if (MODE == kModeAccum && !fresh) {
-              const float4 a = dst[q4];
-              w.x = wa * a.x + wn * w.x;
-              w.y = wa * a.y + wn * w.y;
-              w.z = wa * a.z + wn * w.z;
-              w.w = wa * a.w + wn * w.w;
-            }
-            dst[q4] = w;
-          }
-        }
-      }
-    }
-    if (write) {
-      if (MODE == kModeOut) {
-        if (p.lse) p.lse[lrow] = lse_v;
-      } else {
-        p.lse_part[lrow] = lse_out;
-      }
-    }
-  }
-
-  // ------------------------------------------------------------------ teardown
-  tc_fence_before();
-  __syncthreads();
-  if (warp == 1) {
-    __syncwarp();
-    tc_fence_after();
-    tmem_dealloc(tmem, TMEM_COLS);
-  }
 }
 
 // MMA issue from one elected lane of a converged warp, with descriptors prepared by the whole warp
@@ -1155,32 +749,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   }
 }
 
-// Single-tile kernel (one 128-row query tile per CTA), selected only by CQSA_ATTN_SINGLE_TILE=1 to
-// compare against the two-tile kernel (both compute every row with the same operation sequence).
-bool single_tile_kernel() {
-  const char* e = getenv("CQSA_ATTN_SINGLE_TILE");
-  return e && e[0] == '1';
-}
-
 template <int D, int DT, bool CAUSAL, int MODE>
 int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, KParams kp, int Nq, int BH,
              cudaStream_t stream) {
-  if (single_tile_kernel()) {
-    auto kern = attn_fwd_kernel<D, DT, CAUSAL, MODE>;
-    static bool attr_done = false;  // per instantiation; idempotent
-    if (!attr_done) {
-      cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg<D>::SMEM_BYTES);
-      if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem)");
-      attr_done = true;
-    }
-    kp.n_q_tiles = (Nq + BM - 1) / BM;
-    const long long grid = static_cast<long long>(kp.n_q_tiles) * BH;
-    kern<<<static_cast<int>(grid), NTHREADS, Cfg<D>::SMEM_BYTES, stream>>>(mq, mk, mv, kp);
-    return cuda_status(cudaGetLastError(), "attention kernel launch");
-  }
   auto kern = attn_fwd2_kernel<D, DT, CAUSAL, MODE>;
-  static bool attr2_done = false;
-  if (!attr2_done) {
+  static PerDeviceOnce attr;  // the attributes belong to each device's context
+  int dev = 0;
+  if (!attr.done(&dev)) {
     // setmaxnreg.inc waits until its registers are free: the launch must hold at least the split,
     // or the softmax warpgroups would wait forever. Refuse to launch otherwise.
     cudaFuncAttributes fa;
@@ -1193,7 +768,7 @@ int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
     }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<D, DT>::SMEM_BYTES);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem)");
-    attr2_done = true;
+    attr.mark(dev);
   }
   kp.n_q_tiles = (Nq + 2 * BM - 1) / (2 * BM);  // pairs of query tiles
   const long long grid = static_cast<long long>(kp.n_q_tiles) * BH;
@@ -1232,9 +807,10 @@ EncodeTiledFn get_encode_fn() {
   return fn;
 }
 
-// 4-D map over a [B,H,N,d] (layout BHND) or [B,N,H,d] (BNHD) tensor: dims (d, N, H, B), box (64,128,1,1),
+// 4-D map over tokens [0, N) of a [B,H,Nalloc,d] (layout BHND) or [B,Nalloc,H,d] (BNHD) tensor: dims
+// (d, N, H, B), box (64,128,1,1),
 // 128-byte swizzle (the box row is exactly 128 bytes), zero fill outside the tensor.
-int make_map(CUtensorMap* m, const void* base, int dtype, int layout, int B, int H, int N, int d) {
+int make_map(CUtensorMap* m, const void* base, int dtype, int layout, int B, int H, int N, int d, long long Nalloc) {
   EncodeTiledFn enc = get_encode_fn();
   if (!enc) {
     set_error("cuTensorMapEncodeTiled is not available from the driver");
@@ -1243,15 +819,17 @@ int make_map(CUtensorMap* m, const void* base, int dtype, int layout, int B, int
   const cuuint64_t es = 2;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(d), static_cast<cuuint64_t>(N > 0 ? N : 1),
                         static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  // Nalloc: tokens per head in the buffer (>= N); the map covers tokens [0, N) of each head
+  const cuuint64_t na = static_cast<cuuint64_t>(Nalloc > N ? Nalloc : (N > 0 ? N : 1));
   cuuint64_t strides[3];
   if (layout == CQSA_LAYOUT_BHND) {
     strides[0] = d * es;
-    strides[1] = static_cast<cuuint64_t>(N > 0 ? N : 1) * d * es;
-    strides[2] = static_cast<cuuint64_t>(H) * (N > 0 ? N : 1) * d * es;
+    strides[1] = na * d * es;
+    strides[2] = static_cast<cuuint64_t>(H) * na * d * es;
   } else {
     strides[0] = static_cast<cuuint64_t>(H) * d * es;
     strides[1] = d * es;
-    strides[2] = static_cast<cuuint64_t>(N > 0 ? N : 1) * H * d * es;
+    strides[2] = na * H * d * es;
   }
   cuuint32_t box[4] = {64, 128, 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
@@ -1274,6 +852,18 @@ int device_error_word(DevErr* out, int clear) {
   return cuda_status(cudaMemcpyToSymbol(g_dev_err, &z, sizeof(z)), "clear device error word");
 }
 
+int device_error_word_on(DevErr* out, cudaStream_t s) {
+  int rc = cuda_status(cudaMemcpyFromSymbolAsync(out, g_dev_err, sizeof(DevErr), 0, cudaMemcpyDeviceToHost, s),
+                       "read device error word");
+  if (rc == CQSA_OK) rc = cuda_status(cudaStreamSynchronize(s), "read device error word");
+  if (rc != CQSA_OK || out->code == 0) return rc;
+  static const DevErr z = {0, 0, 0, 0};
+  rc = cuda_status(cudaMemcpyToSymbolAsync(g_dev_err, &z, sizeof(z), 0, cudaMemcpyHostToDevice, s),
+                   "clear device error word");
+  if (rc == CQSA_OK) rc = cuda_status(cudaStreamSynchronize(s), "clear device error word");
+  return rc;
+}
+
 int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   if (a.Nq <= 0) return CQSA_OK;
   CUtensorMap mq, mk, mv;
@@ -1281,9 +871,10 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   const void* kb = a.Nkv > 0 ? a.k : a.q;
   const void* vb = a.Nkv > 0 ? a.v : a.q;
   const int nkv_map = a.Nkv > 0 ? a.Nkv : a.Nq;
-  int rc = make_map(&mq, a.q, a.dtype, a.in_layout, a.B, a.H, a.Nq, a.d);
-  if (rc == CQSA_OK) rc = make_map(&mk, kb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d);
-  if (rc == CQSA_OK) rc = make_map(&mv, vb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d);
+  const long long kv_alloc = a.Nkv > 0 ? a.kv_tokens_alloc : a.q_tokens_alloc;
+  int rc = make_map(&mq, a.q, a.dtype, a.in_layout, a.B, a.H, a.Nq, a.d, a.q_tokens_alloc);
+  if (rc == CQSA_OK) rc = make_map(&mk, kb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d, kv_alloc);
+  if (rc == CQSA_OK) rc = make_map(&mv, vb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d, kv_alloc);
   if (rc != CQSA_OK) return rc;
   KParams kp;
   kp.H = a.H;

@@ -49,18 +49,20 @@ int scratch_for_current_device(void** out) {
   return CQSA_OK;
 }
 
-// out[bh, t0 + i, :] and lse[bh, t0 + i] of one (b, h) query chunk of n rows from the fp32 accumulator
-// acc[i, :] (output [B,H,N,d] in dtype).
+// out[g0 + g, t0 + i, :] and lse[g0 + g, t0 + i] of one query chunk of n rows for heads g0 .. g0 + gn - 1 of
+// a [B*H, N, d] output (dtype) from the fp32 accumulator acc[g, i, :] and lacc[g, i].
 __global__ void static_finalize_kernel(const float* __restrict__ acc, const float* __restrict__ lacc, void* out,
-                                       float* lse, int n, int N, long long bh, int t0, int d, int dtype) {
-  const long long total4 = static_cast<long long>(n) * d / 4;
+                                       float* lse, int gn, int n, int N, long long g0, int t0, int d, int dtype) {
   const int d4 = d / 4;
+  const long long total4 = static_cast<long long>(gn) * n * d4;
   for (long long e = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; e < total4;
        e += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int i = static_cast<int>(e / d4);
+    const long long gi = e / d4;  // g * n + i
     const int c4 = static_cast<int>(e % d4);
+    const int g = static_cast<int>(gi / n);
+    const int i = static_cast<int>(gi % n);
     const float4 v = reinterpret_cast<const float4*>(acc)[e];
-    const long long orow = bh * N + t0 + i;
+    const long long orow = (g0 + g) * N + t0 + i;
     uint2 w;
     if (dtype == CQSA_BF16) {
       __nv_bfloat162 x = __floats2bfloat162_rn(v.x, v.y), y = __floats2bfloat162_rn(v.z, v.w);
@@ -72,7 +74,7 @@ __global__ void static_finalize_kernel(const float* __restrict__ acc, const floa
       w.y = *reinterpret_cast<uint32_t*>(&y);
     }
     reinterpret_cast<uint2*>(out)[orow * d4 + c4] = w;
-    if (lse && c4 == 0) lse[orow] = lacc[i];
+    if (lse && c4 == 0) lse[orow] = lacc[gi];
   }
 }
 
@@ -115,42 +117,48 @@ extern "C" int cqsa_attn_fwd_chunked_static(const void* q, const void* k, const 
     return CQSA_ERR_INVALID;
   }
   const int C = chunk_tokens < N ? chunk_tokens : ((N + 127) / 128) * 128;
-  // One (b, h) at a time: a token range of one head of a [B,H,N,d] tensor is contiguous, so every
-  // chunk is an ordinary [1,1,n,d] tensor for the chunk kernel and only one head's accumulator
-  // (C x d fp32 + C fp32) lives in the scratch at a time.
-  const size_t acc_bytes = static_cast<size_t>(C) * d * sizeof(float);
-  const size_t need = acc_bytes + static_cast<size_t>(C) * sizeof(float);
-  if (need > kScratchBytes) {
+  // Heads are processed in groups of G consecutive (b, h) of the [B*H, N, d] tensors, as many as the
+  // scratch holds accumulators for (C x d fp32 + C fp32 each): one launch per chunk pair covers the
+  // whole group. A token range of the group is a strided view (N tokens per head), which the chunk
+  // kernel's tensor maps address directly.
+  const size_t per_head = static_cast<size_t>(C) * (d + 1) * sizeof(float);
+  if (per_head > kScratchBytes) {
     set_error("a %d-token chunk needs %zu bytes of fp32 accumulator; the static scratch holds %zu "
-              "(lower chunk_tokens)", C, need, kScratchBytes);
+              "(lower chunk_tokens)", C, per_head, kScratchBytes);
     return CQSA_ERR_UNSUPPORTED;
   }
+  const long long BH = static_cast<long long>(B) * H;
+  const long long G = static_cast<long long>(kScratchBytes / per_head) < BH
+                          ? static_cast<long long>(kScratchBytes / per_head) : BH;
   void* base = nullptr;
   int rc = scratch_for_current_device(&base);
   if (rc != CQSA_OK) return rc;
   float* acc = static_cast<float*>(base);
-  float* lacc = reinterpret_cast<float*>(static_cast<unsigned char*>(base) + acc_bytes);
   const float sc = scale == 0.0f ? 1.0f / sqrtf(static_cast<float>(d)) : scale;
   const size_t es = 2;
   const int nch = (N + C - 1) / C;
-  for (long long bh = 0; bh < static_cast<long long>(B) * H; ++bh) {
-    const size_t head = static_cast<size_t>(bh) * N * d * es;
+  for (long long g0 = 0; g0 < BH; g0 += G) {
+    const int gn = static_cast<int>(BH - g0 < G ? BH - g0 : G);
+    const size_t group = static_cast<size_t>(g0) * N * d * es;
     for (int i = 0; i < nch; ++i) {
       const int qt0 = i * C;
       const int qn = N - qt0 < C ? N - qt0 : C;
+      float* lacc = acc + static_cast<size_t>(gn) * qn * d;  // [gn, qn] after the [gn, qn, d] accumulator
       const int last_j = causal ? i : nch - 1;
       for (int j = 0; j <= last_j; ++j) {
         const int kt0 = j * C;
         const int kn = N - kt0 < C ? N - kt0 : C;
         AttnArgs a;
         memset(&a, 0, sizeof(a));
-        a.q = static_cast<const char*>(q) + head + static_cast<size_t>(qt0) * d * es;
-        a.k = static_cast<const char*>(k) + head + static_cast<size_t>(kt0) * d * es;
-        a.v = static_cast<const char*>(v) + head + static_cast<size_t>(kt0) * d * es;
+        a.q = static_cast<const char*>(q) + group + static_cast<size_t>(qt0) * d * es;
+        a.k = static_cast<const char*>(k) + group + static_cast<size_t>(kt0) * d * es;
+        a.v = static_cast<const char*>(v) + group + static_cast<size_t>(kt0) * d * es;
         a.B = 1;
-        a.H = 1;
+        a.H = gn;
         a.Nq = qn;
         a.Nkv = kn;
+        a.q_tokens_alloc = N;
+        a.kv_tokens_alloc = N;
         a.q_off = qt0;
         a.kv_off = kt0;
         a.d = d;
@@ -165,9 +173,10 @@ extern "C" int cqsa_attn_fwd_chunked_static(const void* q, const void* k, const 
         rc = launch_attention(a, stream);
         if (rc != CQSA_OK) return rc;
       }
-      const long long total4 = static_cast<long long>(qn) * d / 4;
-      const int blocks = static_cast<int>((total4 + 255) / 256);
-      static_finalize_kernel<<<blocks, 256, 0, stream>>>(acc, lacc, out, lse, qn, N, bh, qt0, d, dtype);
+      const long long total4 = static_cast<long long>(gn) * qn * d / 4;
+      const long long want = (total4 + 255) / 256;
+      const int blocks = static_cast<int>(want < 4096 ? want : 4096);
+      static_finalize_kernel<<<blocks, 256, 0, stream>>>(acc, lacc, out, lse, gn, qn, N, g0, qt0, d, dtype);
       rc = cuda_status(cudaGetLastError(), "static finalize launch");
       if (rc != CQSA_OK) return rc;
     }

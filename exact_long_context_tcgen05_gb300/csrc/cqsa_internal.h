@@ -4,6 +4,8 @@
 #include <cuda_runtime.h>
 #include <stdint.h>
 
+#include <atomic>
+
 #include "../../include/cqsa.h"
 
 namespace cqsa {
@@ -34,6 +36,9 @@ struct AttnArgs {
   float* o_part;        // kModePart / kModeAccum: fp32 [B,H,Nq,d] (or token-major)
   float* lse_part;      // fp32 [B,H,Nq]
   int out_layout;       // layout of out / o_part
+  long long q_tokens_alloc;   // tokens per head in the q buffer when it is a token range of a longer
+                              // tensor (its strides follow this count); 0: the buffer holds Nq tokens
+  long long kv_tokens_alloc;  // the same for k / v; 0: Nkv
 };
 
 // Validates nothing (the ABI layer does); encodes tensor maps and launches on `stream`.
@@ -94,6 +99,30 @@ int pool_event(cudaEvent_t* e, bool timing);
 void pool_event_free(cudaEvent_t e, bool timing);
 int pool_stream(cudaStream_t* s);
 void pool_stream_free(cudaStream_t s);
+
+// Set-up that belongs to one device's context (kernel function attributes, cached device attributes)
+// runs once per device: bit `dev` records it. Concurrent first calls may both run the set-up, which is
+// idempotent; devices numbered 64 and above repeat it on every call.
+struct PerDeviceOnce {
+  std::atomic<unsigned long long> bits{0};
+  // true when the current device's set-up has run; *dev receives the current device (-1 on error)
+  bool done(int* dev) const {
+    if (cudaGetDevice(dev) != cudaSuccess) {
+      *dev = -1;
+      return false;
+    }
+    return *dev >= 0 && *dev < 64 && ((bits.load(std::memory_order_acquire) >> *dev) & 1ull);
+  }
+  void mark(int dev) {
+    if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_acq_rel);
+  }
+};
+
+// The device error words (set by a kernel whose bounded wait gave up), read after the caller's own
+// streams have drained: each word is copied on `s` and `s` is synchronised, so no other stream of the
+// process is waited for. A set word is cleared and reported as CQSA_ERR_TIMEOUT with its code, block
+// and site in the error message.
+int check_device_error_on(cudaStream_t s);
 
 // Status helpers
 void set_error(const char* fmt, ...);

@@ -523,8 +523,8 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   CK(cudaStreamSynchronize(stream), "synchronize compute stream");
   CK(cudaStreamSynchronize(res.copy), "synchronize copy stream");
   {
-    int code = 0;
-    int r = cqsa_device_error(&code, nullptr, 1);
+    // the call's own streams have drained; read the device error words on the compute stream
+    int r = check_device_error_on(stream);
     if (r != CQSA_OK) return r;
   }
 #undef CK

@@ -165,6 +165,8 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
   // every use of the buffers is complete before they return to the pool
   cudaError_t se = cudaStreamSynchronize(stream);
   if (rc == CQSA_OK) rc = cuda_status(se, "synchronize");
+  // a kernel whose bounded wait gave up leaves its gradients incomplete: report it
+  if (rc == CQSA_OK) rc = check_device_error_on(stream);
   pool_free(stage);
   pool_free(acc_kv);
   return rc;

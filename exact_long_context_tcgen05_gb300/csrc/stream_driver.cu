@@ -374,8 +374,8 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   CK(cudaStreamSynchronize(cx.res.copy), "synchronize copy stream");
   CK(cudaStreamSynchronize(cx.res.d2h), "synchronize d2h stream");
   {
-    int code = 0;
-    int r = cqsa_device_error(&code, nullptr, 1);
+    // the call's own streams have drained; read the device error words on the compute stream
+    int r = check_device_error_on(stream);
     if (r != CQSA_OK) return r;
   }
 #undef CK

@@ -5,7 +5,8 @@ leg may import this package; the library in ``exact_long_context_tcgen05_gb300``
 shares no code with it. The arithmetic is in ``oracle.c`` (plain C, double precision, OpenMP over
 rows), which states the definition it follows and where the pages state the problem.
 
-The backward (``attn_bwd``, ``attn_bwd_f64``) is the chain rule through the softmax, pinned in
+The backward (``attn_bwd``, ``attn_bwd_f64``; at listed rows or columns ``attn_bwd_rows`` and
+``attn_bwd_cols``, which agree with ``attn_bwd`` wherever both run) is the chain rule through the softmax, pinned in
 ``tests/test_oracle_bwd.py`` by central finite differences of the loss sum(dO * O), by sympy's symbolic
 gradient of the written-out loss on a 3-token problem, by the forward
 part agreeing with ``attn_full``, by the key-shift invariance sum_j dK_j = 0 and by the uniform-score
@@ -68,6 +69,12 @@ def _load():
             lib.oracle_attn_bwd.restype = ctypes.c_int
             lib.oracle_attn_bwd.argtypes = [_p, _p, _p, _p, _i64, _i64, _i64, _i64, ctypes.c_int, ctypes.c_double,
                                             _p, _p, _p, _p, _p]
+            lib.oracle_attn_bwd_rows.restype = ctypes.c_int
+            lib.oracle_attn_bwd_rows.argtypes = [_p, _p, _p, _p, ctypes.c_int, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                                 ctypes.c_double, _p, _i64, _p]
+            lib.oracle_attn_bwd_cols.restype = ctypes.c_int
+            lib.oracle_attn_bwd_cols.argtypes = [_p, _p, _p, _p, ctypes.c_int, _i64, _i64, _i64, _i64, ctypes.c_int,
+                                                 ctypes.c_double, _p, _i64, _p, _p]
             _lib = lib
     return _lib
 
@@ -182,3 +189,42 @@ def attn_bwd(q, k, v, dout, *, B, H, N, d, causal, scale=None, dtype=F16):
     shape = (B, H, N, d)
     ws = [widen(x, dtype).reshape(shape) for x in (q, k, v, dout)]
     return attn_bwd_f64(*ws, causal=causal, scale=scale)
+
+
+def _triples(x) -> np.ndarray:
+    x = np.ascontiguousarray(x, dtype=np.int64)
+    if x.ndim != 2 or x.shape[1] != 3:
+        raise ValueError("expected an array of (b, h, index) triples")
+    return x
+
+
+def attn_bwd_rows(q, k, v, dout, *, B, H, N, d, causal, rows, scale=None, dtype=F16):
+    """dq (float64, [nrows, d]) of the listed (b, h, i) query rows of a [B,H,N,d] problem (16-bit bits)."""
+    scale = default_scale(d) if scale is None else float(np.float32(scale))
+    q, k, v, dout = (_u16(x) for x in (q, k, v, dout))
+    if any(x.size != B * H * N * d for x in (q, k, v, dout)):
+        raise ValueError("tensor sizes do not match B, H, N, d")
+    rows = _triples(rows)
+    dq = np.empty((len(rows), d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_rows(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, dtype, B, H, N,
+                                      d, int(bool(causal)), scale, rows.ctypes.data, len(rows), dq.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_rows rejected its arguments")
+    return dq
+
+
+def attn_bwd_cols(q, k, v, dout, *, B, H, N, d, causal, cols, scale=None, dtype=F16):
+    """dk, dv (float64, [ncols, d] each) of the listed (b, h, j) key columns of a [B,H,N,d] problem."""
+    scale = default_scale(d) if scale is None else float(np.float32(scale))
+    q, k, v, dout = (_u16(x) for x in (q, k, v, dout))
+    if any(x.size != B * H * N * d for x in (q, k, v, dout)):
+        raise ValueError("tensor sizes do not match B, H, N, d")
+    cols = _triples(cols)
+    dk = np.empty((len(cols), d), dtype=np.float64)
+    dv = np.empty((len(cols), d), dtype=np.float64)
+    rc = _load().oracle_attn_bwd_cols(q.ctypes.data, k.ctypes.data, v.ctypes.data, dout.ctypes.data, dtype, B, H, N,
+                                      d, int(bool(causal)), scale, cols.ctypes.data, len(cols), dk.ctypes.data,
+                                      dv.ctypes.data)
+    if rc != 0:
+        raise ValueError("oracle_attn_bwd_cols rejected its arguments")
+    return dk, dv

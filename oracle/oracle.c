@@ -351,3 +351,210 @@ int oracle_attn_bwd(const double* q, const double* k, const double* v, const dou
     free(dS);
     return 0;
 }
+
+/*
+ * The same gradients, evaluated only at listed rows or columns, for problems too large for
+ * oracle_attn_bwd (which holds a head's N x N matrices). Inputs are 16-bit storage bits in
+ * [B,H,N,d] (0 fp16, 1 bf16), widened exactly; `scale` as in oracle_attn_rows. The definitions are
+ * those above:
+ *   dQ_i  = scale sum_{j in A_i} dS_ij k_j,  dS_ij = P_ij (dP_ij - D_i),  D_i = sum_j P_ij dP_ij
+ *   dV_j  = sum_{i : j in A_i} P_ij dO_i,    dK_j = scale sum_{i : j in A_i} dS_ij q_i
+ * with P_ij = exp(s_ij - LSE_i), LSE_i = log sum_{j in A_i} exp(s_ij) and dP_ij = dO_i . v_j.
+ *
+ * oracle_attn_bwd_rows: dq (nrows x d) of the listed (b, h, i); each row needs only its own scores.
+ * oracle_attn_bwd_cols: dk, dv (ncols x d) of the listed (b, h, j); for every head holding a listed
+ * column it first evaluates LSE_i and D_i of every row of that head from their definitions, then the
+ * column sums over the rows that see the column.
+ * Both return 0, or -1 on a bad argument or allocation failure.
+ */
+
+/* this head's k, v (and q, dout when wanted) widened exactly to double, [N, d] each */
+static void widen_head(const uint16_t* src, int dtype, int64_t bh, int64_t N, int64_t d, double* dst) {
+#pragma omp parallel for schedule(static)
+    for (int64_t j = 0; j < N; ++j)
+        for (int64_t c = 0; c < d; ++c) dst[j * d + c] = widen(src, (bh * N + j) * d + c, dtype);
+}
+
+/* scores s_ij = scale q_i . k_j for j < jend, their max, and LSE_i = m + log sum exp(s_ij - m) */
+static double row_scores(const double* qi, const double* kd, int64_t jend, int64_t d, double scale, double* s) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < jend; ++j) {
+        double dot = 0.0;
+        for (int64_t c = 0; c < d; ++c) dot += qi[c] * kd[j * d + c];
+        s[j] = scale * dot;
+        if (s[j] > m) m = s[j];
+    }
+    nsum l = {0.0, 0.0};
+    for (int64_t j = 0; j < jend; ++j) nsum_add(&l, exp(s[j] - m));
+    return m + log(nsum_get(&l));
+}
+
+int oracle_attn_bwd_rows(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout, int dtype,
+                         int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                         const int64_t* rows, int64_t nrows, double* dq) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t r = 0; r < nrows; ++r) {
+        const int64_t* t = rows + 3 * r;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= N) return -1;
+    }
+    double* kd = (double*)malloc(sizeof(double) * (size_t)N * (size_t)d);
+    double* vd = (double*)malloc(sizeof(double) * (size_t)N * (size_t)d);
+    int bad = (!kd || !vd);
+    for (int64_t bh = 0; bh < B * H && !bad; ++bh) {
+        int64_t cnt = 0;
+        for (int64_t r = 0; r < nrows; ++r) cnt += (rows[3 * r] * H + rows[3 * r + 1] == bh);
+        if (cnt == 0) continue;
+        widen_head(k, dtype, bh, N, d, kd);
+        widen_head(v, dtype, bh, N, d, vd);
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)N);
+            double* dp = (double*)malloc(sizeof(double) * (size_t)N);
+            double* qi = (double*)malloc(sizeof(double) * (size_t)d);
+            double* gi = (double*)malloc(sizeof(double) * (size_t)d);
+            if (!s || !dp || !qi || !gi) {
+#pragma omp atomic write
+                bad = 1;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < nrows; ++r) {
+                if (bad || rows[3 * r] * H + rows[3 * r + 1] != bh) continue;
+                const int64_t i = rows[3 * r + 2];
+                const int64_t jend = causal ? i + 1 : N;
+                for (int64_t c = 0; c < d; ++c) {
+                    qi[c] = widen(q, (bh * N + i) * d + c, dtype);
+                    gi[c] = widen(dout, (bh * N + i) * d + c, dtype);
+                }
+                const double lse = row_scores(qi, kd, jend, d, scale, s);
+                nsum D = {0.0, 0.0};
+                for (int64_t j = 0; j < jend; ++j) {
+                    s[j] = exp(s[j] - lse); /* P_ij */
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c) dot += gi[c] * vd[j * d + c];
+                    dp[j] = dot;
+                    nsum_add(&D, s[j] * dot);
+                }
+                const double Dv = nsum_get(&D);
+                for (int64_t c = 0; c < d; ++c) {
+                    nsum a = {0.0, 0.0};
+                    for (int64_t j = 0; j < jend; ++j) nsum_add(&a, s[j] * (dp[j] - Dv) * kd[j * d + c]);
+                    dq[r * d + c] = scale * nsum_get(&a);
+                }
+            }
+            free(s);
+            free(dp);
+            free(qi);
+            free(gi);
+        }
+    }
+    free(kd);
+    free(vd);
+    return bad ? -1 : 0;
+}
+
+int oracle_attn_bwd_cols(const uint16_t* q, const uint16_t* k, const uint16_t* v, const uint16_t* dout, int dtype,
+                         int64_t B, int64_t H, int64_t N, int64_t d, int causal, double scale,
+                         const int64_t* cols, int64_t ncols, double* dk, double* dv) {
+    if (B < 1 || H < 1 || N < 1 || d < 1 || (dtype != 0 && dtype != 1)) return -1;
+    for (int64_t r = 0; r < ncols; ++r) {
+        const int64_t* t = cols + 3 * r;
+        if (t[0] < 0 || t[0] >= B || t[1] < 0 || t[1] >= H || t[2] < 0 || t[2] >= N) return -1;
+    }
+    const size_t nd = (size_t)N * (size_t)d;
+    double* qd = (double*)malloc(sizeof(double) * nd);
+    double* kd = (double*)malloc(sizeof(double) * nd);
+    double* vd = (double*)malloc(sizeof(double) * nd);
+    double* gd = (double*)malloc(sizeof(double) * nd);
+    double* lse = (double*)malloc(sizeof(double) * (size_t)N);
+    double* Dr = (double*)malloc(sizeof(double) * (size_t)N);
+    int bad = (!qd || !kd || !vd || !gd || !lse || !Dr);
+    for (int64_t bh = 0; bh < B * H && !bad; ++bh) {
+        int64_t cnt = 0, jmin = N;
+        for (int64_t r = 0; r < ncols; ++r)
+            if (cols[3 * r] * H + cols[3 * r + 1] == bh) {
+                ++cnt;
+                if (cols[3 * r + 2] < jmin) jmin = cols[3 * r + 2];
+            }
+        if (cnt == 0) continue;
+        widen_head(q, dtype, bh, N, d, qd);
+        widen_head(k, dtype, bh, N, d, kd);
+        widen_head(v, dtype, bh, N, d, vd);
+        widen_head(dout, dtype, bh, N, d, gd);
+        /* LSE_i and D_i of every row that sees a listed column (causal: i >= the smallest listed j) */
+        const int64_t i0 = causal ? jmin : 0;
+#pragma omp parallel
+        {
+            double* s = (double*)malloc(sizeof(double) * (size_t)N);
+            if (!s) {
+#pragma omp atomic write
+                bad = 1;
+            }
+#pragma omp for schedule(dynamic, 16)
+            for (int64_t i = i0; i < N; ++i) {
+                if (bad) continue;
+                const int64_t jend = causal ? i + 1 : N;
+                const double* qi = qd + i * d;
+                const double* gi = gd + i * d;
+                lse[i] = row_scores(qi, kd, jend, d, scale, s);
+                nsum D = {0.0, 0.0};
+                for (int64_t j = 0; j < jend; ++j) {
+                    double dot = 0.0;
+                    for (int64_t c = 0; c < d; ++c) dot += gi[c] * vd[j * d + c];
+                    nsum_add(&D, exp(s[j] - lse[i]) * dot);
+                }
+                Dr[i] = nsum_get(&D);
+            }
+            free(s);
+        }
+        if (bad) break;
+        /* the listed columns: sums over the rows i that see key j */
+#pragma omp parallel
+        {
+            nsum* av = (nsum*)malloc(sizeof(nsum) * (size_t)d);
+            nsum* ak = (nsum*)malloc(sizeof(nsum) * (size_t)d);
+            if (!av || !ak) {
+#pragma omp atomic write
+                bad = 1;
+            }
+#pragma omp for schedule(dynamic, 1)
+            for (int64_t r = 0; r < ncols; ++r) {
+                if (bad || cols[3 * r] * H + cols[3 * r + 1] != bh) continue;
+                const int64_t j = cols[3 * r + 2];
+                const double* kj = kd + j * d;
+                const double* vj = vd + j * d;
+                for (int64_t c = 0; c < d; ++c) {
+                    av[c] = (nsum){0.0, 0.0};
+                    ak[c] = (nsum){0.0, 0.0};
+                }
+                for (int64_t i = causal ? j : 0; i < N; ++i) {
+                    const double* qi = qd + i * d;
+                    const double* gi = gd + i * d;
+                    double sd = 0.0, dp = 0.0;
+                    for (int64_t c = 0; c < d; ++c) {
+                        sd += qi[c] * kj[c];
+                        dp += gi[c] * vj[c];
+                    }
+                    const double P = exp(scale * sd - lse[i]);
+                    const double dS = P * (dp - Dr[i]);
+                    for (int64_t c = 0; c < d; ++c) {
+                        nsum_add(&av[c], P * gi[c]);
+                        nsum_add(&ak[c], dS * qi[c]);
+                    }
+                }
+                for (int64_t c = 0; c < d; ++c) {
+                    dv[r * d + c] = nsum_get(&av[c]);
+                    dk[r * d + c] = scale * nsum_get(&ak[c]);
+                }
+            }
+            free(av);
+            free(ak);
+        }
+    }
+    free(qd);
+    free(kd);
+    free(vd);
+    free(gd);
+    free(lse);
+    free(Dr);
+    return bad ? -1 : 0;
+}

@@ -215,23 +215,6 @@ def test_merge_kernel_vs_oracle(cq, d, n):
         assert np.all(o[~fin] == 0)
 
 
-@pytest.mark.parametrize("d,dtype,causal", [(64, syn.F16, True), (64, syn.F16, False), (128, syn.F16, True),
-                                            (128, syn.BF16, False), (64, syn.BF16, True)])
-def test_two_tile_kernel_equals_single_tile_kernel(cq, d, dtype, causal, monkeypatch):
-    """The two-query-tile kernel and the single-tile kernel run the same per-row operation sequence
-    (same key tiles, same order, same reference-max rule), so their results agree bit for bit."""
-    B, H, N = 1, 3, 1000
-    _, (q, k, v) = _inputs(B, H, N, d, dtype, seed=13)
-    o2, l2 = mono(cq, q, k, v, B, H, N, d, causal, dtype)
-    O2, L2 = chunk(cq, q, k, v, 300, 0, B, H, N, N, d, causal, dtype)
-    monkeypatch.setenv("CQSA_ATTN_SINGLE_TILE", "1")
-    o1, l1 = mono(cq, q, k, v, B, H, N, d, causal, dtype)
-    O1, L1 = chunk(cq, q, k, v, 300, 0, B, H, N, N, d, causal, dtype)
-    monkeypatch.delenv("CQSA_ATTN_SINGLE_TILE")
-    assert torch.equal(o1, o2) and torch.equal(l1, l2)
-    assert torch.equal(O1, O2) and torch.equal(L1, L2)
-
-
 def test_determinism(cq):
     B, H, N, d = 1, 4, 2048, 64
     _, (q, k, v) = _inputs(B, H, N, d, syn.F16, seed=9)

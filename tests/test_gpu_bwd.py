@@ -107,6 +107,31 @@ def test_sum_identities_large(cq, causal):
     assert np.all(np.abs(dv64.sum(axis=2) - g64.sum(axis=2)) <= 4 * u * np.abs(dv64).sum(axis=2) + 1e-6)
 
 
+@pytest.mark.slow
+def test_backward_32k_sampled_vs_oracle(cq):
+    """The benchmark's backward shape (B=1 H=8 N=32768 d=64 fp16 causal) against the FP64 oracle: dq on
+    2,048+ seeded sampled query rows (dq_i depends on row i alone), dk and dv on sampled key columns of two
+    heads (each a sum over every query that sees the key), each held to the tolerance above over the
+    sampled values."""
+    B, H, N, d = 1, 8, 32768, 64
+    (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, B, H, N, d, True, syn.F16)
+    rows = syn.sample_rows(B, H, N, 2048, causal_tile=128)
+    js = syn.sample_rows(1, 1, N, 128, seed=5, must_i=(N - 128, N - 129, N // 2))[:, 2]
+    cols = np.concatenate([np.stack([np.zeros_like(js), np.full_like(js, hh), js], axis=1) for hh in (0, H - 1)])
+
+    def gather(t, idx):
+        return to_np64(t[torch.as_tensor(idx[:, 0]), torch.as_tensor(idx[:, 1]), torch.as_tensor(idx[:, 2])])
+
+    ref_dq = oracle.attn_bwd_rows(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=True, rows=rows)
+    ref_dk, ref_dv = oracle.attn_bwd_cols(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=True, cols=cols)
+    rel = {}
+    for name, got, ref in (("dq", gather(dq, rows), ref_dq), ("dk", gather(dk, cols), ref_dk),
+                           ("dv", gather(dv, cols), ref_dv)):
+        rel[name] = _check(got, ref, syn.F16, f"32K {name}")
+    print(f"\nbwd 32K causal on {len(rows)} rows / {len(cols)} columns: " +
+          ", ".join(f"{n} max/maxref {a:.2e} mean/meanref {b:.2e}" for n, (a, b) in rel.items()))
+
+
 def _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype, skip_masked=True):
     """The backward over (query chunk, key chunk) pairs of C tokens through cqsa_attn_bwd_chunk, with
     per-chunk fp32 accumulators cast to dtype at the end."""

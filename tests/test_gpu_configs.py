@@ -67,6 +67,53 @@ def test_noncausal_16k_d128_bf16_peaked(cq):
     print(f"\n16K bf16 peaked (fp32 result) on {len(rows)} rows: max abs {mx:.2e} mean abs {mn:.2e}")
 
 
+def test_bf16_d128_chunked_4096_equals_monolithic(cq):
+    """B=2, H=32, N=16384, d=128, bf16 with K scaled by 3 (peaked rows), non-causal, cut into 4,096-token
+    chunks: the 16 chunk-pair partials merged exactly equal the monolithic fp32 result within 1e-5 per
+    row (relative to the row's largest |O|; LSE relative to max(1, |LSE|)), and the oracle on sampled
+    rows within the stated tolerances."""
+    B, H, N, d, C = 2, 32, 16384, 128, 4096
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=0, dtype=syn.BF16, k_mul=3.0)
+    q, k, v = (to_dev(x, syn.BF16) for x in (qn, kn, vn))
+    Om = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    Lm = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    cq.cqsa_attn_fwd_chunk(q, k, v, 0, 0, B, H, N, N, d, False, 0.0, cq.CQSA_BF16, Om, Lm, False)
+    nch = N // C
+    out32 = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    worst = 0.0
+    ks = [k[:, :, j * C:(j + 1) * C].contiguous() for j in range(nch)]
+    vs = [v[:, :, j * C:(j + 1) * C].contiguous() for j in range(nch)]
+    for i in range(nch):
+        qs = q[:, :, i * C:(i + 1) * C].contiguous()
+        parts_o, parts_l = [], []
+        for j in range(nch):
+            Op = torch.empty((B, H, C, d), dtype=torch.float32, device="cuda")
+            Lp = torch.empty((B, H, C), dtype=torch.float32, device="cuda")
+            cq.cqsa_attn_fwd_chunk(qs, ks[j], vs[j], i * C, j * C, B, H, C, C, d, False, 0.0, cq.CQSA_BF16, Op, Lp,
+                                   False)
+            parts_o.append(Op)
+            parts_l.append(Lp)
+        o32 = torch.empty((B, H, C, d), dtype=torch.float32, device="cuda")
+        l32 = torch.empty((B, H, C), dtype=torch.float32, device="cuda")
+        cq.cqsa_merge_partials(parts_o, parts_l, nch, o32, l32, B, H, C, d, cq.CQSA_F32)
+        out32[:, :, i * C:(i + 1) * C] = o32
+        lse[:, :, i * C:(i + 1) * C] = l32
+        ref = Om[:, :, i * C:(i + 1) * C]
+        den = ref.abs().amax(dim=-1).clamp_min(1e-30)
+        rel = ((o32 - ref).abs().amax(dim=-1) / den).max().item()
+        lref = Lm[:, :, i * C:(i + 1) * C]
+        lrel = ((l32 - lref).abs() / lref.abs().clamp_min(1.0)).max().item()
+        worst = max(worst, rel)
+        assert rel <= 1e-5 and lrel <= 1e-5, f"Q chunk {i}: rel {rel:.2e}, lse rel {lrel:.2e}"
+        del parts_o, parts_l
+    rows = syn.sample_rows(B, H, N, 2048, chunk=C)
+    ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=False, dtype=syn.BF16, rows=rows)
+    mx, mn = assert_close(_gather(out32, rows), ro, _gather(lse, rows), rl, what="16K bf16 d128 chunked vs oracle")
+    print(f"\n16K bf16 d128 4096-token chunks: chunked-vs-mono worst row rel {worst:.2e}; vs oracle max abs "
+          f"{mx:.2e} mean abs {mn:.2e}")
+
+
 def test_chunked_131k_merge_equals_monolithic(cq):
     """B=1, H=8, N=131072, d=64, fp16, causal, 16384-token chunks: 36 pair partials + LSE merge,
     compared with the monolithic fp32 result on every row (1e-5 relative) and with the oracle on

@@ -73,11 +73,25 @@ def test_quorum_vs_oracle_and_stream(cq, c, itr, N, d, dtype, causal, layout, on
     if dtype == syn.F16:
         assert_close(o64, ro, to_np64(lse), rl, what=f"quorum c={c} itr={itr}")
     else:
-        # bf16 output: within half an ulp plus the fp32 tolerance (bf16 reading of the tolerance)
-        err = np.abs(o64 - ro)
-        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(o64), 2.0 ** -126))) - 7)
-        assert np.all(err <= 0.5 * ulp + 4e-3)
-        assert np.abs(to_np64(lse) - rl).max() <= 1e-3
+        # bf16 (the tolerance reading for bf16): the stated tolerances bind the fp32 result of the same
+        # computation. The executor's fp32 accumulator stays inside the call, so the output is anchored
+        # to the fp32 result over the whole key range (the chunk call): that result must meet the fp32
+        # tolerances against the oracle, and the output must be its round-to-nearest-even bf16 value
+        # except at rounding boundaries, where the two fp32 results (~1e-6 apart: merge order) may round
+        # to neighbours one bf16 ulp apart.
+        assert layout == syn.LAYOUT_BHND
+        qd, kd, vd = (to_dev(x, dtype) for x in (qn, kn, vn))
+        O32 = torch.empty((B, H, N, d), dtype=torch.float32, device="cuda")
+        L32 = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        cq.cqsa_attn_fwd_chunk(qd, kd, vd, 0, 0, B, H, N, N, d, causal, 0.0, dtype, O32, L32, False)
+        assert_close(to_np64(O32), ro, to_np64(L32), rl, what=f"quorum bf16 reference fp32 c={c}")
+        r = to_np64(O32.to(torch.bfloat16))
+        ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
+        diff = np.abs(o64 - r)
+        assert np.all(diff <= ulp), f"bf16 output more than one ulp from RNE(fp32): {np.max(diff / ulp):.2f} ulp"
+        assert np.mean(diff == 0) >= 0.99, f"only {np.mean(diff == 0):.4f} of outputs equal RNE(fp32)"
+        lrel = np.abs(to_np64(lse) - to_np64(L32)) / np.maximum(1.0, np.abs(to_np64(L32)))
+        assert lrel.max() <= 1e-5
     # the streaming driver with the same chunk size: same pair partials, merged in key order
     hq, hk, hv = (_host(x, dtype) for x in (qn, kn, vn))
     out2 = torch.empty(shape, dtype=tdt, device="cuda")

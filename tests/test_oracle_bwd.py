@@ -100,3 +100,38 @@ def test_symbolic_gradient_tiny(causal):
         want = np.array([[float(sp.diff(loss, sym[n][i, c]).evalf(subs=subs, n=30)) for c in range(d)]
                          for i in range(N)])
         np.testing.assert_allclose(res[name][0, 0], want, rtol=1e-12, atol=1e-13, err_msg=name)
+
+
+@pytest.mark.parametrize("causal", [False, True])
+@pytest.mark.parametrize("dtype", [syn.F16, syn.BF16])
+def test_sampled_rows_and_columns_match_full_backward(causal, dtype):
+    """attn_bwd_rows / attn_bwd_cols (for problems too large for the full N x N oracle) agree with the
+    full oracle backward, which the other tests here pin, at every row and column of a small problem."""
+    B, H, N, d = 2, 2, 150, 16
+    q, k, v = syn.qkv(B, H, N, d, seed=8, dtype=dtype, k_mul=2.0)
+    g = syn.normal(B, H, N, d, seed=8, tensor_id=syn.TID_DO, dtype=dtype)
+    ref = oracle.attn_bwd(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal, dtype=dtype)
+    bb, hh, ii = np.meshgrid(np.arange(B), np.arange(H), np.arange(N), indexing="ij")
+    idx = np.stack([bb.ravel(), hh.ravel(), ii.ravel()], axis=1)
+    perm = np.random.default_rng(1).permutation(len(idx))  # any order of the listed triples
+    idx = idx[perm]
+    dq = oracle.attn_bwd_rows(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal, rows=idx, dtype=dtype)
+    dk, dv = oracle.attn_bwd_cols(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal, cols=idx, dtype=dtype)
+    sel = (idx[:, 0], idx[:, 1], idx[:, 2])
+    for name, got in (("dq", dq), ("dk", dk), ("dv", dv)):
+        r = ref[name][sel]
+        assert np.max(np.abs(got - r)) <= 1e-12 * max(1.0, np.abs(r).max()), name
+    # a subset of one head only evaluates that head's rows
+    sub = idx[(idx[:, 0] == 1) & (idx[:, 1] == 0)][:7]
+    dk1, dv1 = oracle.attn_bwd_cols(q, k, v, g, B=B, H=H, N=N, d=d, causal=causal, cols=sub, dtype=dtype)
+    s1 = (sub[:, 0], sub[:, 1], sub[:, 2])
+    assert np.max(np.abs(dk1 - ref["dk"][s1])) <= 1e-12 * max(1.0, np.abs(ref["dk"]).max())
+    assert np.max(np.abs(dv1 - ref["dv"][s1])) <= 1e-12 * max(1.0, np.abs(ref["dv"]).max())
+
+
+def test_sampled_backward_rejects_bad_indices():
+    q, k, v = syn.qkv(1, 1, 8, 4, seed=0)
+    with pytest.raises(ValueError):
+        oracle.attn_bwd_rows(q, k, v, q, B=1, H=1, N=8, d=4, causal=True, rows=np.array([[0, 0, 8]]))
+    with pytest.raises(ValueError):
+        oracle.attn_bwd_cols(q, k, v, q, B=1, H=1, N=8, d=4, causal=True, cols=np.array([[0, 1, 0]]))
