@@ -119,7 +119,7 @@ const char* cqsa_status_string(int status) {
 void cqsa_set_timeout_ms(unsigned int ms) { g_timeout_ms = ms; }
 
 int cqsa_debug_set_fault(int kind) {
-  if (kind < 0 || kind > 1) {
+  if (kind < 0 || kind > 2) {
     set_error("unknown fault kind %d", kind);
     return CQSA_ERR_INVALID;
   }

@@ -80,6 +80,7 @@ struct BwdParams {
   long long q_off, kv_off;  // absolute positions of the chunks' first query / key (causal mask)
   float scale, scale_log2;
   unsigned long long timeout_ns;
+  int fault;  // test hook: 2 = block 0 never loads its key/value tile (its waits must time out cleanly)
 };
 
 __device__ __forceinline__ void record_bwd_error(int code, int where) {
@@ -307,9 +308,12 @@ __global__ void __launch_bounds__(NTHR, 1)
         tma_load_4d(sG + slot * BOX, &tmG, &bar_q[slot], 0, (it0 + it) * BT, h, b);
         ++issued[slot];
       };
-      mbar_arrive_expect_tx(bar_kv, 2 * BOX);
-      tma_load_4d(sK, &tmK, bar_kv, 0, k0, h, b);
-      tma_load_4d(sV, &tmV, bar_kv, 0, k0, h, b);
+      const bool skip_kv = (p.fault == 2 && blockIdx.x == 0);  // fault injection: K/V never arrive
+      if (!skip_kv) {
+        mbar_arrive_expect_tx(bar_kv, 2 * BOX);
+        tma_load_4d(sK, &tmK, bar_kv, 0, k0, h, b);
+        tma_load_4d(sV, &tmV, bar_kv, 0, k0, h, b);
+      }
       load_q(0);
       if (nit > 1) load_q(1);
       for (int it = 0; it + 2 < nit; ++it) {
@@ -318,7 +322,8 @@ __global__ void __launch_bounds__(NTHR, 1)
           break;
         load_q(it + 2);
       }
-      mbar_wait_bounded(bar_kv, 0, tmo);
+      // every load issued lands before the CTA exits (bounded waits)
+      if (!skip_kv) mbar_wait_bounded(bar_kv, 0, tmo);
       for (int s = 0; s < 2; ++s)
         if (issued[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued[s] - 1) & 1), tmo);
     } else if (warp == 1) {
@@ -732,6 +737,7 @@ int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cuda
   p.scale = a.scale;
   p.scale_log2 = a.scale * LOG2E;
   p.timeout_ns = timeout_ns();
+  p.fault = debug_fault();
   return accum ? dispatch_main<1>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream)
                : dispatch_main<0>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream);
 }

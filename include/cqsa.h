@@ -290,9 +290,10 @@ void cqsa_set_timeout_ms(unsigned int ms);
 
 /*
  * Test hook for the device-side bounded waits (not for production use): kind 1 makes the next
- * attention launches skip the load of key/value tile 1 in their first CTA, so that CTA's waits run
- * out after the timeout; the kernel then records CQSA_ERR_TIMEOUT in the device error word, drains
- * its own copies and MMAs, frees tensor memory and returns (no trap, no hang). kind 0 turns it off.
+ * attention launches skip the load of key/value tile 1 in their first CTA, and kind 2 makes the next
+ * backward launches skip the key/value load of their first CTA, so that CTA's waits run out after the
+ * timeout; the kernel then records CQSA_ERR_TIMEOUT in its device error word, drains its own copies
+ * and MMAs, frees tensor memory and returns (no trap, no hang). kind 0 turns it off.
  */
 int cqsa_debug_set_fault(int kind);
 

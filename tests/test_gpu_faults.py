@@ -40,3 +40,34 @@ def test_fault_hook_rejects_unknown_kind():
     import exact_long_context_tcgen05_gb300 as cq
     with pytest.raises(cq.CqsaError):
         cq.cqsa_debug_set_fault(7)
+
+
+def test_streamed_backward_reports_a_wait_that_gave_up():
+    """The host-resident backward reads the backward's device error word after its stream drains: a
+    kernel whose bounded wait gave up (the hook skips block 0's key/value load) makes the call return
+    CQSA_ERR_TIMEOUT instead of incomplete gradients; the next call, without the hook, is correct."""
+    import exact_long_context_tcgen05_gb300 as cq
+    B, H, N, d, C = 1, 2, 512, 64, 256
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=33)
+    gn = syn.normal(B, H, N, d, seed=33, tensor_id=syn.TID_DO)
+    q, k, v, g = (to_dev(x, syn.F16) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, False, syn.F16)
+    host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
+    grads = [torch.empty((B, H, N, d), dtype=torch.float16).pin_memory() for _ in range(3)]
+    assert cq.cqsa_device_error(clear=True)[0] == cq.CQSA_OK
+    cq.cqsa_set_timeout_ms(200)
+    try:
+        cq.cqsa_debug_set_fault(2)
+        with pytest.raises(cq.CqsaError) as ei:
+            cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, d, False, 0.0, cq.CQSA_F16, C)
+        assert ei.value.status == cq.CQSA_ERR_TIMEOUT and "gave up" in str(ei.value)
+    finally:
+        cq.cqsa_debug_set_fault(0)
+        cq.cqsa_set_timeout_ms(0)
+    assert cq.cqsa_device_error(clear=True)[0] == cq.CQSA_OK  # the call cleared the word it reported
+    cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, d, False, 0.0, cq.CQSA_F16, C)
+    ref = cq.attention_backward(q, k, v, out, g, lse, causal=False)
+    torch.cuda.synchronize()
+    for got, r in zip(grads, ref):
+        e = (got.float() - r.cpu().float()).abs().max().item()
+        assert e <= 8 * 2.0 ** -11 * r.float().abs().max().item()
