@@ -146,17 +146,20 @@ def whole_job_tflops(flop_per_step: float, steps: int, world: int, max_ms: float
     return world * flop_per_step * steps / (max_ms / 1000.0) / 1e12
 
 
-def oracle_sample(rows: int, seed: int = 1):
-    """Time the FP64 oracle on `rows` seeded rows of the workload; returns (seconds, FLOP, threads)."""
+def oracle_sample(rows: int, seed: int = 1, want=False):
+    """Time the FP64 oracle on `rows` seeded rows of the workload; returns (seconds, FLOP, threads), and
+    with `want` also (rows, out, lse) of the oracle."""
     import oracle
     import synthetic as syn
     qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
     sel = syn.sample_rows(B, H, N, rows, seed=seed)[:rows]
     t0 = time.perf_counter()
-    oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=D, causal=CAUSAL, rows=sel)
+    ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=D, causal=CAUSAL, rows=sel)
     dt = time.perf_counter() - t0
     flop = float(np.sum(4.0 * D * (sel[:, 2] + 1)))  # causal: row i sees i+1 keys
     threads = int(os.environ.get("OMP_NUM_THREADS", os.cpu_count() or 1))
+    if want:
+        return dt, flop, threads, (sel, ro, rl)
     return dt, flop, threads
 
 
@@ -176,15 +179,28 @@ def _cpu_model() -> str:
     return "unknown"
 
 
-def cpu_baseline(target_s: float = 12.0):
+def cpu_baseline(target_s: float = 12.0, out=None, lse=None):
+    """The oracle timed on a bounded row sample of the workload on this host's cores. Given the bench's
+    output (device tensors of the last timed step), its rows are also compared with the oracle's."""
     dt, flop, thr = oracle_sample(256)
     rows = int(min(65536, max(256, 256 * target_s / max(dt, 1e-3))))
-    dt, flop, thr = oracle_sample(rows, seed=2)
-    return {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
-            "sample": f"{rows} seeded query rows (b,h,i uniform) of the workload, each in full over its causal "
-                      f"keys, FP64, {dt:.1f} s",
-            "cpu_model": _cpu_model(), "rows_per_s": rows / dt,
-            "extrapolated_full_s": FLOP_PER_STEP / (flop / dt)}
+    dt, flop, thr, (sel, ro, rl) = oracle_sample(rows, seed=2, want=True)
+    res = {"value": flop / dt / 1e12, "unit": "TFLOP/s", "cores": thr, "kind": "oracle",
+           "sample": f"{rows} seeded query rows (b,h,i uniform) of the workload, each in full over its causal "
+                     f"keys, FP64, {dt:.1f} s",
+           "cpu_model": _cpu_model(), "rows_per_s": rows / dt,
+           "extrapolated_full_s": FLOP_PER_STEP / (flop / dt)}
+    if out is not None:
+        import torch
+        b, h, i = (torch.as_tensor(sel[:, j], device=out.device) for j in range(3))
+        o = out[b, h, i].float().cpu().numpy().astype(np.float64)
+        e = np.abs(o - ro)
+        le = np.abs(lse[b, h, i].cpu().numpy().astype(np.float64) - rl)
+        res["output_check"] = {"rows": int(len(sel)), "max_abs": float(e.max()), "mean_abs": float(e.mean()),
+                               "lse_max_abs": float(le.max()),
+                               "within_tolerance": bool(e.max() <= 4e-3 and e.mean() <= 2e-4 and le.max() <= 1e-3),
+                               "tolerance": "max abs 4e-3, mean abs 2e-4, LSE 1e-3 (fp16 output vs FP64 oracle)"}
+    return res
 
 
 def run_reference(args):
@@ -302,7 +318,9 @@ def run_ours(args):
                 "gpu_launches": args.steps, "wall_s_timed_region": wall,
                 "clocks": clk.summary(), "device_error_free": ok}
         if not args.no_cpu_baseline:
-            line["cpu_baseline"] = cpu_baseline()
+            line["cpu_baseline"] = cpu_baseline(out=out, lse=lse)
+        if args.secondary != "none":
+            line["secondary"] = run_secondary(cq, dev, args)
         print(json.dumps(line), flush=True)
     if world > 1:
         torch.distributed.destroy_process_group()
@@ -412,11 +430,12 @@ def measure_link(dev, reps):
             "method": "1 GiB pinned host buffer, cudaMemcpyAsync, CUDA events, median of %d" % reps}
 
 
-def measure_stream(cq, dev, n_tokens, link_h2d_gbs):
+def measure_stream(cq, dev, n_tokens, link_h2d_gbs, host=None):
     import torch
     Bs, Hs, Ds, C = 1, 8, 64, 262_144
     shape = (Bs, n_tokens, Hs, Ds)
-    host = _host_qkv_token_major(n_tokens, Hs, Ds)
+    if host is None:
+        host = _host_qkv_token_major(n_tokens, Hs, Ds)
     out = torch.empty(shape, dtype=torch.float16).pin_memory()
     lse = torch.empty((Bs, Hs, n_tokens), dtype=torch.float32).pin_memory()
     st = cq.cqsa_stream_stats()
@@ -427,13 +446,18 @@ def measure_stream(cq, dev, n_tokens, link_h2d_gbs):
     wall = time.perf_counter() - t0
     flop = 4.0 * Bs * Hs * n_tokens * n_tokens * Ds / 2.0
     copy_gbs = st.h2d_bytes / (st.h2d_ms / 1e3) / 1e9 if st.h2d_ms > 0 else None
+    peak, src, _ = _peaks()
     return {"measure": "stream", "workload": f"host-resident streaming, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
             f"token-major pinned Q/K/V/out, {C}-token chunks", "wall_s": wall, "tflops": flop / wall / 1e12,
             "compute_s": st.compute_ms / 1e3, "stall_ms": st.stall_ms, "h2d_bytes": st.h2d_bytes,
             "d2h_bytes": st.d2h_bytes, "copy_gbs_overlapped": copy_gbs, "link_h2d_gbs": link_h2d_gbs,
             "copy_frac_of_link": (copy_gbs / link_h2d_gbs) if (copy_gbs and link_h2d_gbs) else None,
             "overlap_wall_over_compute": wall / (st.compute_ms / 1e3) if st.compute_ms > 0 else None,
-            "peak_device_bytes": st.peak_device_bytes, "n_chunk_pairs": st.n_chunks}
+            "peak_device_bytes": st.peak_device_bytes, "n_chunk_pairs": st.n_chunks,
+            "roofline": {"bound": "tensor", "achieved": flop / wall / 1e12, "peak": peak, "unit": "TFLOP/s",
+                         "frac": flop / wall / 1e12 / peak, "peak_source": src},
+            "link_or_tensor_roofline_frac": (max(st.h2d_bytes / (link_h2d_gbs * 1e9), flop / (peak * 1e12)) / wall
+                                             if link_h2d_gbs else None)}
 
 
 def _host_qkv_token_major(n_tokens, Hs=8, Ds=64):
@@ -537,6 +561,106 @@ def measure_bwd(cq, dev, reps, N=32768, H=8):
                          "peak_source": src, "note": "algorithmic FLOP of the five products, whole call"}}
 
 
+def _numa_nodes(t, samples=64):
+    """NUMA nodes of a sample of a host tensor's pages (move_pages with no target nodes reports them);
+    {} where the system call is unavailable."""
+    import ctypes
+    import platform
+    nr = {"aarch64": 239, "x86_64": 279}.get(platform.machine())
+    if nr is None:
+        return {}
+    try:
+        libc = ctypes.CDLL(None, use_errno=True)
+        page = os.sysconf("SC_PAGE_SIZE")
+        base, nbytes = t.data_ptr(), t.numel() * t.element_size()
+        addrs = [(base + (nbytes - 1) * k // max(1, samples - 1)) & ~(page - 1) for k in range(samples)]
+        pages = (ctypes.c_void_p * samples)(*addrs)
+        status = (ctypes.c_int * samples)()
+        if libc.syscall(nr, 0, samples, pages, None, status, 0) != 0:
+            return {}
+        nodes = {}
+        for st in status:
+            nodes[str(st)] = nodes.get(str(st), 0) + 1
+        return nodes
+    except (OSError, AttributeError, ValueError):
+        return {}
+
+
+def measure_link_driver_shaped(cq, dev, host, chunk_tokens, reps=6):
+    """Host-to-device copies shaped like the streaming driver's: one contiguous chunk of the token-major
+    host tensors (chunk_tokens x 8 heads x 64 x 2 bytes) per cudaMemcpyAsync on a non-blocking stream,
+    from the workload's own pinned buffers, alone and while attention kernels run on another stream."""
+    import torch
+    per_tok = 8 * 64 * 2
+    nbytes = chunk_tokens * per_tok
+    dbuf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(dev)
+    n_chunks = host[1].shape[1] // chunk_tokens
+    flat = [t.view(-1).view(torch.uint8) for t in host[1:]]
+
+    def copies():
+        res = []
+        for r in range(reps):
+            src = flat[r % 2][(r % n_chunks) * nbytes:(r % n_chunks + 1) * nbytes]
+            res += _time_events(lambda: dbuf.copy_(src, non_blocking=True), 1, side)
+        return res
+
+    with torch.cuda.stream(side):
+        alone = copies()
+    # the same copies beside the headline attention kernel on the default stream
+    import synthetic as syn
+    qn, kn, vn = syn.qkv(1, 8, 32768, 64, seed=0)
+    q, k, v = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn))
+    out = torch.empty_like(q)
+    lse = torch.empty((1, 8, 32768), dtype=torch.float32, device=dev)
+    main = torch.cuda.current_stream(dev)
+    for _ in range(3 * reps):
+        cq.cqsa_attn_fwd(q, k, v, out, lse, 1, 8, 32768, 64, True, 0.0, cq.CQSA_F16, main)
+    with torch.cuda.stream(side):
+        busy = copies()
+    torch.cuda.synchronize()
+    gbs = lambda ms: [nbytes / (m / 1e3) / 1e9 for m in ms]  # noqa: E731
+    return {"copy_bytes": nbytes, "h2d_gbs_alone": gbs(alone), "h2d_gbs_beside_attention": gbs(busy),
+            "numa_nodes_of_host_pages": _numa_nodes(host[1]),
+            "method": f"{reps} plain cudaMemcpyAsync copies of one {chunk_tokens}-token chunk each from the "
+                      "workload's pinned token-major K/V, non-blocking stream, CUDA events per copy"}
+
+
+def run_secondary(cq, dev, args):
+    """Secondary lines of the other workloads (each with its own CUDA-event timing, clocks and roofline):
+    the bf16 d=128 forward, the LSE merge of the chunked workload, the backward, the host link probed
+    as a 1 GiB copy and as the streaming driver's copies, and the host-resident streaming workload."""
+    import torch
+    res = {}
+    reps = 10
+
+    def run(name, fn):
+        t0 = time.perf_counter()
+        with ClockSampler(dev.index if dev.index is not None else 0) as clk:
+            try:
+                r = fn()
+            except Exception as e:  # noqa: BLE001  (a failed secondary line must not hide the headline)
+                r = {"error": f"{type(e).__name__}: {e}"}
+        r["clocks"] = clk.summary()
+        r["host_s"] = time.perf_counter() - t0
+        res[name] = r
+        torch.cuda.empty_cache()
+
+    run("bf16_d128", lambda: measure_bf16(cq, dev, reps))
+    run("merge_131k", lambda: measure_merge(cq, dev, reps))
+    run("bwd_32k", lambda: measure_bwd(cq, dev, reps))
+    run("link_1gib", lambda: measure_link(dev, 5))
+    if args.secondary == "all":
+        link = res["link_1gib"].get("h2d_gbs")
+        host = _host_qkv_token_major(args.n)
+        run("link_driver_shaped", lambda: measure_link_driver_shaped(cq, dev, host, 262_144))
+        run("stream_4m", lambda: measure_stream(cq, dev, args.n, link, host=host))
+        del host
+    rc, code, _ = cq.cqsa_device_error()
+    res["device_error_free"] = rc == cq.CQSA_OK
+    return res
+
+
 def run_measure(args):
     import torch
     world, rank, local = _dist()
@@ -578,6 +702,8 @@ def main():
     ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")
     ap.add_argument("--bwd-n", type=int, default=32768, help="--measure bwd: tokens")
     ap.add_argument("--bwd-h", type=int, default=8, help="--measure bwd: heads")
+    ap.add_argument("--secondary", choices=("all", "fast", "none"), default="all",
+                    help="secondary lines in the headline JSON: all, fast (no host-streaming workload), none")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

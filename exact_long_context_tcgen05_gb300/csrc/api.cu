@@ -49,6 +49,19 @@ unsigned long long timeout_ns() {
   return static_cast<unsigned long long>(ms) * 1000000ull;
 }
 
+// Status and message of a device error word.
+static int report_device_error(const DevErr& e) {
+  if (e.code == 0) return CQSA_OK;
+  if (e.code == kDevSmSlot) {
+    set_error("a d = 128 attention CTA ran on an SM id beyond the %s (block %d): its running-sum fold was "
+              "skipped, so the result is exact but chunked and monolithic results may differ by more than "
+              "fp32 summation order", "running-sum slots", e.block);
+    return CQSA_ERR_DEVICE;
+  }
+  set_error("device wait gave up (code %d, block %d, site %d)", e.code, e.block, e.where);
+  return CQSA_ERR_TIMEOUT;
+}
+
 int check_device_error_on(cudaStream_t s) {
   DevErr e = {0, 0, 0, 0};
   int rc = device_error_word_on(&e, s);
@@ -57,11 +70,7 @@ int check_device_error_on(cudaStream_t s) {
     rc = bwd_error_word_on(&e, s);
     if (rc != CQSA_OK) return rc;
   }
-  if (e.code != 0) {
-    set_error("device wait gave up (code %d, block %d, site %d)", e.code, e.block, e.where);
-    return CQSA_ERR_TIMEOUT;
-  }
-  return CQSA_OK;
+  return report_device_error(e);
 }
 
 static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -140,11 +149,7 @@ int cqsa_device_error(int* code, int* block, int clear) {
   }
   if (code) *code = e.code;
   if (block) *block = e.block;
-  if (e.code != 0) {
-    set_error("device wait gave up (code %d, block %d, site %d)", e.code, e.block, e.where);
-    return CQSA_ERR_TIMEOUT;
-  }
-  return CQSA_OK;
+  return report_device_error(e);
 }
 
 int cqsa_attn_fwd(const void* q, const void* k, const void* v, void* out, float* lse, int B, int H, int N, int d,

@@ -40,6 +40,12 @@ namespace cqsa {
 
 __device__ DevErr g_dev_err;
 
+// Running sums of the d = 128 attention kernel: one slot of two tiles x 128 features x 128 rows (fp32)
+// per SM id. Contents need no clearing: a CTA writes its slot before it reads it.
+constexpr int kOsumSlots = 256;
+constexpr int kOsumSlotFloats = 2 * 128 * 128;
+__device__ __align__(256) float g_osum[kOsumSlots * kOsumSlotFloats];
+
 namespace {
 
 constexpr int BM = 128;        // query rows per tile
@@ -232,12 +238,18 @@ struct Cfg2 {
   static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
   static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
   static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
-  // d = 64: every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running
-  // sum in shared memory ([tile][feature][row], conflict-free per row), so no tensor-core accumulation
-  // chain exceeds FLUSH * 8 MMAs. (The MMA's fp32 accumulation is biased toward zero: measured
-  // relative drift -1.6e-5 after 16K keys, -6.9e-5 after 65K; the running sum uses RNE adds.)
-  static constexpr int FLUSH = (D == 64) ? 128 : 0;
-  static constexpr uint32_t OSUM_BYTES = (D == 64) ? 2u * D * 128u * 4u : 0u;
+  // Every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running sum, so no
+  // tensor-core accumulation chain exceeds FLUSH * 8 (d = 64) or FLUSH * 8 * 2 (bf16 hi/lo) MMAs. (The
+  // MMA's fp32 accumulation is biased toward zero: measured relative drift -1.6e-5 after 16K keys, -6.9e-5
+  // after 65K; the running sum uses RNE adds.) Chunk partials whose key ranges start at multiples of
+  // FLUSH * 128 tokens then accumulate exactly the segments of the monolithic call. d = 64 keeps the
+  // running sum in shared memory ([tile][feature][row], conflict-free per row); d = 128 has no shared or
+  // tensor memory left for it and keeps it in global memory, one 128 KiB slot per SM (g_osum below): two
+  // CTAs of this kernel never share an SM (each needs more than half of its shared and all its tensor
+  // memory), so the slot of the SM a CTA runs on is its own for the CTA's lifetime.
+  static constexpr int FLUSH = (D == 64) ? 128 : 32;
+  static constexpr bool OSUM_SMEM = (D == 64);
+  static constexpr uint32_t OSUM_BYTES = OSUM_SMEM ? 2u * D * 128u * 4u : 0u;
   static constexpr uint32_t SMEM_BYTES =
       1024 + 2 * QT_BYTES + 2 * STAGES * KV_BYTES + OSUM_BYTES + NBARS * 8 + 16;
   static_assert(COL_O1 + D <= TMEM_COLS, "tensor memory layout exceeds 512 columns");
@@ -257,7 +269,15 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   uint8_t* sQ = smem;  // tile t at sQ + t * QT_BYTES
   uint8_t* sK = sQ + 2 * C::QT_BYTES;
   uint8_t* sV = sK + STAGES * C::KV_BYTES;
-  float* sOsum = reinterpret_cast<float*>(sV + STAGES * C::KV_BYTES);  // d = 64 only
+  // running sum of O: shared memory (d = 64) or this SM's global slot (d = 128), [tile][feature][row]
+  float* sOsum = reinterpret_cast<float*>(sV + STAGES * C::KV_BYTES);
+  bool osum_ok = true;
+  if (!C::OSUM_SMEM) {
+    uint32_t smid;
+    asm volatile("mov.u32 %0, %%smid;" : "=r"(smid));
+    osum_ok = smid < static_cast<uint32_t>(kOsumSlots);
+    sOsum = g_osum + static_cast<size_t>(osum_ok ? smid : 0u) * kOsumSlotFloats;
+  }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES + C::OSUM_BYTES);
   uint64_t* bar_q = bars;
   uint64_t* bar_k_full = bar_q + 1;
@@ -298,6 +318,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   const int n_max = max(nkv0, nkv1);
 
   if (threadIdx.x == 0) {
+    if (!osum_ok) record_error(kDevSmSlot, 30);  // results stay exact; only the fold is skipped
     mbar_init(bar_q, 1);
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_k_full[s], 1);
@@ -416,7 +437,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       auto do_pv = [&](int j) {
         const uint64_t v0 = dV + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
         // O restarts at every segment start of the softmax loop (key tiles 0, FLUSH, 2 FLUSH, ...)
-        const bool first = (j == 0) || (C::FLUSH > 0 && j % (C::FLUSH > 0 ? C::FLUSH : 1) == 0);
+        const bool first = (j == 0) || (C::FLUSH > 0 && osum_ok && j % (C::FLUSH > 0 ? C::FLUSH : 1) == 0);
         const bool last = (j == nkv - 1);
         tc_fence_after();
         if (leader) {
@@ -510,7 +531,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     // the next segment's first PV_t restarts O; O is in the current reference max, O_sum is brought
     // from m_sum to it by an exact power of two. Keeping the fold out of the per-tile loop keeps that
     // loop's code identical to the unsegmented one.
-    constexpr int SEG = C::FLUSH > 0 ? C::FLUSH : (1 << 30);
+    const int SEG = (C::FLUSH > 0 && osum_ok) ? C::FLUSH : (1 << 30);
     for (int j0 = 0; ok && j0 < nkv; j0 += SEG) {
       if (j0 > 0) {
         const int j = j0;
@@ -520,7 +541,6 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           break;
         }
         tc_fence_after();
-        const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
         const bool have = j > C::FLUSH;
         const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
 #pragma unroll
@@ -529,11 +549,22 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           tmem_ld32(trow + colO + c * 32, o);
           tmem_wait_ld();
           reg_fence32(o);
+          if (C::OSUM_SMEM) {
+            const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) {
-            const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
-            const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
-            st_shared_f32(a, prev + __uint_as_float(o[e]));
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
+              const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
+              st_shared_f32(a, prev + __uint_as_float(o[e]));
+            }
+          } else {
+            // this thread's own row of the SM's slot: written before it is read, by this thread only
+            float* og = sOsum + (wg * D + c * 32) * 128 + r;
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float prev = have ? og[e * 128] * sc : 0.0f;
+              og[e * 128] = prev + __uint_as_float(o[e]);
+            }
           }
         }
         m_sum = m_ref;
@@ -697,7 +728,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         for (int e = 0; e < 32; ++e) o[e] = 0u;
       }
       float v[32];
-      if (C::FLUSH > 0 && nkv > C::FLUSH) {
+      if (C::FLUSH > 0 && osum_ok && nkv > C::FLUSH) {
         const float* os = sOsum + (wg * D + c * 32) * 128 + r;
         const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
 #pragma unroll

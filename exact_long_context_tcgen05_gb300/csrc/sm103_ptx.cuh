@@ -16,7 +16,8 @@ enum : int {
   kDevTimeoutQ = 1,       // Q tile never arrived
   kDevTimeoutKV = 2,      // a K/V stage never arrived or was never released
   kDevTimeoutMMA = 3,     // an MMA completion never arrived
-  kDevTimeoutSoftmax = 4  // softmax -> MMA hand-off never arrived
+  kDevTimeoutSoftmax = 4,  // softmax -> MMA hand-off never arrived
+  kDevSmSlot = 5           // an SM id beyond the running-sum slots (the fold was skipped)
 };
 
 struct DevErr {

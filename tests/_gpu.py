@@ -46,3 +46,19 @@ def assert_close(out, ref_o, lse=None, ref_l=None, max_abs=4e-3, mean_abs=2e-4, 
             le = float(np.abs(lse[fin] - ref_l[fin]).max())
             assert le <= lse_abs, f"{what}: lse max abs {le:.3e} (<= {lse_abs})"
     return mx, mn
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    ax = np.maximum(np.abs(x), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def assert_bf16_rounds_fp32_result(got: np.ndarray, o32: np.ndarray, what: str, rel_row: float = 1e-5):
+    """A bf16 output of a path whose fp32 result is not exposed, against the fp32 result of the same
+    attention by another route (o32; the two fp32 results may differ by the chunked-vs-monolithic
+    tolerance, rel_row times the row's largest |O|): each element must be the round-to-nearest-even
+    bf16 value of some number within that tolerance of o32, i.e. within half a bf16 ulp of the output
+    plus the tolerance."""
+    tol = 0.5 * bf16_ulp(got) + rel_row * np.abs(o32).max(axis=-1, keepdims=True)
+    excess = np.abs(got - o32) - tol
+    assert np.all(excess <= 0), f"{what}: bf16 output off the fp32 result by {excess.max():.3e} beyond tolerance"

@@ -16,17 +16,9 @@ import torch
 
 import oracle
 import synthetic as syn
-from tests._gpu import TORCH_DT, assert_close, to_dev, to_np64
+from tests._gpu import TORCH_DT, assert_bf16_rounds_fp32_result, assert_close, to_dev, to_np64
 
 pytestmark = pytest.mark.gpu
-
-
-def _within_one_bf16_ulp_of_rne(got: np.ndarray, o32: torch.Tensor, what: str):
-    r = to_np64(o32.to(torch.bfloat16))
-    ulp = 2.0 ** (np.floor(np.log2(np.maximum(np.abs(r), 2.0 ** -126))) - 7)
-    diff = np.abs(got - r)
-    assert np.all(diff <= ulp), f"{what}: {np.max(diff / ulp):.2f} bf16 ulp from RNE of the fp32 result"
-    assert np.mean(diff == 0) >= 0.99, f"{what}: only {np.mean(diff == 0):.4f} equal RNE of the fp32 result"
 
 
 def _run_both(cq, B, H, N, d, causal, C, seed, dtype=syn.F16, oracle_rows=None):
@@ -58,8 +50,8 @@ def _run_both(cq, B, H, N, d, causal, C, seed, dtype=syn.F16, oracle_rows=None):
         L32 = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
         cq.cqsa_attn_fwd_chunk(q, k, v, 0, 0, B, H, N, N, d, causal, 0.0, dtype, O32, L32, False)
         assert_close(to_np64(O32[b, h, i]), ro, to_np64(L32[b, h, i]), rll, what=what + " fp32 anchor vs oracle")
-        _within_one_bf16_ulp_of_rne(to_np64(out), O32, what)
-        _within_one_bf16_ulp_of_rne(to_np64(ref), O32, what + " (streamed)")
+        assert_bf16_rounds_fp32_result(to_np64(out), to_np64(O32), what)
+        assert_bf16_rounds_fp32_result(to_np64(ref), to_np64(O32), what + " (streamed)")
         lrel = (lse - L32).abs() / L32.abs().clamp_min(1.0)
         assert lrel.max().item() <= 1e-5
     # both entry points run the same chunk pairs: their LSEs agree to fp32 merge-order rounding
