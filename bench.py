@@ -470,19 +470,37 @@ def _host_qkv_token_major(n_tokens, Hs=8, Ds=64):
     return host
 
 
-def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1):
+def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1, engine="classic", device_inputs=False):
+    """The quorum decomposition; with device_inputs, Q/K/V and the output are device-resident (the chunks
+    are read in place) and the call is timed with CUDA events, after one untimed call."""
     import torch
     Hs, Ds, c, D, itr = 8, 64, 31, (0, 1, 3, 8, 12, 18), 1
     host = _host_qkv_token_major(n_tokens, Hs, Ds)
-    out = torch.empty((1, n_tokens, Hs, Ds), dtype=torch.float16).pin_memory()
-    lse = torch.empty((1, Hs, n_tokens), dtype=torch.float32).pin_memory()
+    eng = cq.CQSA_ENGINE_WAVE if engine == "wave" else cq.CQSA_ENGINE_CLASSIC
+    if device_inputs:
+        qkv = [t.to(dev) for t in host]
+        out = torch.empty((1, n_tokens, Hs, Ds), dtype=torch.float16, device=dev)
+        lse = torch.empty((1, Hs, n_tokens), dtype=torch.float32, device=dev)
+    else:
+        qkv = host
+        out = torch.empty((1, n_tokens, Hs, Ds), dtype=torch.float16).pin_memory()
+        lse = torch.empty((1, Hs, n_tokens), dtype=torch.float32).pin_memory()
     st = cq.cqsa_quorum_stats()
     stream = torch.cuda.current_stream(dev)
-    t0 = time.perf_counter()
-    cq.cqsa_quorum_attn_fwd(host[0], host[1], host[2], cq.CQSA_LAYOUT_BNHD, True, out, lse, True, 1, Hs, n_tokens, Ds,
-                            True, 0.0, cq.CQSA_F16, c, D, itr, acc_on_host=acc_on_host, max_parallel=npar, stats=st,
-                            stream=stream)
-    wall = time.perf_counter() - t0
+
+    def call():
+        cq.cqsa_quorum_attn_fwd_ex(qkv[0], qkv[1], qkv[2], cq.CQSA_LAYOUT_BNHD, not device_inputs, out, lse,
+                                   not device_inputs, 1, Hs, n_tokens, Ds, True, 0.0, cq.CQSA_F16, c, D, itr,
+                                   acc_on_host=acc_on_host, max_parallel=npar, engine=eng, stats=st, stream=stream)
+
+    if device_inputs:
+        call()
+        ms = statistics.median(_time_events(call, 3, stream))
+        wall = ms / 1e3
+    else:
+        t0 = time.perf_counter()
+        call()
+        wall = time.perf_counter() - t0
     flop = 4.0 * Hs * n_tokens * n_tokens * Ds / 2.0
     return {"measure": "quorum", "workload": f"cyclic quorum decomposition, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
             f"c={c} interest_set={D} itr={itr}, token-major pinned host Q/K/V/out", "wall_s": wall,
@@ -490,7 +508,8 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1):
             "copy_bytes": st.copy_bytes, "chunk_tokens": st.chunk_tokens, "subproblems": st.n_subproblems,
             "pairs": st.n_pairs, "chunk_loads": st.n_chunk_loads, "peak_device_bytes": st.peak_device_bytes,
             "accumulator": "host (pinned)" if acc_on_host else "device", "acc_host_bytes": st.acc_host_bytes,
-            "max_parallel": npar,
+            "max_parallel": npar, "engine": engine, "launches": st.n_launches,
+            "inputs": "device-resident (read in place), CUDA events" if device_inputs else "pinned host, wall clock",
             "context": "the pages' own run of this example (unnamed GPU): 2 min 06 s, 31 subproblems"}
 
 
@@ -678,7 +697,8 @@ def run_measure(args):
         link = measure_link(dev, 5)
         line = measure_stream(cq, dev, args.n, link["h2d_gbs"])
     elif args.measure == "quorum":
-        line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel)
+        line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel,
+                              engine=args.engine, device_inputs=args.device_inputs)
     elif args.measure == "bwd":
         line = measure_bwd(cq, dev, reps, N=args.bwd_n, H=args.bwd_h)
     else:
@@ -700,6 +720,8 @@ def main():
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream / quorum")
     ap.add_argument("--acc-on-host", action="store_true", help="--measure quorum with the host accumulator")
     ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")
+    ap.add_argument("--engine", choices=("classic", "wave"), default="classic", help="--measure quorum: engine")
+    ap.add_argument("--device-inputs", action="store_true", help="--measure quorum: device-resident Q/K/V/out")
     ap.add_argument("--bwd-n", type=int, default=32768, help="--measure bwd: tokens")
     ap.add_argument("--bwd-h", type=int, default=8, help="--measure bwd: heads")
     ap.add_argument("--secondary", choices=("all", "fast", "none"), default="all",

@@ -18,10 +18,11 @@ CQSA_OK, CQSA_ERR_INVALID, CQSA_ERR_UNSUPPORTED, CQSA_ERR_CUDA, CQSA_ERR_OOM, CQ
     0, -1, -2, -3, -4, -5, -6)
 CQSA_F16, CQSA_BF16, CQSA_F32 = 0, 1, 2
 CQSA_LAYOUT_BHND, CQSA_LAYOUT_BNHD = 0, 1
+CQSA_ENGINE_CLASSIC, CQSA_ENGINE_WAVE = 0, 1
 
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
-            "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd", "cqsa_attn_bwd_dvec",
+            "cqsa_quorum_attn_fwd_ex", "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd", "cqsa_attn_bwd_dvec",
             "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast", "cqsa_stream_attn_bwd",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
             "cqsa_debug_set_fault", "cqsa_version")
@@ -73,6 +74,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_quorum_schedule.restype = _ll
     lib.cqsa_quorum_attn_fwd.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i, _vp,
                                          _i, _i, _i, _i, ctypes.POINTER(cqsa_quorum_stats), _vp]
+    lib.cqsa_quorum_attn_fwd_ex.argtypes = [_vp, _vp, _vp, _i, _i, _vp, _vp, _i, _i, _i, _ll, _i, _i, _f, _i, _i,
+                                            _vp, _i, _i, _i, _i, _i, _ll, ctypes.POINTER(cqsa_quorum_stats), _vp]
     lib.cqsa_attn_bwd_workspace_size.argtypes = [_i, _i, _i, _i]
     lib.cqsa_attn_bwd_workspace_size.restype = ctypes.c_size_t
     lib.cqsa_attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, ctypes.c_size_t, _i, _i, _i, _i,
@@ -97,7 +100,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_version.argtypes = []
     lib.cqsa_version.restype = ctypes.c_char_p
     for name in ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
-                 "cqsa_attn_fwd_chunked_static", "cqsa_device_error", "cqsa_quorum_check", "cqsa_quorum_attn_fwd"):
+                 "cqsa_attn_fwd_chunked_static", "cqsa_device_error", "cqsa_quorum_check", "cqsa_quorum_attn_fwd",
+                 "cqsa_quorum_attn_fwd_ex"):
         getattr(lib, name).restype = _i
     return lib
 
@@ -221,6 +225,18 @@ def cqsa_quorum_attn_fwd(q, k, v, layout, inputs_on_host, out, lse, out_on_host,
                                            float(scale), dtype, c, ctypes.cast(arr, _vp), l, itr,
                                            int(bool(acc_on_host)), int(max_parallel), ctypes.byref(st),
                                            _stream(stream)))
+
+
+def cqsa_quorum_attn_fwd_ex(q, k, v, layout, inputs_on_host, out, lse, out_on_host, B, H, N, d, causal, scale,
+                            dtype, c, interest_set, itr, acc_on_host=False, max_parallel=1, engine=CQSA_ENGINE_WAVE,
+                            wave_tokens=0, stats=None, stream=None) -> int:
+    st = stats if stats is not None else cqsa_quorum_stats()
+    arr, l = _int_array(interest_set)
+    return _check(lib.cqsa_quorum_attn_fwd_ex(_ptr(q), _ptr(k), _ptr(v), layout, int(bool(inputs_on_host)),
+                                              _ptr(out), _ptr(lse), int(bool(out_on_host)), B, H, N, d,
+                                              int(bool(causal)), float(scale), dtype, c, ctypes.cast(arr, _vp), l,
+                                              itr, int(bool(acc_on_host)), int(max_parallel), int(engine),
+                                              int(wave_tokens), ctypes.byref(st), _stream(stream)))
 
 
 def cqsa_attn_bwd_workspace_size(B, H, N, d) -> int:

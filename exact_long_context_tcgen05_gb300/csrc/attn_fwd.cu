@@ -32,9 +32,14 @@
 #include <cuda_fp16.h>
 #include <math.h>
 #include <stdlib.h>
+#include <string.h>
 
 #include "cqsa_internal.h"
 #include "sm103_ptx.cuh"
+
+#ifndef CQSA_EXP_PINGPONG
+#define CQSA_EXP_PINGPONG 0
+#endif
 
 namespace cqsa {
 
@@ -73,6 +78,24 @@ struct KParams {
   unsigned long long timeout_ns;
   unsigned timeout_us;  // the same limit in microseconds (32-bit, for the two-tile kernel's loops)
   int fault;  // test hook: 1 = block 0 never loads key tile 1 (its waits must time out cleanly)
+  int mode;   // output mode of a pair in a multi-pair launch (AttnMode)
+};
+
+// A launch over several chunk pairs at once (the wave engine): one entry per pair, with its own
+// tensor maps, offsets, sizes, output mode and accumulator, and the first unit (CTA) of the pair.
+constexpr int kModeMulti = 3;  // template MODE of the multi-pair kernel: each pair's mode is in its entry
+constexpr int kMaxWavePairs = 32;
+struct PairDesc {
+  CUtensorMap q, k, v;
+  long long q_off, kv_off;
+  float* o_part;
+  float* lse_part;
+  int Nq, Nkv, n_q_tiles, mode, unit_begin;
+};
+struct MultiParams {
+  KParams common;
+  int n_pairs;
+  PairDesc pair[kMaxWavePairs];
 };
 
 
@@ -237,7 +260,7 @@ struct Cfg2 {
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
   static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
   static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
-  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
+  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2 + 8;
   // Every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running sum, so no
   // tensor-core accumulation chain exceeds FLUSH * 8 (d = 64) or FLUSH * 8 * 2 (bf16 hi/lo) MMAs. (The
   // MMA's fp32 accumulation is biased toward zero: measured relative drift -1.6e-5 after 16K keys, -6.9e-5
@@ -255,11 +278,14 @@ struct Cfg2 {
   static_assert(COL_O1 + D <= TMEM_COLS, "tensor memory layout exceeds 512 columns");
 };
 
+// The kernel body, for one work unit (a pair of query tiles of one (batch, head)); the tensor maps are
+// kernel parameters (__grid_constant__), passed by reference so that TMA sees their parameter-space
+// addresses.
 template <int D, int DT, bool CAUSAL, int MODE>
-__global__ void __launch_bounds__(NTHREADS2, 1)
-    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV, const KParams p) {
+__device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                               const KParams& p, const int unit) {
   using C = Cfg2<D, DT>;
+  const int mode = (MODE == kModeMulti) ? p.mode : MODE;
   constexpr int STAGES = C::STAGES;
   constexpr int KSUB = C::KSUB;
   constexpr bool ALIAS = C::ALIAS;
@@ -289,14 +315,14 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
   uint64_t* bar_pv_done = bar_p_full + 2;        // [2]
   uint64_t* bar_o_final = bar_pv_done + 2;       // [2] single phase each
   uint64_t* bar_mma_idle = bar_o_final + 2;     // [2] one per MMA warp
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_idle + 2);
+  uint64_t* bar_tok = bar_mma_idle + 2;          // [2][4]: exp-phase tokens per SM sub-partition
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tok + 8);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
   // Work unit: a pair of query tiles, heaviest (latest) first.
-  const int unit = blockIdx.x;
   const int qp = p.n_q_tiles - 1 - unit / p.BH;
   const int bh = unit % p.BH;
   const int b = bh / p.H;
@@ -332,6 +358,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       mbar_init(&bar_pv_done[t], 1);
       mbar_init(&bar_o_final[t], 1);
       mbar_init(&bar_mma_idle[t], 1);
+      for (int qq = 0; qq < 4; ++qq) mbar_init(&bar_tok[t * 4 + qq], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -516,6 +543,14 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     const int qt0 = wg ? q01 : q00;
     const uint32_t a_s_full = smem_u32(&bar_s_full[wg]), a_s_free = smem_u32(&bar_s_free[wg]);
     const uint32_t a_p_full = smem_u32(&bar_p_full[wg]), a_pv_done = smem_u32(&bar_pv_done[wg]);
+#if CQSA_EXP_PINGPONG
+    // The two softmax warps of one SM sub-partition (tile 0 and tile 1 of lane quarter `quarter`) take turns
+    // in their exponential phase: tile 0's exp(j) follows tile 1's exp(j-1), tile 1's exp(j) follows tile 0's
+    // exp(j). bar_tok[t * 4 + quarter] completes one phase per exp phase of tile t.
+    const uint32_t a_tok_out = smem_u32(&bar_tok[wg * 4 + quarter]);
+    const uint32_t a_tok_in = smem_u32(&bar_tok[(wg ^ 1) * 4 + quarter]);
+    const int nkv_other = wg ? nkv0 : nkv1;
+#endif
     const int nkv = wg ? nkv1 : nkv0;
     const int qi = qt0 + r;
     const long long qpos = p.q_off + qi;
@@ -543,13 +578,13 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
         tc_fence_after();
         const bool have = j > C::FLUSH;
         const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
+        if (C::OSUM_SMEM) {
 #pragma unroll
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t o[32];
-          tmem_ld32(trow + colO + c * 32, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-          if (C::OSUM_SMEM) {
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
             const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
@@ -557,14 +592,22 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
               const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
               st_shared_f32(a, prev + __uint_as_float(o[e]));
             }
-          } else {
-            // this thread's own row of the SM's slot: written before it is read, by this thread only
-            float* og = sOsum + (wg * D + c * 32) * 128 + r;
+          }
+        } else {
+          // this thread's own row of the SM's slot, written before it is read and by this thread only:
+          // every earlier value is loaded first (one round trip to L2), then O is added and stored back
+          float* og = sOsum + (wg * D) * 128 + r;
+          float prev[D];
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              const float prev = have ? og[e * 128] * sc : 0.0f;
-              og[e * 128] = prev + __uint_as_float(o[e]);
-            }
+          for (int e = 0; e < D; ++e) prev[e] = have ? __ldcg(og + e * 128) : 0.0f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) __stcg(og + (c * 32 + e) * 128, prev[c * 32 + e] * sc + __uint_as_float(o[e]));
           }
         }
         m_sum = m_ref;
@@ -624,12 +667,29 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
           // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
           // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
           uint32_t pk[64];
+#if CQSA_EXP_PINGPONG
+          {
+            // tile 0 waits for the partner's exp(j-1), tile 1 for the partner's exp(j), when the partner has them
+            const int pj = wg ? j : j - 1;
+            if (pj >= 0 && pj < nkv_other) {
+              ok = wait_or_abort_a(a_tok_in, static_cast<uint32_t>(pj) & 1u, tmo_us, a_abort, kDevTimeoutSoftmax, 25);
+              if (!__all_sync(0xffffffffu, ok)) {
+                ok = false;
+                break;
+              }
+            }
+          }
+#endif
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
             rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
             pk[c] = pack2(pp.x, pp.y, 0);
           }
+#if CQSA_EXP_PINGPONG
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(a_tok_out);
+#endif
           if (j > 0) {
             ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
             if (!__all_sync(0xffffffffu, ok)) {
@@ -701,7 +761,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     bool write = store;
     bool fresh = true;
     float wa = 0.0f, wn = 1.0f, lse_out = lse_v;
-    if (MODE == kModeAccum && store) {
+    if (mode == kModeAccum && store) {
       if (!has) {
         write = false;
       } else {
@@ -731,14 +791,17 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       if (C::FLUSH > 0 && osum_ok && nkv > C::FLUSH) {
         const float* os = sOsum + (wg * D + c * 32) * 128 + r;
         const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
+        float prev[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) v[e] = (os[e * 128] * sc + __uint_as_float(o[e])) * inv_l;
+        for (int e = 0; e < 32; ++e) prev[e] = C::OSUM_SMEM ? os[e * 128] : __ldcg(os + e * 128);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) v[e] = (prev[e] * sc + __uint_as_float(o[e])) * inv_l;
       } else {
 #pragma unroll
         for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
       }
       if (write) {
-        if (MODE == kModeOut) {
+        if (mode == kModeOut) {
           uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
 #pragma unroll
           for (int q8 = 0; q8 < 4; ++q8) {
@@ -754,7 +817,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {
             float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-            if (MODE == kModeAccum && !fresh) {
+            if (mode == kModeAccum && !fresh) {
               const float4 a = dst[q4];
               w.x = wa * a.x + wn * w.x;
               w.y = wa * a.y + wn * w.y;
@@ -767,7 +830,7 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
       }
     }
     if (write) {
-      if (MODE == kModeOut) {
+      if (mode == kModeOut) {
         if (p.lse) p.lse[lrow] = lse_v;
       } else {
         p.lse_part[lrow] = lse_out;
@@ -778,6 +841,34 @@ __global__ void __launch_bounds__(NTHREADS2, 1)
     tc_fence_before();
     asm volatile("bar.sync 0;" ::: "memory");
   }
+}
+
+template <int D, int DT, bool CAUSAL, int MODE>
+__global__ void __launch_bounds__(NTHREADS2, 1)
+    attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
+                     const __grid_constant__ CUtensorMap tmV, const KParams p) {
+  attn_fwd2_body<D, DT, CAUSAL, MODE>(tmQ, tmK, tmV, p, static_cast<int>(blockIdx.x));
+}
+
+// Several chunk pairs in one launch: CTA blockIdx.x belongs to the last pair whose first unit is at or
+// before it; that pair's maps, offsets, sizes, mode and accumulator replace the single-pair parameters.
+template <int D, int DT, bool CAUSAL>
+__global__ void __launch_bounds__(NTHREADS2, 1) attn_fwd2_multi_kernel(const __grid_constant__ MultiParams mp) {
+  const int u = static_cast<int>(blockIdx.x);
+  int i = 0;
+  for (int k = 1; k < mp.n_pairs; ++k)
+    if (mp.pair[k].unit_begin <= u) i = k;
+  const PairDesc& pd = mp.pair[i];
+  KParams kp = mp.common;
+  kp.q_off = pd.q_off;
+  kp.kv_off = pd.kv_off;
+  kp.Nq = pd.Nq;
+  kp.Nkv = pd.Nkv;
+  kp.n_q_tiles = pd.n_q_tiles;
+  kp.o_part = pd.o_part;
+  kp.lse_part = pd.lse_part;
+  kp.mode = pd.mode;
+  attn_fwd2_body<D, DT, CAUSAL, kModeMulti>(pd.q, pd.k, pd.v, kp, u - pd.unit_begin);
 }
 
 template <int D, int DT, bool CAUSAL, int MODE>
@@ -874,6 +965,28 @@ int make_map(CUtensorMap* m, const void* base, int dtype, int layout, int B, int
   return CQSA_OK;
 }
 
+template <int D, int DT, bool CAUSAL>
+int launch_multi_t(const MultiParams& mp, int grid, cudaStream_t stream) {
+  auto kern = attn_fwd2_multi_kernel<D, DT, CAUSAL>;
+  static PerDeviceOnce attr;  // the attributes belong to each device's context
+  int dev = 0;
+  if (!attr.done(&dev)) {
+    cudaFuncAttributes fa;
+    cudaError_t e = cudaFuncGetAttributes(&fa, kern);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(attention, several pairs)");
+    if (fa.numRegs * NTHREADS2 < 128 * REGS_LOW + 256 * REGS_HIGH) {
+      set_error("multi-pair attention kernel built with %d registers/thread; the register split needs %d",
+                fa.numRegs, (128 * REGS_LOW + 256 * REGS_HIGH + NTHREADS2 - 1) / NTHREADS2);
+      return CQSA_ERR_UNSUPPORTED;
+    }
+    e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, Cfg2<D, DT>::SMEM_BYTES);
+    if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem, several pairs)");
+    attr.mark(dev);
+  }
+  kern<<<grid, NTHREADS2, Cfg2<D, DT>::SMEM_BYTES, stream>>>(mp);
+  return cuda_status(cudaGetLastError(), "attention kernel launch (several pairs)");
+}
+
 }  // namespace
 
 int device_error_word(DevErr* out, int clear) {
@@ -925,6 +1038,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   kp.timeout_us = static_cast<unsigned>(kp.timeout_ns / 1000ull > 0xffffffffull ? 0xffffffffull
                                                                                 : kp.timeout_ns / 1000ull + 1ull);
   kp.fault = debug_fault();
+  kp.mode = a.mode;
   const long long grid = static_cast<long long>((a.Nq + BM - 1) / BM) * kp.BH;
   if (grid > 0x7fffffffLL) {
     set_error("problem too large for one launch (%lld tiles)", grid);
@@ -937,6 +1051,76 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
   }
   return a.dtype == CQSA_BF16 ? dispatch_mode<128, 1>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream)
                               : dispatch_mode<128, 0>(mq, mk, mv, kp, a.Nq, kp.BH, c, a.mode, stream);
+}
+
+int launch_attention_multi(const AttnArgs* pairs, int n, cudaStream_t stream) {
+  if (n < 1 || n > kMaxWavePairs) {
+    set_error("a multi-pair launch takes 1..%d chunk pairs (got %d)", kMaxWavePairs, n);
+    return CQSA_ERR_INVALID;
+  }
+  const AttnArgs& a0 = pairs[0];
+  static thread_local MultiParams mp;  // ~14 KB: kept off the stack
+  memset(&mp, 0, sizeof(mp));
+  KParams& kp = mp.common;
+  kp.H = a0.H;
+  kp.BH = a0.B * a0.H;
+  kp.scale_log2 = a0.scale * 1.4426950408889634f;
+  kp.out = a0.out;
+  kp.lse = a0.lse;
+  kp.out_layout = a0.out_layout;
+  kp.timeout_ns = timeout_ns();
+  kp.timeout_us = static_cast<unsigned>(kp.timeout_ns / 1000ull > 0xffffffffull ? 0xffffffffull
+                                                                                : kp.timeout_ns / 1000ull + 1ull);
+  kp.fault = debug_fault();
+  long long units = 0;
+  int np = 0;
+  for (int i = 0; i < n; ++i) {
+    const AttnArgs& a = pairs[i];
+    if (a.B != a0.B || a.H != a0.H || a.d != a0.d || a.dtype != a0.dtype || a.causal != a0.causal ||
+        a.in_layout != a0.in_layout || a.out_layout != a0.out_layout || a.scale != a0.scale) {
+      set_error("the pairs of a multi-pair launch must share B, H, d, dtype, causal, layouts and scale");
+      return CQSA_ERR_INVALID;
+    }
+    if (a.mode != kModePart && a.mode != kModeAccum) {
+      set_error("a multi-pair launch writes fp32 partials or accumulators (mode %d)", a.mode);
+      return CQSA_ERR_INVALID;
+    }
+    if (a.Nq <= 0) continue;
+    PairDesc& pd = mp.pair[np];
+    const void* kb = a.Nkv > 0 ? a.k : a.q;
+    const void* vb = a.Nkv > 0 ? a.v : a.q;
+    const int nkv_map = a.Nkv > 0 ? a.Nkv : a.Nq;
+    const long long kv_alloc = a.Nkv > 0 ? a.kv_tokens_alloc : a.q_tokens_alloc;
+    int rc = make_map(&pd.q, a.q, a.dtype, a.in_layout, a.B, a.H, a.Nq, a.d, a.q_tokens_alloc);
+    if (rc == CQSA_OK) rc = make_map(&pd.k, kb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d, kv_alloc);
+    if (rc == CQSA_OK) rc = make_map(&pd.v, vb, a.dtype, a.in_layout, a.B, a.H, nkv_map, a.d, kv_alloc);
+    if (rc != CQSA_OK) return rc;
+    pd.q_off = a.q_off;
+    pd.kv_off = a.kv_off;
+    pd.o_part = a.o_part;
+    pd.lse_part = a.lse_part;
+    pd.Nq = a.Nq;
+    pd.Nkv = a.Nkv;
+    pd.n_q_tiles = (a.Nq + 2 * BM - 1) / (2 * BM);
+    pd.mode = a.mode;
+    pd.unit_begin = static_cast<int>(units);
+    units += static_cast<long long>(pd.n_q_tiles) * kp.BH;
+    ++np;
+  }
+  if (np == 0) return CQSA_OK;
+  if (units > 0x7fffffffLL) {
+    set_error("multi-pair launch too large (%lld units)", units);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  mp.n_pairs = np;
+  const int grid = static_cast<int>(units);
+  const bool c = a0.causal != 0;
+  if (a0.d == 64) {
+    if (a0.dtype == CQSA_BF16) return c ? launch_multi_t<64, 1, true>(mp, grid, stream) : launch_multi_t<64, 1, false>(mp, grid, stream);
+    return c ? launch_multi_t<64, 0, true>(mp, grid, stream) : launch_multi_t<64, 0, false>(mp, grid, stream);
+  }
+  if (a0.dtype == CQSA_BF16) return c ? launch_multi_t<128, 1, true>(mp, grid, stream) : launch_multi_t<128, 1, false>(mp, grid, stream);
+  return c ? launch_multi_t<128, 0, true>(mp, grid, stream) : launch_multi_t<128, 0, false>(mp, grid, stream);
 }
 
 }  // namespace cqsa

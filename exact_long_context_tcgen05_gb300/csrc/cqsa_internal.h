@@ -43,6 +43,10 @@ struct AttnArgs {
 
 // Validates nothing (the ABI layer does); encodes tensor maps and launches on `stream`.
 int launch_attention(const AttnArgs& a, cudaStream_t stream);
+// Up to kMaxWavePairs (32) chunk pairs in one launch (the wave engine). The pairs share B, H, d, dtype,
+// causal, layouts and scale; each has its own buffers, offsets, sizes, mode (kModePart or kModeAccum)
+// and accumulator. Pairs writing one accumulator must not share a launch (their epilogues would race).
+int launch_attention_multi(const AttnArgs* pairs, int n, cudaStream_t stream);
 
 // Attention backward (attn_bwd.cu), head dimension 64. The monolithic call (launch_attention_bwd) takes
 // q, k, v, out, dout [B,H,N,64] with Nq = Nkv = N and offsets 0, writes dq, dk, dv, and uses

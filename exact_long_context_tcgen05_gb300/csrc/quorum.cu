@@ -37,6 +37,7 @@ namespace cqsa {
 namespace {
 
 constexpr int kMaxQuorumChunks = 1 << 16;  // c^itr
+constexpr int kMaxWavePairsLaunch = 32;     // pairs in one multi-pair launch (launch_attention_multi)
 
 struct Triple {
   int s, q, k;
@@ -175,6 +176,16 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
                                     int causal, float scale, int dtype, int c, const int* interest_set, int l,
                                     int itr, int acc_on_host, int max_parallel, cqsa_quorum_stats* stats,
                                     cudaStream_t stream) {
+  return cqsa_quorum_attn_fwd_ex(q, k, v, layout, inputs_on_host, out, lse, out_on_host, B, H, N, d, causal, scale,
+                                 dtype, c, interest_set, l, itr, acc_on_host, max_parallel, CQSA_ENGINE_CLASSIC, 0,
+                                 stats, stream);
+}
+
+extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void* v, int layout, int inputs_on_host,
+                                       void* out, float* lse, int out_on_host, int B, int H, long long N, int d,
+                                       int causal, float scale, int dtype, int c, const int* interest_set, int l,
+                                       int itr, int acc_on_host, int max_parallel, int engine, long long wave_tokens,
+                                       cqsa_quorum_stats* stats, cudaStream_t stream) {
   const auto t_start = std::chrono::steady_clock::now();
   if (stats) memset(stats, 0, sizeof(*stats));
   if (!q || !k || !v || !out) {
@@ -205,6 +216,19 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     set_error("max_parallel must be in [1, 16] (got %d)", max_parallel);
     return CQSA_ERR_INVALID;
   }
+  if (engine != CQSA_ENGINE_CLASSIC && engine != CQSA_ENGINE_WAVE) {
+    set_error("engine must be CQSA_ENGINE_CLASSIC or CQSA_ENGINE_WAVE (got %d)", engine);
+    return CQSA_ERR_INVALID;
+  }
+  if (wave_tokens < 0) {
+    set_error("wave_tokens must be >= 0 (0 selects min(2^21, max(2^19, N)))");
+    return CQSA_ERR_INVALID;
+  }
+  const bool wave = engine == CQSA_ENGINE_WAVE;
+  // Device-resident inputs are read in place (each chunk is a token range of the caller's tensors, which
+  // the tensor maps address with the full tensors' strides): nothing is staged, only the bookkeeping of
+  // the Q slots remains (the host accumulator travels with them).
+  const bool in_place = !inputs_on_host;
   int T = 0;
   if (itr < 1 || c < 1 || !ipow_bounded(c, itr, kMaxQuorumChunks, &T)) {
     set_error("quorum depth: need c >= 1, itr >= 1 and c^itr <= %d", kMaxQuorumChunks);
@@ -246,7 +270,7 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
     return CQSA_OK;
   };
   std::vector<void*> qs(nslots), ks(nslots), vs(nslots);
-  for (int s = 0; rc == CQSA_OK && s < nslots; ++s) {
+  for (int s = 0; rc == CQSA_OK && !in_place && s < nslots; ++s) {
     rc = alloc(&qs[s], chunk_elems * es);
     if (rc == CQSA_OK) rc = alloc(&ks[s], chunk_elems * es);
     if (rc == CQSA_OK) rc = alloc(&vs[s], chunk_elems * es);
@@ -276,7 +300,11 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
   }
   if (rc != CQSA_OK) return rc;
   if ((rc = pool_stream(&res.copy)) != CQSA_OK) return rc;
-  const int npar = max_parallel;
+  const int npar = wave ? 1 : max_parallel;  // the wave engine runs on the caller's stream alone
+  // Pairs per wave launch: the token budget in query tokens (default min(2^21, max(2^19, N))) over C,
+  // and at most the launch's table size.
+  const long long wt = wave_tokens > 0 ? wave_tokens : std::min(1LL << 21, std::max(1LL << 19, N));
+  const size_t wave_pairs = static_cast<size_t>(std::max(1LL, std::min(static_cast<long long>(kMaxWavePairsLaunch), wt / C)));
   std::vector<cudaStream_t> lane(npar, stream);
   for (int j = 1; j < npar; ++j) {
     cudaStream_t sj = nullptr;
@@ -368,7 +396,7 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       set_error("quorum executor: no free chunk slot");
       return CQSA_ERR_INVALID;
     }
-    int r;
+    int r = CQSA_OK;
     for (int j = 0; j < npar; ++j)
       if (pool.used[victim * npar + j] &&
           (r = cuda_status(cudaStreamWaitEvent(res.copy, is_q ? q_free[victim * npar + j] : kv_free[victim * npar + j], 0),
@@ -383,9 +411,11 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       if (acc_on_host && pool.chunk[victim] >= 0 && started[pool.chunk[victim]] &&
           (r = acc_copy(pool.chunk[victim], victim, true, res.copy)) != CQSA_OK)
         return r;
-      r = cuda_status(copy_chunk(qs[victim], q, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy Q chunk");
+      if (!in_place)
+        r = cuda_status(copy_chunk(qs[victim], q, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes),
+                        "copy Q chunk");
       if (r == CQSA_OK && acc_on_host && started[chunk]) r = acc_copy(chunk, victim, false, res.copy);
-    } else {
+    } else if (!in_place) {
       r = cuda_status(copy_chunk(ks[victim], k, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes), "copy K chunk");
       if (r == CQSA_OK)
         r = cuda_status(copy_chunk(vs[victim], v, layout, B, H, N, d, t0, n, kind, res.copy, &copy_bytes),
@@ -398,7 +428,7 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       return r;
     pool.chunk[victim] = chunk;
     pool.last_use[victim] = group;
-    ++loads;
+    if (!in_place || is_q) ++loads;
     *slot = victim;
     return CQSA_OK;
   };
@@ -412,20 +442,33 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       if (std::find(needq.begin(), needq.end(), sched[i].q) == needq.end()) needq.push_back(sched[i].q);
       if (std::find(needk.begin(), needk.end(), sched[i].k) == needk.end()) needk.push_back(sched[i].k);
     }
+    // Chunk pointers: the staged slot, or the token range of the caller's device tensors.
+    auto chunk_ptr = [&](const void* base, const std::vector<void*>& slots, int slot, int chunk) -> const void* {
+      if (!in_place) return slots[slot];
+      const long long t0 = static_cast<long long>(chunk) * C;
+      const size_t off = layout == CQSA_LAYOUT_BHND ? static_cast<size_t>(t0) * d * es
+                                                    : static_cast<size_t>(t0) * H * d * es;
+      return static_cast<const char*>(base) + off;
+    };
+    struct Pending {
+      AttnArgs a;
+      int sq, sk, q;
+    };
+    std::vector<Pending> group_pairs;
     for (size_t i = i0; i < i1; ++i) {
       const Triple& t = sched[i];
       int sq = -1, sk = -1;
       if ((rc = stage(qp, true, t.q, groups, needq, &sq)) != CQSA_OK) return rc;
       if ((rc = stage(kp, false, t.k, groups, needk, &sk)) != CQSA_OK) return rc;
-      const int j = t.q % npar;
-      cudaStream_t ls = lane[j];
-      CK(cudaStreamWaitEvent(ls, q_ready[sq], 0), "wait q_ready");
-      CK(cudaStreamWaitEvent(ls, kv_ready[sk], 0), "wait kv_ready");
       AttnArgs a;
       memset(&a, 0, sizeof(a));
-      a.q = qs[sq];
-      a.k = ks[sk];
-      a.v = vs[sk];
+      a.q = chunk_ptr(q, qs, sq, t.q);
+      a.k = chunk_ptr(k, ks, sk, t.k);
+      a.v = chunk_ptr(v, vs, sk, t.k);
+      if (in_place) {
+        a.q_tokens_alloc = N;
+        a.kv_tokens_alloc = N;
+      }
       a.B = B;
       a.H = H;
       a.Nq = ntok(t.q);
@@ -441,6 +484,15 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       a.o_part = dacc(t.q, sq);
       a.lse_part = dlacc(t.q, sq);
       a.out_layout = CQSA_LAYOUT_BHND;
+      started[t.q] = true;
+      if (wave) {
+        group_pairs.push_back({a, sq, sk, t.q});
+        continue;
+      }
+      const int j = t.q % npar;
+      cudaStream_t ls = lane[j];
+      CK(cudaStreamWaitEvent(ls, q_ready[sq], 0), "wait q_ready");
+      CK(cudaStreamWaitEvent(ls, kv_ready[sk], 0), "wait kv_ready");
       Span sp;
       if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
       CK(cudaEventRecord(sp.a, ls), "record");
@@ -450,8 +502,60 @@ extern "C" int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v,
       CK(cudaEventRecord(kv_free[sk * npar + j], ls), "record kv_free");
       qp.used[sq * npar + j] = true;
       kp.used[sk * npar + j] = true;
-      started[t.q] = true;
       ++launches;
+    }
+    if (wave && !group_pairs.empty()) {
+      // Waves: one launch takes at most one pair of each query chunk (pairs of one chunk accumulate into
+      // one buffer, in schedule order, wave after wave) and at most wave_pairs pairs in all. Pairs with a
+      // full key chunk come first in a launch, the (lighter) diagonal pairs last.
+      std::vector<int> qlist;
+      std::vector<std::vector<size_t>> byq;
+      for (size_t i = 0; i < group_pairs.size(); ++i) {
+        const int qc = group_pairs[i].q;
+        size_t pos = std::find(qlist.begin(), qlist.end(), qc) - qlist.begin();
+        if (pos == qlist.size()) {
+          qlist.push_back(qc);
+          byq.emplace_back();
+        }
+        byq[pos].push_back(i);
+      }
+      size_t depth = 0;
+      for (const auto& v_ : byq) depth = std::max(depth, v_.size());
+      for (size_t w = 0; w < depth; ++w) {
+        std::vector<size_t> members;
+        for (const auto& v_ : byq)
+          if (w < v_.size()) members.push_back(v_[w]);
+        std::stable_sort(members.begin(), members.end(), [&](size_t x, size_t y) {
+          const AttnArgs& ax = group_pairs[x].a;
+          const AttnArgs& ay = group_pairs[y].a;
+          const bool fx = !causal || ax.kv_off + ax.Nkv <= ax.q_off + 1;
+          const bool fy = !causal || ay.kv_off + ay.Nkv <= ay.q_off + 1;
+          return fx && !fy;
+        });
+        for (size_t m0 = 0; m0 < members.size(); m0 += wave_pairs) {
+          const size_t m1 = std::min(members.size(), m0 + wave_pairs);
+          std::vector<AttnArgs> batch;
+          for (size_t m = m0; m < m1; ++m) {
+            const Pending& pd = group_pairs[members[m]];
+            CK(cudaStreamWaitEvent(stream, q_ready[pd.sq], 0), "wait q_ready");
+            CK(cudaStreamWaitEvent(stream, kv_ready[pd.sk], 0), "wait kv_ready");
+            batch.push_back(pd.a);
+          }
+          Span sp;
+          if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
+          CK(cudaEventRecord(sp.a, stream), "record");
+          if ((rc = launch_attention_multi(batch.data(), static_cast<int>(batch.size()), stream)) != CQSA_OK) return rc;
+          CK(cudaEventRecord(sp.b, stream), "record");
+          for (size_t m = m0; m < m1; ++m) {
+            const Pending& pd = group_pairs[members[m]];
+            CK(cudaEventRecord(q_free[pd.sq * npar], stream), "record q_free");
+            CK(cudaEventRecord(kv_free[pd.sk * npar], stream), "record kv_free");
+            qp.used[pd.sq * npar] = true;
+            kp.used[pd.sk * npar] = true;
+          }
+          ++launches;
+        }
+      }
     }
     ++groups;
     i0 = i1;

@@ -153,8 +153,9 @@ typedef struct {
 
 /*
  * Exact attention through the quorum decomposition. q, k, v: [B,H,N,d] (layout BHND) or [B,N,H,d]
- * (layout BNHD), fp16/bf16, in host memory (inputs_on_host, pinned for speed) or device memory. Each
- * subproblem's chunks are staged into two sets of l^itr device slots. acc_on_host = 0: one fp32
+ * (layout BNHD), fp16/bf16, in host memory (inputs_on_host, pinned for speed) or device memory. Host
+ * inputs: each subproblem's chunks are staged into two sets of l^itr device slots; device inputs are
+ * read in place (a chunk is a token range of the caller's tensor). acc_on_host = 0: one fp32
  * accumulator per query chunk on the device; acc_on_host = 1 (the pages' accumulate_on_gpu=False,
  * "stream-cqsa 2.2.0 -> 2.2.2" README): the accumulators live in pinned host memory allocated by the
  * call and travel with their Q slot, so device memory is bounded by the slots. out/lse as in
@@ -169,6 +170,28 @@ int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout
                          float* lse, int out_on_host, int B, int H, long long N, int d, int causal, float scale,
                          int dtype, int c, const int* interest_set, int l, int itr, int acc_on_host,
                          int max_parallel, cqsa_quorum_stats* stats, cudaStream_t stream);
+
+/*
+ * The same decomposition with a choice of engine (the pages' classic and wave engines, "stream-cqsa
+ * 2.2.0 -> 2.2.2" diff: README, peak memory of the wave engine and its wave budget, and `api.py`
+ * `_pick_wave`, whose default budget is min(2M, max(512K, N)) packed tokens).
+ * engine = CQSA_ENGINE_CLASSIC: one chunk-pair launch after another on max_parallel lanes (as
+ *   cqsa_quorum_attn_fwd).
+ * engine = CQSA_ENGINE_WAVE: the pairs of each subproblem run in waves, one multi-pair launch per wave
+ *   (up to 32 pairs, at most one per query chunk, so each pair's epilogue merges into its query
+ *   chunk's accumulator without a race); a wave holds at most wave_tokens query tokens (0 selects
+ *   min(2^21, max(2^19, N))). Partials are merged in place by the kernel's epilogue, so no packed
+ *   partial buffer is needed and the budget only caps a launch's size. max_parallel is ignored (one
+ *   stream). Pairs of a query chunk are merged in the same order as by the classic engine, so the two
+ *   engines give bit-identical results.
+ * Device-resident inputs (inputs_on_host = 0) are read in place by either engine; nothing is staged.
+ */
+enum { CQSA_ENGINE_CLASSIC = 0, CQSA_ENGINE_WAVE = 1 };
+int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void* v, int layout, int inputs_on_host, void* out,
+                            float* lse, int out_on_host, int B, int H, long long N, int d, int causal, float scale,
+                            int dtype, int c, const int* interest_set, int l, int itr, int acc_on_host,
+                            int max_parallel, int engine, long long wave_tokens, cqsa_quorum_stats* stats,
+                            cudaStream_t stream);
 
 /*
  * The host-driven entry points (cqsa_stream_attn_fwd, cqsa_quorum_attn_fwd) take their device buffers,

@@ -186,3 +186,50 @@ def test_quorum_batched_heads(cq, layout, on_host):
     if layout == syn.LAYOUT_BNHD:
         o64 = o64.transpose(0, 2, 1, 3)
     assert_close(o64, ro, to_np64(lse), rl, what="quorum B=2")
+
+
+@pytest.mark.parametrize("c,itr,N,d,dtype,causal,layout,on_host,acc_host", [
+    (7, 1, 3000, 64, syn.F16, True, syn.LAYOUT_BHND, False, False),
+    (3, 2, 2300, 64, syn.F16, False, syn.LAYOUT_BNHD, True, False),
+    (13, 1, 4000, 128, syn.BF16, True, syn.LAYOUT_BHND, False, True),
+    (31, 1, 9000, 64, syn.F16, True, syn.LAYOUT_BNHD, True, True),
+])
+def test_wave_engine_equals_classic_and_oracle(cq, c, itr, N, d, dtype, causal, layout, on_host, acc_host):
+    """The wave engine (one multi-pair launch per wave, at most one pair per query chunk) merges each query
+    chunk's pairs in the classic engine's order, so the two agree bit for bit; also with a token budget of
+    one chunk per launch. Both against the oracle (fp16 outputs; bf16 through the classic test above)."""
+    B, H = 1, 2
+    D = {3: (0, 1), 7: (0, 1, 3), 13: (0, 1, 3, 9), 31: (0, 1, 3, 8, 12, 18)}[c]
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=40 + c, dtype=dtype, layout=layout)
+    shape = (B, H, N, d) if layout == syn.LAYOUT_BHND else (B, N, H, d)
+    tdt = torch.float16 if dtype == syn.F16 else torch.bfloat16
+    if on_host:
+        q, k, v = (_host(x, dtype) for x in (qn, kn, vn))
+    else:
+        q, k, v = (to_dev(x, dtype) for x in (qn, kn, vn))
+    res = []
+    for engine, wt in ((cq.CQSA_ENGINE_CLASSIC, 0), (cq.CQSA_ENGINE_WAVE, 0), (cq.CQSA_ENGINE_WAVE, 1)):
+        out = torch.empty(shape, dtype=tdt, device="cuda")
+        lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+        st = cq.cqsa_quorum_stats()
+        cq.cqsa_quorum_attn_fwd_ex(q, k, v, layout, on_host, out, lse, False, B, H, N, d, causal, 0.0, dtype, c, D,
+                                   itr, acc_on_host=acc_host, engine=engine, wave_tokens=wt, stats=st)
+        res.append((out, lse, st.n_launches, st.n_pairs))
+    for o, l_, nl, npairs in res[1:]:
+        assert torch.equal(o, res[0][0]) and torch.equal(l_, res[0][1])
+        assert npairs == res[0][3]
+    # fewer launches than pairs with the default budget; one launch per pair with a one-token budget
+    assert res[1][2] < res[0][2] and res[2][2] >= res[0][3]
+    if dtype == syn.F16:
+        ro, rl = _oracle(qn, kn, vn, B, H, N, d, causal, dtype, layout)
+        o64 = to_np64(res[1][0])
+        if layout == syn.LAYOUT_BNHD:
+            o64 = o64.transpose(0, 2, 1, 3)
+        assert_close(o64, ro, to_np64(res[1][1]), rl, what=f"wave engine c={c} itr={itr}")
+
+
+def test_wave_engine_rejects_bad_engine(cq):
+    x = torch.zeros((1, 1, 256, 64), dtype=torch.float16, device="cuda")
+    with pytest.raises(cq.CqsaError):
+        cq.cqsa_quorum_attn_fwd_ex(x, x, x, syn.LAYOUT_BHND, False, torch.empty_like(x), None, False, 1, 1, 256, 64,
+                                   True, 0.0, syn.F16, 7, (0, 1, 3), 1, engine=5)
