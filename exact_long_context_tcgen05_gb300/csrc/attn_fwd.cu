@@ -37,8 +37,8 @@
 #include "cqsa_internal.h"
 #include "sm103_ptx.cuh"
 
-#ifndef CQSA_EXP_PINGPONG
-#define CQSA_EXP_PINGPONG 0
+#ifndef CQSA_D128_FLUSH
+#define CQSA_D128_FLUSH 32
 #endif
 
 namespace cqsa {
@@ -260,7 +260,7 @@ struct Cfg2 {
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
   static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
   static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
-  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2 + 8;
+  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
   // Every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running sum, so no
   // tensor-core accumulation chain exceeds FLUSH * 8 (d = 64) or FLUSH * 8 * 2 (bf16 hi/lo) MMAs. (The
   // MMA's fp32 accumulation is biased toward zero: measured relative drift -1.6e-5 after 16K keys, -6.9e-5
@@ -270,7 +270,7 @@ struct Cfg2 {
   // tensor memory left for it and keeps it in global memory, one 128 KiB slot per SM (g_osum below): two
   // CTAs of this kernel never share an SM (each needs more than half of its shared and all its tensor
   // memory), so the slot of the SM a CTA runs on is its own for the CTA's lifetime.
-  static constexpr int FLUSH = (D == 64) ? 128 : 32;
+  static constexpr int FLUSH = (D == 64) ? 128 : CQSA_D128_FLUSH;
   static constexpr bool OSUM_SMEM = (D == 64);
   static constexpr uint32_t OSUM_BYTES = OSUM_SMEM ? 2u * D * 128u * 4u : 0u;
   static constexpr uint32_t SMEM_BYTES =
@@ -315,8 +315,7 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
   uint64_t* bar_pv_done = bar_p_full + 2;        // [2]
   uint64_t* bar_o_final = bar_pv_done + 2;       // [2] single phase each
   uint64_t* bar_mma_idle = bar_o_final + 2;     // [2] one per MMA warp
-  uint64_t* bar_tok = bar_mma_idle + 2;          // [2][4]: exp-phase tokens per SM sub-partition
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_tok + 8);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_idle + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
@@ -358,7 +357,6 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
       mbar_init(&bar_pv_done[t], 1);
       mbar_init(&bar_o_final[t], 1);
       mbar_init(&bar_mma_idle[t], 1);
-      for (int qq = 0; qq < 4; ++qq) mbar_init(&bar_tok[t * 4 + qq], 1);
     }
     *abort_flag = 0;
     fence_mbar_init();
@@ -543,14 +541,6 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
     const int qt0 = wg ? q01 : q00;
     const uint32_t a_s_full = smem_u32(&bar_s_full[wg]), a_s_free = smem_u32(&bar_s_free[wg]);
     const uint32_t a_p_full = smem_u32(&bar_p_full[wg]), a_pv_done = smem_u32(&bar_pv_done[wg]);
-#if CQSA_EXP_PINGPONG
-    // The two softmax warps of one SM sub-partition (tile 0 and tile 1 of lane quarter `quarter`) take turns
-    // in their exponential phase: tile 0's exp(j) follows tile 1's exp(j-1), tile 1's exp(j) follows tile 0's
-    // exp(j). bar_tok[t * 4 + quarter] completes one phase per exp phase of tile t.
-    const uint32_t a_tok_out = smem_u32(&bar_tok[wg * 4 + quarter]);
-    const uint32_t a_tok_in = smem_u32(&bar_tok[(wg ^ 1) * 4 + quarter]);
-    const int nkv_other = wg ? nkv0 : nkv1;
-#endif
     const int nkv = wg ? nkv1 : nkv0;
     const int qi = qt0 + r;
     const long long qpos = p.q_off + qi;
@@ -667,29 +657,12 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
           // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
           // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
           uint32_t pk[64];
-#if CQSA_EXP_PINGPONG
-          {
-            // tile 0 waits for the partner's exp(j-1), tile 1 for the partner's exp(j), when the partner has them
-            const int pj = wg ? j : j - 1;
-            if (pj >= 0 && pj < nkv_other) {
-              ok = wait_or_abort_a(a_tok_in, static_cast<uint32_t>(pj) & 1u, tmo_us, a_abort, kDevTimeoutSoftmax, 25);
-              if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
-              }
-            }
-          }
-#endif
 #pragma unroll
           for (int c = 0; c < 64; ++c) {
             const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
             rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
             pk[c] = pack2(pp.x, pp.y, 0);
           }
-#if CQSA_EXP_PINGPONG
-          __syncwarp();
-          if (lane == 0) mbar_arrive_a(a_tok_out);
-#endif
           if (j > 0) {
             ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
             if (!__all_sync(0xffffffffu, ok)) {

@@ -433,6 +433,72 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
     return CQSA_OK;
   };
 
+  // Wave launches of a list of pairs (waves: see the header of cqsa_quorum_attn_fwd_ex).
+  struct Pending {
+    AttnArgs a;
+    int sq, sk, q;
+  };
+  auto launch_waves = [&](std::vector<Pending>& group_pairs) -> int {
+    int rc = CQSA_OK;
+    // Waves: one launch takes at most one pair of each query chunk (pairs of one chunk accumulate into
+    // one buffer, in schedule order, wave after wave) and at most wave_pairs pairs in all. Pairs with a
+    // full key chunk come first in a launch, the (lighter) diagonal pairs last.
+    std::vector<int> qlist;
+    std::vector<std::vector<size_t>> byq;
+    for (size_t i = 0; i < group_pairs.size(); ++i) {
+      const int qc = group_pairs[i].q;
+      size_t pos = std::find(qlist.begin(), qlist.end(), qc) - qlist.begin();
+      if (pos == qlist.size()) {
+        qlist.push_back(qc);
+        byq.emplace_back();
+      }
+      byq[pos].push_back(i);
+    }
+    size_t depth = 0;
+    for (const auto& v_ : byq) depth = std::max(depth, v_.size());
+    for (size_t w = 0; w < depth; ++w) {
+      std::vector<size_t> members;
+      for (const auto& v_ : byq)
+        if (w < v_.size()) members.push_back(v_[w]);
+      std::stable_sort(members.begin(), members.end(), [&](size_t x, size_t y) {
+        const AttnArgs& ax = group_pairs[x].a;
+        const AttnArgs& ay = group_pairs[y].a;
+        const bool fx = !causal || ax.kv_off + ax.Nkv <= ax.q_off + 1;
+        const bool fy = !causal || ay.kv_off + ay.Nkv <= ay.q_off + 1;
+        return fx && !fy;
+      });
+      for (size_t m0 = 0; m0 < members.size(); m0 += wave_pairs) {
+        const size_t m1 = std::min(members.size(), m0 + wave_pairs);
+        std::vector<AttnArgs> batch;
+        for (size_t m = m0; m < m1; ++m) {
+          const Pending& pd = group_pairs[members[m]];
+          CK(cudaStreamWaitEvent(stream, q_ready[pd.sq], 0), "wait q_ready");
+          CK(cudaStreamWaitEvent(stream, kv_ready[pd.sk], 0), "wait kv_ready");
+          batch.push_back(pd.a);
+        }
+        Span sp;
+        if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
+        CK(cudaEventRecord(sp.a, stream), "record");
+        if ((rc = launch_attention_multi(batch.data(), static_cast<int>(batch.size()), stream)) != CQSA_OK) return rc;
+        CK(cudaEventRecord(sp.b, stream), "record");
+        for (size_t m = m0; m < m1; ++m) {
+          const Pending& pd = group_pairs[members[m]];
+          CK(cudaEventRecord(q_free[pd.sq * npar], stream), "record q_free");
+          CK(cudaEventRecord(kv_free[pd.sk * npar], stream), "record kv_free");
+          qp.used[pd.sq * npar] = true;
+          kp.used[pd.sk * npar] = true;
+        }
+        ++launches;
+      }
+    }
+    group_pairs.clear();
+    return CQSA_OK;
+  };
+  // Device-resident inputs without the host accumulator: every chunk is always at hand, so a wave may
+  // take pairs of every subproblem (one launch holds the w-th pair, in schedule order, of each query chunk).
+  const bool global_waves = wave && in_place && !acc_on_host;
+  std::vector<Pending> group_pairs;
+
   size_t i0 = 0;
   while (i0 < sched.size()) {
     size_t i1 = i0;
@@ -450,11 +516,6 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
                                                     : static_cast<size_t>(t0) * H * d * es;
       return static_cast<const char*>(base) + off;
     };
-    struct Pending {
-      AttnArgs a;
-      int sq, sk, q;
-    };
-    std::vector<Pending> group_pairs;
     for (size_t i = i0; i < i1; ++i) {
       const Triple& t = sched[i];
       int sq = -1, sk = -1;
@@ -504,62 +565,12 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
       kp.used[sk * npar + j] = true;
       ++launches;
     }
-    if (wave && !group_pairs.empty()) {
-      // Waves: one launch takes at most one pair of each query chunk (pairs of one chunk accumulate into
-      // one buffer, in schedule order, wave after wave) and at most wave_pairs pairs in all. Pairs with a
-      // full key chunk come first in a launch, the (lighter) diagonal pairs last.
-      std::vector<int> qlist;
-      std::vector<std::vector<size_t>> byq;
-      for (size_t i = 0; i < group_pairs.size(); ++i) {
-        const int qc = group_pairs[i].q;
-        size_t pos = std::find(qlist.begin(), qlist.end(), qc) - qlist.begin();
-        if (pos == qlist.size()) {
-          qlist.push_back(qc);
-          byq.emplace_back();
-        }
-        byq[pos].push_back(i);
-      }
-      size_t depth = 0;
-      for (const auto& v_ : byq) depth = std::max(depth, v_.size());
-      for (size_t w = 0; w < depth; ++w) {
-        std::vector<size_t> members;
-        for (const auto& v_ : byq)
-          if (w < v_.size()) members.push_back(v_[w]);
-        std::stable_sort(members.begin(), members.end(), [&](size_t x, size_t y) {
-          const AttnArgs& ax = group_pairs[x].a;
-          const AttnArgs& ay = group_pairs[y].a;
-          const bool fx = !causal || ax.kv_off + ax.Nkv <= ax.q_off + 1;
-          const bool fy = !causal || ay.kv_off + ay.Nkv <= ay.q_off + 1;
-          return fx && !fy;
-        });
-        for (size_t m0 = 0; m0 < members.size(); m0 += wave_pairs) {
-          const size_t m1 = std::min(members.size(), m0 + wave_pairs);
-          std::vector<AttnArgs> batch;
-          for (size_t m = m0; m < m1; ++m) {
-            const Pending& pd = group_pairs[members[m]];
-            CK(cudaStreamWaitEvent(stream, q_ready[pd.sq], 0), "wait q_ready");
-            CK(cudaStreamWaitEvent(stream, kv_ready[pd.sk], 0), "wait kv_ready");
-            batch.push_back(pd.a);
-          }
-          Span sp;
-          if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
-          CK(cudaEventRecord(sp.a, stream), "record");
-          if ((rc = launch_attention_multi(batch.data(), static_cast<int>(batch.size()), stream)) != CQSA_OK) return rc;
-          CK(cudaEventRecord(sp.b, stream), "record");
-          for (size_t m = m0; m < m1; ++m) {
-            const Pending& pd = group_pairs[members[m]];
-            CK(cudaEventRecord(q_free[pd.sq * npar], stream), "record q_free");
-            CK(cudaEventRecord(kv_free[pd.sk * npar], stream), "record kv_free");
-            qp.used[pd.sq * npar] = true;
-            kp.used[pd.sk * npar] = true;
-          }
-          ++launches;
-        }
-      }
-    }
+    if (wave && !global_waves && (rc = launch_waves(group_pairs)) != CQSA_OK) return rc;
     ++groups;
     i0 = i1;
   }
+
+  if (global_waves && (rc = launch_waves(group_pairs)) != CQSA_OK) return rc;
 
   // Every lane's kernels finish before the caller's stream finalizes.
   for (int j = 1; j < npar; ++j) {
