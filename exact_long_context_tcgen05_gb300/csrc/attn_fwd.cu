@@ -40,6 +40,9 @@
 #ifndef CQSA_D128_FLUSH
 #define CQSA_D128_FLUSH 32
 #endif
+#ifndef CQSA_KV_GROUP_MB
+#define CQSA_KV_GROUP_MB 64
+#endif
 
 namespace cqsa {
 
@@ -79,6 +82,7 @@ struct KParams {
   unsigned timeout_us;  // the same limit in microseconds (32-bit, for the two-tile kernel's loops)
   int fault;  // test hook: 1 = block 0 never loads key tile 1 (its waits must time out cleanly)
   int mode;   // output mode of a pair in a multi-pair launch (AttnMode)
+  int head_group;  // heads whose units are interleaved (the rest follow group by group); >= 1
 };
 
 // A launch over several chunk pairs at once (the wave engine): one entry per pair, with its own
@@ -322,8 +326,15 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
   const int lane = threadIdx.x & 31;
 
   // Work unit: a pair of query tiles, heaviest (latest) first.
-  const int qp = p.n_q_tiles - 1 - unit / p.BH;
-  const int bh = unit % p.BH;
+  // Units of head_group heads at a time (heads interleaved, query-tile pairs heaviest first), so that the
+  // K/V of the heads in flight stay in L2; one group of all heads when they fit.
+  const int gsz = p.head_group;
+  const int per_group = gsz * p.n_q_tiles;
+  const int g0 = (unit / per_group) * gsz;
+  const int gn = min(gsz, p.BH - g0);
+  const int ur = unit - (unit / per_group) * per_group;
+  const int qp = p.n_q_tiles - 1 - ur / gn;
+  const int bh = g0 + ur % gn;
   const int b = bh / p.H;
   const int h = bh % p.H;
   // Per query tile: first row and number of key tiles (scalars: no runtime-indexed local arrays).
@@ -884,6 +895,16 @@ int dispatch_mode(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMa
   return launch_t<D, DT, false, kModeAccum>(mq, mk, mv, kp, Nq, BH, s);
 }
 
+// Heads per group of work units: every head when the K/V of all heads fit in half of L2 (64 MB),
+// otherwise as many as do (at least one).
+int head_group_for(int BH, long long Nkv, int d) {
+  const long long per_head = 2LL * (Nkv > 0 ? Nkv : 1) * d * 2;
+  const long long budget = static_cast<long long>(CQSA_KV_GROUP_MB) << 20;
+  if (budget <= 0 || per_head * BH <= budget) return BH;
+  const long long g = budget / per_head;
+  return static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+}
+
 // cuTensorMapEncodeTiled through the runtime's driver entry point (no link-time libcuda dependency).
 typedef CUresult (*EncodeTiledFn)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
                                   const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
@@ -1012,6 +1033,7 @@ int launch_attention(const AttnArgs& a, cudaStream_t stream) {
                                                                                 : kp.timeout_ns / 1000ull + 1ull);
   kp.fault = debug_fault();
   kp.mode = a.mode;
+  kp.head_group = head_group_for(kp.BH, a.Nkv, a.d);
   const long long grid = static_cast<long long>((a.Nq + BM - 1) / BM) * kp.BH;
   if (grid > 0x7fffffffLL) {
     set_error("problem too large for one launch (%lld tiles)", grid);
@@ -1045,6 +1067,9 @@ int launch_attention_multi(const AttnArgs* pairs, int n, cudaStream_t stream) {
   kp.timeout_us = static_cast<unsigned>(kp.timeout_ns / 1000ull > 0xffffffffull ? 0xffffffffull
                                                                                 : kp.timeout_ns / 1000ull + 1ull);
   kp.fault = debug_fault();
+  long long max_kv = 0;
+  for (int i = 0; i < n; ++i) max_kv = pairs[i].Nkv > max_kv ? pairs[i].Nkv : max_kv;
+  kp.head_group = head_group_for(kp.BH, max_kv, a0.d);
   long long units = 0;
   int np = 0;
   for (int i = 0; i < n; ++i) {
