@@ -128,6 +128,9 @@ struct PerDeviceOnce {
 // and site in the error message.
 int check_device_error_on(cudaStream_t s);
 
+// Number of SMs of the current device (cached per device; 152 if the query fails).
+int sm_count();
+
 // Status helpers
 void set_error(const char* fmt, ...);
 int cuda_status(cudaError_t e, const char* what);

@@ -119,20 +119,6 @@ __global__ void __launch_bounds__(256) merge_kernel(const PartPtrs<MAXN> parts, 
   }
 }
 
-// SM count of the current device, cached per device.
-int sm_count() {
-  static std::atomic<int> cache[64];
-  int dev = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
-  if (dev >= 0 && dev < 64) {
-    const int c = cache[dev].load(std::memory_order_relaxed);
-    if (c > 0) return c;
-  }
-  int n = 0;
-  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
-  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
-  return n;
-}
 
 template <int D, int MAXN>
 int launch_n(const float* const* O_parts, const float* const* LSE_parts, int n, void* out, float* lse, long long rows,
@@ -167,6 +153,21 @@ int launch_merge(const float* const* O_parts, const float* const* LSE_parts, int
   if (rows == 0) return CQSA_OK;
   if (d == 64) return launch_d<64>(O_parts, LSE_parts, n, out, lse, rows, out_dtype, stream);
   return launch_d<128>(O_parts, LSE_parts, n, out, lse, rows, out_dtype, stream);
+}
+
+// SM count of the current device, cached per device.
+int sm_count() {
+  static std::atomic<int> cache[64];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 152;
+  if (dev >= 0 && dev < 64) {
+    const int c = cache[dev].load(std::memory_order_relaxed);
+    if (c > 0) return c;
+  }
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 152;
+  if (dev >= 0 && dev < 64) cache[dev].store(n, std::memory_order_relaxed);
+  return n;
 }
 
 }  // namespace cqsa
