@@ -39,6 +39,10 @@
 #include "cqsa_internal.h"
 #include "sm103_ptx.cuh"
 
+#ifndef CQSA_BWD_GROUP_MB
+#define CQSA_BWD_GROUP_MB 48
+#endif
+
 namespace cqsa {
 namespace {
 
@@ -81,6 +85,8 @@ struct BwdParams {
   float scale, scale_log2;
   unsigned long long timeout_ns;
   int fault;  // test hook: 2 = block 0 never loads its key/value tile (its waits must time out cleanly)
+  int head_group;  // heads whose key tiles are interleaved; the rest follow group by group
+  int n_kv_tiles;
 };
 
 __device__ __forceinline__ void record_bwd_error(int code, int where) {
@@ -248,7 +254,14 @@ __global__ void __launch_bounds__(NTHR, 1)
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int bh = blockIdx.x % p.BH, jt = blockIdx.x / p.BH;
+  // Key tiles of head_group heads at a time, heaviest (first) key tiles first within a group, so that the
+  // fp32 dQ accumulators and the Q / dO tiles of the heads in flight stay in L2.
+  const int unit = static_cast<int>(blockIdx.x);
+  const int per_group = p.head_group * p.n_kv_tiles;
+  const int g0 = (unit / per_group) * p.head_group;
+  const int gn = min(p.head_group, p.BH - g0);
+  const int ur = unit - (unit / per_group) * per_group;
+  const int bh = g0 + ur % gn, jt = ur / gn;
   const int b = bh / p.H, h = bh % p.H;
   const int k0 = jt * BT;
   const int Nkv = ACCUM ? p.Nkv : p.Nq;
@@ -732,6 +745,15 @@ int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cuda
   p.Nq = a.Nq;
   p.Nkv = a.Nkv;
   p.n_q_tiles = static_cast<int>(n_q_tiles);
+  p.n_kv_tiles = static_cast<int>(n_kv_tiles);
+  {
+    // per head: the fp32 dQ accumulator and the Q and dO rows streamed past every key tile
+    const long long per_head = static_cast<long long>(a.Nq) * HD * (4 + 2 + 2);
+    const long long budget = static_cast<long long>(CQSA_BWD_GROUP_MB) << 20;
+    const int BH = a.B * a.H;
+    long long g = (budget <= 0 || per_head * BH <= budget) ? BH : budget / per_head;
+    p.head_group = static_cast<int>(g < 1 ? 1 : (g > BH ? BH : g));
+  }
   p.q_off = a.q_off;
   p.kv_off = a.kv_off;
   p.scale = a.scale;

@@ -264,7 +264,7 @@ struct Cfg2 {
   static constexpr uint32_t COL_S0 = 0, COL_S1 = 128;
   static constexpr uint32_t COL_P0 = ALIAS ? 0u : 256u, COL_P1 = ALIAS ? 128u : 320u;
   static constexpr uint32_t COL_O0 = ALIAS ? 256u : 384u, COL_O1 = COL_O0 + D;
-  static constexpr int NBARS = 2 + 3 * STAGES + 2 * 7;
+  static constexpr int NBARS = 1 + 3 * STAGES + 2 * 5 + 2;
   // Every FLUSH key tiles the softmax folds the tensor-memory accumulator into an fp32 running sum, so no
   // tensor-core accumulation chain exceeds FLUSH * 8 (d = 64) or FLUSH * 8 * 2 (bf16 hi/lo) MMAs. (The
   // MMA's fp32 accumulation is biased toward zero: measured relative drift -1.6e-5 after 16K keys, -6.9e-5
@@ -282,122 +282,14 @@ struct Cfg2 {
   static_assert(COL_O1 + D <= TMEM_COLS, "tensor memory layout exceeds 512 columns");
 };
 
-// One work unit: a pair of query tiles of one (batch, head) of one chunk pair, with everything the roles
-// of the CTA need to process it.
-struct Unit {
-  const CUtensorMap* mq;
-  const CUtensorMap* mk;
-  const CUtensorMap* mv;
-  long long q_off, kv_off;
-  float* o_part;
-  float* lse_part;
-  int Nq, Nkv, mode;
-  int b, h, bh, q00, q01, nkv0, nkv1, n_max;
-};
-
-// Position of work unit `unit` (of n_q_tiles query-tile pairs x BH heads) in the head-grouped,
-// heaviest-first order, and the key-tile counts of its two query tiles.
-template <bool CAUSAL>
-__device__ __forceinline__ void locate_unit(const KParams& p, int n_q_tiles, int unit, Unit& u) {
-  // Units of head_group heads at a time (heads interleaved, query-tile pairs heaviest first), so that the
-  // K/V of the heads in flight stay in L2; one group of all heads when they fit.
-  const int gsz = p.head_group;
-  const int per_group = gsz * n_q_tiles;
-  const int g0 = (unit / per_group) * gsz;
-  const int gn = min(gsz, p.BH - g0);
-  const int ur = unit - (unit / per_group) * per_group;
-  const int qp = n_q_tiles - 1 - ur / gn;
-  u.bh = g0 + ur % gn;
-  u.b = u.bh / p.H;
-  u.h = u.bh % p.H;
-  u.q00 = qp * 2 * BM;
-  u.q01 = u.q00 + BM;
-  // Per query tile: number of key tiles (scalars: no runtime-indexed local arrays).
-  auto tile_kv = [&](int qt0) -> int {
-    const int rows = min(BM, u.Nq - qt0);
-    int n = (u.Nkv + BN - 1) / BN;
-    if (rows <= 0) {
-      n = 0;
-    } else if (CAUSAL) {
-      const long long last_key = u.q_off + qt0 + rows - 1 - u.kv_off;
-      n = last_key < 0 ? 0 : (last_key / BN + 1 < n ? static_cast<int>(last_key / BN + 1) : n);
-    }
-    return n;
-  };
-  u.nkv0 = tile_kv(u.q00);
-  u.nkv1 = tile_kv(u.q01);
-  u.n_max = max(u.nkv0, u.nkv1);
-}
-
-// The k-th unit of this CTA (a persistent CTA walks units k * G + c, G CTAs, c its index, in
-// alternating directions round by round, so the heaviest-first order balances across CTAs).
-__device__ __forceinline__ int unit_index(int k, int units) {
-  const int G = static_cast<int>(gridDim.x), c = static_cast<int>(blockIdx.x);
-  const long long idx = static_cast<long long>(k) * G + ((k & 1) ? (G - 1 - c) : c);
-  return idx < units ? static_cast<int>(idx) : -1;
-}
-
-// Units of one chunk pair (the maps and sizes of the launch).
-struct SingleSource {
-  const CUtensorMap* mq;
-  const CUtensorMap* mk;
-  const CUtensorMap* mv;
-  const KParams* p;
-  template <bool CAUSAL>
-  __device__ __forceinline__ bool get(int k, Unit& u) const {
-    const int units = p->n_q_tiles * p->BH;
-    const int idx = unit_index(k, units);
-    if (idx < 0) return false;
-    u.mq = mq;
-    u.mk = mk;
-    u.mv = mv;
-    u.q_off = p->q_off;
-    u.kv_off = p->kv_off;
-    u.o_part = p->o_part;
-    u.lse_part = p->lse_part;
-    u.Nq = p->Nq;
-    u.Nkv = p->Nkv;
-    u.mode = p->mode;
-    locate_unit<CAUSAL>(*p, p->n_q_tiles, idx, u);
-    return true;
-  }
-};
-
-// Units of several chunk pairs: unit index -> the last pair whose first unit is at or before it.
-struct MultiSource {
-  const MultiParams* mp;
-  int units;
-  template <bool CAUSAL>
-  __device__ __forceinline__ bool get(int k, Unit& u) const {
-    const int idx = unit_index(k, units);
-    if (idx < 0) return false;
-    int i = 0;
-    for (int t = 1; t < mp->n_pairs; ++t)
-      if (mp->pair[t].unit_begin <= idx) i = t;
-    const PairDesc& pd = mp->pair[i];
-    u.mq = &pd.q;
-    u.mk = &pd.k;
-    u.mv = &pd.v;
-    u.q_off = pd.q_off;
-    u.kv_off = pd.kv_off;
-    u.o_part = pd.o_part;
-    u.lse_part = pd.lse_part;
-    u.Nq = pd.Nq;
-    u.Nkv = pd.Nkv;
-    u.mode = pd.mode;
-    locate_unit<CAUSAL>(mp->common, pd.n_q_tiles, idx - pd.unit_begin, u);
-    return true;
-  }
-};
-
-// The kernel body: a persistent CTA processes its work units one after another. Every barrier keeps
-// counting across units (each role derives the same phase counts from the same unit sequence), so the
-// producer loads the next unit's Q and K/V tiles and the MMA issuers start its first S while the
-// softmax warps finish the previous unit's epilogue. The tensor maps are kernel parameters
-// (__grid_constant__), addressed in parameter space by TMA.
-template <int D, int DT, bool CAUSAL, int MODE, class Source>
-__device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& src) {
+// The kernel body, for one work unit (a pair of query tiles of one (batch, head)); the tensor maps are
+// kernel parameters (__grid_constant__), passed by reference so that TMA sees their parameter-space
+// addresses.
+template <int D, int DT, bool CAUSAL, int MODE>
+__device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUtensorMap& tmK, const CUtensorMap& tmV,
+                                               const KParams& p, const int unit) {
   using C = Cfg2<D, DT>;
+  const int mode = (MODE == kModeMulti) ? p.mode : MODE;
   constexpr int STAGES = C::STAGES;
   constexpr int KSUB = C::KSUB;
   constexpr bool ALIAS = C::ALIAS;
@@ -417,28 +309,53 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
     sOsum = g_osum + static_cast<size_t>(osum_ok ? smid : 0u) * kOsumSlotFloats;
   }
   uint64_t* bars = reinterpret_cast<uint64_t*>(sV + STAGES * C::KV_BYTES + C::OSUM_BYTES);
-  uint64_t* bar_q = bars;                          // one phase per unit with work (Q loaded)
-  uint64_t* bar_q_free = bar_q + 1;                // both MMA issuers are done with the unit's Q
-  uint64_t* bar_k_full = bar_q_free + 1;
+  uint64_t* bar_q = bars;
+  uint64_t* bar_k_full = bar_q + 1;
   uint64_t* bar_v_full = bar_k_full + STAGES;
   uint64_t* bar_kv_empty = bar_v_full + STAGES;
   uint64_t* bar_s_full = bar_kv_empty + STAGES;  // [2]
   uint64_t* bar_s_free = bar_s_full + 2;         // [2] (P kept apart only)
   uint64_t* bar_p_full = bar_s_free + 2;         // [2]
   uint64_t* bar_pv_done = bar_p_full + 2;        // [2]
-  uint64_t* bar_o_final = bar_pv_done + 2;       // [2] one phase per unit with key tiles
-  uint64_t* bar_o_free = bar_o_final + 2;        // [2] the epilogue has read O
-  uint64_t* bar_mma_idle = bar_o_free + 2;       // [2] one per MMA warp
+  uint64_t* bar_o_final = bar_pv_done + 2;       // [2] single phase each
+  uint64_t* bar_mma_idle = bar_o_final + 2;     // [2] one per MMA warp
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bar_mma_idle + 2);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
   const int warp = threadIdx.x >> 5;
   const int lane = threadIdx.x & 31;
 
+  // Work unit: a pair of query tiles, heaviest (latest) first.
+  // Units of head_group heads at a time (heads interleaved, query-tile pairs heaviest first), so that the
+  // K/V of the heads in flight stay in L2; one group of all heads when they fit.
+  const int gsz = p.head_group;
+  const int per_group = gsz * p.n_q_tiles;
+  const int g0 = (unit / per_group) * gsz;
+  const int gn = min(gsz, p.BH - g0);
+  const int ur = unit - (unit / per_group) * per_group;
+  const int qp = p.n_q_tiles - 1 - ur / gn;
+  const int bh = g0 + ur % gn;
+  const int b = bh / p.H;
+  const int h = bh % p.H;
+  // Per query tile: first row and number of key tiles (scalars: no runtime-indexed local arrays).
+  auto tile_kv = [&](int qt0) -> int {
+    const int rows = min(BM, p.Nq - qt0);
+    int n = (p.Nkv + BN - 1) / BN;
+    if (rows <= 0) {
+      n = 0;
+    } else if (CAUSAL) {
+      const long long last_key = p.q_off + qt0 + rows - 1 - p.kv_off;
+      n = last_key < 0 ? 0 : (last_key / BN + 1 < n ? static_cast<int>(last_key / BN + 1) : n);
+    }
+    return n;
+  };
+  const int q00 = qp * 2 * BM, q01 = q00 + BM;
+  const int nkv0 = tile_kv(q00), nkv1 = tile_kv(q01);
+  const int n_max = max(nkv0, nkv1);
+
   if (threadIdx.x == 0) {
     if (!osum_ok) record_error(kDevSmSlot, 30);  // results stay exact; only the fold is skipped
     mbar_init(bar_q, 1);
-    mbar_init(bar_q_free, 2);  // one arrival per MMA warp
     for (int s = 0; s < STAGES; ++s) {
       mbar_init(&bar_k_full[s], 1);
       mbar_init(&bar_v_full[s], 1);
@@ -450,7 +367,6 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
       mbar_init(&bar_p_full[t], 128);
       mbar_init(&bar_pv_done[t], 1);
       mbar_init(&bar_o_final[t], 1);
-      mbar_init(&bar_o_free[t], 128);
       mbar_init(&bar_mma_idle[t], 1);
     }
     *abort_flag = 0;
@@ -460,6 +376,11 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
     __syncwarp();
     tmem_alloc(tmem_slot, TMEM_COLS);
     tmem_relinquish();
+  }
+  if (warp == 0 && lane == 0) {
+    prefetch_tensormap(&tmQ);
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
   }
   tc_fence_before();
   __syncthreads();
@@ -474,66 +395,46 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
     asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(REGS_LOW));
   if (warp == 0) {
     // ------------------------------------------------------------------ TMA producer
-    if (lane == 0) {
-      long long gj = 0;       // K/V tiles issued so far (stage and phase of the ring)
-      int kq = 0;             // Q loads issued so far
-      int skipped = -1;       // fault injection: the key/value tile never loaded (global index)
-      bool ok = true;
-      const CUtensorMap* last_map = nullptr;
-      Unit u;
-      for (int k = 0; ok && src.template get<CAUSAL>(k, u); ++k) {
-        if (u.n_max == 0) continue;
-        if (u.mq != last_map) {
-          prefetch_tensormap(u.mq);
-          prefetch_tensormap(u.mk);
-          prefetch_tensormap(u.mv);
-          last_map = u.mq;
+    if (lane == 0 && n_max > 0) {
+      mbar_arrive_expect_tx(bar_q, 2 * C::QT_BYTES);
+#pragma unroll
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sQ + t * C::QT_BYTES + s * TILE_BYTES, &tmQ, bar_q, s * 64, t ? q01 : q00, h, b);
+      int issued = 0;
+      int skipped = -1;  // fault injection: the key/value tile never loaded
+      for (int j = 0; j < n_max; ++j) {
+        const int stage = j % STAGES;
+        const uint32_t round = j / STAGES;
+        if (!wait_or_abort_a(smem_u32(&bar_kv_empty[stage]), (round & 1u) ^ 1u, tmo_us, a_abort, kDevTimeoutKV, 10)) break;
+        if (p.fault == 1 && blockIdx.x == 0 && j == 1) {
+          skipped = j;
+          issued = j + 1;
+          continue;
         }
-        // Q of the previous unit is free once every MMA that read it has completed.
-        if (kq > 0 &&
-            !wait_or_abort_a(smem_u32(bar_q_free), static_cast<uint32_t>(kq - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 26)) {
-          ok = false;
-          break;
-        }
-        mbar_arrive_expect_tx(bar_q, 2 * C::QT_BYTES);
+        mbar_arrive_expect_tx(&bar_k_full[stage], C::KV_BYTES);
 #pragma unroll
-        for (int t = 0; t < 2; ++t)
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sK + stage * C::KV_BYTES + s * TILE_BYTES, &tmK, &bar_k_full[stage], s * 64, j * BN, h, b);
+        mbar_arrive_expect_tx(&bar_v_full[stage], C::KV_BYTES);
 #pragma unroll
-          for (int s = 0; s < KSUB; ++s)
-            tma_load_4d(sQ + t * C::QT_BYTES + s * TILE_BYTES, u.mq, bar_q, s * 64, t ? u.q01 : u.q00, u.h, u.b);
-        ++kq;
-        for (int j = 0; j < u.n_max; ++j, ++gj) {
-          const int stage = static_cast<int>(gj % STAGES);
-          const uint32_t round = static_cast<uint32_t>(gj / STAGES);
-          if (!wait_or_abort_a(smem_u32(&bar_kv_empty[stage]), (round & 1u) ^ 1u, tmo_us, a_abort, kDevTimeoutKV, 10)) {
-            ok = false;
-            break;
-          }
-          if (p.fault == 1 && blockIdx.x == 0 && gj == 1) {
-            skipped = 1;
-            continue;
-          }
-          mbar_arrive_expect_tx(&bar_k_full[stage], C::KV_BYTES);
-#pragma unroll
-          for (int s = 0; s < KSUB; ++s)
-            tma_load_4d(sK + stage * C::KV_BYTES + s * TILE_BYTES, u.mk, &bar_k_full[stage], s * 64, j * BN, u.h, u.b);
-          mbar_arrive_expect_tx(&bar_v_full[stage], C::KV_BYTES);
-#pragma unroll
-          for (int s = 0; s < KSUB; ++s)
-            tma_load_4d(sV + stage * C::KV_BYTES + s * TILE_BYTES, u.mv, &bar_v_full[stage], s * 64, j * BN, u.h, u.b);
-        }
+        for (int s = 0; s < KSUB; ++s)
+          tma_load_4d(sV + stage * C::KV_BYTES + s * TILE_BYTES, &tmV, &bar_v_full[stage], s * 64, j * BN, h, b);
+        issued = j + 1;
       }
-      // Every load issued must land before the CTA exits (bounded waits, no abort check); on the
-      // normal path these phases are already complete. (gj counts a tile whose wait gave up only when
-      // its load was issued: the loop breaks before the increment.)
-      for (long long g = (gj > STAGES ? gj - STAGES : 0); g < gj; ++g) {
-        if (g == skipped) continue;
-        const int stage = static_cast<int>(g % STAGES);
-        const uint32_t par = static_cast<uint32_t>(g / STAGES) & 1u;
-        mbar_wait_bounded(&bar_k_full[stage], par, tmo);
-        mbar_wait_bounded(&bar_v_full[stage], par, tmo);
+      {
+        // Every load issued must land before the CTA exits (bounded waits, no abort check); on the
+        // normal path these phases are already complete.
+        for (int j = max(0, issued - STAGES); j < issued; ++j) {
+          if (j == skipped) continue;
+          const int stage = j % STAGES;
+          const uint32_t par = (j / STAGES) & 1u;
+          mbar_wait_bounded(&bar_k_full[stage], par, tmo);
+          mbar_wait_bounded(&bar_v_full[stage], par, tmo);
+        }
+        mbar_wait_bounded(bar_q, 0, tmo);
       }
-      if (kq > 0) mbar_wait_bounded(bar_q, static_cast<uint32_t>(kq - 1) & 1u, tmo);
     }
   } else if (warp == 1 || warp == 2) {
     // ------------------------------------------------------------------ MMA issuers
@@ -542,93 +443,73 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
     // converged (warp-uniform values); one elected lane issues each MMA group and commit.
     const int t = warp - 1;
     const bool leader = elect_one();
-    constexpr uint32_t IDESC_S = idesc_f16(DT, 0, 128, 128);
-    constexpr uint32_t IDESC_O = idesc_f16(DT, 1, 128, D);  // N = d: one MMA covers every feature
-    // Shared-memory descriptors are built once; each MMA adds a compile-time offset (16-byte units)
-    // to the start-address field, which cannot carry out of its 14 bits below 256 KiB. V is MN-major:
-    // 8 keys x 64 features per 1024-byte atom (SBO = 1024 along keys); the second 64-feature box of
-    // d = 128 starts TILE_BYTES further (LBO).
-    const uint64_t dQ = smem_desc_sw128(smem_u32(sQ + t * C::QT_BYTES), 16, 1024);
-    const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
-    const uint64_t dV = smem_desc_sw128(smem_u32(sV), D == 128 ? TILE_BYTES : 1024, 1024);
-    const uint32_t col_s = tmem + (t ? C::COL_S1 : C::COL_S0);
-    const uint32_t col_p = tmem + (t ? C::COL_P1 : C::COL_P0);
-    const uint32_t col_o = tmem + (t ? C::COL_O1 : C::COL_O0);
-    auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
-      const bool w = wait_or_abort_a(smem_u32(bar), parity, tmo_us, a_abort, code, where);
-      return __all_sync(0xffffffffu, w);
-    };
-    // S of global tile jt (of this query tile) from K/V tile gs of the ring
-    auto do_s = [&](long long gs) {
-      const uint64_t b0 = dK + static_cast<uint32_t>(gs % STAGES) * (C::KV_BYTES >> 4);
-      tc_fence_after();
-      if (leader) {
-        issue_qk<D>(col_s, dQ, b0, IDESC_S);
-        tc_commit(&bar_s_full[t]);
-      }
-      __syncwarp();
-    };
-    // PV of the unit's key tile j (K/V tile gs of the ring); the last one also completes o_final and q_free
-    auto do_pv = [&](int j, long long gs, int nkv) {
-      const uint64_t v0 = dV + static_cast<uint32_t>(gs % STAGES) * (C::KV_BYTES >> 4);
-      // O restarts at every segment start of the softmax loop (key tiles 0, FLUSH, 2 FLUSH, ...)
-      const bool first = (j == 0) || (C::FLUSH > 0 && osum_ok && j % (C::FLUSH > 0 ? C::FLUSH : 1) == 0);
-      const bool last = (j == nkv - 1);
-      tc_fence_after();
-      if (leader) {
-        if (first) issue_pv<D, DT, true>(col_o, col_p, v0, IDESC_O);
-        else issue_pv<D, DT, false>(col_o, col_p, v0, IDESC_O);
-        tc_commit(&bar_pv_done[t]);
-        if (last) {
-          tc_commit(&bar_o_final[t]);
-          tc_commit(bar_q_free);  // every MMA reading this unit's Q (its S MMAs) precedes this commit
+    const int nkv = t ? nkv1 : nkv0;
+    if (n_max > 0) {
+      constexpr uint32_t IDESC_S = idesc_f16(DT, 0, 128, 128);
+      constexpr uint32_t IDESC_O = idesc_f16(DT, 1, 128, D);  // N = d: one MMA covers every feature
+      // Shared-memory descriptors are built once; each MMA adds a compile-time offset (16-byte units)
+      // to the start-address field, which cannot carry out of its 14 bits below 256 KiB. V is MN-major:
+      // 8 keys x 64 features per 1024-byte atom (SBO = 1024 along keys); the second 64-feature box of
+      // d = 128 starts TILE_BYTES further (LBO).
+      const uint64_t dQ = smem_desc_sw128(smem_u32(sQ + t * C::QT_BYTES), 16, 1024);
+      const uint64_t dK = smem_desc_sw128(smem_u32(sK), 16, 1024);
+      const uint64_t dV = smem_desc_sw128(smem_u32(sV), D == 128 ? TILE_BYTES : 1024, 1024);
+      const uint32_t col_s = tmem + (t ? C::COL_S1 : C::COL_S0);
+      const uint32_t col_p = tmem + (t ? C::COL_P1 : C::COL_P0);
+      const uint32_t col_o = tmem + (t ? C::COL_O1 : C::COL_O0);
+      auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
+        const bool w = wait_or_abort_a(smem_u32(bar), parity, tmo_us, a_abort, code, where);
+        return __all_sync(0xffffffffu, w);
+      };
+      auto do_s = [&](int j) {
+        const uint64_t b0 = dK + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
+        tc_fence_after();
+        if (leader) {
+          issue_qk<D>(col_s, dQ, b0, IDESC_S);
+          tc_commit(&bar_s_full[t]);
         }
-      }
-      __syncwarp();
-    };
-    long long gj = 0;  // K/V tiles of the ring consumed so far (the producer's count)
-    long long jt = 0;  // S / P / PV phases of this query tile so far
-    int kq = 0;        // units with a Q load so far
-    int ko = 0;        // units whose O this tile produced (o_final / o_free phases)
-    bool ok = true;
-    Unit u;
-    for (int k = 0; ok && src.template get<CAUSAL>(k, u); ++k) {
-      if (u.n_max == 0) continue;
-      const int nkv = t ? u.nkv1 : u.nkv0;
-      ok = wait_all(bar_q, static_cast<uint32_t>(kq) & 1u, kDevTimeoutQ, 11);
+        __syncwarp();
+      };
+      auto do_pv = [&](int j) {
+        const uint64_t v0 = dV + static_cast<uint32_t>(j % STAGES) * (C::KV_BYTES >> 4);
+        // O restarts at every segment start of the softmax loop (key tiles 0, FLUSH, 2 FLUSH, ...)
+        const bool first = (j == 0) || (C::FLUSH > 0 && osum_ok && j % (C::FLUSH > 0 ? C::FLUSH : 1) == 0);
+        const bool last = (j == nkv - 1);
+        tc_fence_after();
+        if (leader) {
+          if (first) issue_pv<D, DT, true>(col_o, col_p, v0, IDESC_O);
+          else issue_pv<D, DT, false>(col_o, col_p, v0, IDESC_O);
+          tc_commit(&bar_pv_done[t]);
+          if (last) tc_commit(&bar_o_final[t]);
+        }
+        __syncwarp();
+      };
+      bool ok = wait_all(bar_q, 0, kDevTimeoutQ, 11);
       if (ok && nkv > 0) {
-        ok = wait_all(&bar_k_full[gj % STAGES], static_cast<uint32_t>(gj / STAGES) & 1u, kDevTimeoutKV, 12);
-        // P kept apart: S of this tile's previous phase must have been read (ALIAS: ordered behind PV)
-        if (ok && !ALIAS && jt > 0) ok = wait_all(&bar_s_free[t], static_cast<uint32_t>(jt - 1) & 1u, kDevTimeoutSoftmax, 14);
-        if (ok) do_s(gj);
+        ok = wait_all(&bar_k_full[0], 0, kDevTimeoutKV, 12);
+        if (ok) do_s(0);
       }
-      for (int j = 0; ok && j < u.n_max; ++j) {
-        const long long g = gj + j;
-        const int stage = static_cast<int>(g % STAGES);
-        const uint32_t gpar = static_cast<uint32_t>(g / STAGES) & 1u;
+      for (int j = 0; ok && j < n_max; ++j) {
+        const int stage = j % STAGES;
         if (j < nkv) {
-          const uint32_t tpar = static_cast<uint32_t>(jt + j) & 1u;
           if (!ALIAS) {
             if (j + 1 < nkv) {
-              ok = wait_all(&bar_k_full[(g + 1) % STAGES], static_cast<uint32_t>((g + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
-              if (ok) ok = wait_all(&bar_s_free[t], tpar, kDevTimeoutSoftmax, 14);
-              if (ok) do_s(g + 1);
+              ok = wait_all(&bar_k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
+              if (ok) ok = wait_all(&bar_s_free[t], j & 1u, kDevTimeoutSoftmax, 14);
+              if (ok) do_s(j + 1);
             }
-            if (ok) ok = wait_all(&bar_v_full[stage], gpar, kDevTimeoutKV, 15);
-            if (ok) ok = wait_all(&bar_p_full[t], tpar, kDevTimeoutSoftmax, 16);
-            // the first PV of a unit overwrites O: the previous unit's epilogue must have read it
-            if (ok && j == 0 && ko > 0) ok = wait_all(&bar_o_free[t], static_cast<uint32_t>(ko - 1) & 1u, kDevTimeoutSoftmax, 27);
-            if (ok) do_pv(j, g, nkv);
+            if (ok) ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 15);
+            if (ok) ok = wait_all(&bar_p_full[t], j & 1u, kDevTimeoutSoftmax, 16);
+            if (ok) do_pv(j);
           } else {
-            ok = wait_all(&bar_v_full[stage], gpar, kDevTimeoutKV, 15);
-            if (ok) ok = wait_all(&bar_p_full[t], tpar, kDevTimeoutSoftmax, 16);
-            if (ok && j == 0 && ko > 0) ok = wait_all(&bar_o_free[t], static_cast<uint32_t>(ko - 1) & 1u, kDevTimeoutSoftmax, 27);
-            if (ok) do_pv(j, g, nkv);
+            ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 15);
+            if (ok) ok = wait_all(&bar_p_full[t], j & 1u, kDevTimeoutSoftmax, 16);
+            if (ok) do_pv(j);
             if (ok && j + 1 < nkv) {
-              ok = wait_all(&bar_k_full[(g + 1) % STAGES], static_cast<uint32_t>((g + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
+              ok = wait_all(&bar_k_full[(j + 1) % STAGES], ((j + 1) / STAGES) & 1u, kDevTimeoutKV, 13);
               // P_t(j) lives in S_t's columns: S_t(j+1) is issued by this thread after PV_t(j), and MMAs
               // of one issuing thread run in issue order, so PV_t(j) reads P_t(j) before it is overwritten.
-              if (ok) do_s(g + 1);
+              if (ok) do_s(j + 1);
             }
           }
           // This tile's use of the K/V stage ends when its MMAs complete.
@@ -638,24 +519,17 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
           // count toward this load's phase only; waiting for the load first keeps this warp from
           // arriving a phase early (with fewer stages than key tiles it would otherwise free a stage
           // the other warp is still reading).
-          ok = wait_all(&bar_k_full[stage], gpar, kDevTimeoutKV, 21);
-          if (ok) ok = wait_all(&bar_v_full[stage], gpar, kDevTimeoutKV, 22);
+          ok = wait_all(&bar_k_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 21);
+          if (ok) ok = wait_all(&bar_v_full[stage], (j / STAGES) & 1u, kDevTimeoutKV, 22);
           if (ok && leader) mbar_arrive(&bar_kv_empty[stage]);
         }
         __syncwarp();
       }
-      // a query tile without key tiles issues no MMA on this unit's Q: it releases Q at once
-      if (ok && nkv == 0 && leader) mbar_arrive(bar_q_free);
+      // Every MMA of this warp must be complete before tensor memory is released.
+      if (leader) tc_commit(&bar_mma_idle[t]);
       __syncwarp();
-      gj += u.n_max;
-      jt += nkv;
-      ++kq;
-      if (nkv > 0) ++ko;
+      mbar_wait_bounded(&bar_mma_idle[t], 0, tmo);
     }
-    // Every MMA of this warp must be complete before tensor memory is released.
-    if (leader) tc_commit(&bar_mma_idle[t]);
-    __syncwarp();
-    mbar_wait_bounded(&bar_mma_idle[t], 0, tmo);
   }
     // ------------------------------------------------------------------ teardown (warpgroup 0)
     tc_fence_before();
@@ -675,297 +549,278 @@ __device__ __forceinline__ void attn_fwd2_body(const KParams& p, const Source& s
     const uint32_t colS = wg ? C::COL_S1 : C::COL_S0;
     const uint32_t colP = wg ? C::COL_P1 : C::COL_P0;
     const uint32_t colO = wg ? C::COL_O1 : C::COL_O0;
+    const int qt0 = wg ? q01 : q00;
     const uint32_t a_s_full = smem_u32(&bar_s_full[wg]), a_s_free = smem_u32(&bar_s_free[wg]);
     const uint32_t a_p_full = smem_u32(&bar_p_full[wg]), a_pv_done = smem_u32(&bar_pv_done[wg]);
-    const uint32_t a_o_final = smem_u32(&bar_o_final[wg]), a_o_free = smem_u32(&bar_o_free[wg]);
+    const int nkv = wg ? nkv1 : nkv0;
+    const int qi = qt0 + r;
+    // Masks in key positions relative to the key block (|positions| < 2^31): the query tile starts at
+    // key position rel, this thread's row at rel + r; keys at or past p.Nkv are outside the block.
+    const int rel = static_cast<int>(p.q_off + qt0 - p.kv_off);
     const float sl2 = p.scale_log2;
-    const int SEG = (C::FLUSH > 0 && osum_ok) ? C::FLUSH : (1 << 30);
-    long long jt = 0;  // S / P / PV phases of this query tile so far
-    int ko = 0;        // units whose O this tile produced
+    float m_ref = -INFINITY;
+    float l = 0.0f;
+    float m_sum = -INFINITY;  // reference max of O_sum (the m_ref of its last fold); O_sum holds
+                              // values scaled by 2^-m_sum and is only brought to m_ref when read
     bool ok = true;
-    Unit u;
-    for (int k = 0; ok && src.template get<CAUSAL>(k, u); ++k) {
-      const int nkv = wg ? u.nkv1 : u.nkv0;
-      // Masks in key positions relative to the key block (|positions| < 2^31): the query tile starts at
-      // key position rel, this thread's row at rel + r; keys at or past nkv_tok are outside the block.
-      const int nkv_tok = u.Nkv;
-      const int rel = static_cast<int>(u.q_off + (wg ? u.q01 : u.q00) - u.kv_off);
-      float m_ref = -INFINITY;
-      float l = 0.0f;
-      float m_sum = -INFINITY;  // reference max of O_sum (the m_ref of its last fold); O_sum holds
-                                // values scaled by 2^-m_sum and is only brought to m_ref when read
 
-      // Key tiles in segments of FLUSH (one segment when FLUSH = 0). Between segments, once PV_t of the
-      // segment's last tile is complete, O is folded into the fp32 running sum O_sum (RNE adds) and
-      // the next segment's first PV_t restarts O; O is in the current reference max, O_sum is brought
-      // from m_sum to it by an exact power of two. Keeping the fold out of the per-tile loop keeps that
-      // loop's code identical to the unsegmented one.
-      for (int j0 = 0; ok && j0 < nkv; j0 += SEG) {
-        if (j0 > 0) {
-          ok = wait_or_abort_a(a_pv_done, static_cast<uint32_t>(jt + j0 - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 23);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const bool have = j0 > C::FLUSH;
-          const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
-          if (C::OSUM_SMEM) {
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(trow + colO + c * 32, o);
-              tmem_wait_ld();
-              reg_fence32(o);
-              const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) {
-                const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
-                const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
-                st_shared_f32(a, prev + __uint_as_float(o[e]));
-              }
-            }
-          } else {
-            // this thread's own row of the SM's slot, written before it is read and by this thread only:
-            // every earlier value is loaded first (one round trip to L2), then O is added and stored back
-            float* og = sOsum + (wg * D) * 128 + r;
-            float prev[D];
-#pragma unroll
-            for (int e = 0; e < D; ++e) prev[e] = have ? __ldcg(og + e * 128) : 0.0f;
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(trow + colO + c * 32, o);
-              tmem_wait_ld();
-              reg_fence32(o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e)
-                __stcg(og + (c * 32 + e) * 128, prev[c * 32 + e] * sc + __uint_as_float(o[e]));
-            }
-          }
-          m_sum = m_ref;
+    // Key tiles in segments of FLUSH (one segment when FLUSH = 0). Between segments, once PV_t of the
+    // segment's last tile is complete, O is folded into the fp32 running sum O_sum (RNE adds) and
+    // the next segment's first PV_t restarts O; O is in the current reference max, O_sum is brought
+    // from m_sum to it by an exact power of two. Keeping the fold out of the per-tile loop keeps that
+    // loop's code identical to the unsegmented one.
+    const int SEG = (C::FLUSH > 0 && osum_ok) ? C::FLUSH : (1 << 30);
+    for (int j0 = 0; ok && j0 < nkv; j0 += SEG) {
+      if (j0 > 0) {
+        const int j = j0;
+        ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 23);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
         }
-        const int j1 = (nkv - j0 < SEG) ? nkv : j0 + SEG;
-        for (int j = j0; j < j1; ++j) {
-          const long long jg = jt + j;  // this tile's global phase
-          ok = wait_or_abort_a(a_s_full, static_cast<uint32_t>(jg) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
-          if (!__all_sync(0xffffffffu, ok)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          uint32_t sr[128];
+        tc_fence_after();
+        const bool have = j > C::FLUSH;
+        const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
+        if (C::OSUM_SMEM) {
 #pragma unroll
-          for (int c = 0; c < 4; ++c) tmem_ld32(trow + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-          tmem_wait_ld();
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+            const uint32_t os = smem_u32(sOsum) + static_cast<uint32_t>(((wg * D) * 128 + r) * 4);
 #pragma unroll
-          for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
-          if (!ALIAS) {
-            tc_fence_before();
-            mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+            for (int e = 0; e < 32; ++e) {
+              const uint32_t a = os + static_cast<uint32_t>((c * 32 + e) * 128 * 4);
+              const float prev = have ? ld_shared_f32(a) * sc : 0.0f;
+              st_shared_f32(a, prev + __uint_as_float(o[e]));
+            }
           }
+        } else {
+          // this thread's own row of the SM's slot, written before it is read and by this thread only:
+          // every earlier value is loaded first (one round trip to L2), then O is added and stored back
+          float* og = sOsum + (wg * D) * 128 + r;
+          float prev[D];
+#pragma unroll
+          for (int e = 0; e < D; ++e) prev[e] = have ? __ldcg(og + e * 128) : 0.0f;
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) __stcg(og + (c * 32 + e) * 128, prev[c * 32 + e] * sc + __uint_as_float(o[e]));
+          }
+        }
+        m_sum = m_ref;
+      }
+      const int j1 = (nkv - j0 < SEG) ? nkv : j0 + SEG;
+      for (int j = j0; j < j1; ++j) {
+        ok = wait_or_abort_a(a_s_full, j & 1u, tmo_us, a_abort, kDevTimeoutMMA, 18);
+        if (!__all_sync(0xffffffffu, ok)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        uint32_t sr[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c) tmem_ld32(trow + colS + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        tmem_wait_ld();
+#pragma unroll
+        for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
+        if (!ALIAS) {
+          tc_fence_before();
+          mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+        }
 
-          float x[128];
+        float x[128];
 #pragma unroll
-          for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
-          const int k0 = j * BN;
-          const bool tail = (k0 + BN > nkv_tok);
-          const bool diag = CAUSAL && (k0 + BN - 1 > rel);
-          if (tail || diag) {
-            int lim = nkv_tok - k0;
-            if (CAUSAL) {
-              const int lc = rel + r - k0 + 1;
-              lim = lc < lim ? lc : lim;
-            }
-#pragma unroll
-            for (int c = 0; c < 128; ++c)
-              if (c >= lim) x[c] = -INFINITY;
+        for (int c = 0; c < 128; ++c) x[c] = __uint_as_float(sr[c]);
+        const int k0 = j * BN;
+        const bool tail = (k0 + BN > p.Nkv);
+        const bool diag = CAUSAL && (k0 + BN - 1 > rel);
+        if (tail || diag) {
+          int lim = p.Nkv - k0;
+          if (CAUSAL) {
+            const int lc = rel + r - k0 + 1;
+            lim = lc < lim ? lc : lim;
           }
-          const float tmax = row_max128(x) * sl2;
-          float alpha = 1.0f;
-          bool rescale = false;
-          if (tmax > m_ref + TAU) {
-            const float m_new = ceilf(tmax);
-            if (m_ref != -INFINITY) {
-              alpha = exp2_int(m_ref - m_new);
-              rescale = true;
-            }
-            m_ref = m_new;
-          }
-          const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
-          const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
-          float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
-          const uint32_t pbuf = trow + colP;
-          if (!ALIAS) {
-            // fp16, P kept apart and single-buffered: compute all of P in registers first, then wait for
-            // PV_t of the previous phase to have read the previous P (parity wait on that phase is exact:
-            // S of this phase was issued after PV of the phase before it, and PV of this phase waits for
-            // this thread's p_full arrival), then store it.
-            uint32_t pk[64];
 #pragma unroll
-            for (int c = 0; c < 64; ++c) {
+          for (int c = 0; c < 128; ++c)
+            if (c >= lim) x[c] = -INFINITY;
+        }
+        const float tmax = row_max128(x) * sl2;
+        float alpha = 1.0f;
+        bool rescale = false;
+        if (tmax > m_ref + TAU) {
+          const float m_new = ceilf(tmax);
+          if (m_ref != -INFINITY) {
+            alpha = exp2_int(m_ref - m_new);
+            rescale = true;
+          }
+          m_ref = m_new;
+        }
+        const float cm = 192.0f + ((m_ref == -INFINITY) ? 0.0f : m_ref);
+        const float2 sl2v = make_float2(sl2, sl2), ncm = make_float2(-cm, -cm);
+        float2 rs2[2] = {make_float2(0.0f, 0.0f), make_float2(0.0f, 0.0f)};
+        const uint32_t pbuf = trow + colP;
+        if (!ALIAS) {
+          // fp16, P kept apart and single-buffered: compute all of P in registers first, then wait for
+          // PV_t(j-1) to have read the previous P (parity wait on phase j-1 is exact: S_t(j) was issued
+          // after PV_t(j-2), and PV_t(j) waits for this thread's p_full arrival), then store it.
+          uint32_t pk[64];
+#pragma unroll
+          for (int c = 0; c < 64; ++c) {
+            const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
+            rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
+            pk[c] = pack2(pp.x, pp.y, 0);
+          }
+          if (j > 0) {
+            ok = wait_or_abort_a(a_pv_done, (j - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
+            if (!__all_sync(0xffffffffu, ok)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+          }
+          tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
+          tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
+        } else {
+          // P over S: S_t(j) is complete, and its commit covers every earlier MMA of the issuing
+          // thread, PV_t(j-1) included, so P_t(j-1) has been read and O_t is settled.
+#pragma unroll
+          for (int c4 = 0; c4 < 4; ++c4) {
+            uint32_t hi[16], lo[16];
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int c = c4 * 16 + e;
               const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
               rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
-              pk[c] = pack2(pp.x, pp.y, 0);
-            }
-            if (jg > 0) {
-              ok = wait_or_abort_a(a_pv_done, static_cast<uint32_t>(jg - 1) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 19);
-              if (!__all_sync(0xffffffffu, ok)) {
-                ok = false;
-                break;
+              if (DT) {
+                __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
+                const float2 hf = __bfloat1622float2(h2);
+                __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
+                hi[e] = *reinterpret_cast<uint32_t*>(&h2);
+                lo[e] = *reinterpret_cast<uint32_t*>(&l2);
+              } else {
+                hi[e] = pack2(pp.x, pp.y, 0);
               }
-              tc_fence_after();
             }
-            tmem_st32(pbuf, *reinterpret_cast<const uint32_t(*)[32]>(&pk[0]));
-            tmem_st32(pbuf + 32, *reinterpret_cast<const uint32_t(*)[32]>(&pk[32]));
-          } else {
-            // P over S: S_t of this phase is complete, and its commit covers every earlier MMA of the
-            // issuing thread, the previous PV_t included, so the previous P has been read and O_t is settled.
-#pragma unroll
-            for (int c4 = 0; c4 < 4; ++c4) {
-              uint32_t hi[16], lo[16];
-#pragma unroll
-              for (int e = 0; e < 16; ++e) {
-                const int c = c4 * 16 + e;
-                const float2 pp = exp_pair(x[2 * c], x[2 * c + 1], sl2v, ncm);
-                rs2[c & 1] = __fadd2_rn(rs2[c & 1], pp);
-                if (DT) {
-                  __nv_bfloat162 h2 = __floats2bfloat162_rn(pp.x, pp.y);
-                  const float2 hf = __bfloat1622float2(h2);
-                  __nv_bfloat162 l2 = __floats2bfloat162_rn(pp.x - hf.x, pp.y - hf.y);
-                  hi[e] = *reinterpret_cast<uint32_t*>(&h2);
-                  lo[e] = *reinterpret_cast<uint32_t*>(&l2);
-                } else {
-                  hi[e] = pack2(pp.x, pp.y, 0);
-                }
-              }
-              tmem_st16(pbuf + c4 * 16, hi);
-              if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
-            }
+            tmem_st16(pbuf + c4 * 16, hi);
+            if (DT) tmem_st16(pbuf + 64 + c4 * 16, lo);
           }
-          l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
-          // The previous PV_t is complete here (waited for above, or implied by S_t when P is over S).
-          if (__any_sync(0xffffffffu, rescale) && j > 0) {
-            // O takes the new reference max (O_sum keeps its own, m_sum).
-#pragma unroll
-            for (int c = 0; c < D / 32; ++c) {
-              uint32_t o[32];
-              tmem_ld32(trow + colO + c * 32, o);
-              tmem_wait_ld();
-              reg_fence32(o);
-#pragma unroll
-              for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-              tmem_st32(trow + colO + c * 32, o);
-            }
-          }
-          tmem_wait_st();
-          tc_fence_before();
-          mbar_arrive_a(a_p_full);
         }
+        l = l * alpha + ((rs2[0].x + rs2[1].x) + (rs2[0].y + rs2[1].y));
+        // PV_t(j-1) is complete here (waited for above, or implied by S_t(j) when P is over S).
+        if (__any_sync(0xffffffffu, rescale) && j > 0) {
+          // O takes the new reference max (O_sum keeps its own, m_sum).
+#pragma unroll
+          for (int c = 0; c < D / 32; ++c) {
+            uint32_t o[32];
+            tmem_ld32(trow + colO + c * 32, o);
+            tmem_wait_ld();
+            reg_fence32(o);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(trow + colO + c * 32, o);
+          }
+        }
+        tmem_wait_st();
+        tc_fence_before();
+        mbar_arrive_a(a_p_full);
       }
+    }
 
-      // ---------------------------------------------------------------- epilogue of the unit
-      // The unit's addresses are fetched again here, so nothing of them stays live through the tile loop.
-      src.template get<CAUSAL>(k, u);
-      const int mode = (MODE == kModeMulti) ? u.mode : MODE;
-      const int qi = (wg ? u.q01 : u.q00) + r;
-      const bool have_o = ok && nkv > 0;
-      if (have_o) {
-        ok = wait_or_abort_a(a_o_final, static_cast<uint32_t>(ko) & 1u, tmo_us, a_abort, kDevTimeoutMMA, 20);
-        ok = __all_sync(0xffffffffu, ok);
-        tc_fence_after();
-      }
-      const bool has = (nkv > 0) && (l > 0.0f);
-      const float inv_l = has ? 1.0f / l : 0.0f;
-      const float lse_v = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
-      const bool store = ok && qi < u.Nq;
-      const long long row = out_row_index(p.out_layout, u.b, u.h, p.H, u.Nq, qi);
-      const long long lrow = static_cast<long long>(u.bh) * u.Nq + qi;
-      bool write = store;
-      bool fresh = true;
-      float wa = 0.0f, wn = 1.0f, lse_out = lse_v;
-      if (mode == kModeAccum && store) {
-        if (!has) {
-          write = false;
-        } else {
-          const float la = u.lse_part[lrow];
-          if (la != -INFINITY) {
-            fresh = false;
-            const float M = fmaxf(la, lse_v);
-            const float L = M + logf(expf(la - M) + expf(lse_v - M));
-            wa = expf(la - L);
-            wn = expf(lse_v - L);
-            lse_out = L;
-          }
+    // ---------------------------------------------------------------- epilogue
+    if (ok && nkv > 0) {
+      ok = wait_or_abort_a(smem_u32(&bar_o_final[wg]), 0, tmo_us, a_abort, kDevTimeoutMMA, 20);
+      ok = __all_sync(0xffffffffu, ok);
+      tc_fence_after();
+    }
+    const bool has = (nkv > 0) && (l > 0.0f);
+    const float inv_l = has ? 1.0f / l : 0.0f;
+    const float lse_v = has ? (m_ref + log2f(l)) * 0.69314718055994531f : -INFINITY;
+    const bool store = ok && qi < p.Nq;
+    const long long row = out_row_index(p.out_layout, b, h, p.H, p.Nq, qi);
+    const long long lrow = static_cast<long long>(bh) * p.Nq + qi;
+    bool write = store;
+    bool fresh = true;
+    float wa = 0.0f, wn = 1.0f, lse_out = lse_v;
+    if (mode == kModeAccum && store) {
+      if (!has) {
+        write = false;
+      } else {
+        const float la = p.lse_part[lrow];
+        if (la != -INFINITY) {
+          fresh = false;
+          const float M = fmaxf(la, lse_v);
+          const float L = M + logf(expf(la - M) + expf(lse_v - M));
+          wa = expf(la - L);
+          wn = expf(lse_v - L);
+          lse_out = L;
         }
       }
+    }
 #pragma unroll
-      for (int c = 0; c < D / 32; ++c) {
-        uint32_t o[32];
-        if (have_o && ok) {
-          tmem_ld32(trow + colO + c * 32, o);
-          tmem_wait_ld();
-          reg_fence32(o);
-          if (c == D / 32 - 1) {
-            // O has been read: the next unit's first PV may overwrite it
-            tc_fence_before();
-            mbar_arrive_a(a_o_free);
-          }
-        } else {
+    for (int c = 0; c < D / 32; ++c) {
+      uint32_t o[32];
+      if (ok && nkv > 0) {
+        tmem_ld32(trow + colO + c * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) o[e] = 0u;
-        }
-        float v[32];
-        if (C::FLUSH > 0 && osum_ok && nkv > C::FLUSH) {
-          const float* os = sOsum + (wg * D + c * 32) * 128 + r;
-          const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
-          float prev[32];
+        for (int e = 0; e < 32; ++e) o[e] = 0u;
+      }
+      float v[32];
+      if (C::FLUSH > 0 && osum_ok && nkv > C::FLUSH) {
+        const float* os = sOsum + (wg * D + c * 32) * 128 + r;
+        const float sc = (m_sum == -INFINITY) ? 0.0f : exp2_int(m_sum - m_ref);
+        float prev[32];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) prev[e] = C::OSUM_SMEM ? os[e * 128] : __ldcg(os + e * 128);
+        for (int e = 0; e < 32; ++e) prev[e] = C::OSUM_SMEM ? os[e * 128] : __ldcg(os + e * 128);
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = (prev[e] * sc + __uint_as_float(o[e])) * inv_l;
-        } else {
+        for (int e = 0; e < 32; ++e) v[e] = (prev[e] * sc + __uint_as_float(o[e])) * inv_l;
+      } else {
 #pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
-        }
-        if (write) {
-          if (mode == kModeOut) {
-            uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
-#pragma unroll
-            for (int q8 = 0; q8 < 4; ++q8) {
-              uint4 w;
-              w.x = pack2(v[8 * q8 + 0], v[8 * q8 + 1], DT);
-              w.y = pack2(v[8 * q8 + 2], v[8 * q8 + 3], DT);
-              w.z = pack2(v[8 * q8 + 4], v[8 * q8 + 5], DT);
-              w.w = pack2(v[8 * q8 + 6], v[8 * q8 + 7], DT);
-              dst[q8] = w;
-            }
-          } else {
-            float4* dst = reinterpret_cast<float4*>(u.o_part + row * D + c * 32);
-#pragma unroll
-            for (int q4 = 0; q4 < 8; ++q4) {
-              float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
-              if (mode == kModeAccum && !fresh) {
-                const float4 a = dst[q4];
-                w.x = wa * a.x + wn * w.x;
-                w.y = wa * a.y + wn * w.y;
-                w.z = wa * a.z + wn * w.z;
-                w.w = wa * a.w + wn * w.w;
-              }
-              dst[q4] = w;
-            }
-          }
-        }
+        for (int e = 0; e < 32; ++e) v[e] = __uint_as_float(o[e]) * inv_l;
       }
       if (write) {
         if (mode == kModeOut) {
-          if (p.lse) p.lse[lrow] = lse_v;
+          uint4* dst = reinterpret_cast<uint4*>(static_cast<uint16_t*>(p.out) + row * D + c * 32);
+#pragma unroll
+          for (int q8 = 0; q8 < 4; ++q8) {
+            uint4 w;
+            w.x = pack2(v[8 * q8 + 0], v[8 * q8 + 1], DT);
+            w.y = pack2(v[8 * q8 + 2], v[8 * q8 + 3], DT);
+            w.z = pack2(v[8 * q8 + 4], v[8 * q8 + 5], DT);
+            w.w = pack2(v[8 * q8 + 6], v[8 * q8 + 7], DT);
+            dst[q8] = w;
+          }
         } else {
-          u.lse_part[lrow] = lse_out;
+          float4* dst = reinterpret_cast<float4*>(p.o_part + row * D + c * 32);
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {
+            float4 w = make_float4(v[4 * q4], v[4 * q4 + 1], v[4 * q4 + 2], v[4 * q4 + 3]);
+            if (mode == kModeAccum && !fresh) {
+              const float4 a = dst[q4];
+              w.x = wa * a.x + wn * w.x;
+              w.y = wa * a.y + wn * w.y;
+              w.z = wa * a.z + wn * w.z;
+              w.w = wa * a.w + wn * w.w;
+            }
+            dst[q4] = w;
+          }
         }
       }
-      jt += nkv;
-      if (nkv > 0) ++ko;
+    }
+    if (write) {
+      if (mode == kModeOut) {
+        if (p.lse) p.lse[lrow] = lse_v;
+      } else {
+        p.lse_part[lrow] = lse_out;
+      }
     }
 
     // ------------------------------------------------------------------ teardown (softmax warpgroups)
@@ -978,17 +833,28 @@ template <int D, int DT, bool CAUSAL, int MODE>
 __global__ void __launch_bounds__(NTHREADS2, 1)
     attn_fwd2_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV, const KParams p) {
-  const SingleSource src{&tmQ, &tmK, &tmV, &p};
-  attn_fwd2_body<D, DT, CAUSAL, MODE>(p, src);
+  attn_fwd2_body<D, DT, CAUSAL, MODE>(tmQ, tmK, tmV, p, static_cast<int>(blockIdx.x));
 }
 
-// Several chunk pairs in one launch: each unit's maps, offsets, sizes, mode and accumulator are its pair's.
+// Several chunk pairs in one launch: CTA blockIdx.x belongs to the last pair whose first unit is at or
+// before it; that pair's maps, offsets, sizes, mode and accumulator replace the single-pair parameters.
 template <int D, int DT, bool CAUSAL>
 __global__ void __launch_bounds__(NTHREADS2, 1) attn_fwd2_multi_kernel(const __grid_constant__ MultiParams mp) {
-  int units = 0;
-  for (int i = 0; i < mp.n_pairs; ++i) units += mp.pair[i].n_q_tiles * mp.common.BH;
-  const MultiSource src{&mp, units};
-  attn_fwd2_body<D, DT, CAUSAL, kModeMulti>(mp.common, src);
+  const int u = static_cast<int>(blockIdx.x);
+  int i = 0;
+  for (int k = 1; k < mp.n_pairs; ++k)
+    if (mp.pair[k].unit_begin <= u) i = k;
+  const PairDesc& pd = mp.pair[i];
+  KParams kp = mp.common;
+  kp.q_off = pd.q_off;
+  kp.kv_off = pd.kv_off;
+  kp.Nq = pd.Nq;
+  kp.Nkv = pd.Nkv;
+  kp.n_q_tiles = pd.n_q_tiles;
+  kp.o_part = pd.o_part;
+  kp.lse_part = pd.lse_part;
+  kp.mode = pd.mode;
+  attn_fwd2_body<D, DT, CAUSAL, kModeMulti>(pd.q, pd.k, pd.v, kp, u - pd.unit_begin);
 }
 
 template <int D, int DT, bool CAUSAL, int MODE>
@@ -1013,8 +879,7 @@ int launch_t(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv
     attr.mark(dev);
   }
   kp.n_q_tiles = (Nq + 2 * BM - 1) / (2 * BM);  // pairs of query tiles
-  const long long units = static_cast<long long>(kp.n_q_tiles) * BH;
-  const long long grid = units < sm_count() ? units : sm_count();  // persistent: one CTA per SM
+  const long long grid = static_cast<long long>(kp.n_q_tiles) * BH;
   kern<<<static_cast<int>(grid), NTHREADS2, Cfg2<D, DT>::SMEM_BYTES, stream>>>(mq, mk, mv, kp);
   return cuda_status(cudaGetLastError(), "attention kernel launch");
 }
@@ -1114,8 +979,7 @@ int launch_multi_t(const MultiParams& mp, int grid, cudaStream_t stream) {
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncSetAttribute(attention smem, several pairs)");
     attr.mark(dev);
   }
-  const int g = grid < sm_count() ? grid : sm_count();  // persistent: one CTA per SM
-  kern<<<g, NTHREADS2, Cfg2<D, DT>::SMEM_BYTES, stream>>>(mp);
+  kern<<<grid, NTHREADS2, Cfg2<D, DT>::SMEM_BYTES, stream>>>(mp);
   return cuda_status(cudaGetLastError(), "attention kernel launch (several pairs)");
 }
 
