@@ -54,6 +54,13 @@ def test_quorum_validation(cq):
     st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 64, True,
                                                   0.0, cq.CQSA_F16, 7, (0, 1, 2), 1, stream=0))
     assert st == cq.CQSA_ERR_INVALID and "difference" in msg
+    # the engine-selecting entry: unknown engine and negative budget are rejected before any launch
+    st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd_ex(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 64,
+                                                     True, 0.0, cq.CQSA_F16, 7, (0, 1, 3), 1, engine=9, stream=0))
+    assert st == cq.CQSA_ERR_INVALID and "engine" in msg
+    st, msg = _rc(lambda: cq.cqsa_quorum_attn_fwd_ex(FAKE, FAKE, FAKE, 0, False, FAKE, None, False, 1, 1, 256, 64,
+                                                     True, 0.0, cq.CQSA_F16, 7, (0, 1, 3), 1, wave_tokens=-1, stream=0))
+    assert st == cq.CQSA_ERR_INVALID and "wave_tokens" in msg
 
 
 def _rc(fn):
