@@ -580,6 +580,96 @@ def measure_bwd(cq, dev, reps, N=32768, H=8):
                          "peak_source": src, "note": "algorithmic FLOP of the five products, whole call"}}
 
 
+def measure_copy_series(dev, seconds=15.0):
+    """Host-to-device copy rate over time: 256 MiB copies alternating between a freshly pinned buffer and
+    pinned buffers filled by the synthetic generator (as the streaming workload's are), to tell host-side
+    contention (both move together) from an effect of the buffers (they differ)."""
+    import torch
+    import synthetic as syn
+    reg = 256 << 20
+    dbuf = torch.empty(reg, dtype=torch.uint8, device=dev)
+    side = torch.cuda.Stream(dev)
+    fresh = torch.empty(1 << 30, dtype=torch.uint8, pin_memory=True)
+    fresh.numpy()[:] = 7
+    gen = []
+    for tid in range(3):
+        t = torch.empty((1, 1 << 20, 8, 64), dtype=torch.float16).pin_memory()
+        syn.normal(1, 8, 1 << 20, 64, seed=0, tensor_id=tid, layout=syn.LAYOUT_BNHD, out=t.numpy().view(np.uint16))
+        gen.append(t.view(-1).view(torch.uint8))
+
+    def rate(src):
+        with torch.cuda.stream(side):
+            a = torch.cuda.Event(enable_timing=True)
+            b = torch.cuda.Event(enable_timing=True)
+            a.record(side)
+            dbuf.copy_(src, non_blocking=True)
+            b.record(side)
+        side.synchronize()
+        return reg / (a.elapsed_time(b) / 1e3) / 1e9
+
+    t0 = time.perf_counter()
+    f, g = [], []
+    i = 0
+    while time.perf_counter() - t0 < seconds:
+        off = (i % 4) * reg
+        f.append(rate(fresh[off:off + reg]))
+        g.append(rate(gen[i % 3][off:off + reg]))
+        i += 1
+    fa, ga = np.array(f), np.array(g)
+    return {"measure": "copy_series", "copies_each": len(f), "seconds": seconds,
+            "fresh_gbs": {"median": float(np.median(fa)), "min": float(fa.min()), "max": float(fa.max()),
+                          "frac_above_150": float(np.mean(fa > 150))},
+            "generated_gbs": {"median": float(np.median(ga)), "min": float(ga.min()), "max": float(ga.max()),
+                              "frac_above_150": float(np.mean(ga > 150))},
+            "correlation": float(np.corrcoef(fa, ga)[0, 1]) if len(f) > 2 else None,
+            "method": "alternating 256 MiB cudaMemcpyAsync copies, CUDA events per copy"}
+
+
+def measure_stream_bwd(cq, dev, N=131072, C=16384, H=8):
+    """The host-resident backward (cqsa_stream_attn_bwd: pinned host q, k, v, out, dout, lse in, dq, dk, dv
+    out, 16,384-token chunks, copies double-buffered beside the kernels) against the device-resident
+    backward of the same problem (cqsa_attn_bwd, CUDA events): wall time, TFLOP/s and their ratio."""
+    import torch
+    import synthetic as syn
+    B, D = 1, 64
+    qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
+    gn = syn.normal(B, H, N, D, seed=0, tensor_id=syn.TID_DO)
+    q, k, v, g = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn, gn))
+    out = torch.empty_like(q)
+    lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    cq.cqsa_attn_fwd(q, k, v, out, lse, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+    dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
+    ws_bytes = cq.cqsa_attn_bwd_workspace_size(B, H, N, D)
+    ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
+
+    def dev_step():
+        cq.cqsa_attn_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+
+    dev_step()
+    dev_ms = statistics.median(_time_events(dev_step, 3, stream))
+    host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
+    grads = [torch.empty((B, H, N, D), dtype=torch.float16).pin_memory() for _ in range(3)]
+
+    def host_step():
+        cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, D, True, 0.0, cq.CQSA_F16, C, stream)
+
+    host_step()
+    walls = []
+    for _ in range(3):
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        host_step()
+        walls.append(time.perf_counter() - t0)
+    wall = statistics.median(walls)
+    flop = 2.5 * 4.0 * B * H * N * N * D / 2
+    return {"measure": "stream_bwd", "workload": f"host-resident backward, B=1 H={H} N={N} d=64 fp16 causal, "
+            f"{C}-token chunks, pinned host tensors", "wall_s": wall, "tflops": flop / wall / 1e12,
+            "device_resident_ms": dev_ms, "device_resident_tflops": flop / (dev_ms / 1e3) / 1e12,
+            "wall_over_device_resident": wall / (dev_ms / 1e3),
+            "h2d_bytes_min": int(5 * B * H * N * D * 2 + B * H * N * 4)}
+
+
 def _numa_nodes(t, samples=64):
     """NUMA nodes of a sample of a host tensor's pages (move_pages with no target nodes reports them);
     {} where the system call is unavailable."""
@@ -668,6 +758,7 @@ def run_secondary(cq, dev, args):
     run("bf16_d128", lambda: measure_bf16(cq, dev, reps))
     run("merge_131k", lambda: measure_merge(cq, dev, reps))
     run("bwd_32k", lambda: measure_bwd(cq, dev, reps))
+    run("stream_bwd_131k", lambda: measure_stream_bwd(cq, dev))
     run("link_1gib", lambda: measure_link(dev, 5))
     if args.secondary == "all":
         link = res["link_1gib"].get("h2d_gbs")
@@ -701,6 +792,10 @@ def run_measure(args):
                               engine=args.engine, device_inputs=args.device_inputs)
     elif args.measure == "bwd":
         line = measure_bwd(cq, dev, reps, N=args.bwd_n, H=args.bwd_h)
+    elif args.measure == "stream-bwd":
+        line = measure_stream_bwd(cq, dev)
+    elif args.measure == "copy-series":
+        line = measure_copy_series(dev)
     else:
         line = measure_bf16(cq, dev, reps)
     rc, code, _ = cq.cqsa_device_error()
@@ -716,7 +811,9 @@ def main():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=("ours", "reference"), default="ours")
     ap.add_argument("--no-cpu-baseline", action="store_true")
-    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum", "bwd"), default=None)
+    ap.add_argument("--measure", choices=("merge", "link", "stream", "bf16", "quorum", "bwd", "stream-bwd",
+                                          "copy-series"),
+                    default=None)
     ap.add_argument("--n", type=int, default=4_000_000, help="tokens for --measure stream / quorum")
     ap.add_argument("--acc-on-host", action="store_true", help="--measure quorum with the host accumulator")
     ap.add_argument("--max-parallel", type=int, default=1, help="--measure quorum: parallel subproblem lanes")

@@ -5,15 +5,20 @@
 // explicit entry points) works subproblem by subproblem from the forward's saved lse ("stream-cqsa
 // 2.2.2 -> 2.2.3" diff, stream_cqsa/oom_fallback.py, `stream_cqsa_auto` docstring).
 //
-// Schedule (query-outer, one stream, in order): for each query chunk, copy its q, out, dout and lse,
-// form D = rowsum(dout * out) and zero its fp32 dq accumulator; for each key chunk it needs (every
-// chunk, or those starting at or before the query chunk's last token when causal) copy k, v and add
-// the pair into dq and into that key chunk's fp32 dk / dv accumulators; then round dq to the input
-// dtype and copy it out. Once every query chunk is done, dk and dv of each key chunk follow. Device
-// memory: the dk / dv accumulators of the whole sequence (2 * B*H*N*64 * 4 bytes) plus one chunk of
-// each input, D, lse, the dq accumulator and an output staging buffer.
+// Schedule (query-outer): for each query chunk, its q, out, dout and lse are copied on a copy stream
+// into one of two query-side slots (the next chunk's copies overlap this chunk's kernels), D =
+// rowsum(dout * out) is formed and its fp32 dq accumulator zeroed; the key chunks it needs (every chunk,
+// or those starting at or before the query chunk's last token when causal) go through two K/V slots on
+// the copy stream, in alternating directions from one query chunk to the next, so the chunk that ends
+// one query chunk is not copied again for the next; each pair adds into dq and into that key chunk's
+// fp32 dk / dv accumulators. dq is rounded to the input dtype into one of two staging buffers and leaves
+// on a second stream; once every query chunk is done, dk and dv of each key chunk follow the same way.
+// Device memory: the dk / dv accumulators of the whole sequence (2 * B*H*N*64 * 4 bytes) plus two slots
+// of each streamed chunk.
 #include <math.h>
 #include <string.h>
+
+#include <vector>
 
 #include "cqsa_internal.h"
 
@@ -77,61 +82,130 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
   const size_t chunk16 = BH * static_cast<size_t>(C) * 64 * 2;  // one 16-bit chunk
   const size_t chunk32 = BH * static_cast<size_t>(C) * 64 * 4;  // one fp32 chunk
   const size_t rows32 = BH * static_cast<size_t>(C) * 4;
+  const float sc = scale == 0.0f ? 0.125f : scale;  // 1/sqrt(64)
 
-  // device buffers: per-key-chunk dk / dv accumulators, then one chunk of everything else
+  // Device memory: the dk / dv accumulators of every key chunk, and two slots of everything that
+  // streams: the query side (q, out, dout, lse, D, the dq accumulator), the key side (k, v) and the
+  // output staging.
+  struct QSlot {
+    void *q, *out, *g;
+    float *lse, *dvec, *dq;
+  } qsl[2];
+  struct KSlot {
+    void *k, *v;
+  } ksl[2];
+  void* ostage[2] = {nullptr, nullptr};
+  std::vector<void*> bufs;
+  cudaStream_t copy = nullptr, d2h = nullptr;
+  std::vector<cudaEvent_t> events;
+  auto alloc = [&](void** ptr, size_t n) -> int {
+    const int r = pool_alloc(ptr, n);
+    if (r == CQSA_OK) bufs.push_back(*ptr);
+    return r;
+  };
+  auto event = [&](cudaEvent_t* e) -> int {
+    const int r = pool_event(e, false);
+    if (r == CQSA_OK) events.push_back(*e);
+    return r;
+  };
   void* acc_kv = nullptr;
-  void* stage = nullptr;
   const size_t acc_bytes = 2 * static_cast<size_t>(n_chunks) * chunk32;
-  const size_t stage_bytes = 6 * chunk16 + chunk32 + 2 * rows32 + 256;
-  int rc = pool_alloc(&acc_kv, acc_bytes);
-  if (rc == CQSA_OK) rc = pool_alloc(&stage, stage_bytes);
-  if (rc != CQSA_OK) {
-    pool_free(acc_kv);
-    return rc;
+  int rc = alloc(&acc_kv, acc_bytes);
+  for (int s2 = 0; s2 < 2 && rc == CQSA_OK; ++s2) {
+    void* pq = nullptr;
+    rc = alloc(&pq, 3 * chunk16 + chunk32 + 2 * rows32 + 256);
+    if (rc != CQSA_OK) break;
+    char* c = static_cast<char*>(pq);
+    qsl[s2].q = c;
+    qsl[s2].out = c + chunk16;
+    qsl[s2].g = c + 2 * chunk16;
+    qsl[s2].dq = reinterpret_cast<float*>(c + 3 * chunk16);
+    qsl[s2].lse = reinterpret_cast<float*>(c + 3 * chunk16 + chunk32);
+    qsl[s2].dvec = reinterpret_cast<float*>(c + 3 * chunk16 + chunk32 + rows32);
+    void* pk = nullptr;
+    if (rc == CQSA_OK) rc = alloc(&pk, 2 * chunk16);
+    if (rc != CQSA_OK) break;
+    ksl[s2].k = pk;
+    ksl[s2].v = static_cast<char*>(pk) + chunk16;
+    if (rc == CQSA_OK) rc = alloc(&ostage[s2], chunk16);
+  }
+  if (rc == CQSA_OK) rc = pool_stream(&copy);
+  if (rc == CQSA_OK) rc = pool_stream(&d2h);
+  cudaEvent_t q_ready[2], q_free[2], kv_ready[2], kv_free[2], o_ready[2], o_free[2];
+  bool q_free_set[2] = {false, false}, kv_free_set[2] = {false, false}, o_free_set[2] = {false, false};
+  for (int s2 = 0; s2 < 2 && rc == CQSA_OK; ++s2) {
+    if ((rc = event(&q_ready[s2])) == CQSA_OK && (rc = event(&q_free[s2])) == CQSA_OK &&
+        (rc = event(&kv_ready[s2])) == CQSA_OK && (rc = event(&kv_free[s2])) == CQSA_OK &&
+        (rc = event(&o_ready[s2])) == CQSA_OK)
+      rc = event(&o_free[s2]);
   }
   float* dk_acc0 = static_cast<float*>(acc_kv);
   float* dv_acc0 = dk_acc0 + static_cast<size_t>(n_chunks) * (chunk32 / 4);
-  char* sp = static_cast<char*>(stage);
-  void* q_c = sp;
-  void* out_c = sp + chunk16;
-  void* g_c = sp + 2 * chunk16;
-  void* k_c = sp + 3 * chunk16;
-  void* v_c = sp + 4 * chunk16;
-  void* o_c = sp + 5 * chunk16;  // output staging (dtype)
-  float* dq_acc = reinterpret_cast<float*>(sp + 6 * chunk16);
-  float* lse_c = reinterpret_cast<float*>(sp + 6 * chunk16 + chunk32);
-  float* dvec_c = reinterpret_cast<float*>(sp + 6 * chunk16 + chunk32 + rows32);
 
   long long bytes = 0;
+  int out_slot = 0;  // output staging slots alternate over every chunk written out (dq, then dk, dv)
+  // A 16-bit [B,H,n,64] result into staging slot out_slot (after its previous D2H), then to host rows [t0, t0+n).
+  auto write_out = [&](const float* acc, void* host, long long t0, int n) {
+    const int os = out_slot;
+    out_slot ^= 1;
+    if (o_free_set[os]) CQSA_STEP(cudaStreamWaitEvent(stream, o_free[os], 0), "wait staging");
+    if (rc == CQSA_OK) rc = launch_bwd_cast(acc, ostage[os], static_cast<long long>(BH) * n * 64, dtype, stream);
+    CQSA_STEP(cudaEventRecord(o_ready[os], stream), "record");
+    CQSA_STEP(cudaStreamWaitEvent(d2h, o_ready[os], 0), "wait cast");
+    CQSA_STEP(copy_chunk_out(host, ostage[os], B, H, N, t0, n, d2h), "copy out");
+    CQSA_STEP(cudaEventRecord(o_free[os], d2h), "record");
+    o_free_set[os] = true;
+  };
+
   CQSA_STEP(cudaMemsetAsync(acc_kv, 0, acc_bytes, stream), "zero dk/dv accumulators");
+  int kv_chunk[2] = {-1, -1};  // key chunk resident in each K/V slot
+  int next_kv = 0;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
   for (int qi = 0; qi < n_chunks && rc == CQSA_OK; ++qi) {
     const long long qs = static_cast<long long>(qi) * C;
     const int nq = static_cast<int>(N - qs < C ? N - qs : C);
-    const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
-    CQSA_STEP(copy_chunk(q_c, q, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, stream, &bytes), "copy q");
-    CQSA_STEP(copy_chunk(out_c, out, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, stream, &bytes), "copy out");
-    CQSA_STEP(copy_chunk(g_c, dout, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, stream, &bytes), "copy dout");
-    CQSA_STEP(cudaMemcpy2DAsync(lse_c, static_cast<size_t>(nq) * 4, lse + qs, static_cast<size_t>(N) * 4,
-                                static_cast<size_t>(nq) * 4, BH, h2d, stream),
+    const QSlot& Q = qsl[qi & 1];
+    // the query side of chunk qi - 2 is done with this slot
+    if (q_free_set[qi & 1]) CQSA_STEP(cudaStreamWaitEvent(copy, q_free[qi & 1], 0), "wait q slot");
+    CQSA_STEP(copy_chunk(Q.q, q, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy q");
+    CQSA_STEP(copy_chunk(Q.out, out, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy out");
+    CQSA_STEP(copy_chunk(Q.g, dout, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy dout");
+    CQSA_STEP(cudaMemcpy2DAsync(Q.lse, static_cast<size_t>(nq) * 4, lse + qs, static_cast<size_t>(N) * 4,
+                                static_cast<size_t>(nq) * 4, BH, h2d, copy),
               "copy lse");
-    if (rc == CQSA_OK) rc = launch_bwd_dvec(out_c, g_c, dvec_c, static_cast<long long>(BH) * nq, dtype, stream);
-    CQSA_STEP(cudaMemsetAsync(dq_acc, 0, BH * static_cast<size_t>(nq) * 64 * 4, stream), "zero dq accumulator");
-    for (int ki = 0; ki < n_chunks && rc == CQSA_OK; ++ki) {
+    CQSA_STEP(cudaEventRecord(q_ready[qi & 1], copy), "record");
+    CQSA_STEP(cudaStreamWaitEvent(stream, q_ready[qi & 1], 0), "wait q");
+    if (rc == CQSA_OK) rc = launch_bwd_dvec(Q.out, Q.g, Q.dvec, static_cast<long long>(BH) * nq, dtype, stream);
+    CQSA_STEP(cudaMemsetAsync(Q.dq, 0, BH * static_cast<size_t>(nq) * 64 * 4, stream), "zero dq accumulator");
+    // key chunks this query chunk needs (every chunk, or those at or before its last token when causal),
+    // in alternating directions, so the chunk that ends one query chunk starts the next one
+    int last = n_chunks - 1;
+    if (causal) last = static_cast<int>((qs + nq - 1) / C);
+    for (int t = 0; t <= last && rc == CQSA_OK; ++t) {
+      const int ki = (qi & 1) ? last - t : t;
       const long long ks = static_cast<long long>(ki) * C;
-      if (causal && ks > qs + nq - 1) break;  // this and every later key chunk follow the whole query chunk
       const int nk = static_cast<int>(N - ks < C ? N - ks : C);
-      CQSA_STEP(copy_chunk(k_c, k, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, stream, &bytes), "copy k");
-      CQSA_STEP(copy_chunk(v_c, v, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, stream, &bytes), "copy v");
+      int slot = kv_chunk[0] == ki ? 0 : (kv_chunk[1] == ki ? 1 : -1);
+      if (slot < 0) {
+        slot = next_kv;
+        if (kv_free_set[slot]) CQSA_STEP(cudaStreamWaitEvent(copy, kv_free[slot], 0), "wait kv slot");
+        CQSA_STEP(copy_chunk(ksl[slot].k, k, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, copy, &bytes), "copy k");
+        CQSA_STEP(copy_chunk(ksl[slot].v, v, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, copy, &bytes), "copy v");
+        CQSA_STEP(cudaEventRecord(kv_ready[slot], copy), "record");
+        kv_chunk[slot] = ki;
+      }
+      next_kv = slot ^ 1;  // the other slot is the next to refill
+      CQSA_STEP(cudaStreamWaitEvent(stream, kv_ready[slot], 0), "wait kv");
       if (rc != CQSA_OK) break;
       BwdArgs a;
       memset(&a, 0, sizeof(a));
-      a.q = q_c;
-      a.k = k_c;
-      a.v = v_c;
-      a.dout = g_c;
-      a.lse = lse_c;
-      a.dvec = dvec_c;
-      a.dq_acc = dq_acc;
+      a.q = Q.q;
+      a.k = ksl[slot].k;
+      a.v = ksl[slot].v;
+      a.dout = Q.g;
+      a.lse = Q.lse;
+      a.dvec = Q.dvec;
+      a.dq_acc = Q.dq;
       a.dk_acc = dk_acc0 + static_cast<size_t>(ki) * (chunk32 / 4);
       a.dv_acc = dv_acc0 + static_cast<size_t>(ki) * (chunk32 / 4);
       a.B = B;
@@ -142,32 +216,38 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
       a.q_off = qs;
       a.kv_off = ks;
       a.causal = causal != 0;
-      a.scale = scale == 0.0f ? 0.125f : scale;  // 1/sqrt(64)
+      a.scale = sc;
       a.dtype = dtype;
       rc = launch_attention_bwd_chunk(a, stream);
+      CQSA_STEP(cudaEventRecord(kv_free[slot], stream), "record");
+      kv_free_set[slot] = true;
     }
-    if (rc == CQSA_OK) rc = launch_bwd_cast(dq_acc, o_c, static_cast<long long>(BH) * nq * 64, dtype, stream);
-    CQSA_STEP(copy_chunk_out(dq, o_c, B, H, N, qs, nq, stream), "copy dq out");
-    // the staging buffer is reused by the next chunk's cast: wait for this copy
-    CQSA_STEP(cudaStreamSynchronize(stream), "synchronize");
+    write_out(Q.dq, dq, qs, nq);
+    CQSA_STEP(cudaEventRecord(q_free[qi & 1], stream), "record");
+    q_free_set[qi & 1] = true;
   }
   for (int ki = 0; ki < n_chunks && rc == CQSA_OK; ++ki) {
     const long long ks = static_cast<long long>(ki) * C;
     const int nk = static_cast<int>(N - ks < C ? N - ks : C);
-    const long long n = static_cast<long long>(BH) * nk * 64;
-    if (rc == CQSA_OK) rc = launch_bwd_cast(dk_acc0 + static_cast<size_t>(ki) * (chunk32 / 4), o_c, n, dtype, stream);
-    CQSA_STEP(copy_chunk_out(dk, o_c, B, H, N, ks, nk, stream), "copy dk out");
-    CQSA_STEP(cudaStreamSynchronize(stream), "synchronize");
-    if (rc == CQSA_OK) rc = launch_bwd_cast(dv_acc0 + static_cast<size_t>(ki) * (chunk32 / 4), o_c, n, dtype, stream);
-    CQSA_STEP(copy_chunk_out(dv, o_c, B, H, N, ks, nk, stream), "copy dv out");
-    CQSA_STEP(cudaStreamSynchronize(stream), "synchronize");
+    write_out(dk_acc0 + static_cast<size_t>(ki) * (chunk32 / 4), dk, ks, nk);
+    write_out(dv_acc0 + static_cast<size_t>(ki) * (chunk32 / 4), dv, ks, nk);
   }
   // every use of the buffers is complete before they return to the pool
   cudaError_t se = cudaStreamSynchronize(stream);
   if (rc == CQSA_OK) rc = cuda_status(se, "synchronize");
+  if (copy) {
+    se = cudaStreamSynchronize(copy);
+    if (rc == CQSA_OK) rc = cuda_status(se, "synchronize copy stream");
+  }
+  if (d2h) {
+    se = cudaStreamSynchronize(d2h);
+    if (rc == CQSA_OK) rc = cuda_status(se, "synchronize output stream");
+  }
   // a kernel whose bounded wait gave up leaves its gradients incomplete: report it
   if (rc == CQSA_OK) rc = check_device_error_on(stream);
-  pool_free(stage);
-  pool_free(acc_kv);
+  for (cudaEvent_t e : events) pool_event_free(e, false);
+  pool_stream_free(copy);
+  pool_stream_free(d2h);
+  for (void* b : bufs) pool_free(b);
   return rc;
 }

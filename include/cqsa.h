@@ -260,11 +260,13 @@ int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cuda
  * v, out, dout [B,H,N,64] (fp16/bf16, layout BHND) and lse [B,H,N] fp32 in host memory (pinned for
  * speed); dq, dk, dv [B,H,N,64] written to host memory. Query-outer over chunks of chunk_tokens (a
  * positive multiple of 128): each query chunk's q/out/dout/lse and each needed key chunk's k/v are
- * copied to the device, the pair runs cqsa_attn_bwd_chunk's kernel, dq leaves after its query chunk,
- * dk and dv after the last one. Device memory: 2 * B*H*N*64*4 bytes of dk/dv accumulators plus one
- * chunk of each input, D, lse, the dq accumulator and an output buffer (from the library's pool;
- * CQSA_ERR_OOM if they do not fit). Synchronous; the result equals cqsa_attn_bwd's up to the fp32
- * summation order.
+ * copied to the device on a copy stream, double-buffered so copies overlap the kernels, the key chunks
+ * in alternating directions so consecutive query chunks share one copy; each pair runs
+ * cqsa_attn_bwd_chunk's kernel on `stream`; dq leaves after its query chunk, dk and dv after the last
+ * one, on a second stream. Device memory: 2 * B*H*N*64*4 bytes of dk/dv accumulators plus two slots of
+ * each streamed chunk (inputs, D, lse, the dq accumulator, output staging), from the library's pool
+ * (CQSA_ERR_OOM if they do not fit). Synchronous; the result equals cqsa_attn_bwd's up to the fp32
+ * summation order. Returns CQSA_ERR_TIMEOUT if a kernel's bounded wait gave up.
  */
 int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d, int causal,
