@@ -542,28 +542,30 @@ def measure_bf16(cq, dev, reps):
                          "peak_source": src, "note": "algorithmic FLOP; the P hi/lo split issues 1.5x the MMA work"}}
 
 
-def measure_bwd(cq, dev, reps, N=32768, H=8):
+def measure_bwd(cq, dev, reps, N=32768, H=8, B=1, D=64, causal=True, bf16=False, k_mul=1.0):
     """Attention backward, by default on the headline shape (B=1 H=8 N=32768 d=64 fp16 causal): the whole
     cqsa_attn_bwd call (D = rowsum(dO * O), zeroing the dQ accumulator, the tcgen05 kernel, the dQ
     conversion) timed with CUDA events, inputs and forward outputs resident. Algorithmic FLOP: five
     products of 2*N*N*d per head (S, dP, dV, dK, dQ), halved by the causal mask = 2.5x the forward."""
     import torch
     import synthetic as syn
-    B, D = 1, 64
-    qn, kn, vn = syn.qkv(B, H, N, D, seed=0)
-    gn = syn.normal(B, H, N, D, seed=0, tensor_id=syn.TID_DO)
-    q, k, v, g = (torch.from_numpy(x.view(np.int16)).view(torch.float16).to(dev) for x in (qn, kn, vn, gn))
+    dt = syn.BF16 if bf16 else syn.F16
+    tdt = torch.bfloat16 if bf16 else torch.float16
+    code = cq.CQSA_BF16 if bf16 else cq.CQSA_F16
+    qn, kn, vn = syn.qkv(B, H, N, D, seed=0, dtype=dt, k_mul=k_mul)
+    gn = syn.normal(B, H, N, D, seed=0, tensor_id=syn.TID_DO, dtype=dt)
+    q, k, v, g = (torch.from_numpy(x.view(np.int16)).view(tdt).to(dev) for x in (qn, kn, vn, gn))
     out = torch.empty_like(q)
     lse = torch.empty((B, H, N), dtype=torch.float32, device=dev)
     stream = torch.cuda.current_stream(dev)
-    cq.cqsa_attn_fwd(q, k, v, out, lse, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+    cq.cqsa_attn_fwd(q, k, v, out, lse, B, H, N, D, causal, 0.0, code, stream)
     dq, dk, dv = torch.empty_like(q), torch.empty_like(k), torch.empty_like(v)
     ws_bytes = cq.cqsa_attn_bwd_workspace_size(B, H, N, D)
     ws = torch.empty(ws_bytes, dtype=torch.uint8, device=dev)
     flush = torch.empty(256 << 20, dtype=torch.uint8, device=dev)
 
     def step():
-        cq.cqsa_attn_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, True, 0.0, cq.CQSA_F16, stream)
+        cq.cqsa_attn_bwd(q, k, v, out, g, lse, dq, dk, dv, ws, ws_bytes, B, H, N, D, causal, 0.0, code, stream)
 
     for _ in range(3):
         step()
@@ -571,10 +573,12 @@ def measure_bwd(cq, dev, reps, N=32768, H=8):
     for i in range(reps):
         flush.fill_(i & 0xFF)
         ms += _time_events(step, 1, stream)
-    flop = 2.5 * 4.0 * B * H * N * N * D / 2
+    flop = 2.5 * 4.0 * B * H * N * N * D / (2 if causal else 1)
     tf = flop / (statistics.median(ms) / 1e3) / 1e12
     peak, src, _ = _peaks()
-    return {"measure": "bwd", "workload": f"B=1 H={H} N={N} d=64 fp16 causal backward (dq, dk, dv)",
+    kind = ("bf16" if bf16 else "fp16") + (" causal" if causal else " non-causal")
+    kind += f", K x{k_mul:g}" if k_mul != 1.0 else ""
+    return {"measure": "bwd", "workload": f"B={B} H={H} N={N} d={D} {kind} backward (dq, dk, dv)",
             "ms_per_step": statistics.median(ms), "ms_min": min(ms), "tflops": tf,
             "roofline": {"bound": "tensor", "achieved": tf, "peak": peak, "unit": "TFLOP/s", "frac": tf / peak,
                          "peak_source": src, "note": "algorithmic FLOP of the five products, whole call"}}
@@ -758,6 +762,8 @@ def run_secondary(cq, dev, args):
     run("bf16_d128", lambda: measure_bf16(cq, dev, reps))
     run("merge_131k", lambda: measure_merge(cq, dev, reps))
     run("bwd_32k", lambda: measure_bwd(cq, dev, reps))
+    run("bwd_bf16_d128", lambda: measure_bwd(cq, dev, max(3, reps // 2), N=16384, H=32, B=2, D=128, causal=False,
+                                             bf16=True, k_mul=3.0))
     run("stream_bwd_131k", lambda: measure_stream_bwd(cq, dev))
     run("link_1gib", lambda: measure_link(dev, 5))
     if args.secondary == "all":

@@ -316,8 +316,8 @@ def attention(q, k, v, *, causal=False, scale=None, return_lse=False, stream=Non
 
 
 def attention_backward(q, k, v, out, dout, lse, *, causal=False, scale=None, stream=None):
-    """Gradients (dq, dk, dv) of attention on device tensors [B,H,N,64] (fp16/bf16), from the forward's
-    out and lse ([B,H,N] fp32) and the upstream gradient dout."""
+    """Gradients (dq, dk, dv) of attention on device tensors [B,H,N,d], d = 64 or 128 (fp16/bf16), from
+    the forward's out and lse ([B,H,N] fp32) and the upstream gradient dout."""
     import torch
     B, H, N, d = q.shape
     for t in (k, v, out, dout):

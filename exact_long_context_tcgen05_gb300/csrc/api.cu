@@ -277,10 +277,6 @@ int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, 
   t_err[0] = 0;
   int rc = check_problem(B, H, N, N, d, scale, dtype, false);
   if (rc != CQSA_OK) return rc;
-  if (d != 64) {
-    set_error("the backward supports head dim 64 (got %d)", d);
-    return CQSA_ERR_UNSUPPORTED;
-  }
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv || !workspace) {
     set_error("q, k, v, out, dout, lse, dq, dk, dv and workspace must be non-null device pointers");
     return CQSA_ERR_INVALID;
@@ -324,16 +320,12 @@ int cqsa_attn_bwd_dvec(const void* out_blk, const void* dout_blk, float* dvec_bl
   t_err[0] = 0;
   int rc = check_problem(B, H, Nq, Nq, d, 0.0f, dtype, false);
   if (rc != CQSA_OK) return rc;
-  if (d != 64) {
-    set_error("the backward supports head dim 64 (got %d)", d);
-    return CQSA_ERR_UNSUPPORTED;
-  }
   if (!out_blk || !dout_blk || !dvec_blk || !aligned16(out_blk) || !aligned16(dout_blk) ||
       (reinterpret_cast<uintptr_t>(dvec_blk) & 3u)) {
     set_error("out_blk and dout_blk must be non-null 16-byte aligned device pointers, dvec_blk 4-byte aligned");
     return CQSA_ERR_INVALID;
   }
-  return launch_bwd_dvec(out_blk, dout_blk, dvec_blk, static_cast<long long>(B) * H * Nq, dtype, stream);
+  return launch_bwd_dvec(out_blk, dout_blk, dvec_blk, static_cast<long long>(B) * H * Nq, d, dtype, stream);
 }
 
 int cqsa_attn_bwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk, const void* dout_blk,
@@ -343,10 +335,6 @@ int cqsa_attn_bwd_chunk(const void* q_blk, const void* k_blk, const void* v_blk,
   t_err[0] = 0;
   int rc = check_problem(B, H, Nq, Nkv, d, scale, dtype, false);
   if (rc != CQSA_OK) return rc;
-  if (d != 64) {
-    set_error("the backward supports head dim 64 (got %d)", d);
-    return CQSA_ERR_UNSUPPORTED;
-  }
   if (q_off < 0 || kv_off < 0) {
     set_error("q_off and kv_off must be >= 0");
     return CQSA_ERR_INVALID;

@@ -27,7 +27,9 @@
 //                    an MMA issuer warp, a dQ reduction warp and two elementwise warpgroups, joined by
 //                    mbarriers. dK_j, dV_j are written once, after the last query tile.
 //   bwd_dq_kernel    fp32 dQ accumulator -> dQ in the input dtype
-// P and dS enter the MMAs rounded to the input dtype; everything else is fp32. Head dimension 64.
+// P and dS enter the MMAs rounded to the input dtype; everything else is fp32. Head dimension 64 or 128
+// (d = 128 holds one Q/dO tile instead of two, and shares tensor and shared memory between phases: see
+// BwdCfg).
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -49,18 +51,41 @@ namespace {
 __device__ DevErr g_bwd_err;
 
 constexpr int BT = 128;                         // keys per CTA tile, queries per step
-constexpr int HD = 64;                          // head dimension
-constexpr uint32_t BOX = BT * HD * 2;           // one 128 x 64 tile of 16-bit elements (16 KiB)
-constexpr uint32_t OFF_K = 0, OFF_V = BOX, OFF_Q = 2 * BOX, OFF_G = 4 * BOX, OFF_DS = 6 * BOX;
-constexpr uint32_t OFF_DQ = 8 * BOX;            // dQ staging: 2 slots of 128 x 64 fp32
-constexpr uint32_t DQ_SLOT = BT * HD * 4;
-constexpr uint32_t OFF_ROW = OFF_DQ + 2 * DQ_SLOT;  // per elementwise warpgroup and slot: lse2[64], D[64]
-constexpr uint32_t OFF_BAR = OFF_ROW + 4 * BT * 4;
-constexpr int NBAR = 14;
-constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
-// Tensor memory: S^T, dP^T, the dV, dK and dQ accumulators, and P^T (16-bit pairs) as the A operand of dV.
-constexpr uint32_t COL_S = 0, COL_DP = 128, COL_DV = 256, COL_DK = 320, COL_DQ = 384, COL_PT = 448;
+constexpr uint32_t BOX = BT * 64 * 2;           // one 128 x 64 box of 16-bit elements (16 KiB)
 constexpr uint32_t TMEM_COLS = 512;
+constexpr int NBAR = 14;
+
+// Shared- and tensor-memory layout per head dimension.
+// d = 64: K, V, a two-slot ring of Q and dO tiles, the dS^T tile and two dQ staging slots of
+//   128 x 64 fp32 (195 KiB). Tensor memory: S^T, dP^T, dV, dK, dQ and P^T (16-bit pairs), 512 columns.
+// d = 128: every 128-row tile is two boxes, so K, V, one Q and one dO tile and dS^T take 160 KiB; dQ
+//   (128 x 128 fp32, 64 KiB) is staged over the dS^T tile and the 32 KiB behind it once the step's
+//   products have read dS^T. Tensor memory: S^T 0-127 (each warpgroup writes its P^T over the first
+//   half of its own S^T columns), dP^T 128-255 (dQ is accumulated over it after dS is formed), dV
+//   256-383, dK 384-511.
+template <int HD>
+struct BwdCfg {
+  static constexpr int NSLOT = HD == 64 ? 2 : 1;          // Q/dO ring slots
+  static constexpr uint32_t TILE = BOX * (HD / 64);       // one 128-row tile of Q, dO, K or V
+  static constexpr uint32_t OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;
+  static constexpr uint32_t OFF_G = OFF_Q + NSLOT * TILE;
+  static constexpr uint32_t OFF_DS = OFF_G + NSLOT * TILE;  // dS^T: two 64-query boxes
+  static constexpr uint32_t OFF_DQ = OFF_DS + 2 * BOX;
+  static constexpr uint32_t DQ_SLOT = BT * 64 * 4;        // d = 64: one staging slot (128 x 64 fp32)
+  static constexpr uint32_t OFF_ROW = HD == 64 ? OFF_DQ + 2 * DQ_SLOT : OFF_DQ + 2 * BOX;
+  static constexpr uint32_t OFF_BAR = OFF_ROW + 4 * BT * 4;  // rows: per warpgroup and slot lse2[64], D[64]
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
+  static constexpr uint32_t COL_S = 0, COL_DP = 128;
+  static constexpr uint32_t COL_DV = 256, COL_DK = 256 + HD;
+  static constexpr uint32_t COL_DQ = HD == 64 ? 384 : 128;
+  static_assert(SMEM_BYTES <= 232448, "shared memory exceeds 227 KiB");
+  static_assert(COL_DK + HD <= TMEM_COLS, "tensor memory exceeds 512 columns");
+  // P^T column of query k-step ks (16 queries = 8 columns of 16-bit pairs)
+  static __device__ __forceinline__ uint32_t col_pt(int ks) {
+    return HD == 64 ? 448u + static_cast<uint32_t>(ks) * 8u
+                    : static_cast<uint32_t>((ks >> 2) * 64 + (ks & 3) * 8);
+  }
+};
 constexpr float LOG2E = 1.4426950408889634f;
 // Twelve warps: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
 // reductions (warp 2), one idle warp; warpgroups 1 and 2 = the elementwise step, each on half the query
@@ -194,60 +219,73 @@ __device__ __forceinline__ float2 unpack_pair(uint32_t w, int bf16) {
   return __half22float2(*reinterpret_cast<__half2*>(&w));
 }
 
-// S^T = K Q^T (or dP^T = V dO^T): 4 MMAs of 128 x 128 x 16, both operands K-major, 128-byte swizzle.
+// S^T = K Q^T (or dP^T = V dO^T): d/16 MMAs of 128 x 128 x 16, both operands K-major, 128-byte swizzle;
+// features 64..127 of d = 128 are in each tile's second box.
+template <int HD>
 __device__ __forceinline__ void issue_t(uint32_t dcol, uint64_t a0, uint64_t b0, uint32_t idesc) {
   mma_ss_imm<0>(dcol, a0, b0, idesc);
 #pragma unroll
-  for (int ks = 1; ks < HD / 16; ++ks) mma_ss_imm<1>(dcol, a0 + ks * 2, b0 + ks * 2, idesc);
+  for (int ks = 1; ks < HD / 16; ++ks) {
+    const uint32_t off = static_cast<uint32_t>((ks >> 2) * (BOX >> 4) + (ks & 3) * 2);
+    mma_ss_imm<1>(dcol, a0 + off, b0 + off, idesc);
+  }
 }
 
 // dV += P^T dO (A = P^T from tensor memory), dK += dS^T Q (A = dS^T K-major in shared memory) and
 // dQ = dS K (A = the same dS^T tile read MN-major): 8 steps of 16 queries (dV, dK) or keys (dQ); the
-// B operands dO, Q and K are MN-major.
-template <int FIRST>
+// B operands dO, Q and K are MN-major with N = d (the second 64-feature box at the descriptor's
+// leading-byte offset when d = 128).
+template <int FIRST, int HD>
 __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t dQm, uint64_t dS_k, uint64_t dS_mn,
                                             uint64_t dK, uint32_t idesc_g, uint32_t idesc_q) {
+  using C = BwdCfg<HD>;
 #pragma unroll
   for (int ks = 0; ks < BT / 16; ++ks) {
     const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));                        // 16 rows of 128 bytes
     const uint32_t koff = static_cast<uint32_t>((ks >> 2) * (BOX >> 4) + (ks & 3) * 2);  // 16 columns, K-major
     if (FIRST && ks == 0) {
-      mma_ts_imm<0>(tmem + COL_DV, tmem + COL_PT + ks * 8, dG + off, idesc_g);
-      mma_ss_imm<0>(tmem + COL_DK, dS_k + koff, dQm + off, idesc_g);
+      mma_ts_imm<0>(tmem + C::COL_DV, tmem + C::col_pt(ks), dG + off, idesc_g);
+      mma_ss_imm<0>(tmem + C::COL_DK, dS_k + koff, dQm + off, idesc_g);
     } else {
-      mma_ts_imm<1>(tmem + COL_DV, tmem + COL_PT + ks * 8, dG + off, idesc_g);
-      mma_ss_imm<1>(tmem + COL_DK, dS_k + koff, dQm + off, idesc_g);
+      mma_ts_imm<1>(tmem + C::COL_DV, tmem + C::col_pt(ks), dG + off, idesc_g);
+      mma_ss_imm<1>(tmem + C::COL_DK, dS_k + koff, dQm + off, idesc_g);
     }
-    if (ks == 0) mma_ss_imm<0>(tmem + COL_DQ, dS_mn + off, dK + off, idesc_q);
-    else mma_ss_imm<1>(tmem + COL_DQ, dS_mn + off, dK + off, idesc_q);
+    if (ks == 0) mma_ss_imm<0>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
+    else mma_ss_imm<1>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
   }
 }
 
 // ACCUM = 0: monolithic (dK, dV written in the input dtype); ACCUM = 1: one chunk pair, dK and dV
 // added into fp32 accumulators.
-template <int DT, bool CAUSAL, int ACCUM>
+template <int DT, bool CAUSAL, int ACCUM, int HD>
 __global__ void __launch_bounds__(NTHR, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
+  using C = BwdCfg<HD>;
+  constexpr int NSLOT = C::NSLOT;
+  constexpr uint32_t TILE = C::TILE;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  uint8_t* sK = sm + OFF_K;
-  uint8_t* sV = sm + OFF_V;
-  uint8_t* sQ = sm + OFF_Q;    // [2][BOX]
-  uint8_t* sG = sm + OFF_G;    // [2][BOX] (dO)
-  uint8_t* sdS = sm + OFF_DS;  // dS^T [128 keys][128 queries], two 64-query boxes
-  uint8_t* sdQ = sm + OFF_DQ;  // [2][128 x 64 fp32], two 32-float boxes each
-  float* sRow = reinterpret_cast<float*>(sm + OFF_ROW);  // [wg 2][slot 2][lse2 64 | D 64]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + OFF_BAR);
+  uint8_t* sK = sm + C::OFF_K;
+  uint8_t* sV = sm + C::OFF_V;
+  uint8_t* sQ = sm + C::OFF_Q;    // [NSLOT][TILE]
+  uint8_t* sG = sm + C::OFF_G;    // [NSLOT][TILE] (dO)
+  uint8_t* sdS = sm + C::OFF_DS;  // dS^T [128 keys][128 queries], two 64-query boxes
+  // dQ staging: d = 64, two slots of 128 x 64 fp32 (two 32-float boxes each); d = 128, one 128 x 128 fp32
+  // tile in four 32-float boxes over dS^T and the 32 KiB behind it
+  uint8_t* sdQ = HD == 64 ? sm + C::OFF_DQ : sdS;
+  float* sRow = reinterpret_cast<float*>(sm + C::OFF_ROW);  // [wg 2][slot 2][lse2 64 | D 64]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* bar_kv = bars + 0;
-  uint64_t* bar_q = bars + 1;       // [2] Q/dO slot loaded
-  uint64_t* bar_qfree = bars + 3;   // [2] Q/dO slot read by every MMA (commit)
+  uint64_t* bar_q = bars + 1;       // [NSLOT] Q/dO slot loaded
+  uint64_t* bar_qfree = bars + 3;   // [NSLOT] Q/dO slot read by every MMA (commit)
   uint64_t* bar_m1 = bars + 5;      // S^T, dP^T ready (commit)
   uint64_t* bar_m2 = bars + 6;      // dV, dK, dQ products done (commit)
   uint64_t* bar_sfree = bars + 7;   // S^T, dP^T read into registers (256 elementwise threads)
   uint64_t* bar_ready = bars + 8;   // P^T and dS^T written, previous dQ read out (256 threads)
-  uint64_t* bar_staged = bars + 9;  // [2] dQ staging slot written (256 threads)
+  uint64_t* bar_staged = bars + 9;  // [2] dQ staging slot written (256 threads); d = 128: slot 0 only, and it
+                                    // also tells the MMA issuer that dQ has left the dP^T columns
   uint64_t* bar_dqfree = bars + 11; // [2] dQ staging slot read by its reduction
   uint64_t* bar_idle = bars + 13;   // every MMA done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
@@ -315,29 +353,35 @@ __global__ void __launch_bounds__(NTHR, 1)
       prefetch_tensormap(&tmG);
       int issued[2] = {0, 0};
       auto load_q = [&](int it) {
-        const int slot = it & 1;
-        mbar_arrive_expect_tx(&bar_q[slot], 2 * BOX);
-        tma_load_4d(sQ + slot * BOX, &tmQ, &bar_q[slot], 0, (it0 + it) * BT, h, b);
-        tma_load_4d(sG + slot * BOX, &tmG, &bar_q[slot], 0, (it0 + it) * BT, h, b);
+        const int slot = it % NSLOT;
+        mbar_arrive_expect_tx(&bar_q[slot], 2 * TILE);
+#pragma unroll
+        for (int x = 0; x < HD / 64; ++x) {
+          tma_load_4d(sQ + slot * TILE + x * BOX, &tmQ, &bar_q[slot], x * 64, (it0 + it) * BT, h, b);
+          tma_load_4d(sG + slot * TILE + x * BOX, &tmG, &bar_q[slot], x * 64, (it0 + it) * BT, h, b);
+        }
         ++issued[slot];
       };
       const bool skip_kv = (p.fault == 2 && blockIdx.x == 0);  // fault injection: K/V never arrive
       if (!skip_kv) {
-        mbar_arrive_expect_tx(bar_kv, 2 * BOX);
-        tma_load_4d(sK, &tmK, bar_kv, 0, k0, h, b);
-        tma_load_4d(sV, &tmV, bar_kv, 0, k0, h, b);
+        mbar_arrive_expect_tx(bar_kv, 2 * TILE);
+#pragma unroll
+        for (int x = 0; x < HD / 64; ++x) {
+          tma_load_4d(sK + x * BOX, &tmK, bar_kv, x * 64, k0, h, b);
+          tma_load_4d(sV + x * BOX, &tmV, bar_kv, x * 64, k0, h, b);
+        }
       }
-      load_q(0);
-      if (nit > 1) load_q(1);
-      for (int it = 0; it + 2 < nit; ++it) {
-        // slot it&1 is free once every MMA of step it has read it
-        if (!wait_abort(&bar_qfree[it & 1], static_cast<uint32_t>((it >> 1) & 1), tmo, abort_flag, kBwdTimeoutLoad, 5))
+      for (int it = 0; it < NSLOT && it < nit; ++it) load_q(it);
+      for (int it = 0; it + NSLOT < nit; ++it) {
+        // slot it % NSLOT is free once every MMA of step it has read it
+        if (!wait_abort(&bar_qfree[it % NSLOT], static_cast<uint32_t>((it / NSLOT) & 1), tmo, abort_flag,
+                        kBwdTimeoutLoad, 5))
           break;
-        load_q(it + 2);
+        load_q(it + NSLOT);
       }
       // every load issued lands before the CTA exits (bounded waits)
       if (!skip_kv) mbar_wait_bounded(bar_kv, 0, tmo);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < NSLOT; ++s)
         if (issued[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued[s] - 1) & 1), tmo);
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
@@ -345,28 +389,41 @@ __global__ void __launch_bounds__(NTHR, 1)
       constexpr uint32_t IDESC_V = idesc_f16(DT, 1, 128, HD);               // dV: A (P^T) in TMEM, B MN-major
       constexpr uint32_t IDESC_Q = idesc_f16(DT, 1, 128, HD) | (1u << 15);  // dQ: A (dS) MN-major
       const bool leader = elect_lane();
-      // descriptors, prepared by the whole warp before any issue
+      // descriptors, prepared by the whole warp before any issue; MN-major operands with N = d reach the
+      // second 64-feature box of d = 128 through the leading-byte offset
+      constexpr uint32_t LBO_MN = HD == 64 ? 1024u : BOX;
       const uint64_t dK_k = smem_desc_sw128(smem_u32(sK), 16, 1024);
       const uint64_t dV_k = smem_desc_sw128(smem_u32(sV), 16, 1024);
-      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 1024, 1024);
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), LBO_MN, 1024);
       const uint64_t dS_k = smem_desc_sw128(smem_u32(sdS), 16, 1024);     // dS^T as K-major A (M = keys)
       const uint64_t dS_mn = smem_desc_sw128(smem_u32(sdS), BOX, 1024);   // dS^T as MN-major A (M = queries)
       const uint64_t dQ0_k = smem_desc_sw128(smem_u32(sQ), 16, 1024);
       const uint64_t dG0_k = smem_desc_sw128(smem_u32(sG), 16, 1024);
-      const uint64_t dQ0_mn = smem_desc_sw128(smem_u32(sQ), 1024, 1024);
-      const uint64_t dG0_mn = smem_desc_sw128(smem_u32(sG), 1024, 1024);
-      constexpr uint32_t SLOT16 = BOX >> 4;  // one slot in descriptor address units
+      const uint64_t dQ0_mn = smem_desc_sw128(smem_u32(sQ), LBO_MN, 1024);
+      const uint64_t dG0_mn = smem_desc_sw128(smem_u32(sG), LBO_MN, 1024);
+      constexpr uint32_t SLOT16 = TILE >> 4;  // one slot in descriptor address units
       auto wait_all = [&](uint64_t* bar, uint32_t parity, int code, int where) -> bool {
         const bool w = wait_abort(bar, parity, tmo, abort_flag, code, where);
         return __all_sync(0xffffffffu, w);
       };
       auto issue_m1 = [&](int it) {
-        const uint32_t so = static_cast<uint32_t>(it & 1) * SLOT16;
+        const uint32_t so = static_cast<uint32_t>(it % NSLOT) * SLOT16;
         tc_fence_after();
         if (leader) {
-          issue_t(tmem + COL_S, dK_k, dQ0_k + so, IDESC_T);
-          issue_t(tmem + COL_DP, dV_k, dG0_k + so, IDESC_T);
+          issue_t<HD>(tmem + C::COL_S, dK_k, dQ0_k + so, IDESC_T);
+          issue_t<HD>(tmem + C::COL_DP, dV_k, dG0_k + so, IDESC_T);
           tc_commit(bar_m1);
+        }
+        __syncwarp();
+      };
+      auto issue_m2 = [&](int it) {
+        const uint32_t so = static_cast<uint32_t>(it % NSLOT) * SLOT16;
+        tc_fence_after();
+        if (leader) {
+          if (it == 0) issue_grads<1, HD>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+          else issue_grads<0, HD>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+          tc_commit(bar_m2);
+          tc_commit(&bar_qfree[it % NSLOT]);
         }
         __syncwarp();
       };
@@ -374,24 +431,26 @@ __global__ void __launch_bounds__(NTHR, 1)
       if (ok) ok = wait_all(&bar_q[0], 0, kBwdTimeoutLoad, 2);
       if (ok) issue_m1(0);
       for (int it = 0; ok && it < nit; ++it) {
-        const int slot = it & 1;
-        if (it + 1 < nit) {
-          // S^T / dP^T of step it are in registers: the next step's products may overwrite them
-          ok = wait_all(bar_sfree, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 6);
-          if (ok) ok = wait_all(&bar_q[(it + 1) & 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), kBwdTimeoutLoad, 2);
-          if (ok) issue_m1(it + 1);
-        }
-        if (ok) ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
-        if (ok) {
-          const uint32_t so = static_cast<uint32_t>(slot) * SLOT16;
-          tc_fence_after();
-          if (leader) {
-            if (it == 0) issue_grads<1>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
-            else issue_grads<0>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
-            tc_commit(bar_m2);
-            tc_commit(&bar_qfree[slot]);
+        if constexpr (HD == 64) {
+          if (it + 1 < nit) {
+            // S^T / dP^T of step it are in registers: the next step's products may overwrite them
+            ok = wait_all(bar_sfree, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 6);
+            if (ok) ok = wait_all(&bar_q[(it + 1) & 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), kBwdTimeoutLoad, 2);
+            if (ok) issue_m1(it + 1);
           }
-          __syncwarp();
+          if (ok) ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
+          if (ok) issue_m2(it);
+        } else {
+          // d = 128: the gradient products of step it first (dV reads P^T from the S^T columns before the
+          // next S^T is issued behind it by this thread); the next step's S^T and dP^T once the single
+          // Q/dO slot holds step it + 1 and dQ of step it has left the dP^T columns
+          ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
+          if (ok) issue_m2(it);
+          if (ok && it + 1 < nit) {
+            ok = wait_all(&bar_staged[0], static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 10);
+            if (ok) ok = wait_all(&bar_q[0], static_cast<uint32_t>((it + 1) & 1), kBwdTimeoutLoad, 2);
+            if (ok) issue_m1(it + 1);
+          }
         }
       }
       if (leader) tc_commit(bar_idle);
@@ -400,12 +459,12 @@ __global__ void __launch_bounds__(NTHR, 1)
     } else if (warp == 2 && lane == 0) {
       // ---------------------------------------------------------------- dQ reductions
       for (int it = 0; it < nit; ++it) {
-        const int slot = it & 1;
-        if (!wait_abort(&bar_staged[slot], static_cast<uint32_t>((it >> 1) & 1), tmo, abort_flag, kBwdTimeoutSoftmax, 8))
-          break;
-        const uint32_t src = smem_u32(sdQ) + static_cast<uint32_t>(slot * DQ_SLOT);
-        tma_reduce_add_3d(src, &tmDQ, 0, (it0 + it) * BT, bh);
-        tma_reduce_add_3d(src + BT * 128, &tmDQ, 32, (it0 + it) * BT, bh);
+        const int slot = HD == 64 ? (it & 1) : 0;
+        const uint32_t par = static_cast<uint32_t>(HD == 64 ? ((it >> 1) & 1) : (it & 1));
+        if (!wait_abort(&bar_staged[slot], par, tmo, abort_flag, kBwdTimeoutSoftmax, 8)) break;
+        const uint32_t src = smem_u32(sdQ) + static_cast<uint32_t>(slot * C::DQ_SLOT);
+#pragma unroll
+        for (int x = 0; x < HD / 32; ++x) tma_reduce_add_3d(src + x * (BT * 128), &tmDQ, 32 * x, (it0 + it) * BT, bh);
         bulk_commit();
         bulk_wait_read_all();
         mbar_arrive(&bar_dqfree[slot]);
@@ -416,7 +475,7 @@ __global__ void __launch_bounds__(NTHR, 1)
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BWD_REGS_HIGH));
     // ------------------------------------------------------------------ elementwise warpgroups
     // warpgroup wg owns query columns [64 wg, 64 wg + 64) of each step, and feature columns
-    // [32 wg, 32 wg + 32) of the dQ, dK and dV read-outs; its warp q owns tensor-memory lanes [32q, 32q + 32)
+    // [d/2 wg, d/2 wg + d/2) of the dQ, dK and dV read-outs; its warp q owns tensor-memory lanes [32q, 32q + 32)
     const int wg = (warp >> 2) - 1;
     const int quarter = warp & 3;
     const int t128 = tid & 127;
@@ -439,24 +498,32 @@ __global__ void __launch_bounds__(NTHR, 1)
     bool ok = wg_bar_and(wg, true);
     // dQ of step it (after its products completed): scaled rows into the staging slot, then hand-off
     auto stage_dq = [&](int it) -> bool {
-      const int slot = it & 1;
-      bool w = true;
-      if (it >= 2) w = wait_abort(&bar_dqfree[slot], static_cast<uint32_t>(((it - 2) >> 1) & 1), tmo, abort_flag,
-                                  kBwdTimeoutSoftmax, 9);
-      w = __all_sync(0xffffffffu, w);
-      if (!w) return false;
-      uint32_t o[32];
-      tmem_ld32(trow + COL_DQ + wg * 32, o);
-      tmem_wait_ld();
-      reg_fence32(o);
-      const uint32_t dst = dq_row + static_cast<uint32_t>(slot * DQ_SLOT);
+      const int slot = HD == 64 ? (it & 1) : 0;
+      if constexpr (HD == 64) {
+        bool w = true;
+        if (it >= 2) w = wait_abort(&bar_dqfree[slot], static_cast<uint32_t>(((it - 2) >> 1) & 1), tmo, abort_flag,
+                                    kBwdTimeoutSoftmax, 9);
+        w = __all_sync(0xffffffffu, w);
+        if (!w) return false;
+      }
+      // (d = 128: the staging area was released before this step's dS^T was written over it)
 #pragma unroll
-      for (int u = 0; u < 8; ++u)
-        st_shared_v4(dst + static_cast<uint32_t>((u ^ sw) * 16), __float_as_uint(__uint_as_float(o[4 * u]) * p.scale),
-                     __float_as_uint(__uint_as_float(o[4 * u + 1]) * p.scale),
-                     __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
-                     __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
+      for (int c = 0; c < HD / 64; ++c) {
+        uint32_t o[32];
+        tmem_ld32(trow + C::COL_DQ + wg * (HD / 2) + c * 32, o);
+        tmem_wait_ld();
+        reg_fence32(o);
+        const uint32_t dst = HD == 64 ? dq_row + static_cast<uint32_t>(slot * C::DQ_SLOT)
+                                      : smem_u32(sdQ) + static_cast<uint32_t>((2 * wg + c) * (BT * 128) + r * 128);
+#pragma unroll
+        for (int u = 0; u < 8; ++u)
+          st_shared_v4(dst + static_cast<uint32_t>((u ^ sw) * 16), __float_as_uint(__uint_as_float(o[4 * u]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
+      }
       fence_proxy_async_smem();
+      if (HD == 128) tc_fence_before();  // dQ has left the dP^T columns the next S^T / dP^T products reuse
       mbar_arrive(&bar_staged[slot]);
       return true;
     };
@@ -487,12 +554,12 @@ __global__ void __launch_bounds__(NTHR, 1)
 #pragma unroll
         for (int c2 = 0; c2 < 2; ++c2) {
           uint32_t s[32], g[32];
-          tmem_ld32(trow + COL_S + wg * 64 + c2 * 32, s);
-          tmem_ld32(trow + COL_DP + wg * 64 + c2 * 32, g);
+          tmem_ld32(trow + C::COL_S + wg * 64 + c2 * 32, s);
+          tmem_ld32(trow + C::COL_DP + wg * 64 + c2 * 32, g);
           tmem_wait_ld();
           reg_fence32(s);
           reg_fence32(g);
-          if (c2 == 1) {
+          if (HD == 64 && c2 == 1) {
             tc_fence_before();
             mbar_arrive(bar_sfree);
           }
@@ -520,18 +587,27 @@ __global__ void __launch_bounds__(NTHR, 1)
           }
         }
       }
-      // P^T and dS^T of the previous step are consumed once its products are done; its dQ is then read out
-      if (ok && it > 0) {
-        ok = wait_abort(bar_m2, static_cast<uint32_t>((it - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
-        ok = __all_sync(0xffffffffu, ok);
-        if (ok) {
-          tc_fence_after();
-          ok = stage_dq(it - 1);
+      if constexpr (HD == 64) {
+        // P^T and dS^T of the previous step are consumed once its products are done; its dQ is then read out
+        if (ok && it > 0) {
+          ok = wait_abort(bar_m2, static_cast<uint32_t>((it - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+            ok = stage_dq(it - 1);
+          }
+        }
+      } else {
+        // the previous step's dQ, staged over the dS^T tile, must have been read by its reduction
+        if (ok && it > 0) {
+          ok = wait_abort(&bar_dqfree[0], static_cast<uint32_t>((it - 1) & 1), tmo, abort_flag, kBwdTimeoutSoftmax, 9);
+          ok = __all_sync(0xffffffffu, ok);
         }
       }
       if (ok) {
-        tmem_st16(trow + COL_PT + wg * 32, &pw[0]);
-        tmem_st16(trow + COL_PT + wg * 32 + 16, &pw[16]);
+        // P^T (d = 128: over the first half of this warpgroup's own S^T columns, already read)
+        tmem_st16(trow + C::col_pt(wg * 4), &pw[0]);
+        tmem_st16(trow + C::col_pt(wg * 4) + 16, &pw[16]);
         // dS^T row r, queries [64 wg, 64 wg + 64): box wg, all eight 16-byte chunks, 128-byte swizzle
 #pragma unroll
         for (int u = 0; u < 8; ++u)
@@ -543,9 +619,20 @@ __global__ void __launch_bounds__(NTHR, 1)
         mbar_arrive(bar_ready);
         rows[(slot ^ 1) * 128 + t128] = nrow;
       }
+      if constexpr (HD == 128) {
+        // this step's dQ, out of the dP^T columns before the next step's products may be issued
+        if (ok) {
+          ok = wait_abort(bar_m2, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
+          ok = __all_sync(0xffffffffu, ok);
+          if (ok) {
+            tc_fence_after();
+            ok = stage_dq(it);
+          }
+        }
+      }
       ok = wg_bar_and(wg, ok);
     }
-    if (ok) {
+    if (HD == 64 && ok) {
       // last step: dQ, then dV_j and dK_j rows (key row = tensor-memory lane), written once
       ok = wait_abort(bar_m2, static_cast<uint32_t>((nit - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
       ok = __all_sync(0xffffffffu, ok);
@@ -554,17 +641,20 @@ __global__ void __launch_bounds__(NTHR, 1)
         ok = stage_dq(nit - 1);
       }
     }
-    if (ok) {
+#pragma unroll
+    for (int c = 0; c < HD / 64; ++c) {
+      if (!ok) break;
+      const int fb = wg * (HD / 2) + c * 32;  // first feature of this chunk
       uint32_t a[32], g[32];
-      tmem_ld32(trow + COL_DV + wg * 32, a);
-      tmem_ld32(trow + COL_DK + wg * 32, g);
+      tmem_ld32(trow + C::COL_DV + fb, a);
+      tmem_ld32(trow + C::COL_DK + fb, g);
       tmem_wait_ld();
       reg_fence32(a);
       reg_fence32(g);
       if (ACCUM && key_ok) {
         const long long row = static_cast<long long>(bh) * Nkv + k0 + r;
-        float4* dv = reinterpret_cast<float4*>(p.dv_acc + row * HD + wg * 32);
-        float4* dk = reinterpret_cast<float4*>(p.dk_acc + row * HD + wg * 32);
+        float4* dv = reinterpret_cast<float4*>(p.dv_acc + row * HD + fb);
+        float4* dk = reinterpret_cast<float4*>(p.dk_acc + row * HD + fb);
 #pragma unroll
         for (int u = 0; u < 8; ++u) {
           atomicAdd(dv + u, make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
@@ -575,8 +665,8 @@ __global__ void __launch_bounds__(NTHR, 1)
         }
       } else if (!ACCUM && key_ok) {
         const long long row = static_cast<long long>(bh) * Nkv + k0 + r;
-        uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + wg * 32);
-        uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + wg * 32);
+        uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + fb);
+        uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + fb);
 #pragma unroll
         for (int u = 0; u < 4; ++u) {
           uint4 wv, wk;
@@ -603,11 +693,13 @@ __global__ void __launch_bounds__(NTHR, 1)
   }
 }
 
-// D_i = dO_i . O_i in fp32: eight threads per 64-feature row, one 16-byte load of each per thread.
-template <int DT>
+// D_i = dO_i . O_i in fp32: d/8 threads per row (8 for d = 64, 16 for d = 128), one 16-byte load of
+// each per thread, summed across the row's threads by shuffles.
+template <int DT, int HD>
 __global__ void __launch_bounds__(256) bwd_dot_kernel(const uint4* o, const uint4* g, float* dvec, long long rows) {
+  constexpr int TPR = HD / 8;
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
-  const long long row = t >> 3;
+  const long long row = t / TPR;
   float acc = 0.0f;
   if (row < rows) {
     const uint4 a = __ldg(o + t), c = __ldg(g + t);
@@ -619,10 +711,9 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const uint4* o, const uint
       acc = fmaf(x.y, y.y, acc);
     }
   }
-  acc += __shfl_xor_sync(0xffffffffu, acc, 4);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 2);
-  acc += __shfl_xor_sync(0xffffffffu, acc, 1);
-  if (row < rows && (t & 7) == 0) dvec[row] = acc;
+#pragma unroll
+  for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
+  if (row < rows && (t % TPR) == 0) dvec[row] = acc;
 }
 
 // fp32 dQ accumulator -> input dtype, four elements per thread.
@@ -664,29 +755,32 @@ int encode_map(CUtensorMap* m, CUtensorMapDataType type, cuuint32_t rank, const 
   return CQSA_OK;
 }
 
-// [B,H,N,64] 16-bit tensor: dims (64, N, H, B), box (64, 128, 1, 1), 128-byte swizzle, zero fill.
-int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N) {
+// [B,H,N,d] 16-bit tensor: dims (d, N, H, B), box (64, 128, 1, 1), 128-byte swizzle, zero fill.
+int make_bhnd_map(CUtensorMap* m, const void* base, int dtype, int B, int H, int N, int d) {
   const cuuint64_t es = 2;
-  const cuuint64_t dims[4] = {HD, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
-  const cuuint64_t strides[3] = {HD * es, static_cast<cuuint64_t>(N) * HD * es,
-                                 static_cast<cuuint64_t>(H) * N * HD * es};
+  const cuuint64_t HDd = static_cast<cuuint64_t>(d);
+  const cuuint64_t dims[4] = {HDd, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[3] = {HDd * es, static_cast<cuuint64_t>(N) * HDd * es,
+                                 static_cast<cuuint64_t>(H) * N * HDd * es};
   const cuuint32_t box[4] = {64, BT, 1, 1};
   return encode_map(m, dtype == CQSA_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 4,
                     base, dims, strides, box);
 }
 
-// fp32 dQ accumulator [BH, N, 64]: dims (64, N, BH), box (32, 128, 1) (128-byte rows), 128-byte swizzle.
-int make_dq_map(CUtensorMap* m, float* base, int BH, int N) {
-  const cuuint64_t dims[3] = {HD, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
-  const cuuint64_t strides[2] = {HD * 4, static_cast<cuuint64_t>(N) * HD * 4};
+// fp32 dQ accumulator [BH, N, d]: dims (d, N, BH), box (32, 128, 1) (128-byte rows), 128-byte swizzle.
+int make_dq_map(CUtensorMap* m, float* base, int BH, int N, int d) {
+  const cuuint64_t HDd = static_cast<cuuint64_t>(d);
+  const cuuint64_t dims[3] = {HDd, static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {HDd * 4, static_cast<cuuint64_t>(N) * HDd * 4};
   const cuuint32_t box[3] = {32, BT, 1};
   return encode_map(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 3, base, dims, strides, box);
 }
 
-template <int DT, bool CAUSAL, int ACCUM>
+template <int DT, bool CAUSAL, int ACCUM, int HD>
 int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
                 const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, cudaStream_t s) {
-  auto kern = attn_bwd_kernel<DT, CAUSAL, ACCUM>;
+  auto kern = attn_bwd_kernel<DT, CAUSAL, ACCUM, HD>;
+  constexpr uint32_t SMEM_BYTES = BwdCfg<HD>::SMEM_BYTES;
   static PerDeviceOnce attr;  // the attributes belong to each device's context
   int dev = 0;
   if (!attr.done(&dev)) {
@@ -708,14 +802,14 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
   return cuda_status(cudaGetLastError(), "attention backward kernel launch");
 }
 
-template <int ACCUM>
+template <int ACCUM, int HD>
 int dispatch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap& mv, const CUtensorMap& mg,
                   const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, int dtype, int causal, cudaStream_t s) {
   if (dtype == CQSA_BF16)
-    return causal ? launch_main<1, true, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
-                  : launch_main<1, false, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
-  return causal ? launch_main<0, true, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
-                : launch_main<0, false, ACCUM>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
+    return causal ? launch_main<1, true, ACCUM, HD>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
+                  : launch_main<1, false, ACCUM, HD>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
+  return causal ? launch_main<0, true, ACCUM, HD>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s)
+                : launch_main<0, false, ACCUM, HD>(mq, mk, mv, mg, mdq, p, n_kv_tiles, s);
 }
 
 // Maps and parameters of one launch of the main kernel (the monolithic call or one chunk pair).
@@ -725,12 +819,16 @@ int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cuda
     set_error("problem too large for one launch");
     return CQSA_ERR_UNSUPPORTED;
   }
+  if (a.d != 64 && a.d != 128) {
+    set_error("the backward supports head dim 64 or 128 (got %d)", a.d);
+    return CQSA_ERR_UNSUPPORTED;
+  }
   CUtensorMap mq, mk, mv, mg, mdq;
-  int rc = make_bhnd_map(&mq, a.q, a.dtype, a.B, a.H, a.Nq);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mk, a.k, a.dtype, a.B, a.H, a.Nkv);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mv, a.v, a.dtype, a.B, a.H, a.Nkv);
-  if (rc == CQSA_OK) rc = make_bhnd_map(&mg, a.dout, a.dtype, a.B, a.H, a.Nq);
-  if (rc == CQSA_OK) rc = make_dq_map(&mdq, dq_acc, a.B * a.H, a.Nq);
+  int rc = make_bhnd_map(&mq, a.q, a.dtype, a.B, a.H, a.Nq, a.d);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mk, a.k, a.dtype, a.B, a.H, a.Nkv, a.d);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mv, a.v, a.dtype, a.B, a.H, a.Nkv, a.d);
+  if (rc == CQSA_OK) rc = make_bhnd_map(&mg, a.dout, a.dtype, a.B, a.H, a.Nq, a.d);
+  if (rc == CQSA_OK) rc = make_dq_map(&mdq, dq_acc, a.B * a.H, a.Nq, a.d);
   if (rc != CQSA_OK) return rc;
   BwdParams p;
   p.lse = a.lse;
@@ -748,7 +846,7 @@ int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cuda
   p.n_kv_tiles = static_cast<int>(n_kv_tiles);
   {
     // per head: the fp32 dQ accumulator and the Q and dO rows streamed past every key tile
-    const long long per_head = static_cast<long long>(a.Nq) * HD * (4 + 2 + 2);
+    const long long per_head = static_cast<long long>(a.Nq) * a.d * (4 + 2 + 2);
     const long long budget = static_cast<long long>(CQSA_BWD_GROUP_MB) << 20;
     const int BH = a.B * a.H;
     long long g = (budget <= 0 || per_head * BH <= budget) ? BH : budget / per_head;
@@ -760,8 +858,12 @@ int run_main(const BwdArgs& a, float* dq_acc, const float* dvec, int accum, cuda
   p.scale_log2 = a.scale * LOG2E;
   p.timeout_ns = timeout_ns();
   p.fault = debug_fault();
-  return accum ? dispatch_main<1>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream)
-               : dispatch_main<0>(mq, mk, mv, mg, mdq, p, static_cast<int>(n_kv_tiles), a.dtype, a.causal, stream);
+  const int nkt = static_cast<int>(n_kv_tiles);
+  if (a.d == 128)
+    return accum ? dispatch_main<1, 128>(mq, mk, mv, mg, mdq, p, nkt, a.dtype, a.causal, stream)
+                 : dispatch_main<0, 128>(mq, mk, mv, mg, mdq, p, nkt, a.dtype, a.causal, stream);
+  return accum ? dispatch_main<1, 64>(mq, mk, mv, mg, mdq, p, nkt, a.dtype, a.causal, stream)
+               : dispatch_main<0, 64>(mq, mk, mv, mg, mdq, p, nkt, a.dtype, a.causal, stream);
 }
 
 }  // namespace
@@ -772,16 +874,20 @@ size_t attention_bwd_workspace(int B, int H, int N, int d) {
   return dq + rows * sizeof(float);
 }
 
-int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int dtype, cudaStream_t stream) {
+int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int d, int dtype,
+                    cudaStream_t stream) {
   if (rows <= 0) return CQSA_OK;
-  const long long dot_threads = rows * 8;
+  const long long dot_threads = rows * (d / 8);
   const unsigned dot_blocks = static_cast<unsigned>((dot_threads + 255) / 256);
-  if (dtype == CQSA_BF16)
-    bwd_dot_kernel<1><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
-                                                      dvec, rows);
-  else
-    bwd_dot_kernel<0><<<dot_blocks, 256, 0, stream>>>(static_cast<const uint4*>(out), static_cast<const uint4*>(dout),
-                                                      dvec, rows);
+  const uint4* o = static_cast<const uint4*>(out);
+  const uint4* g = static_cast<const uint4*>(dout);
+  if (d == 128) {
+    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+    else bwd_dot_kernel<0, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+  } else {
+    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+    else bwd_dot_kernel<0, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+  }
   return cuda_status(cudaGetLastError(), "attention backward dot kernel launch");
 }
 
@@ -800,16 +906,16 @@ int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream) {
   const long long rows = static_cast<long long>(a.B) * a.H * a.Nq;
   float* dq_acc = static_cast<float*>(a.workspace);
   float* dvec = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) +
-                                         ((static_cast<size_t>(rows) * HD * sizeof(float) + 255) & ~size_t(255)));
+                                         ((static_cast<size_t>(rows) * a.d * sizeof(float) + 255) & ~size_t(255)));
   // D_i, then the zeroed dQ accumulator, the main kernel and the dQ conversion
-  int rc = launch_bwd_dvec(a.out, a.dout, dvec, rows, a.dtype, stream);
+  int rc = launch_bwd_dvec(a.out, a.dout, dvec, rows, a.d, a.dtype, stream);
   if (rc != CQSA_OK) return rc;
-  rc = cuda_status(cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * HD * sizeof(float), stream),
+  rc = cuda_status(cudaMemsetAsync(dq_acc, 0, static_cast<size_t>(rows) * a.d * sizeof(float), stream),
                    "zero dQ accumulator");
   if (rc != CQSA_OK) return rc;
   rc = run_main(a, dq_acc, dvec, 0, stream);
   if (rc != CQSA_OK) return rc;
-  return launch_bwd_cast(dq_acc, a.dq, rows * HD, a.dtype, stream);
+  return launch_bwd_cast(dq_acc, a.dq, rows * a.d, a.dtype, stream);
 }
 
 int launch_attention_bwd_chunk(const BwdArgs& a, cudaStream_t stream) {

@@ -79,7 +79,8 @@ size_t attention_bwd_workspace(int B, int H, int N, int d);
 int launch_attention_bwd(const BwdArgs& a, cudaStream_t stream);
 int launch_attention_bwd_chunk(const BwdArgs& a, cudaStream_t stream);
 // D_i = dout_i . out_i (fp32) for `rows` rows of 64 features; fp32 -> dtype for n elements (n % 4 == 0).
-int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int dtype, cudaStream_t stream);
+int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int d, int dtype,
+                    cudaStream_t stream);
 int launch_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream);
 
 // LSE merge of n partials (device pointer arrays passed by value).

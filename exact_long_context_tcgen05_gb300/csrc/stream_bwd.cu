@@ -13,7 +13,7 @@
 // one query chunk is not copied again for the next; each pair adds into dq and into that key chunk's
 // fp32 dk / dv accumulators. dq is rounded to the input dtype into one of two staging buffers and leaves
 // on a second stream; once every query chunk is done, dk and dv of each key chunk follow the same way.
-// Device memory: the dk / dv accumulators of the whole sequence (2 * B*H*N*64 * 4 bytes) plus two slots
+// Device memory: the dk / dv accumulators of the whole sequence (2 * B*H*N*d * 4 bytes) plus two slots
 // of each streamed chunk.
 #include <math.h>
 #include <string.h>
@@ -31,12 +31,12 @@
 namespace cqsa {
 namespace {
 
-// A packed [B,H,n,64] device chunk into tokens [t0, t0 + n) of a [B,H,N,64] host tensor (16-bit).
-cudaError_t copy_chunk_out(void* host, const void* dev, int B, int H, long long N, long long t0, int n,
+// A packed [B,H,n,d] device chunk into tokens [t0, t0 + n) of a [B,H,N,d] host tensor (16-bit).
+cudaError_t copy_chunk_out(void* host, const void* dev, int B, int H, long long N, int d, long long t0, int n,
                            cudaStream_t s) {
-  const size_t row = static_cast<size_t>(n) * 64 * 2;
-  char* dst = static_cast<char*>(host) + static_cast<size_t>(t0) * 64 * 2;
-  return cudaMemcpy2DAsync(dst, static_cast<size_t>(N) * 64 * 2, dev, row, row, static_cast<size_t>(B) * H,
+  const size_t row = static_cast<size_t>(n) * d * 2;
+  char* dst = static_cast<char*>(host) + static_cast<size_t>(t0) * d * 2;
+  return cudaMemcpy2DAsync(dst, static_cast<size_t>(N) * d * 2, dev, row, row, static_cast<size_t>(B) * H,
                            cudaMemcpyDeviceToHost, s);
 }
 
@@ -56,12 +56,12 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
     set_error("sizes must be positive (B=%d H=%d N=%lld)", B, H, N);
     return CQSA_ERR_INVALID;
   }
-  if (d != 64) {
-    set_error("the backward supports head dim 64 (got %d)", d);
-    return CQSA_ERR_UNSUPPORTED;
-  }
   if (dtype != CQSA_F16 && dtype != CQSA_BF16) {
     set_error("dtype %d is not supported (fp16 or bf16)", dtype);
+    return CQSA_ERR_UNSUPPORTED;
+  }
+  if (d != 64 && d != 128) {
+    set_error("the backward supports head dim 64 or 128 (got %d)", d);
     return CQSA_ERR_UNSUPPORTED;
   }
   if (chunk_tokens < 128 || chunk_tokens % 128 != 0) {
@@ -73,16 +73,16 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
     return CQSA_ERR_INVALID;
   }
   const long long C = chunk_tokens < N ? chunk_tokens : N;
-  if (static_cast<long long>(B) * H * C > (1LL << 31) / 64 || N > 0x7fffffffLL) {
+  if (static_cast<long long>(B) * H * C > (1LL << 31) / d || N > 0x7fffffffLL) {
     set_error("B*H*chunk_tokens too large for one chunk launch");
     return CQSA_ERR_UNSUPPORTED;
   }
   const int n_chunks = static_cast<int>((N + C - 1) / C);
   const size_t BH = static_cast<size_t>(B) * H;
-  const size_t chunk16 = BH * static_cast<size_t>(C) * 64 * 2;  // one 16-bit chunk
-  const size_t chunk32 = BH * static_cast<size_t>(C) * 64 * 4;  // one fp32 chunk
+  const size_t chunk16 = BH * static_cast<size_t>(C) * d * 2;  // one 16-bit chunk
+  const size_t chunk32 = BH * static_cast<size_t>(C) * d * 4;  // one fp32 chunk
   const size_t rows32 = BH * static_cast<size_t>(C) * 4;
-  const float sc = scale == 0.0f ? 0.125f : scale;  // 1/sqrt(64)
+  const float sc = scale == 0.0f ? 1.0f / sqrtf(static_cast<float>(d)) : scale;
 
   // Device memory: the dk / dv accumulators of every key chunk, and two slots of everything that
   // streams: the query side (q, out, dout, lse, D, the dq accumulator), the key side (k, v) and the
@@ -144,15 +144,15 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
 
   long long bytes = 0;
   int out_slot = 0;  // output staging slots alternate over every chunk written out (dq, then dk, dv)
-  // A 16-bit [B,H,n,64] result into staging slot out_slot (after its previous D2H), then to host rows [t0, t0+n).
+  // A 16-bit [B,H,n,d] result into staging slot out_slot (after its previous D2H), then to host rows [t0, t0+n).
   auto write_out = [&](const float* acc, void* host, long long t0, int n) {
     const int os = out_slot;
     out_slot ^= 1;
     if (o_free_set[os]) CQSA_STEP(cudaStreamWaitEvent(stream, o_free[os], 0), "wait staging");
-    if (rc == CQSA_OK) rc = launch_bwd_cast(acc, ostage[os], static_cast<long long>(BH) * n * 64, dtype, stream);
+    if (rc == CQSA_OK) rc = launch_bwd_cast(acc, ostage[os], static_cast<long long>(BH) * n * d, dtype, stream);
     CQSA_STEP(cudaEventRecord(o_ready[os], stream), "record");
     CQSA_STEP(cudaStreamWaitEvent(d2h, o_ready[os], 0), "wait cast");
-    CQSA_STEP(copy_chunk_out(host, ostage[os], B, H, N, t0, n, d2h), "copy out");
+    CQSA_STEP(copy_chunk_out(host, ostage[os], B, H, N, d, t0, n, d2h), "copy out");
     CQSA_STEP(cudaEventRecord(o_free[os], d2h), "record");
     o_free_set[os] = true;
   };
@@ -167,16 +167,16 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
     const QSlot& Q = qsl[qi & 1];
     // the query side of chunk qi - 2 is done with this slot
     if (q_free_set[qi & 1]) CQSA_STEP(cudaStreamWaitEvent(copy, q_free[qi & 1], 0), "wait q slot");
-    CQSA_STEP(copy_chunk(Q.q, q, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy q");
-    CQSA_STEP(copy_chunk(Q.out, out, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy out");
-    CQSA_STEP(copy_chunk(Q.g, dout, CQSA_LAYOUT_BHND, B, H, N, 64, qs, nq, h2d, copy, &bytes), "copy dout");
+    CQSA_STEP(copy_chunk(Q.q, q, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy q");
+    CQSA_STEP(copy_chunk(Q.out, out, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy out");
+    CQSA_STEP(copy_chunk(Q.g, dout, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy dout");
     CQSA_STEP(cudaMemcpy2DAsync(Q.lse, static_cast<size_t>(nq) * 4, lse + qs, static_cast<size_t>(N) * 4,
                                 static_cast<size_t>(nq) * 4, BH, h2d, copy),
               "copy lse");
     CQSA_STEP(cudaEventRecord(q_ready[qi & 1], copy), "record");
     CQSA_STEP(cudaStreamWaitEvent(stream, q_ready[qi & 1], 0), "wait q");
-    if (rc == CQSA_OK) rc = launch_bwd_dvec(Q.out, Q.g, Q.dvec, static_cast<long long>(BH) * nq, dtype, stream);
-    CQSA_STEP(cudaMemsetAsync(Q.dq, 0, BH * static_cast<size_t>(nq) * 64 * 4, stream), "zero dq accumulator");
+    if (rc == CQSA_OK) rc = launch_bwd_dvec(Q.out, Q.g, Q.dvec, static_cast<long long>(BH) * nq, d, dtype, stream);
+    CQSA_STEP(cudaMemsetAsync(Q.dq, 0, BH * static_cast<size_t>(nq) * d * 4, stream), "zero dq accumulator");
     // key chunks this query chunk needs (every chunk, or those at or before its last token when causal),
     // in alternating directions, so the chunk that ends one query chunk starts the next one
     int last = n_chunks - 1;
@@ -189,8 +189,8 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
       if (slot < 0) {
         slot = next_kv;
         if (kv_free_set[slot]) CQSA_STEP(cudaStreamWaitEvent(copy, kv_free[slot], 0), "wait kv slot");
-        CQSA_STEP(copy_chunk(ksl[slot].k, k, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, copy, &bytes), "copy k");
-        CQSA_STEP(copy_chunk(ksl[slot].v, v, CQSA_LAYOUT_BHND, B, H, N, 64, ks, nk, h2d, copy, &bytes), "copy v");
+        CQSA_STEP(copy_chunk(ksl[slot].k, k, CQSA_LAYOUT_BHND, B, H, N, d, ks, nk, h2d, copy, &bytes), "copy k");
+        CQSA_STEP(copy_chunk(ksl[slot].v, v, CQSA_LAYOUT_BHND, B, H, N, d, ks, nk, h2d, copy, &bytes), "copy v");
         CQSA_STEP(cudaEventRecord(kv_ready[slot], copy), "record");
         kv_chunk[slot] = ki;
       }
@@ -212,7 +212,7 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
       a.H = H;
       a.Nq = nq;
       a.Nkv = nk;
-      a.d = 64;
+      a.d = d;
       a.q_off = qs;
       a.kv_off = ks;
       a.causal = causal != 0;

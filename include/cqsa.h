@@ -213,12 +213,12 @@ int cqsa_release_cache(void);
  *   P_ij = exp(s_ij - lse_i) on A_i (0 elsewhere),  D_i = dout_i . out_i,  dP_ij = dout_i . v_j,
  *   dS_ij = P_ij (dP_ij - D_i),  dv_j = sum_i P_ij dout_i,  dk_j = scale sum_i dS_ij q_i,
  *   dq_i = scale sum_j dS_ij k_j.
- * q, k, v, out (the forward's output), dout: device [B,H,N,64], fp16 or bf16 (dtype), contiguous
- * (layout BHND); lse: device [B,H,N] fp32 as cqsa_attn_fwd wrote it (natural log). dq, dk, dv:
- * device [B,H,N,64] in dtype, written in full. P and dS enter the tensor-core products rounded to
+ * q, k, v, out (the forward's output), dout: device [B,H,N,d], d = 64 or 128, fp16 or bf16 (dtype),
+ * contiguous (layout BHND); lse: device [B,H,N] fp32 as cqsa_attn_fwd wrote it (natural log). dq, dk,
+ * dv: device [B,H,N,d] in dtype, written in full. P and dS enter the tensor-core products rounded to
  * dtype; all sums are fp32. workspace: caller-owned device memory of at least
  * cqsa_attn_bwd_workspace_size(B, H, N, d) bytes (the fp32 dq accumulator and D), 16-byte aligned;
- * its contents on entry do not matter. Head dimension 64 only (CQSA_ERR_UNSUPPORTED otherwise).
+ * its contents on entry do not matter. Other head dimensions return CQSA_ERR_UNSUPPORTED.
  * Asynchronous on `stream`; allocates nothing. Runs are bitwise reproducible except dq, whose fp32
  * accumulation order across key tiles follows the atomic adds (differences of a few fp32 ulps
  * before the final rounding to dtype).
@@ -235,14 +235,14 @@ int cqsa_attn_bwd(const void* q, const void* k, const void* v, const void* out, 
  * against the full-row lse, so accumulating every needed pair gives the monolithic gradient up to the
  * fp32 summation order.
  *
- * cqsa_attn_bwd_dvec: D_i = dout_i . out_i (fp32) of a query chunk: out_blk, dout_blk [B,H,Nq,64]
+ * cqsa_attn_bwd_dvec: D_i = dout_i . out_i (fp32) of a query chunk: out_blk, dout_blk [B,H,Nq,d]
  *   (dtype), dvec_blk [B,H,Nq] fp32. out is the forward's full output for those rows.
- * cqsa_attn_bwd_chunk: one pair. q_blk, dout_blk [B,H,Nq,64] with lse_blk (the forward's full-row lse)
- *   and dvec_blk [B,H,Nq] of the query chunk at absolute position q_off; k_blk, v_blk [B,H,Nkv,64] of
+ * cqsa_attn_bwd_chunk: one pair. q_blk, dout_blk [B,H,Nq,d] with lse_blk (the forward's full-row lse)
+ *   and dvec_blk [B,H,Nq] of the query chunk at absolute position q_off; k_blk, v_blk [B,H,Nkv,d] of
  *   the key chunk at kv_off (causal masking on absolute positions; a pair with every key after every
- *   query adds nothing). Adds scale * dS K into dq_acc [B,H,Nq,64], scale * dS^T Q into dk_acc and
- *   P^T dout into dv_acc [B,H,Nkv,64], all fp32, which the caller zeroes before its first pair and
- *   keeps until its last; pairs on one stream may share accumulators. Head dim 64; asynchronous;
+ *   query adds nothing). Adds scale * dS K into dq_acc [B,H,Nq,d], scale * dS^T Q into dk_acc and
+ *   P^T dout into dv_acc [B,H,Nkv,d], all fp32, which the caller zeroes before its first pair and
+ *   keeps until its last; pairs on one stream may share accumulators. d = 64 or 128; asynchronous;
  *   allocates nothing.
  * cqsa_attn_bwd_cast: n fp32 values (n a multiple of 4) rounded to dtype (RNE), e.g. the accumulators
  *   into dq, dk, dv.
@@ -257,13 +257,13 @@ int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cuda
 
 /*
  * Host-resident backward over chunk pairs (the pages' streamed backward, `stream_cqsa_backward`): q, k,
- * v, out, dout [B,H,N,64] (fp16/bf16, layout BHND) and lse [B,H,N] fp32 in host memory (pinned for
- * speed); dq, dk, dv [B,H,N,64] written to host memory. Query-outer over chunks of chunk_tokens (a
+ * v, out, dout [B,H,N,d] (d = 64 or 128, fp16/bf16, layout BHND) and lse [B,H,N] fp32 in host memory
+ * (pinned for speed); dq, dk, dv [B,H,N,d] written to host memory. Query-outer over chunks of chunk_tokens (a
  * positive multiple of 128): each query chunk's q/out/dout/lse and each needed key chunk's k/v are
  * copied to the device on a copy stream, double-buffered so copies overlap the kernels, the key chunks
  * in alternating directions so consecutive query chunks share one copy; each pair runs
  * cqsa_attn_bwd_chunk's kernel on `stream`; dq leaves after its query chunk, dk and dv after the last
- * one, on a second stream. Device memory: 2 * B*H*N*64*4 bytes of dk/dv accumulators plus two slots of
+ * one, on a second stream. Device memory: 2 * B*H*N*d*4 bytes of dk/dv accumulators plus two slots of
  * each streamed chunk (inputs, D, lse, the dq accumulator, output staging), from the library's pool
  * (CQSA_ERR_OOM if they do not fit). Synchronous; the result equals cqsa_attn_bwd's up to the fp32
  * summation order. Returns CQSA_ERR_TIMEOUT if a kernel's bounded wait gave up.

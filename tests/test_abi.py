@@ -141,7 +141,7 @@ def test_bwd_validation(cq):
     def call(d=64, ws_bytes=need, q=FAKE, lse=FAKE, dtype=cq.CQSA_F16):
         return L.cqsa_attn_bwd(q, FAKE, FAKE, FAKE, FAKE, lse, FAKE, FAKE, FAKE, FAKE, ws_bytes, 1, 2, 256, d, 1, 0.0,
                                dtype, None)
-    assert call(d=128) == cq.CQSA_ERR_UNSUPPORTED and "head dim 64" in cq.last_error()
+    assert call(d=96) == cq.CQSA_ERR_UNSUPPORTED and "head dim" in cq.last_error()
     assert call(ws_bytes=need - 16) == cq.CQSA_ERR_INVALID and "workspace" in cq.last_error()
     assert call(q=None) == cq.CQSA_ERR_INVALID
     assert call(q=FAKE + 8) == cq.CQSA_ERR_INVALID and "aligned" in cq.last_error()
@@ -159,12 +159,12 @@ def test_bwd_chunk_validation(cq):
         return L.cqsa_attn_bwd_chunk(a["q"], a["k"], a["v"], a["g"], a["lse"], a["dvec"], a["qo"], a["ko"], a["B"],
                                      a["H"], a["Nq"], a["Nkv"], a["d"], a["c"], a["s"], a["dt"], a["dq"], a["dk"],
                                      a["dv"], None)
-    assert call(d=128) == cq.CQSA_ERR_UNSUPPORTED
+    assert call(d=96) == cq.CQSA_ERR_UNSUPPORTED
     assert call(qo=-1) == cq.CQSA_ERR_INVALID
     assert call(dk=None) == cq.CQSA_ERR_INVALID
     assert call(dv=FAKE + 4) == cq.CQSA_ERR_INVALID
     assert call(Nkv=0) == cq.CQSA_ERR_INVALID
-    assert L.cqsa_attn_bwd_dvec(FAKE, FAKE, FAKE, 1, 1, 128, 128, cq.CQSA_F16, None) == cq.CQSA_ERR_UNSUPPORTED
+    assert L.cqsa_attn_bwd_dvec(FAKE, FAKE, FAKE, 1, 1, 128, 96, cq.CQSA_F16, None) == cq.CQSA_ERR_UNSUPPORTED
     assert L.cqsa_attn_bwd_dvec(FAKE, FAKE + 8, FAKE, 1, 1, 128, 64, cq.CQSA_F16, None) == cq.CQSA_ERR_INVALID
     assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 6, cq.CQSA_F16, None) == cq.CQSA_ERR_INVALID
     assert L.cqsa_attn_bwd_cast(FAKE, FAKE, 8, cq.CQSA_F32, None) == cq.CQSA_ERR_UNSUPPORTED
@@ -177,6 +177,6 @@ def test_stream_bwd_validation(cq):
         kw.get("q", FAKE), FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, FAKE, 1, 1, kw.get("N", 1000), kw.get("d", 64), 1,
         0.0, cq.CQSA_F16, kw.get("C", 256), None)
     assert f(C=100) == cq.CQSA_ERR_INVALID
-    assert f(d=128) == cq.CQSA_ERR_UNSUPPORTED
+    assert f(d=96) == cq.CQSA_ERR_UNSUPPORTED and "head dim" in cq.last_error()
     assert f(q=None) == cq.CQSA_ERR_INVALID
     assert f(N=0) == cq.CQSA_ERR_INVALID

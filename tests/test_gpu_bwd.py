@@ -50,23 +50,27 @@ def _check(got: np.ndarray, ref: np.ndarray, dtype, what):
     return mx / ref_max, mn / ref_mean
 
 
-@pytest.mark.parametrize("B,H,N,causal,dtype", [
-    (1, 2, 1024, True, syn.F16),     # several tiles, diagonal masking
-    (1, 2, 640, False, syn.F16),
-    (2, 3, 333, True, syn.F16),      # ragged last tile, several heads and batches
-    (1, 2, 200, False, syn.F16),
-    (1, 1, 77, True, syn.F16),       # one partial tile
-    (1, 2, 512, True, syn.BF16),
-    (1, 1, 384, False, syn.BF16),
+@pytest.mark.parametrize("B,H,N,d,causal,dtype", [
+    (1, 2, 1024, 64, True, syn.F16),     # several tiles, diagonal masking
+    (1, 2, 640, 64, False, syn.F16),
+    (2, 3, 333, 64, True, syn.F16),      # ragged last tile, several heads and batches
+    (1, 2, 200, 64, False, syn.F16),
+    (1, 1, 77, 64, True, syn.F16),       # one partial tile
+    (1, 2, 512, 64, True, syn.BF16),
+    (1, 1, 384, 64, False, syn.BF16),
+    (1, 2, 640, 128, True, syn.F16),     # head dim 128: one Q/dO slot, dQ staged over dS^T
+    (2, 2, 333, 128, False, syn.F16),    # ragged, several heads and batches
+    (1, 1, 77, 128, True, syn.F16),      # one partial tile
+    (1, 2, 512, 128, True, syn.BF16),
+    (1, 1, 384, 128, False, syn.BF16),
 ])
-def test_backward_matches_oracle(cq, B, H, N, causal, dtype):
-    d = 64
+def test_backward_matches_oracle(cq, B, H, N, d, causal, dtype):
     (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, B, H, N, d, causal, dtype)
     ref = oracle.attn_bwd(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=causal, dtype=dtype)
     rel = {}
     for name, t in (("dq", dq), ("dk", dk), ("dv", dv)):
         rel[name] = _check(to_np64(t), ref[name], dtype, f"{name} N={N} causal={causal}")
-    print(f"\nbwd N={N} causal={causal} dtype={dtype}: " +
+    print(f"\nbwd N={N} d={d} causal={causal} dtype={dtype}: " +
           ", ".join(f"{n} max/maxref {a:.2e} mean/meanref {b:.2e}" for n, (a, b) in rel.items()))
 
 
@@ -92,12 +96,12 @@ def test_dk_dv_bitwise_reproducible(cq):
     assert float((dq1.float() - dq2.float()).abs().max()) <= 2.0 ** -10 * float(dq1.float().abs().max())
 
 
-@pytest.mark.parametrize("causal", [True, False])
-def test_sum_identities_large(cq, causal):
+@pytest.mark.parametrize("causal,d", [(True, 64), (False, 64), (True, 128)])
+def test_sum_identities_large(cq, causal, d):
     """At a size the oracle cannot evaluate in full (8 heads x 8,192 tokens), two identities that hold
     for any inputs: sum_j dk_j = 0 (keys shifted together leave the softmax unchanged) and
     sum_j dv_j = sum_i dout_i (every P row sums to one)."""
-    B, H, N, d = 1, 8, 8192, 64
+    B, H, N = 1, 8, 8192
     (qn, kn, vn, gn), (dq, dk, dv) = _run(cq, B, H, N, d, causal, syn.F16, seed=2)
     dk64, dv64 = to_np64(dk), to_np64(dv)
     g64 = oracle.widen(gn).reshape(B, H, N, d)
@@ -132,6 +136,32 @@ def test_backward_32k_sampled_vs_oracle(cq):
           ", ".join(f"{n} max/maxref {a:.2e} mean/meanref {b:.2e}" for n, (a, b) in rel.items()))
 
 
+def test_backward_d128_8k_sampled_vs_oracle(cq):
+    """Head dim 128 at 8,192 tokens (B=1 H=4 bf16 non-causal, K scaled by 3 for peaked rows) against the
+    FP64 oracle on 512 sampled query rows (dq) and 128 sampled key columns of two heads (dk, dv)."""
+    B, H, N, d, dtype = 1, 4, 8192, 128, syn.BF16
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=7, dtype=dtype, k_mul=3.0)
+    gn = syn.normal(B, H, N, d, seed=7, tensor_id=syn.TID_DO, dtype=dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, False, dtype)
+    dq, dk, dv = cq.attention_backward(q, k, v, out, g, lse, causal=False)
+    torch.cuda.synchronize()
+    rc, code, _ = cq.cqsa_device_error()
+    assert rc == cq.CQSA_OK and code == 0
+    rows = syn.sample_rows(B, H, N, 512, seed=8)
+    js = syn.sample_rows(1, 1, N, 64, seed=9, must_i=(0, N - 1, N // 2))[:, 2]
+    cols = np.concatenate([np.stack([np.zeros_like(js), np.full_like(js, hh), js], axis=1) for hh in (0, H - 1)])
+
+    def gather(t, idx):
+        return to_np64(t[torch.as_tensor(idx[:, 0]), torch.as_tensor(idx[:, 1]), torch.as_tensor(idx[:, 2])])
+
+    ref_dq = oracle.attn_bwd_rows(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=False, rows=rows, dtype=dtype)
+    ref_dk, ref_dv = oracle.attn_bwd_cols(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=False, cols=cols, dtype=dtype)
+    for name, got, ref in (("dq", gather(dq, rows), ref_dq), ("dk", gather(dk, cols), ref_dk),
+                           ("dv", gather(dv, cols), ref_dv)):
+        _check(got, ref, dtype, f"8K d=128 {name}")
+
+
 def _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype, skip_masked=True):
     """The backward over (query chunk, key chunk) pairs of C tokens through cqsa_attn_bwd_chunk, with
     per-chunk fp32 accumulators cast to dtype at the end."""
@@ -164,15 +194,17 @@ def _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype, sk
     return res
 
 
-@pytest.mark.parametrize("N,C,causal,dtype", [
-    (768, 256, True, syn.F16),    # 3 x 3 chunks of two tiles, 6 causal pairs
-    (640, 200, True, syn.F16),    # chunks not aligned to the 128-token tiles, ragged last chunk
-    (512, 192, False, syn.BF16),  # every pair
+@pytest.mark.parametrize("N,C,causal,dtype,d", [
+    (768, 256, True, syn.F16, 64),    # 3 x 3 chunks of two tiles, 6 causal pairs
+    (640, 200, True, syn.F16, 64),    # chunks not aligned to the 128-token tiles, ragged last chunk
+    (512, 192, False, syn.BF16, 64),  # every pair
+    (640, 200, True, syn.F16, 128),
+    (512, 256, False, syn.BF16, 128),
 ])
-def test_chunked_backward(cq, N, C, causal, dtype):
+def test_chunked_backward(cq, N, C, causal, dtype, d):
     """Accumulating every chunk pair gives the oracle's gradients (same tolerance as the monolithic
     call) and the monolithic call's, within a few ulps of dtype (fp32 summation order differs)."""
-    B, H, d = 1, 2, 64
+    B, H = 1, 2
     (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, causal, dtype)
     q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
     out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
@@ -204,11 +236,12 @@ def test_chunk_pair_above_diagonal_adds_nothing(cq):
     assert all(bool((a == 0.5).all()) for a in accs)
 
 
-@pytest.mark.parametrize("B,H,N,C,causal", [(2, 2, 640, 256, True), (1, 2, 384, 128, False)])
-def test_stream_backward(cq, B, H, N, C, causal):
+@pytest.mark.parametrize("B,H,N,C,causal,d", [(2, 2, 640, 256, True, 64), (1, 2, 384, 128, False, 64),
+                                             (1, 2, 640, 256, True, 128)])
+def test_stream_backward(cq, B, H, N, C, causal, d):
     """Host-resident backward over chunks (ragged last chunk, several batches and heads): equal to the
     monolithic device call within a few ulps (fp32 summation order differs)."""
-    d, dtype = 64, syn.F16
+    dtype = syn.F16
     (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, causal, dtype)
     q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
     out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
