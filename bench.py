@@ -656,22 +656,29 @@ def measure_stream_bwd(cq, dev, N=131072, C=16384, H=8):
     grads = [torch.empty((B, H, N, D), dtype=torch.float16).pin_memory() for _ in range(3)]
 
     def host_step():
-        cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, D, True, 0.0, cq.CQSA_F16, C, stream)
+        return cq.cqsa_stream_attn_bwd_ex(*host, *grads, B, H, N, D, True, 0.0, cq.CQSA_F16, C, None, stream)
 
     host_step()
-    walls = []
+    runs = []
     for _ in range(3):
         torch.cuda.synchronize()
         t0 = time.perf_counter()
-        host_step()
-        walls.append(time.perf_counter() - t0)
-    wall = statistics.median(walls)
+        st = host_step()
+        runs.append((time.perf_counter() - t0, st))
+    runs.sort(key=lambda r: r[0])
+    wall, st = runs[len(runs) // 2]
     flop = 2.5 * 4.0 * B * H * N * N * D / 2
+    comp_s = st.compute_ms / 1e3
     return {"measure": "stream_bwd", "workload": f"host-resident backward, B=1 H={H} N={N} d=64 fp16 causal, "
             f"{C}-token chunks, pinned host tensors", "wall_s": wall, "tflops": flop / wall / 1e12,
+            "compute_s": comp_s, "wall_over_compute": wall / comp_s if comp_s > 0 else None,
+            "stall_ms": st.stall_ms, "h2d_bytes": st.h2d_bytes, "d2h_bytes": st.d2h_bytes,
+            "copy_gbs": st.h2d_bytes / (st.h2d_ms / 1e3) / 1e9 if st.h2d_ms > 0 else None,
+            "n_pairs": st.n_chunks, "peak_device_bytes": st.peak_device_bytes,
             "device_resident_ms": dev_ms, "device_resident_tflops": flop / (dev_ms / 1e3) / 1e12,
             "wall_over_device_resident": wall / (dev_ms / 1e3),
-            "h2d_bytes_min": int(5 * B * H * N * D * 2 + B * H * N * 4)}
+            "note": "compute_s sums the call's own kernel segments (D, zeroing, 36 chunk pairs, output casts); "
+                    "the chunk-pair kernels run below the monolithic call's rate"}
 
 
 def _numa_nodes(t, samples=64):
@@ -797,7 +804,8 @@ def run_measure(args):
         line = measure_quorum(cq, dev, args.n, acc_on_host=args.acc_on_host, npar=args.max_parallel,
                               engine=args.engine, device_inputs=args.device_inputs)
     elif args.measure == "bwd":
-        line = measure_bwd(cq, dev, reps, N=args.bwd_n, H=args.bwd_h)
+        line = measure_bwd(cq, dev, reps, N=args.bwd_n, H=args.bwd_h, B=args.bwd_b, D=args.bwd_d,
+                           causal=not args.bwd_noncausal, bf16=args.bwd_bf16, k_mul=args.bwd_kmul)
     elif args.measure == "stream-bwd":
         line = measure_stream_bwd(cq, dev)
     elif args.measure == "copy-series":
@@ -827,6 +835,11 @@ def main():
     ap.add_argument("--device-inputs", action="store_true", help="--measure quorum: device-resident Q/K/V/out")
     ap.add_argument("--bwd-n", type=int, default=32768, help="--measure bwd: tokens")
     ap.add_argument("--bwd-h", type=int, default=8, help="--measure bwd: heads")
+    ap.add_argument("--bwd-b", type=int, default=1, help="--measure bwd: batch")
+    ap.add_argument("--bwd-d", type=int, default=64, choices=(64, 128), help="--measure bwd: head dim")
+    ap.add_argument("--bwd-bf16", action="store_true", help="--measure bwd: bf16 instead of fp16")
+    ap.add_argument("--bwd-noncausal", action="store_true", help="--measure bwd: no causal mask")
+    ap.add_argument("--bwd-kmul", type=float, default=1.0, help="--measure bwd: scale of K (peaked rows)")
     ap.add_argument("--secondary", choices=("all", "fast", "none"), default="all",
                     help="secondary lines in the headline JSON: all, fast (no host-streaming workload), none")
     args = ap.parse_args()

@@ -23,7 +23,7 @@ CQSA_ENGINE_CLASSIC, CQSA_ENGINE_WAVE = 0, 1
 EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa_stream_attn_fwd",
             "cqsa_attn_fwd_chunked_static", "cqsa_quorum_check", "cqsa_quorum_schedule", "cqsa_quorum_attn_fwd",
             "cqsa_quorum_attn_fwd_ex", "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd", "cqsa_attn_bwd_dvec",
-            "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast", "cqsa_stream_attn_bwd",
+            "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast", "cqsa_stream_attn_bwd", "cqsa_stream_attn_bwd_ex",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
             "cqsa_debug_set_fault", "cqsa_version")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
@@ -86,6 +86,8 @@ def _load() -> ctypes.CDLL:
     lib.cqsa_attn_bwd_cast.argtypes = [_vp, _vp, _ll, _i, _vp]
     lib.cqsa_stream_attn_bwd.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _ll, _i, _i, _f, _i,
                                          _ll, _vp]
+    lib.cqsa_stream_attn_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _ll, _i, _i, _f, _i,
+                                            _ll, ctypes.POINTER(cqsa_stream_stats), _vp]
     lib.cqsa_release_cache.argtypes = []
     lib.cqsa_release_cache.restype = _i
     lib.cqsa_status_string.argtypes = [_i]
@@ -273,6 +275,16 @@ def cqsa_stream_attn_bwd(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal
     return _check(lib.cqsa_stream_attn_bwd(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
                                            _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), dtype,
                                            chunk_tokens, _stream(stream)))
+
+
+def cqsa_stream_attn_bwd_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, dtype, chunk_tokens,
+                            stats=None, stream=None):
+    """cqsa_stream_attn_bwd that also fills a cqsa_stream_stats (kernel, copy and stall times); returns it."""
+    st = stats if stats is not None else cqsa_stream_stats()
+    _check(lib.cqsa_stream_attn_bwd_ex(_ptr(q), _ptr(k), _ptr(v), _ptr(out), _ptr(dout), _ptr(lse), _ptr(dq),
+                                       _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), dtype,
+                                       chunk_tokens, ctypes.byref(st), _stream(stream)))
+    return st
 
 
 def cqsa_release_cache() -> int:

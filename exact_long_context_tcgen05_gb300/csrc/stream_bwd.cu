@@ -18,6 +18,7 @@
 #include <math.h>
 #include <string.h>
 
+#include <chrono>
 #include <vector>
 
 #include "cqsa_internal.h"
@@ -48,6 +49,16 @@ using namespace cqsa;
 extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                                     const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d,
                                     int causal, float scale, int dtype, long long chunk_tokens, cudaStream_t stream) {
+  return cqsa_stream_attn_bwd_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, causal, scale, dtype, chunk_tokens,
+                                 nullptr, stream);
+}
+
+extern "C" int cqsa_stream_attn_bwd_ex(const void* q, const void* k, const void* v, const void* out,
+                                       const void* dout, const float* lse, void* dq, void* dk, void* dv, int B, int H,
+                                       long long N, int d, int causal, float scale, int dtype,
+                                       long long chunk_tokens, cqsa_stream_stats* stats, cudaStream_t stream) {
+  const auto t_start = std::chrono::steady_clock::now();
+  if (stats) memset(stats, 0, sizeof(*stats));
   if (!q || !k || !v || !out || !dout || !lse || !dq || !dk || !dv) {
     set_error("q, k, v, out, dout, lse, dq, dk and dv must be non-null host pointers");
     return CQSA_ERR_INVALID;
@@ -98,9 +109,13 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
   std::vector<void*> bufs;
   cudaStream_t copy = nullptr, d2h = nullptr;
   std::vector<cudaEvent_t> events;
+  long long dev_bytes = 0;
   auto alloc = [&](void** ptr, size_t n) -> int {
     const int r = pool_alloc(ptr, n);
-    if (r == CQSA_OK) bufs.push_back(*ptr);
+    if (r == CQSA_OK) {
+      bufs.push_back(*ptr);
+      dev_bytes += static_cast<long long>(n);
+    }
     return r;
   };
   auto event = [&](cudaEvent_t* e) -> int {
@@ -139,6 +154,28 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
         (rc = event(&o_ready[s2])) == CQSA_OK)
       rc = event(&o_free[s2]);
   }
+  // with stats: timing events around every kernel segment on `stream` and every copy group on `copy`
+  struct Span {
+    cudaEvent_t a, b;
+  };
+  std::vector<Span> kspans, cspans;
+  std::vector<cudaEvent_t> tevents;
+  auto tspan = [&](std::vector<Span>& v, cudaStream_t s, bool begin) {
+    if (!stats || rc != CQSA_OK) return;
+    if (begin) {
+      Span sp{nullptr, nullptr};
+      if ((rc = pool_event(&sp.a, true)) != CQSA_OK) return;
+      tevents.push_back(sp.a);
+      if ((rc = pool_event(&sp.b, true)) != CQSA_OK) return;
+      tevents.push_back(sp.b);
+      v.push_back(sp);
+      rc = cuda_status(cudaEventRecord(sp.a, s), "record");
+    } else {
+      rc = cuda_status(cudaEventRecord(v.back().b, s), "record");
+    }
+  };
+  long long d2h_bytes = 0;
+  int n_pairs = 0, n_launches = 0;
   float* dk_acc0 = static_cast<float*>(acc_kv);
   float* dv_acc0 = dk_acc0 + static_cast<size_t>(n_chunks) * (chunk32 / 4);
 
@@ -149,7 +186,11 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
     const int os = out_slot;
     out_slot ^= 1;
     if (o_free_set[os]) CQSA_STEP(cudaStreamWaitEvent(stream, o_free[os], 0), "wait staging");
+    tspan(kspans, stream, true);
     if (rc == CQSA_OK) rc = launch_bwd_cast(acc, ostage[os], static_cast<long long>(BH) * n * d, dtype, stream);
+    tspan(kspans, stream, false);
+    ++n_launches;
+    d2h_bytes += static_cast<long long>(BH) * n * d * 2;
     CQSA_STEP(cudaEventRecord(o_ready[os], stream), "record");
     CQSA_STEP(cudaStreamWaitEvent(d2h, o_ready[os], 0), "wait cast");
     CQSA_STEP(copy_chunk_out(host, ostage[os], B, H, N, d, t0, n, d2h), "copy out");
@@ -167,16 +208,22 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
     const QSlot& Q = qsl[qi & 1];
     // the query side of chunk qi - 2 is done with this slot
     if (q_free_set[qi & 1]) CQSA_STEP(cudaStreamWaitEvent(copy, q_free[qi & 1], 0), "wait q slot");
+    tspan(cspans, copy, true);
     CQSA_STEP(copy_chunk(Q.q, q, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy q");
     CQSA_STEP(copy_chunk(Q.out, out, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy out");
     CQSA_STEP(copy_chunk(Q.g, dout, CQSA_LAYOUT_BHND, B, H, N, d, qs, nq, h2d, copy, &bytes), "copy dout");
     CQSA_STEP(cudaMemcpy2DAsync(Q.lse, static_cast<size_t>(nq) * 4, lse + qs, static_cast<size_t>(N) * 4,
                                 static_cast<size_t>(nq) * 4, BH, h2d, copy),
               "copy lse");
+    bytes += static_cast<long long>(BH) * nq * 4;
+    tspan(cspans, copy, false);
     CQSA_STEP(cudaEventRecord(q_ready[qi & 1], copy), "record");
     CQSA_STEP(cudaStreamWaitEvent(stream, q_ready[qi & 1], 0), "wait q");
+    tspan(kspans, stream, true);
     if (rc == CQSA_OK) rc = launch_bwd_dvec(Q.out, Q.g, Q.dvec, static_cast<long long>(BH) * nq, d, dtype, stream);
     CQSA_STEP(cudaMemsetAsync(Q.dq, 0, BH * static_cast<size_t>(nq) * d * 4, stream), "zero dq accumulator");
+    tspan(kspans, stream, false);
+    ++n_launches;
     // key chunks this query chunk needs (every chunk, or those at or before its last token when causal),
     // in alternating directions, so the chunk that ends one query chunk starts the next one
     int last = n_chunks - 1;
@@ -189,8 +236,10 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
       if (slot < 0) {
         slot = next_kv;
         if (kv_free_set[slot]) CQSA_STEP(cudaStreamWaitEvent(copy, kv_free[slot], 0), "wait kv slot");
+        tspan(cspans, copy, true);
         CQSA_STEP(copy_chunk(ksl[slot].k, k, CQSA_LAYOUT_BHND, B, H, N, d, ks, nk, h2d, copy, &bytes), "copy k");
         CQSA_STEP(copy_chunk(ksl[slot].v, v, CQSA_LAYOUT_BHND, B, H, N, d, ks, nk, h2d, copy, &bytes), "copy v");
+        tspan(cspans, copy, false);
         CQSA_STEP(cudaEventRecord(kv_ready[slot], copy), "record");
         kv_chunk[slot] = ki;
       }
@@ -218,7 +267,11 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
       a.causal = causal != 0;
       a.scale = sc;
       a.dtype = dtype;
-      rc = launch_attention_bwd_chunk(a, stream);
+      tspan(kspans, stream, true);
+      if (rc == CQSA_OK) rc = launch_attention_bwd_chunk(a, stream);
+      tspan(kspans, stream, false);
+      ++n_pairs;
+      ++n_launches;
       CQSA_STEP(cudaEventRecord(kv_free[slot], stream), "record");
       kv_free_set[slot] = true;
     }
@@ -245,9 +298,30 @@ extern "C" int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v,
   }
   // a kernel whose bounded wait gave up leaves its gradients incomplete: report it
   if (rc == CQSA_OK) rc = check_device_error_on(stream);
+  if (rc == CQSA_OK && stats) {
+    double comp = 0.0, h2d = 0.0, stall = 0.0;
+    float ms = 0.0f;
+    for (size_t i = 0; i < kspans.size(); ++i) {
+      if (cudaEventElapsedTime(&ms, kspans[i].a, kspans[i].b) == cudaSuccess) comp += ms;
+      if (i > 0 && cudaEventElapsedTime(&ms, kspans[i - 1].b, kspans[i].a) == cudaSuccess && ms > 0) stall += ms;
+    }
+    for (const Span& s : cspans)
+      if (cudaEventElapsedTime(&ms, s.a, s.b) == cudaSuccess) h2d += ms;
+    stats->compute_ms = comp;
+    stats->h2d_ms = h2d;
+    stats->stall_ms = stall;
+    stats->h2d_bytes = bytes;
+    stats->d2h_bytes = d2h_bytes;
+    stats->peak_device_bytes = dev_bytes;
+    stats->n_chunks = n_pairs;
+    stats->n_launches = n_launches;
+  }
+  for (cudaEvent_t e : tevents) pool_event_free(e, true);
   for (cudaEvent_t e : events) pool_event_free(e, false);
   pool_stream_free(copy);
   pool_stream_free(d2h);
   for (void* b : bufs) pool_free(b);
+  if (rc == CQSA_OK && stats)
+    stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
   return rc;
 }

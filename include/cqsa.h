@@ -271,6 +271,13 @@ int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cuda
 int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d, int causal,
                          float scale, int dtype, long long chunk_tokens, cudaStream_t stream);
+/* The same call, filling *stats (may be NULL): compute_ms sums the event intervals of its kernel segments
+ * (D and the dq zeroing of each query chunk, each pair, each output cast), h2d_ms those of its copy
+ * groups, stall_ms the gaps between consecutive kernel segments, n_chunks the pairs run. */
+int cqsa_stream_attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const void* dout,
+                            const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d,
+                            int causal, float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,
+                            cudaStream_t stream);
 
 /*
  * Size of the file-scope device array that cqsa_attn_fwd_chunked_static uses as its scratch (32 MiB).

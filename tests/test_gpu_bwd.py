@@ -247,7 +247,13 @@ def test_stream_backward(cq, B, H, N, C, causal, d):
     out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
     host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
     grads = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
-    cq.cqsa_stream_attn_bwd(*host, *grads, B, H, N, d, causal, 0.0, dtype, C)
+    st = cq.cqsa_stream_attn_bwd_ex(*host, *grads, B, H, N, d, causal, 0.0, dtype, C)
+    n_chunks = -(-N // C)
+    pairs = n_chunks * (n_chunks + 1) // 2 if causal else n_chunks * n_chunks
+    assert st.n_chunks == pairs and st.compute_ms > 0 and st.wall_ms >= st.compute_ms * 0.5
+    # every input crosses the link at least once: q, out, dout, k, v and lse
+    assert st.h2d_bytes >= 5 * B * H * N * d * 2 + B * H * N * 4
+    assert st.d2h_bytes == 3 * B * H * N * d * 2
     u = U[dtype]
     for name, t, m in zip(("dq", "dk", "dv"), grads, mono_grads):
         m = m.float().cpu()
