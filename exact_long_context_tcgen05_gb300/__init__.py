@@ -25,7 +25,7 @@ EXPORTED = ("cqsa_attn_fwd", "cqsa_attn_fwd_chunk", "cqsa_merge_partials", "cqsa
             "cqsa_quorum_attn_fwd_ex", "cqsa_release_cache", "cqsa_attn_bwd_workspace_size", "cqsa_attn_bwd", "cqsa_attn_bwd_dvec",
             "cqsa_attn_bwd_chunk", "cqsa_attn_bwd_cast", "cqsa_stream_attn_bwd", "cqsa_stream_attn_bwd_ex",
             "cqsa_status_string", "cqsa_last_error", "cqsa_device_error", "cqsa_set_timeout_ms",
-            "cqsa_debug_set_fault", "cqsa_version")
+            "cqsa_debug_set_fault", "cqsa_version", "cqsa_set_stream_kv_resident_bytes")
 CQSA_STATIC_SCRATCH_BYTES = 32 << 20
 
 
@@ -88,6 +88,8 @@ def _load() -> ctypes.CDLL:
                                          _ll, _vp]
     lib.cqsa_stream_attn_bwd_ex.argtypes = [_vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _i, _ll, _i, _i, _f, _i,
                                             _ll, ctypes.POINTER(cqsa_stream_stats), _vp]
+    lib.cqsa_set_stream_kv_resident_bytes.argtypes = [_ll]
+    lib.cqsa_set_stream_kv_resident_bytes.restype = None
     lib.cqsa_release_cache.argtypes = []
     lib.cqsa_release_cache.restype = _i
     lib.cqsa_status_string.argtypes = [_i]
@@ -285,6 +287,12 @@ def cqsa_stream_attn_bwd_ex(q, k, v, out, dout, lse, dq, dk, dv, B, H, N, d, cau
                                        _ptr(dk), _ptr(dv), B, H, N, d, int(bool(causal)), float(scale), dtype,
                                        chunk_tokens, ctypes.byref(st), _stream(stream)))
     return st
+
+
+def cqsa_set_stream_kv_resident_bytes(nbytes: int) -> None:
+    """K/V of cqsa_stream_attn_fwd stay on the device when they take at most nbytes (< 0: half of the free
+    device memory, the default; 0: never, every pair through the fp32 accumulator)."""
+    lib.cqsa_set_stream_kv_resident_bytes(int(nbytes))
 
 
 def cqsa_release_cache() -> int:

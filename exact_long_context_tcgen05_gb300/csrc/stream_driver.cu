@@ -12,6 +12,7 @@
 // the accumulator to the output dtype and layout; host outputs leave on a second copy stream.
 // The KV order alternates direction between consecutive Q chunks (serpentine), so the chunk that
 // ended one Q chunk starts the next and is not copied again.
+#include <atomic>
 #include <chrono>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -62,17 +63,19 @@ __global__ void finalize_kernel(const float* __restrict__ acc, const float* __re
 struct Resources {
   std::vector<void*> dev;
   std::vector<std::pair<cudaEvent_t, bool>> events;
-  cudaStream_t copy = nullptr, d2h = nullptr;
+  cudaStream_t copy = nullptr, d2h = nullptr, compute2 = nullptr;
   cudaStream_t compute = nullptr;  // caller's stream: drained before buffers are returned
   bool compute_set = false;
   ~Resources() {
     if (compute_set) cudaStreamSynchronize(compute);
+    if (compute2) cudaStreamSynchronize(compute2);
     if (copy) cudaStreamSynchronize(copy);
     if (d2h) cudaStreamSynchronize(d2h);
     for (void* p : dev) pool_free(p);
     for (const auto& e : events) pool_event_free(e.first, e.second);
     pool_stream_free(copy);
     pool_stream_free(d2h);
+    pool_stream_free(compute2);
   }
 };
 
@@ -132,6 +135,263 @@ int launch_finalize(const float* acc, const float* lse_acc, void* out, float* ls
   return cuda_status(cudaGetLastError(), "finalize launch");
 }
 
+// ---------------------------------------------------------------------------------------------------
+// Resident inputs. When Q, K, V and the output together fit the budget (cqsa_set_stream_kv_resident_bytes;
+// by default half of the device's free memory), each chunk of Q, K and V is copied once, beside the
+// kernels, into full-length device tensors where it stays, and each Q chunk runs as ONE launch against
+// the key prefix it sees (every key when not causal) in output mode, into its own packed segment of a
+// full-size output staging buffer: no fp32 accumulator, no merge, no finalize, and no buffer is reused,
+// so the copy stream never waits for a kernel. Q chunks alternate between the caller's stream and a
+// second compute stream, so one launch's last wave overlaps the next launch.
+namespace {
+std::atomic<long long> g_kv_resident_bytes{-1};
+
+bool kv_resident_ok(size_t bytes) {
+  const long long lim = g_kv_resident_bytes.load();
+  if (lim == 0) return false;
+  if (lim > 0) return static_cast<long long>(bytes) <= lim;
+  size_t fr = 0, tot = 0;
+  if (cudaMemGetInfo(&fr, &tot) != cudaSuccess) return false;
+  return bytes <= fr / 2;
+}
+
+// Tokens [t0, t0+n) of a (layout, N tokens) tensor into the same positions of another tensor of the
+// same shape (host -> device here).
+cudaError_t copy_range(void* dst, const void* src, int layout, int B, int H, long long N, int d, long long t0, int n,
+                       cudaMemcpyKind kind, cudaStream_t s, long long* bytes) {
+  const size_t es = 2;
+  size_t width, height, pitch, off;
+  if (layout == CQSA_LAYOUT_BHND) {
+    width = static_cast<size_t>(n) * d * es;
+    height = static_cast<size_t>(B) * H;
+    pitch = static_cast<size_t>(N) * d * es;
+    off = static_cast<size_t>(t0) * d * es;
+  } else {
+    width = static_cast<size_t>(n) * H * d * es;
+    height = static_cast<size_t>(B);
+    pitch = static_cast<size_t>(N) * H * d * es;
+    off = static_cast<size_t>(t0) * H * d * es;
+  }
+  *bytes += static_cast<long long>(width * height);
+  if (height == 1 || pitch == width)
+    return cudaMemcpyAsync(static_cast<char*>(dst) + off, static_cast<const char*>(src) + off, width * height, kind, s);
+  return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off, pitch, width,
+                           height, kind, s);
+}
+}  // namespace
+
+int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_host, int layout, void* out, float* lse,
+                        int out_on_host, int B, int H, long long N, int d, int causal, float sc, int dtype, long long C,
+                        int nch, cqsa_stream_stats* stats, cudaStream_t stream,
+                        std::chrono::steady_clock::time_point t_start) {
+  const size_t es = 2;
+  const size_t full_elems = static_cast<size_t>(B) * H * N * d;
+  const cudaMemcpyKind h2d = cudaMemcpyHostToDevice;
+  Ctx cx;
+  cx.res.compute = stream;
+  cx.res.compute_set = true;
+  void *qfull = nullptr, *kfull = nullptr, *vfull = nullptr, *ostage = nullptr, *lstage = nullptr;
+  int rc = cx.alloc(&qfull, full_elems * es);
+  if (rc == CQSA_OK) rc = cx.alloc(&kfull, full_elems * es);
+  if (rc == CQSA_OK) rc = cx.alloc(&vfull, full_elems * es);
+  if (rc == CQSA_OK) rc = cx.alloc(&ostage, full_elems * es);  // chunk i packed at B*H*i*C*d elements
+  if (rc == CQSA_OK && lse) rc = cx.alloc(&lstage, static_cast<size_t>(B) * H * N * 4);
+  if (rc != CQSA_OK) return rc;
+  if ((rc = pool_stream(&cx.res.copy)) != CQSA_OK) return rc;
+  if ((rc = pool_stream(&cx.res.d2h)) != CQSA_OK) return rc;
+  if ((rc = pool_stream(&cx.res.compute2)) != CQSA_OK) return rc;
+  cudaStream_t comp[2] = {stream, cx.res.compute2};
+  // Copies run kPrefetch chunks ahead of the launches (enqueued early, so the link never waits for the
+  // host); ready[] cycles over 2 * kPrefetch events, each re-recorded only after its previous wait was
+  // enqueued. k_done[] is re-recorded per chunk after the D2H stream's wait on it.
+  constexpr int kPrefetch = 4;
+  // With at most kDeferMax chunks, every output copy is enqueued after the last launch, behind a wait
+  // for the last input copy (the two directions slow each other on the link, and the launches still
+  // running then leave time for the early chunks' outputs); each chunk has its own k_done event then.
+  constexpr int kDeferMax = 64;
+  const bool defer = nch <= kDeferMax;
+  cudaEvent_t ready[2 * kPrefetch], k_done[kDeferMax], h2d_all, start_ev, end_ev;
+  for (int s = 0; s < 2 * kPrefetch; ++s)
+    if ((rc = cx.event(&ready[s], false)) != CQSA_OK) return rc;
+  for (int s = 0; s < (defer ? nch : 2); ++s)
+    if ((rc = cx.event(&k_done[s], false)) != CQSA_OK) return rc;
+  if ((rc = cx.event(&h2d_all, false)) != CQSA_OK) return rc;
+  if ((rc = cx.event(&start_ev, false)) != CQSA_OK || (rc = cx.event(&end_ev, false)) != CQSA_OK) return rc;
+  struct Span {
+    cudaEvent_t a, b;
+  };
+  std::vector<Span> copies, kernels;
+  auto span = [&](std::vector<Span>& v, Span* sp) -> int {
+    int r = cx.event(&sp->a, true);
+    if (r == CQSA_OK) r = cx.event(&sp->b, true);
+    if (r == CQSA_OK) v.push_back(*sp);
+    return r;
+  };
+  long long h2d_bytes = 0, d2h_bytes = 0;
+#define CK(call, what)                              \
+  do {                                              \
+    int _r = cuda_status((call), what);             \
+    if (_r != CQSA_OK) return _r;                   \
+  } while (0)
+  // work the caller queued on its stream comes first on every stream of this call
+  CK(cudaEventRecord(start_ev, stream), "record");
+  CK(cudaStreamWaitEvent(cx.res.copy, start_ev, 0), "wait start");
+  CK(cudaStreamWaitEvent(comp[1], start_ev, 0), "wait start");
+  if (!causal) {
+    // every Q chunk needs every key: K and V travel first, whole
+    Span sp;
+    if ((rc = span(copies, &sp)) != CQSA_OK) return rc;
+    CK(cudaEventRecord(sp.a, cx.res.copy), "record");
+    CK(copy_range(kfull, k_host, layout, B, H, N, d, 0, static_cast<int>(N), h2d, cx.res.copy, &h2d_bytes), "copy K");
+    CK(copy_range(vfull, v_host, layout, B, H, N, d, 0, static_cast<int>(N), h2d, cx.res.copy, &h2d_bytes), "copy V");
+    CK(cudaEventRecord(sp.b, cx.res.copy), "record");
+  }
+  // copies of chunk c: Q_c and (causal) K_c, V_c into their places; launch c needs these and every
+  // earlier chunk's, which the copy stream's order gives
+  auto enqueue_copies = [&](int c) -> int {
+    const long long t0 = static_cast<long long>(c) * C;
+    const int n = static_cast<int>(N - t0 < C ? N - t0 : C);
+    Span sp;
+    int r = span(copies, &sp);
+    if (r != CQSA_OK) return r;
+    if ((r = cuda_status(cudaEventRecord(sp.a, cx.res.copy), "record")) != CQSA_OK) return r;
+    r = cuda_status(copy_range(qfull, q_host, layout, B, H, N, d, t0, n, h2d, cx.res.copy, &h2d_bytes), "copy Q");
+    if (r == CQSA_OK && causal)
+      r = cuda_status(copy_range(kfull, k_host, layout, B, H, N, d, t0, n, h2d, cx.res.copy, &h2d_bytes), "copy K");
+    if (r == CQSA_OK && causal)
+      r = cuda_status(copy_range(vfull, v_host, layout, B, H, N, d, t0, n, h2d, cx.res.copy, &h2d_bytes), "copy V");
+    if (r == CQSA_OK) r = cuda_status(cudaEventRecord(sp.b, cx.res.copy), "record");
+    if (r == CQSA_OK) r = cuda_status(cudaEventRecord(ready[c % (2 * kPrefetch)], cx.res.copy), "record ready");
+    if (r == CQSA_OK && c == nch - 1) r = cuda_status(cudaEventRecord(h2d_all, cx.res.copy), "record");
+    return r;
+  };
+  for (int c = 0; c < kPrefetch && c < nch; ++c)
+    if ((rc = enqueue_copies(c)) != CQSA_OK) return rc;
+  // the output rows (and lse) of chunk i from its staging segment, on the D2H stream after launch i
+  const cudaMemcpyKind okind = out_on_host ? cudaMemcpyDeviceToHost : cudaMemcpyDeviceToDevice;
+  auto enqueue_out = [&](int i, cudaEvent_t done) -> int {
+    const long long qt0 = static_cast<long long>(i) * C;
+    const int qn = static_cast<int>(N - qt0 < C ? N - qt0 : C);
+    const char* oseg = static_cast<const char*>(ostage) + static_cast<size_t>(B) * H * qt0 * d * es;
+    int r = cuda_status(cudaStreamWaitEvent(cx.res.d2h, done, 0), "wait k_done");
+    size_t width, height, dpitch;
+    char* obase = static_cast<char*>(out);
+    if (layout == CQSA_LAYOUT_BHND) {
+      width = static_cast<size_t>(qn) * d * es;
+      height = static_cast<size_t>(B) * H;
+      dpitch = static_cast<size_t>(N) * d * es;
+      obase += static_cast<size_t>(qt0) * d * es;
+    } else {
+      width = static_cast<size_t>(qn) * H * d * es;
+      height = static_cast<size_t>(B);
+      dpitch = static_cast<size_t>(N) * H * d * es;
+      obase += static_cast<size_t>(qt0) * H * d * es;
+    }
+    if (r == CQSA_OK)
+      r = cuda_status(height == 1 || dpitch == width
+                          ? cudaMemcpyAsync(obase, oseg, width * height, okind, cx.res.d2h)
+                          : cudaMemcpy2DAsync(obase, dpitch, oseg, width, width, height, okind, cx.res.d2h),
+                      "copy out");
+    d2h_bytes += static_cast<long long>(width * height);
+    if (r == CQSA_OK && lse) {
+      const size_t lw = static_cast<size_t>(qn) * 4;
+      const float* lseg = static_cast<const float*>(lstage) + static_cast<size_t>(B) * H * qt0;
+      r = cuda_status(cudaMemcpy2DAsync(lse + qt0, static_cast<size_t>(N) * 4, lseg, lw, lw,
+                                        static_cast<size_t>(B) * H, okind, cx.res.d2h),
+                      "copy lse");
+      d2h_bytes += static_cast<long long>(lw) * B * H;
+    }
+    return r;
+  };
+  for (int i = 0; i < nch; ++i) {
+    const int s = i & 1;
+    const long long qt0 = static_cast<long long>(i) * C;
+    const int qn = static_cast<int>(N - qt0 < C ? N - qt0 : C);
+    cudaStream_t cs = comp[s];
+    if (i + kPrefetch < nch && (rc = enqueue_copies(i + kPrefetch)) != CQSA_OK) return rc;
+    CK(cudaStreamWaitEvent(cs, ready[i % (2 * kPrefetch)], 0), "wait ready");
+    // Q chunk i in place in the full tensor; its packed output segment
+    const size_t qoff = layout == CQSA_LAYOUT_BHND ? static_cast<size_t>(qt0) * d * es
+                                                   : static_cast<size_t>(qt0) * H * d * es;
+    char* oseg = static_cast<char*>(ostage) + static_cast<size_t>(B) * H * qt0 * d * es;
+    float* lseg = lse ? static_cast<float*>(lstage) + static_cast<size_t>(B) * H * qt0 : nullptr;
+    AttnArgs a;
+    memset(&a, 0, sizeof(a));
+    a.q = static_cast<char*>(qfull) + qoff;
+    a.q_tokens_alloc = N;
+    a.k = kfull;
+    a.v = vfull;
+    a.B = B;
+    a.H = H;
+    a.Nq = qn;
+    a.Nkv = static_cast<int>(causal ? qt0 + qn : N);
+    a.q_off = qt0;
+    a.kv_off = 0;
+    a.kv_tokens_alloc = N;
+    a.d = d;
+    a.causal = causal != 0;
+    a.scale = sc;
+    a.dtype = dtype;
+    a.in_layout = layout;
+    a.mode = kModeOut;
+    a.out = oseg;
+    a.lse = lseg;
+    a.out_layout = layout;
+    {
+      Span sp;
+      if ((rc = span(kernels, &sp)) != CQSA_OK) return rc;
+      CK(cudaEventRecord(sp.a, cs), "record");
+      if ((rc = launch_attention(a, cs)) != CQSA_OK) return rc;
+      CK(cudaEventRecord(sp.b, cs), "record");
+    }
+    cudaEvent_t done = k_done[defer ? i : s];
+    CK(cudaEventRecord(done, cs), "record k_done");
+    if (!defer && (rc = enqueue_out(i, done)) != CQSA_OK) return rc;
+  }
+  if (defer) {
+    CK(cudaStreamWaitEvent(cx.res.d2h, h2d_all, 0), "wait h2d_all");
+    for (int i = 0; i < nch; ++i)
+      if ((rc = enqueue_out(i, k_done[i])) != CQSA_OK) return rc;
+  }
+  // the caller's stream ends after every stream of this call
+  CK(cudaEventRecord(end_ev, comp[1]), "record");
+  CK(cudaStreamWaitEvent(stream, end_ev, 0), "wait end");
+  CK(cudaStreamSynchronize(comp[1]), "synchronize second compute stream");
+  CK(cudaStreamSynchronize(stream), "synchronize compute stream");
+  CK(cudaStreamSynchronize(cx.res.copy), "synchronize copy stream");
+  CK(cudaStreamSynchronize(cx.res.d2h), "synchronize d2h stream");
+#undef CK
+  if ((rc = check_device_error_on(stream)) != CQSA_OK) return rc;
+  if (stats) {
+    double h2d_ms = 0.0, comp_ms = 0.0, stall = 0.0;
+    float ms = 0.0f;
+    for (const Span& s : copies)
+      if (cudaEventElapsedTime(&ms, s.a, s.b) == cudaSuccess) h2d_ms += ms;
+    // kernel time: the union of the launches' intervals (they overlap on two streams); stall: the gaps
+    // of that union after the first launch begins
+    double end_rel = 0.0;  // end of the union so far, relative to the first launch's start
+    for (size_t k = 0; k < kernels.size(); ++k) {
+      float a0 = 0.0f, b0 = 0.0f;
+      if (cudaEventElapsedTime(&a0, kernels[0].a, kernels[k].a) != cudaSuccess) continue;
+      if (cudaEventElapsedTime(&b0, kernels[0].a, kernels[k].b) != cudaSuccess) continue;
+      if (k > 0 && a0 > end_rel) stall += a0 - end_rel;
+      const double lo = a0 > end_rel ? a0 : end_rel;
+      if (b0 > lo) comp_ms += b0 - lo;
+      if (b0 > end_rel) end_rel = b0;
+    }
+    stats->h2d_ms = h2d_ms;
+    stats->compute_ms = comp_ms;
+    stats->stall_ms = stall;
+    stats->h2d_bytes = h2d_bytes;
+    stats->d2h_bytes = d2h_bytes;
+    stats->peak_device_bytes = cx.bytes;
+    stats->n_chunks = nch;
+    stats->n_launches = static_cast<int>(kernels.size());
+    stats->wall_ms = std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
+  }
+  return CQSA_OK;
+}
+
 }  // namespace cqsa
 
 using namespace cqsa;
@@ -179,6 +439,10 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   const int nch = static_cast<int>((N + C - 1) / C);
   const size_t es = 2;
   const size_t chunk_elems = static_cast<size_t>(B) * H * C * d;
+  if (N <= 0x7fffffffLL &&
+      kv_resident_ok(4 * static_cast<size_t>(B) * H * N * d * es + static_cast<size_t>(B) * H * N * 4))
+    return stream_fwd_resident(q_host, k_host, v_host, layout, out, lse, out_on_host, B, H, N, d, causal, sc, dtype, C,
+                               nch, stats, stream, t_start);
 
   Ctx cx;
   cx.res.compute = stream;
@@ -400,4 +664,8 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
         std::chrono::duration<double, std::milli>(std::chrono::steady_clock::now() - t_start).count();
   }
   return CQSA_OK;
+}
+
+extern "C" void cqsa_set_stream_kv_resident_bytes(long long bytes) {
+  g_kv_resident_bytes.store(bytes < 0 ? -1 : bytes);
 }

@@ -114,6 +114,20 @@ int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_h
                          float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,
                          cudaStream_t stream);
 
+/*
+ * Resident inputs for cqsa_stream_attn_fwd. When Q, K, V and the output (4 * B*H*N*d*2 bytes, plus
+ * B*H*N*4 of lse) take at most `bytes` of device memory (bytes < 0, the default: at most half of the
+ * device's free memory at the call; 0: never), each chunk is still copied from the host once, chunk by
+ * chunk beside the kernels, but into full-length device tensors where it stays; each Q chunk then runs
+ * as one launch over the key prefix it sees (every key when not causal) and writes its output rows
+ * directly (no fp32 accumulator, no merge), which return to `out` chunk by chunk.
+ * Consecutive Q chunks alternate between `stream` and a second stream of the call, so one launch's
+ * last wave overlaps the next one. Every query tile then sees the same key tiles in the same order
+ * as in cqsa_attn_fwd, so the results are bitwise equal to it (the accumulating schedule agrees up to
+ * fp32 summation order). Process-wide setting.
+ */
+void cqsa_set_stream_kv_resident_bytes(long long bytes);
+
 /* ------------------------------------------------------------------------------------------------
  * Cyclic quorum-set decomposition ("stream-cqsa 2.2.0 -> 2.2.2" diff, README and autoconfig.plan: a
  * configuration is (c, interest_set, itr) with c**itr subproblems and cost (l^2/c)^itr, l the size of

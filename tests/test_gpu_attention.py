@@ -226,7 +226,10 @@ def test_determinism(cq):
 @pytest.mark.parametrize("layout", [syn.LAYOUT_BNHD, syn.LAYOUT_BHND])
 @pytest.mark.parametrize("causal", [True, False])
 @pytest.mark.parametrize("out_on_host", [True, False])
-def test_stream_driver_small(cq, layout, causal, out_on_host):
+@pytest.mark.parametrize("resident", [True, False])
+def test_stream_driver_small(cq, layout, causal, out_on_host, resident):
+    """Both schedules of the host-streaming driver against the oracle: K/V resident (one launch per Q chunk
+    over its key prefix) and every (Q chunk, KV chunk) pair through the fp32 accumulator."""
     B, H, N, d, C = 2, 3, 1000, 64, 256
     qn, kn, vn = syn.qkv(B, H, N, d, seed=11, layout=layout)
     hq, hk, hv = (torch.from_numpy(x.view(np.int16)).view(torch.float16).pin_memory() for x in (qn, kn, vn))
@@ -238,7 +241,17 @@ def test_stream_driver_small(cq, layout, causal, out_on_host):
         out = torch.empty(shape, dtype=torch.float16, device="cuda")
         lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
     st = cq.cqsa_stream_stats()
-    cq.cqsa_stream_attn_fwd(hq, hk, hv, layout, out, lse, out_on_host, B, H, N, d, causal, 0.0, cq.CQSA_F16, C, st)
+    cq.cqsa_set_stream_kv_resident_bytes(1 << 40 if resident else 0)
+    try:
+        cq.cqsa_stream_attn_fwd(hq, hk, hv, layout, out, lse, out_on_host, B, H, N, d, causal, 0.0, cq.CQSA_F16, C,
+                                st)
+    finally:
+        cq.cqsa_set_stream_kv_resident_bytes(-1)
+    if resident and layout == syn.LAYOUT_BHND:
+        # the same tiles, key order and fold segments as the monolithic call: bitwise equal
+        q, k, v = (to_dev(x, syn.F16) for x in (qn, kn, vn))
+        o_m, l_m = mono(cq, q, k, v, B, H, N, d, causal, syn.F16)
+        assert torch.equal(out.cuda(), o_m) and torch.equal(lse.cuda(), l_m)
     o = to_np64(out)
     if layout == syn.LAYOUT_BNHD:
         o = o.transpose(0, 2, 1, 3)
@@ -248,8 +261,10 @@ def test_stream_driver_small(cq, layout, causal, out_on_host):
     ref_o, ref_l = oracle.attn_full(qb, kb, vb, B=B, H=H, N=N, d=d, causal=causal)
     assert_close(o, ref_o, to_np64(lse), ref_l, what="stream driver")
     nq = (N + C - 1) // C
-    assert st.n_chunks == (nq * (nq + 1) // 2 if causal else nq * nq)
-    assert st.h2d_bytes > 0 and st.peak_device_bytes > 0
+    assert st.n_chunks == (nq if resident else (nq * (nq + 1) // 2 if causal else nq * nq))
+    assert st.h2d_bytes >= 3 * B * H * N * d * 2 and st.peak_device_bytes > 0
+    if out_on_host:
+        assert st.d2h_bytes == B * H * N * d * 2 + B * H * N * 4
 
 
 def test_no_device_error(cq):
