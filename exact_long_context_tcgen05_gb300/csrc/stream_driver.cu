@@ -63,19 +63,20 @@ __global__ void finalize_kernel(const float* __restrict__ acc, const float* __re
 struct Resources {
   std::vector<void*> dev;
   std::vector<std::pair<cudaEvent_t, bool>> events;
-  cudaStream_t copy = nullptr, d2h = nullptr, compute2 = nullptr;
+  cudaStream_t copy = nullptr, d2h = nullptr;
+  std::vector<cudaStream_t> extra;  // further compute streams (pool)
   cudaStream_t compute = nullptr;  // caller's stream: drained before buffers are returned
   bool compute_set = false;
   ~Resources() {
     if (compute_set) cudaStreamSynchronize(compute);
-    if (compute2) cudaStreamSynchronize(compute2);
+    for (cudaStream_t s : extra) cudaStreamSynchronize(s);
     if (copy) cudaStreamSynchronize(copy);
     if (d2h) cudaStreamSynchronize(d2h);
     for (void* p : dev) pool_free(p);
     for (const auto& e : events) pool_event_free(e.first, e.second);
     pool_stream_free(copy);
     pool_stream_free(d2h);
-    pool_stream_free(compute2);
+    for (cudaStream_t s : extra) pool_stream_free(s);
   }
 };
 
@@ -141,8 +142,9 @@ int launch_finalize(const float* acc, const float* lse_acc, void* out, float* ls
 // kernels, into full-length device tensors where it stays, and each Q chunk runs as ONE launch against
 // the key prefix it sees (every key when not causal) in output mode, into its own packed segment of a
 // full-size output staging buffer: no fp32 accumulator, no merge, no finalize, and no buffer is reused,
-// so the copy stream never waits for a kernel. Q chunks alternate between the caller's stream and a
-// second compute stream, so one launch's last wave overlaps the next launch.
+// so the copy stream never waits for a kernel. Q chunks go round-robin over up to kComputeStreams
+// streams (the caller's first), so launches whose inputs have landed run side by side: a small chunk's
+// launch has fewer CTAs than the GPU has SMs, and one launch's last wave overlaps the next ones.
 namespace {
 std::atomic<long long> g_kv_resident_bytes{-1};
 
@@ -199,8 +201,13 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
   if (rc != CQSA_OK) return rc;
   if ((rc = pool_stream(&cx.res.copy)) != CQSA_OK) return rc;
   if ((rc = pool_stream(&cx.res.d2h)) != CQSA_OK) return rc;
-  if ((rc = pool_stream(&cx.res.compute2)) != CQSA_OK) return rc;
-  cudaStream_t comp[2] = {stream, cx.res.compute2};
+  constexpr int kComputeStreams = 8;
+  const int ncs = nch < kComputeStreams ? nch : kComputeStreams;
+  cudaStream_t comp[kComputeStreams] = {stream};
+  for (int s = 1; s < ncs; ++s) {
+    if ((rc = pool_stream(&comp[s])) != CQSA_OK) return rc;
+    cx.res.extra.push_back(comp[s]);
+  }
   // Copies run kPrefetch chunks ahead of the launches (enqueued early, so the link never waits for the
   // host); ready[] cycles over 2 * kPrefetch events, each re-recorded only after its previous wait was
   // enqueued. k_done[] is re-recorded per chunk after the D2H stream's wait on it.
@@ -210,13 +217,15 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
   // running then leave time for the early chunks' outputs); each chunk has its own k_done event then.
   constexpr int kDeferMax = 64;
   const bool defer = nch <= kDeferMax;
-  cudaEvent_t ready[2 * kPrefetch], k_done[kDeferMax], h2d_all, start_ev, end_ev;
+  cudaEvent_t ready[2 * kPrefetch], k_done[kDeferMax], h2d_all, start_ev, end_ev[kComputeStreams];
   for (int s = 0; s < 2 * kPrefetch; ++s)
     if ((rc = cx.event(&ready[s], false)) != CQSA_OK) return rc;
-  for (int s = 0; s < (defer ? nch : 2); ++s)
+  for (int s = 0; s < (defer ? nch : kComputeStreams); ++s)
     if ((rc = cx.event(&k_done[s], false)) != CQSA_OK) return rc;
   if ((rc = cx.event(&h2d_all, false)) != CQSA_OK) return rc;
-  if ((rc = cx.event(&start_ev, false)) != CQSA_OK || (rc = cx.event(&end_ev, false)) != CQSA_OK) return rc;
+  if ((rc = cx.event(&start_ev, false)) != CQSA_OK) return rc;
+  for (int s = 0; s < kComputeStreams; ++s)
+    if ((rc = cx.event(&end_ev[s], false)) != CQSA_OK) return rc;
   struct Span {
     cudaEvent_t a, b;
   };
@@ -236,7 +245,7 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
   // work the caller queued on its stream comes first on every stream of this call
   CK(cudaEventRecord(start_ev, stream), "record");
   CK(cudaStreamWaitEvent(cx.res.copy, start_ev, 0), "wait start");
-  CK(cudaStreamWaitEvent(comp[1], start_ev, 0), "wait start");
+  for (int s = 1; s < ncs; ++s) CK(cudaStreamWaitEvent(comp[s], start_ev, 0), "wait start");
   if (!causal) {
     // every Q chunk needs every key: K and V travel first, whole
     Span sp;
@@ -304,7 +313,7 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
     return r;
   };
   for (int i = 0; i < nch; ++i) {
-    const int s = i & 1;
+    const int s = i % ncs;
     const long long qt0 = static_cast<long long>(i) * C;
     const int qn = static_cast<int>(N - qt0 < C ? N - qt0 : C);
     cudaStream_t cs = comp[s];
@@ -354,9 +363,11 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
       if ((rc = enqueue_out(i, k_done[i])) != CQSA_OK) return rc;
   }
   // the caller's stream ends after every stream of this call
-  CK(cudaEventRecord(end_ev, comp[1]), "record");
-  CK(cudaStreamWaitEvent(stream, end_ev, 0), "wait end");
-  CK(cudaStreamSynchronize(comp[1]), "synchronize second compute stream");
+  for (int s = 1; s < ncs; ++s) {
+    CK(cudaEventRecord(end_ev[s], comp[s]), "record");
+    CK(cudaStreamWaitEvent(stream, end_ev[s], 0), "wait end");
+  }
+  for (int s = 1; s < ncs; ++s) CK(cudaStreamSynchronize(comp[s]), "synchronize compute streams");
   CK(cudaStreamSynchronize(stream), "synchronize compute stream");
   CK(cudaStreamSynchronize(cx.res.copy), "synchronize copy stream");
   CK(cudaStreamSynchronize(cx.res.d2h), "synchronize d2h stream");

@@ -87,13 +87,14 @@ int cqsa_merge_partials(const float* const* O_parts, const float* const* LSE_par
 /* Statistics of one streaming call (times in milliseconds). */
 typedef struct {
   double wall_ms;        /* host clock around the whole call */
-  double compute_ms;     /* sum of chunk-kernel event intervals on the compute stream */
+  double compute_ms;     /* sum of chunk-kernel event intervals on the compute stream (resident
+                            schedule: the union of its launches' intervals, which overlap) */
   double h2d_ms;         /* sum of host-to-device copy event intervals */
   double stall_ms;       /* time the compute stream waited for a copy (event gaps) */
   long long h2d_bytes;   /* bytes copied host -> device */
   long long d2h_bytes;   /* bytes copied device -> host */
   long long peak_device_bytes; /* device memory the driver allocated */
-  int n_chunks;          /* Q chunks x KV chunks processed (non-empty pairs) */
+  int n_chunks;          /* Q chunks x KV chunks processed (non-empty pairs); resident schedule: Q chunks */
   int n_launches;        /* kernels launched */
 } cqsa_stream_stats;
 

@@ -87,11 +87,16 @@ def test_quorum_vs_oracle_and_stream(cq, c, itr, N, d, dtype, causal, layout, on
         assert_bf16_rounds_fp32_result(o64, to_np64(O32), f"quorum bf16 c={c}")
         lrel = np.abs(to_np64(lse) - to_np64(L32)) / np.maximum(1.0, np.abs(to_np64(L32)))
         assert lrel.max() <= 1e-5
-    # the streaming driver with the same chunk size: same pair partials, merged in key order
+    # the streaming driver's accumulating schedule with the same chunk size: same pair partials, merged
+    # in key order (its resident schedule runs one launch per query chunk instead)
     hq, hk, hv = (_host(x, dtype) for x in (qn, kn, vn))
     out2 = torch.empty(shape, dtype=tdt, device="cuda")
     lse2 = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
-    cq.cqsa_stream_attn_fwd(hq, hk, hv, layout, out2, lse2, False, B, H, N, d, causal, 0.0, dtype, C)
+    cq.cqsa_set_stream_kv_resident_bytes(0)
+    try:
+        cq.cqsa_stream_attn_fwd(hq, hk, hv, layout, out2, lse2, False, B, H, N, d, causal, 0.0, dtype, C)
+    finally:
+        cq.cqsa_set_stream_kv_resident_bytes(-1)
     lrel = ((lse - lse2).abs() / lse2.abs().clamp_min(1.0)).max().item()
     assert lrel <= 1e-6, lrel
     diff = (out.float() - out2.float()).abs()
