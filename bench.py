@@ -505,17 +505,33 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1, engine="classic
                                    not device_inputs, 1, Hs, n_tokens, Ds, True, 0.0, cq.CQSA_F16, c, D, itr,
                                    acc_on_host=acc_on_host, max_parallel=npar, engine=eng, stats=st, stream=stream)
 
+    mono_s = None
     if device_inputs:
         call()
         ms = statistics.median(_time_events(call, 3, stream))
         wall = ms / 1e3
+        # the monolithic call on the same problem ([B,H,N,d] copies of the same device inputs)
+        qb, kb, vb = (x.permute(0, 2, 1, 3).contiguous() for x in qkv)
+        ob = torch.empty_like(qb)
+        lb = torch.empty((1, Hs, n_tokens), dtype=torch.float32, device=dev)
+
+        def mono_call():
+            cq.cqsa_attn_fwd(qb, kb, vb, ob, lb, 1, Hs, n_tokens, Ds, True, 0.0, cq.CQSA_F16, stream)
+
+        mono_call()
+        mono_s = statistics.median(_time_events(mono_call, 3, stream)) / 1e3
+        del qb, kb, vb, ob
     else:
         t0 = time.perf_counter()
         call()
         wall = time.perf_counter() - t0
     flop = 4.0 * Hs * n_tokens * n_tokens * Ds / 2.0
+    where = "device-resident token-major Q/K/V/out" if device_inputs else "token-major pinned host Q/K/V/out"
+    extra = {}
+    if mono_s:
+        extra = {"mono_tflops": flop / mono_s / 1e12, "over_mono": mono_s / wall}
     return {"measure": "quorum", "workload": f"cyclic quorum decomposition, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
-            f"c={c} interest_set={D} itr={itr}, token-major pinned host Q/K/V/out", "wall_s": wall,
+            f"c={c} interest_set={D} itr={itr}, {where}", "wall_s": wall, **extra,
             "tflops": flop / wall / 1e12, "compute_s": st.compute_ms / 1e3, "copy_s": st.copy_ms / 1e3,
             "copy_bytes": st.copy_bytes, "chunk_tokens": st.chunk_tokens, "subproblems": st.n_subproblems,
             "pairs": st.n_pairs, "chunk_loads": st.n_chunk_loads, "peak_device_bytes": st.peak_device_bytes,
@@ -784,6 +800,7 @@ def run_secondary(cq, dev, args):
     run("bwd_bf16_d128", lambda: measure_bwd(cq, dev, max(3, reps // 2), N=16384, H=32, B=2, D=128, causal=False,
                                              bf16=True, k_mul=3.0))
     run("stream_bwd_131k", lambda: measure_stream_bwd(cq, dev))
+    run("quorum_wave_262k", lambda: measure_quorum(cq, dev, 262_144, engine="wave", device_inputs=True))
     run("link_1gib", lambda: measure_link(dev, 5))
     if args.secondary == "all":
         link = res["link_1gib"].get("h2d_gbs")

@@ -116,8 +116,10 @@ struct PerDeviceOnce {
       *dev = -1;
       return false;
     }
-    return *dev >= 0 && *dev < 64 && ((bits.load(std::memory_order_acquire) >> *dev) & 1ull);
+    return seen(*dev);
   }
+  // the bookkeeping alone: has device `dev` been marked (ids outside [0, 64) never are)
+  bool seen(int dev) const { return dev >= 0 && dev < 64 && ((bits.load(std::memory_order_acquire) >> dev) & 1ull); }
   void mark(int dev) {
     if (dev >= 0 && dev < 64) bits.fetch_or(1ull << dev, std::memory_order_acq_rel);
   }

@@ -437,9 +437,49 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
   struct Pending {
     AttnArgs a;
     int sq, sk, q;
+    std::vector<int> sks;  // key slots of every pair fused into this one
   };
   auto launch_waves = [&](std::vector<Pending>& group_pairs) -> int {
     int rc = CQSA_OK;
+    if (in_place) {
+      // Pairs of one query chunk whose key chunks are adjacent read one contiguous key range of the
+      // caller's tensors: they run as one pair over the whole range. The online softmax over the
+      // concatenated keys is the exact merge of the parts, and a CTA walks more key tiles for its fixed
+      // cost, with fewer passes over the accumulator. The first of a chunk's pairs that runs writes the
+      // accumulator (when this group starts the chunk), the rest merge into it.
+      std::vector<Pending> fused;
+      std::vector<int> qorder;
+      for (const Pending& pd : group_pairs)
+        if (std::find(qorder.begin(), qorder.end(), pd.q) == qorder.end()) qorder.push_back(pd.q);
+      for (int qc : qorder) {
+        std::vector<const Pending*> mine;
+        bool starts = false;
+        for (const Pending& pd : group_pairs)
+          if (pd.q == qc) {
+            mine.push_back(&pd);
+            starts = starts || pd.a.mode == kModePart;
+          }
+        std::stable_sort(mine.begin(), mine.end(),
+                         [](const Pending* x, const Pending* y) { return x->a.kv_off < y->a.kv_off; });
+        bool first = true;
+        for (size_t m = 0; m < mine.size();) {
+          Pending f = *mine[m];
+          f.sks.assign(1, mine[m]->sk);
+          size_t e = m + 1;
+          while (e < mine.size() && mine[e]->a.kv_off == f.a.kv_off + f.a.Nkv &&
+                 static_cast<long long>(f.a.Nkv) + mine[e]->a.Nkv <= 0x7fffffffLL) {
+            f.a.Nkv += mine[e]->a.Nkv;
+            f.sks.push_back(mine[e]->sk);
+            ++e;
+          }
+          f.a.mode = (first && starts) ? kModePart : kModeAccum;
+          first = false;
+          fused.push_back(f);
+          m = e;
+        }
+      }
+      group_pairs.swap(fused);
+    }
     // Waves: one launch takes at most one pair of each query chunk (pairs of one chunk accumulate into
     // one buffer, in schedule order, wave after wave) and at most wave_pairs pairs in all. Pairs with a
     // full key chunk come first in a launch, the (lighter) diagonal pairs last.
@@ -465,7 +505,8 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
         const AttnArgs& ay = group_pairs[y].a;
         const bool fx = !causal || ax.kv_off + ax.Nkv <= ax.q_off + 1;
         const bool fy = !causal || ay.kv_off + ay.Nkv <= ay.q_off + 1;
-        return fx && !fy;
+        if (fx != fy) return fx;
+        return ax.Nkv > ay.Nkv;  // then the longest key ranges first
       });
       for (size_t m0 = 0; m0 < members.size(); m0 += wave_pairs) {
         const size_t m1 = std::min(members.size(), m0 + wave_pairs);
@@ -473,7 +514,7 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
         for (size_t m = m0; m < m1; ++m) {
           const Pending& pd = group_pairs[members[m]];
           CK(cudaStreamWaitEvent(stream, q_ready[pd.sq], 0), "wait q_ready");
-          CK(cudaStreamWaitEvent(stream, kv_ready[pd.sk], 0), "wait kv_ready");
+          for (int sk : pd.sks) CK(cudaStreamWaitEvent(stream, kv_ready[sk], 0), "wait kv_ready");
           batch.push_back(pd.a);
         }
         Span sp;
@@ -484,9 +525,11 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
         for (size_t m = m0; m < m1; ++m) {
           const Pending& pd = group_pairs[members[m]];
           CK(cudaEventRecord(q_free[pd.sq * npar], stream), "record q_free");
-          CK(cudaEventRecord(kv_free[pd.sk * npar], stream), "record kv_free");
           qp.used[pd.sq * npar] = true;
-          kp.used[pd.sk * npar] = true;
+          for (int sk : pd.sks) {
+            CK(cudaEventRecord(kv_free[sk * npar], stream), "record kv_free");
+            kp.used[sk * npar] = true;
+          }
         }
         ++launches;
       }
@@ -547,7 +590,7 @@ extern "C" int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void*
       a.out_layout = CQSA_LAYOUT_BHND;
       started[t.q] = true;
       if (wave) {
-        group_pairs.push_back({a, sq, sk, t.q});
+        group_pairs.push_back({a, sq, sk, t.q, {sk}});
         continue;
       }
       const int j = t.q % npar;

@@ -201,8 +201,13 @@ int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_ho
   if (rc != CQSA_OK) return rc;
   if ((rc = pool_stream(&cx.res.copy)) != CQSA_OK) return rc;
   if ((rc = pool_stream(&cx.res.d2h)) != CQSA_OK) return rc;
+  // As many streams as it takes for the launches in flight to hold about eight CTAs per SM (a launch has
+  // B*H CTAs per 256 query rows), two at least (one launch's last wave beside the next), at most eight.
   constexpr int kComputeStreams = 8;
-  const int ncs = nch < kComputeStreams ? nch : kComputeStreams;
+  const long long ctas = static_cast<long long>(B) * H * ((C + 255) / 256);
+  long long want = (8LL * sm_count() + ctas - 1) / ctas;
+  want = want < 2 ? 2 : (want > kComputeStreams ? kComputeStreams : want);
+  const int ncs = static_cast<int>(nch < want ? nch : want);
   cudaStream_t comp[kComputeStreams] = {stream};
   for (int s = 1; s < ncs; ++s) {
     if ((rc = pool_stream(&comp[s])) != CQSA_OK) return rc;

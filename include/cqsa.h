@@ -197,9 +197,14 @@ int cqsa_quorum_attn_fwd(const void* q, const void* k, const void* v, int layout
  *   chunk's accumulator without a race); a wave holds at most wave_tokens query tokens (0 selects
  *   min(2^21, max(2^19, N))). Partials are merged in place by the kernel's epilogue, so no packed
  *   partial buffer is needed and the budget only caps a launch's size. max_parallel is ignored (one
- *   stream). Pairs of a query chunk are merged in the same order as by the classic engine, so the two
- *   engines give bit-identical results.
+ *   stream). With host inputs, pairs of a query chunk are merged in the same order as by the classic
+ *   engine, so the two engines give bit-identical results.
  * Device-resident inputs (inputs_on_host = 0) are read in place by either engine; nothing is staged.
+ *   The wave engine then runs the pairs of a query chunk whose key chunks are adjacent as one pair over
+ *   the joined key range (the online softmax over the joined keys is the exact merge of the parts), and
+ *   without a host accumulator its waves span every subproblem: a causal problem then runs one pair per
+ *   query chunk over its whole key prefix, bitwise equal to cqsa_attn_fwd on the same inputs; with a
+ *   host accumulator, within the fp32 merge error of the classic engine.
  */
 enum { CQSA_ENGINE_CLASSIC = 0, CQSA_ENGINE_WAVE = 1 };
 int cqsa_quorum_attn_fwd_ex(const void* q, const void* k, const void* v, int layout, int inputs_on_host, void* out,
