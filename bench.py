@@ -807,7 +807,6 @@ def run_secondary(cq, dev, args):
         host = _host_qkv_token_major(args.n)
         run("link_driver_shaped", lambda: measure_link_driver_shaped(cq, dev, host, 262_144))
         run("stream_4m", lambda: measure_stream(cq, dev, args.n, link, host=host))
-        run("stream_4m_accumulating", lambda: measure_stream(cq, dev, args.n, link, host=host, accumulating=True))
         del host
     rc, code, _ = cq.cqsa_device_error()
     res["device_error_free"] = rc == cq.CQSA_OK

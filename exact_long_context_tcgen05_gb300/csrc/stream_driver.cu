@@ -455,7 +455,11 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   const int nch = static_cast<int>((N + C - 1) / C);
   const size_t es = 2;
   const size_t chunk_elems = static_cast<size_t>(B) * H * C * d;
-  if (N <= 0x7fffffffLL &&
+  // Resident inputs when they fit the budget and one head's whole K and V fit the L2 share the kernel
+  // groups heads by (64 MB): a launch over the key prefix has every CTA sweep its head's keys, which
+  // stay in L2 only then (4M tokens, 1 GB per head: 1,091 TFLOP/s resident against 1,145 accumulating).
+  const bool kv_fits_l2 = 2.0 * static_cast<double>(N) * d * es <= 64.0 * 1024 * 1024;
+  if (N <= 0x7fffffffLL && kv_fits_l2 &&
       kv_resident_ok(4 * static_cast<size_t>(B) * H * N * d * es + static_cast<size_t>(B) * H * N * 4))
     return stream_fwd_resident(q_host, k_host, v_host, layout, out, lse, out_on_host, B, H, N, d, causal, sc, dtype, C,
                                nch, stats, stream, t_start);

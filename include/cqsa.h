@@ -118,7 +118,9 @@ int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_h
 /*
  * Resident inputs for cqsa_stream_attn_fwd. When Q, K, V and the output (4 * B*H*N*d*2 bytes, plus
  * B*H*N*4 of lse) take at most `bytes` of device memory (bytes < 0, the default: at most half of the
- * device's free memory at the call; 0: never), each chunk is still copied from the host once, chunk by
+ * device's free memory at the call; 0: never), and one head's K and V (2*N*d*2 bytes) fit the 64 MiB
+ * of L2 the kernel groups heads by (longer prefixes would have every CTA sweep keys L2 cannot hold, and
+ * the accumulating schedule is faster there), each chunk is still copied from the host once, chunk by
  * chunk beside the kernels, but into full-length device tensors where it stays; each Q chunk then runs
  * as one launch over the key prefix it sees (every key when not causal) and writes its output rows
  * directly (no fp32 accumulator, no merge), which return to `out` chunk by chunk.
