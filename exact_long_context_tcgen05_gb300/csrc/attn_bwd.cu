@@ -11,21 +11,22 @@
 //   dV_j  = sum_i P_ij dO_i,  dK_j = scale sum_i dS_ij q_i,  dQ_i = scale sum_j dS_ij k_j
 //
 // Kernels, in stream order:
-//   bwd_dot_kernel   D_i in fp32 (eight threads per row, 16-byte loads of O and dO)
+//   bwd_dot_kernel   D_i in fp32 (d / 8 threads per row, 16-byte loads of O and dO)
 //   attn_bwd_kernel  one CTA per (key tile j of 128 keys, batch-head), heaviest key tiles first. K_j
 //                    and V_j stay in shared memory; Q_i and dO_i of the query tiles that see key
 //                    tile j (every i, or i >= j when causal) stream through a two-slot TMA ring.
 //                    Per query tile, with the key dimension on the 128 tensor-memory lanes:
 //                      S^T = K_j Q_i^T, dP^T = V_j dO_i^T         (tcgen05, fp32 in tensor memory)
-//                      P^T and dS^T: one thread per key row and 64 queries, in registers; P^T goes
+//                      P^T and dS^T: one thread per key row and 32 queries (d = 128: 64), in registers; P^T goes
 //                                    to tensor memory, dS^T to a 128-byte-swizzled shared tile
 //                      dV_j += P^T dO_i                           (A operand from tensor memory)
 //                      dK_j += dS^T Q_i, dQ_i = dS K_j            (the dS^T tile read K-major / MN-major)
 //                    The dQ tile is scaled, staged in shared memory and added into an fp32
 //                    accumulator by TMA bulk reduce-add. S^T and dP^T of the next tile are computed
 //                    while the elementwise warps work on the current one. Roles: a TMA producer warp,
-//                    an MMA issuer warp, a dQ reduction warp and two elementwise warpgroups, joined by
-//                    mbarriers. dK_j, dV_j are written once, after the last query tile.
+//                    an MMA issuer warp, a dQ reduction warp and four (d = 128: two) elementwise
+//                    warpgroups, joined by mbarriers. dK_j, dV_j are written once, after the last
+//                    query tile.
 //   bwd_dq_kernel    fp32 dQ accumulator -> dQ in the input dtype
 // P and dS enter the MMAs rounded to the input dtype; everything else is fp32. Head dimension 64 or 128
 // (d = 128 holds one Q/dO tile instead of two, and shares tensor and shared memory between phases: see
@@ -87,13 +88,39 @@ struct BwdCfg {
   }
 };
 constexpr float LOG2E = 1.4426950408889634f;
-// Twelve warps: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
-// reductions (warp 2), one idle warp; warpgroups 1 and 2 = the elementwise step, each on half the query
-// columns (two warps per tensor-memory lane quarter). setmaxnreg moves registers from warpgroup 0 (96 per
-// thread) to the elementwise warpgroups (200): 128 * 96 + 256 * 200 <= 384 * 168.
-constexpr int NTHR = 384;
-constexpr int BWD_REGS_LOW = 96, BWD_REGS_HIGH = 200;
-static_assert(128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH <= NTHR * 168, "register split exceeds the launch allocation");
+// 16 columns of 32 lanes (thread t of the warp receives lane base + t), and the matching register pin.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, uint32_t (&r)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+}
+__device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
+  asm volatile(""
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15])
+               :
+               : "memory");
+}
+// Warp roles: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
+// reductions (warp 2), one idle warp; then the elementwise warpgroups, each on an equal share of the
+// step's 128 query columns, so each tensor-memory lane quarter (SM sub-partition) interleaves one warp of
+// each: four at d = 64 (32 columns each; 640 threads), two at d = 128 (64 each; 384 threads, whose
+// tensor and shared memory leave no room for more). setmaxnreg moves registers from warpgroup 0 to the
+// elementwise warpgroups: d = 64, 128 * 64 + 512 * 104 <= 640 * 96; d = 128, 128 * 96 + 256 * 200 <=
+// 384 * 168. (Two warpgroups at d = 64: 860 TFLOP/s on the 32K causal backward; four: 913, with
+// 104 registers; four with 96: 888.)
+template <int HD>
+struct BwdThreads {
+  static constexpr int NWG = HD == 64 ? 4 : 2;
+  static constexpr int NTHR = 128 * (NWG + 1);
+  static constexpr int LOW = HD == 64 ? 64 : 96, HIGH = HD == 64 ? 104 : 200;
+  static constexpr int LAUNCH_REGS = HD == 64 ? 96 : 168;
+  static_assert(128 * LOW + 128 * NWG * HIGH <= NTHR * LAUNCH_REGS, "register split exceeds the launch allocation");
+};
 
 enum : int { kBwdTimeoutLoad = 1, kBwdTimeoutMMA = 3, kBwdTimeoutSoftmax = 4 };
 
@@ -258,11 +285,15 @@ __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t
 // ACCUM = 0: monolithic (dK, dV written in the input dtype); ACCUM = 1: one chunk pair, dK and dV
 // added into fp32 accumulators.
 template <int DT, bool CAUSAL, int ACCUM, int HD>
-__global__ void __launch_bounds__(NTHR, 1)
+__global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
     attn_bwd_kernel(const __grid_constant__ CUtensorMap tmQ, const __grid_constant__ CUtensorMap tmK,
                     const __grid_constant__ CUtensorMap tmV, const __grid_constant__ CUtensorMap tmG,
                     const __grid_constant__ CUtensorMap tmDQ, const BwdParams p) {
   using C = BwdCfg<HD>;
+  using TH = BwdThreads<HD>;
+  constexpr int NWG = TH::NWG;
+  constexpr int QC = 128 / NWG;  // query columns of a warpgroup
+  constexpr int CW = NWG == 4 ? 16 : 32;  // columns per tensor-memory load
   constexpr int NSLOT = C::NSLOT;
   constexpr uint32_t TILE = C::TILE;
   extern __shared__ uint8_t smem_raw[];
@@ -324,13 +355,13 @@ __global__ void __launch_bounds__(NTHR, 1)
     for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_q[s], 1);
       mbar_init(&bar_qfree[s], 1);
-      mbar_init(&bar_staged[s], 256);
+      mbar_init(&bar_staged[s], NWG * 128);
       mbar_init(&bar_dqfree[s], 1);
     }
     mbar_init(bar_m1, 1);
     mbar_init(bar_m2, 1);
-    mbar_init(bar_sfree, 256);
-    mbar_init(bar_ready, 256);
+    mbar_init(bar_sfree, NWG * 128);
+    mbar_init(bar_ready, NWG * 128);
     mbar_init(bar_idle, 1);
     *abort_flag = 0;
     fence_mbar_init();
@@ -344,7 +375,7 @@ __global__ void __launch_bounds__(NTHR, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp < 4) {
-    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(BWD_REGS_LOW));
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(TH::LOW));
     if (warp == 0 && lane == 0) {
       // ---------------------------------------------------------------- TMA producer
       prefetch_tensormap(&tmQ);
@@ -472,7 +503,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       bulk_wait_all();
     }
   } else {
-    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(BWD_REGS_HIGH));
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TH::HIGH));
     // ------------------------------------------------------------------ elementwise warpgroups
     // warpgroup wg owns query columns [64 wg, 64 wg + 64) of each step, and feature columns
     // [d/2 wg, d/2 wg + d/2) of the dQ, dK and dV read-outs; its warp q owns tensor-memory lanes [32q, 32q + 32)
@@ -483,18 +514,22 @@ __global__ void __launch_bounds__(NTHR, 1)
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool key_ok = k0 + r < Nkv;
     const float sl2 = p.scale_log2;
-    const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(wg * BOX + r * 128);
-    const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>(wg * (BT * 128) + r * 128);
+    // dS^T row r, queries [QC wg, QC wg + QC): box (QC wg) / 64, 16-byte chunks from ((QC wg) % 64) / 8
+    const uint32_t ds_row = smem_u32(sdS) + static_cast<uint32_t>(((wg * QC) / 64) * BOX + r * 128);
+    const int ds_c0 = ((wg * QC) % 64) / 8;
+    // dQ staging (d = 64): features [16 wg, 16 wg + 16) = box wg / 2, chunks from 4 (wg % 2)
+    const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>((NWG == 4 ? wg / 2 : wg) * (BT * 128) + r * 128);
+    const int dq_c0 = NWG == 4 ? (wg % 2) * 4 : 0;
     const int sw = r & 7;
-    float* rows = sRow + wg * 256;  // [slot][lse2 64 | D 64]
-    // one value per thread: lse2 (t128 < 64) or D (t128 >= 64) of query 64 wg + (t128 & 63) of step it
+    float* rows = sRow + wg * 4 * QC;  // [slot][lse2 QC | D QC]
+    // one value per thread t < 2 QC: lse2 (t < QC) or D of query QC wg + (t % QC) of step it
     auto row_val = [&](int it) -> float {
-      const long long i = static_cast<long long>(it0 + it) * BT + wg * 64 + (t128 & 63);
-      if (it >= nit || i >= p.Nq) return t128 < 64 ? INFINITY : 0.0f;  // P = 0 for rows past the end
+      const long long i = static_cast<long long>(it0 + it) * BT + wg * QC + (t128 % QC);
+      if (it >= nit || i >= p.Nq) return t128 < QC ? INFINITY : 0.0f;  // P = 0 for rows past the end
       const long long at = static_cast<long long>(bh) * p.Nq + i;
-      return t128 < 64 ? p.lse[at] * LOG2E : p.dvec[at];
+      return t128 < QC ? p.lse[at] * LOG2E : p.dvec[at];
     };
-    rows[t128] = row_val(0);
+    if (t128 < 2 * QC) rows[t128] = row_val(0);
     bool ok = wg_bar_and(wg, true);
     // dQ of step it (after its products completed): scaled rows into the staging slot, then hand-off
     auto stage_dq = [&](int it) -> bool {
@@ -507,6 +542,20 @@ __global__ void __launch_bounds__(NTHR, 1)
         if (!w) return false;
       }
       // (d = 128: the staging area was released before this step's dS^T was written over it)
+      if constexpr (NWG == 4) {
+        uint32_t o[16];
+        tmem_ld16(trow + C::COL_DQ + wg * 16, o);
+        tmem_wait_ld();
+        reg_fence16(o);
+        const uint32_t dst = dq_row + static_cast<uint32_t>(slot * C::DQ_SLOT);
+#pragma unroll
+        for (int u = 0; u < 4; ++u)
+          st_shared_v4(dst + static_cast<uint32_t>(((dq_c0 + u) ^ sw) * 16),
+                       __float_as_uint(__uint_as_float(o[4 * u]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 1]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
+                       __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
+      } else {
 #pragma unroll
       for (int c = 0; c < HD / 64; ++c) {
         uint32_t o[32];
@@ -522,6 +571,7 @@ __global__ void __launch_bounds__(NTHR, 1)
                        __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
                        __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
       }
+      }
       fence_proxy_async_smem();
       if (HD == 128) tc_fence_before();  // dQ has left the dP^T columns the next S^T / dP^T products reuse
       mbar_arrive(&bar_staged[slot]);
@@ -533,7 +583,7 @@ __global__ void __launch_bounds__(NTHR, 1)
       const float nrow = row_val(it + 1);  // next step's row value, stored at the end of this one
       ok = wait_abort(bar_m1, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 3);
       ok = __all_sync(0xffffffffu, ok);
-      uint32_t pw[32], dw[32];
+      uint32_t pw[QC / 2], dw[QC / 2];
       if (ok) {
         tc_fence_after();
         // causal: key k0 + r hides from query i0 + q when r - q > dlt (absolute positions; |dlt| < 2^31
@@ -547,26 +597,34 @@ __global__ void __launch_bounds__(NTHR, 1)
         } else {
           diag = CAUSAL && ((it0 + it) * BT == k0);
         }
-        const float* lrow = rows + slot * 128;
-        const float* drow = lrow + 64;
+        const float* lrow = rows + slot * 2 * QC;
+        const float* drow = lrow + QC;
         // two 32-query chunks: S^T and dP^T columns in registers, then P and dS packed to 16-bit pairs;
         // S^T / dP^T are released to the next step's products once both chunks are read
 #pragma unroll
-        for (int c2 = 0; c2 < 2; ++c2) {
-          uint32_t s[32], g[32];
-          tmem_ld32(trow + C::COL_S + wg * 64 + c2 * 32, s);
-          tmem_ld32(trow + C::COL_DP + wg * 64 + c2 * 32, g);
-          tmem_wait_ld();
-          reg_fence32(s);
-          reg_fence32(g);
-          if (HD == 64 && c2 == 1) {
+        for (int c2 = 0; c2 < QC / CW; ++c2) {
+          uint32_t s[CW], g[CW];
+          if constexpr (CW == 16) {
+            tmem_ld16(trow + C::COL_S + wg * QC + c2 * CW, s);
+            tmem_ld16(trow + C::COL_DP + wg * QC + c2 * CW, g);
+            tmem_wait_ld();
+            reg_fence16(s);
+            reg_fence16(g);
+          } else {
+            tmem_ld32(trow + C::COL_S + wg * QC + c2 * CW, s);
+            tmem_ld32(trow + C::COL_DP + wg * QC + c2 * CW, g);
+            tmem_wait_ld();
+            reg_fence32(s);
+            reg_fence32(g);
+          }
+          if (HD == 64 && c2 == QC / CW - 1) {
             tc_fence_before();
             mbar_arrive(bar_sfree);
           }
 #pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const int ql = c2 * 32 + 2 * e;  // query within this warpgroup's 64
-            const int q0 = wg * 64 + ql;     // query within the tile
+          for (int e = 0; e < CW / 2; ++e) {
+            const int ql = c2 * CW + 2 * e;  // query within this warpgroup's QC
+            const int q0 = wg * QC + ql;     // query within the tile
             const float2 l2 = *reinterpret_cast<const float2*>(lrow + ql);
             const float2 dd = *reinterpret_cast<const float2*>(drow + ql);
             float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -l2.x));
@@ -581,8 +639,8 @@ __global__ void __launch_bounds__(NTHR, 1)
                 if (r > q0 + 1) p1 = 0.0f;
               }
             }
-            pw[c2 * 16 + e] = pack_pair(p0, p1, DT);
-            dw[c2 * 16 + e] = pack_pair(p0 * (__uint_as_float(g[2 * e]) - dd.x),
+            pw[c2 * (CW / 2) + e] = pack_pair(p0, p1, DT);
+            dw[c2 * (CW / 2) + e] = pack_pair(p0 * (__uint_as_float(g[2 * e]) - dd.x),
                                         p1 * (__uint_as_float(g[2 * e + 1]) - dd.y), DT);
           }
         }
@@ -606,18 +664,21 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
       if (ok) {
         // P^T (d = 128: over the first half of this warpgroup's own S^T columns, already read)
-        tmem_st16(trow + C::col_pt(wg * 4), &pw[0]);
-        tmem_st16(trow + C::col_pt(wg * 4) + 16, &pw[16]);
-        // dS^T row r, queries [64 wg, 64 wg + 64): box wg, all eight 16-byte chunks, 128-byte swizzle
+        {
+          const uint32_t pt = NWG == 4 ? 448u + static_cast<uint32_t>(wg * (QC / 2)) : C::col_pt(wg * 4);
 #pragma unroll
-        for (int u = 0; u < 8; ++u)
-          st_shared_v4(ds_row + static_cast<uint32_t>((u ^ sw) * 16), dw[4 * u], dw[4 * u + 1], dw[4 * u + 2],
-                       dw[4 * u + 3]);
+          for (int k = 0; k < QC / 32; ++k) tmem_st16(trow + pt + 16 * k, &pw[16 * k]);
+        }
+        // dS^T row r, this warpgroup's QC queries: QC / 8 16-byte chunks, 128-byte swizzle
+#pragma unroll
+        for (int u = 0; u < QC / 8; ++u)
+          st_shared_v4(ds_row + static_cast<uint32_t>(((ds_c0 + u) ^ sw) * 16), dw[4 * u], dw[4 * u + 1],
+                       dw[4 * u + 2], dw[4 * u + 3]);
         tmem_wait_st();
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_ready);
-        rows[(slot ^ 1) * 128 + t128] = nrow;
+        if (t128 < 2 * QC) rows[(slot ^ 1) * 2 * QC + t128] = nrow;
       }
       if constexpr (HD == 128) {
         // this step's dQ, out of the dP^T columns before the next step's products may be issued
@@ -642,7 +703,47 @@ __global__ void __launch_bounds__(NTHR, 1)
       }
     }
 #pragma unroll
-    for (int c = 0; c < HD / 64; ++c) {
+    if (NWG == 4 && ok) {
+      // d = 64: features [16 wg, 16 wg + 16) of dV_j and dK_j
+      const int fb = wg * 16;
+      uint32_t a[16], g[16];
+      tmem_ld16(trow + C::COL_DV + fb, a);
+      tmem_ld16(trow + C::COL_DK + fb, g);
+      tmem_wait_ld();
+      reg_fence16(a);
+      reg_fence16(g);
+      const long long row = static_cast<long long>(bh) * Nkv + k0 + r;
+      if (ACCUM && key_ok) {
+        float4* dv = reinterpret_cast<float4*>(p.dv_acc + row * HD + fb);
+        float4* dk = reinterpret_cast<float4*>(p.dk_acc + row * HD + fb);
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+          atomicAdd(dv + u, make_float4(__uint_as_float(a[4 * u]), __uint_as_float(a[4 * u + 1]),
+                                        __uint_as_float(a[4 * u + 2]), __uint_as_float(a[4 * u + 3])));
+          atomicAdd(dk + u, make_float4(__uint_as_float(g[4 * u]) * p.scale, __uint_as_float(g[4 * u + 1]) * p.scale,
+                                        __uint_as_float(g[4 * u + 2]) * p.scale,
+                                        __uint_as_float(g[4 * u + 3]) * p.scale));
+        }
+      } else if (!ACCUM && key_ok) {
+        uint4* dv = reinterpret_cast<uint4*>(p.dv + row * HD + fb);
+        uint4* dk = reinterpret_cast<uint4*>(p.dk + row * HD + fb);
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          uint4 wv, wk;
+          wv.x = pack_pair(__uint_as_float(a[8 * u]), __uint_as_float(a[8 * u + 1]), DT);
+          wv.y = pack_pair(__uint_as_float(a[8 * u + 2]), __uint_as_float(a[8 * u + 3]), DT);
+          wv.z = pack_pair(__uint_as_float(a[8 * u + 4]), __uint_as_float(a[8 * u + 5]), DT);
+          wv.w = pack_pair(__uint_as_float(a[8 * u + 6]), __uint_as_float(a[8 * u + 7]), DT);
+          wk.x = pack_pair(__uint_as_float(g[8 * u]) * p.scale, __uint_as_float(g[8 * u + 1]) * p.scale, DT);
+          wk.y = pack_pair(__uint_as_float(g[8 * u + 2]) * p.scale, __uint_as_float(g[8 * u + 3]) * p.scale, DT);
+          wk.z = pack_pair(__uint_as_float(g[8 * u + 4]) * p.scale, __uint_as_float(g[8 * u + 5]) * p.scale, DT);
+          wk.w = pack_pair(__uint_as_float(g[8 * u + 6]) * p.scale, __uint_as_float(g[8 * u + 7]) * p.scale, DT);
+          dv[u] = wv;
+          dk[u] = wk;
+        }
+      }
+    }
+    for (int c = 0; NWG == 2 && c < HD / 64; ++c) {
       if (!ok) break;
       const int fb = wg * (HD / 2) + c * 32;  // first feature of this chunk
       uint32_t a[32], g[32];
@@ -781,6 +882,9 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
                 const CUtensorMap& mdq, const BwdParams& p, int n_kv_tiles, cudaStream_t s) {
   auto kern = attn_bwd_kernel<DT, CAUSAL, ACCUM, HD>;
   constexpr uint32_t SMEM_BYTES = BwdCfg<HD>::SMEM_BYTES;
+  using TH = BwdThreads<HD>;
+  constexpr int NTHR = TH::NTHR;
+  constexpr int BWD_REGS_LOW = TH::LOW, BWD_REGS_HIGH = TH::HIGH;
   static PerDeviceOnce attr;  // the attributes belong to each device's context
   int dev = 0;
   if (!attr.done(&dev)) {
@@ -788,9 +892,9 @@ int launch_main(const CUtensorMap& mq, const CUtensorMap& mk, const CUtensorMap&
     cudaFuncAttributes fa;
     cudaError_t e = cudaFuncGetAttributes(&fa, kern);
     if (e != cudaSuccess) return cuda_status(e, "cudaFuncGetAttributes(attention backward)");
-    if (fa.numRegs * NTHR < 128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH) {
+    if (fa.numRegs * NTHR < 128 * BWD_REGS_LOW + 128 * TH::NWG * BWD_REGS_HIGH) {
       set_error("attention backward kernel built with %d registers/thread; the register split needs %d", fa.numRegs,
-                (128 * BWD_REGS_LOW + 256 * BWD_REGS_HIGH + NTHR - 1) / NTHR);
+                (128 * BWD_REGS_LOW + 128 * TH::NWG * BWD_REGS_HIGH + NTHR - 1) / NTHR);
       return CQSA_ERR_UNSUPPORTED;
     }
     e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, SMEM_BYTES);
