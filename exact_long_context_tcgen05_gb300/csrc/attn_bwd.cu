@@ -74,7 +74,8 @@ struct BwdCfg {
   static constexpr uint32_t OFF_DQ = OFF_DS + 2 * BOX;
   static constexpr uint32_t DQ_SLOT = BT * 64 * 4;        // d = 64: one staging slot (128 x 64 fp32)
   static constexpr uint32_t OFF_ROW = HD == 64 ? OFF_DQ + 2 * DQ_SLOT : OFF_DQ + 2 * BOX;
-  static constexpr uint32_t OFF_BAR = OFF_ROW + 4 * BT * 4;  // rows: per warpgroup and slot lse2[64], D[64]
+  // row values: per elementwise warp and slot, lse2 and D of the step's 128 / NWG queries (8 KiB)
+  static constexpr uint32_t OFF_BAR = OFF_ROW + 2 * 256 * 4 * 4;
   static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
   static constexpr uint32_t COL_S = 0, COL_DP = 128;
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + HD;
@@ -149,22 +150,28 @@ __device__ __forceinline__ void record_bwd_error(int code, int where) {
 }
 
 // Bounded wait that returns early once another thread of the CTA has given up.
-__device__ __forceinline__ bool wait_abort(uint64_t* bar, uint32_t parity, unsigned long long tmo,
-                                           volatile int* abort_flag, int code, int where) {
-  if (mbar_try_wait(bar, parity)) return true;
+// (32-bit shared-window addresses for the barrier and the abort flag: fewer live registers in the
+// issuer warp, which runs at 64 registers.)
+__device__ __forceinline__ bool wait_abort_a(uint32_t bar, uint32_t parity, unsigned long long tmo, uint32_t abort_a,
+                                             int code, int where) {
+  if (mbar_try_wait_a(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   uint32_t spins = 0;
   while (true) {
-    if (mbar_try_wait(bar, parity)) return true;
+    if (mbar_try_wait_a(bar, parity)) return true;
     if ((++spins & 15u) == 0) {
-      if (*abort_flag) return false;
+      if (ld_shared_volatile_u32(abort_a)) return false;
       if (globaltimer_ns() - t0 > tmo) {
         record_bwd_error(code, where);
-        *abort_flag = 1;
+        st_shared_volatile_u32(abort_a, 1u);
         return false;
       }
     }
   }
+}
+__device__ __forceinline__ bool wait_abort(uint64_t* bar, uint32_t parity, unsigned long long tmo,
+                                           volatile int* abort_flag, int code, int where) {
+  return wait_abort_a(smem_u32(bar), parity, tmo, smem_u32(const_cast<int*>(abort_flag)), code, where);
 }
 
 __device__ __forceinline__ bool elect_lane() {
@@ -214,17 +221,6 @@ __device__ __forceinline__ void tma_reduce_add_3d(uint32_t src, const CUtensorMa
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_read_all() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-// AND of `v` over the 128 threads of elementwise warpgroup wg (named barrier wg + 1).
-__device__ __forceinline__ bool wg_bar_and(int wg, bool v) {
-  uint32_t r;
-  asm volatile(
-      "{\n\t.reg .pred p, q;\n\tsetp.ne.u32 p, %1, 0;\n\tbar.red.and.pred q, %2, 128, p;\n\tselp.u32 %0, 1, 0, q;\n\t}"
-      : "=r"(r)
-      : "r"(static_cast<uint32_t>(v)), "r"(wg + 1)
-      : "memory");
-  return r != 0;
-}
 
 __device__ __forceinline__ float ex2(float x) {
   float y;
@@ -306,7 +302,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
   // dQ staging: d = 64, two slots of 128 x 64 fp32 (two 32-float boxes each); d = 128, one 128 x 128 fp32
   // tile in four 32-float boxes over dS^T and the 32 KiB behind it
   uint8_t* sdQ = HD == 64 ? sm + C::OFF_DQ : sdS;
-  float* sRow = reinterpret_cast<float*>(sm + C::OFF_ROW);  // [wg 2][slot 2][lse2 64 | D 64]
+  float* sRow = reinterpret_cast<float*>(sm + C::OFF_ROW);  // per elementwise warp: [slot 2][lse2 | D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* bar_kv = bars + 0;
   uint64_t* bar_q = bars + 1;       // [NSLOT] Q/dO slot loaded
@@ -521,16 +517,39 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
     const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>((NWG == 4 ? wg / 2 : wg) * (BT * 128) + r * 128);
     const int dq_c0 = NWG == 4 ? (wg % 2) * 4 : 0;
     const int sw = r & 7;
-    float* rows = sRow + wg * 4 * QC;  // [slot][lse2 QC | D QC]
-    // one value per thread t < 2 QC: lse2 (t < QC) or D of query QC wg + (t % QC) of step it
-    auto row_val = [&](int it) -> float {
-      const long long i = static_cast<long long>(it0 + it) * BT + wg * QC + (t128 % QC);
-      if (it >= nit || i >= p.Nq) return t128 < QC ? INFINITY : 0.0f;  // P = 0 for rows past the end
-      const long long at = static_cast<long long>(bh) * p.Nq + i;
-      return t128 < QC ? p.lse[at] * LOG2E : p.dvec[at];
+    // Row values private to this warp ([slot][lse2 QC | D QC]): each lane fetches QC / 32 queries' lse2
+    // and D one step ahead and the warp shares them through shared memory after a __syncwarp, so no
+    // barrier across the warpgroup is needed per step.
+    float* rows = sRow + (warp - 4) * 4 * QC;
+    struct RowVals {
+      float l[QC / 32], d[QC / 32];
     };
-    if (t128 < 2 * QC) rows[t128] = row_val(0);
-    bool ok = wg_bar_and(wg, true);
+    auto row_vals = [&](int it) -> RowVals {
+      RowVals v;
+#pragma unroll
+      for (int k = 0; k < QC / 32; ++k) {
+        const long long i = static_cast<long long>(it0 + it) * BT + wg * QC + k * 32 + lane;
+        if (it >= nit || i >= p.Nq) {
+          v.l[k] = -INFINITY;  // P = 0 for rows past the end
+          v.d[k] = 0.0f;
+        } else {
+          const long long at = static_cast<long long>(bh) * p.Nq + i;
+          v.l[k] = -(p.lse[at] * LOG2E);  // negated: the packed products below add them
+          v.d[k] = -p.dvec[at];
+        }
+      }
+      return v;
+    };
+    auto put_rows = [&](int slot, const RowVals& v) {
+#pragma unroll
+      for (int k = 0; k < QC / 32; ++k) {
+        rows[slot * 2 * QC + k * 32 + lane] = v.l[k];
+        rows[slot * 2 * QC + QC + k * 32 + lane] = v.d[k];
+      }
+      __syncwarp();
+    };
+    put_rows(0, row_vals(0));
+    bool ok = true;
     // dQ of step it (after its products completed): scaled rows into the staging slot, then hand-off
     auto stage_dq = [&](int it) -> bool {
       const int slot = HD == 64 ? (it & 1) : 0;
@@ -580,7 +599,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
 
     for (int it = 0; ok && it < nit; ++it) {
       const int slot = it & 1;
-      const float nrow = row_val(it + 1);  // next step's row value, stored at the end of this one
+      const RowVals nrow = row_vals(it + 1);  // next step's row values, stored at the end of this one
       ok = wait_abort(bar_m1, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutMMA, 3);
       ok = __all_sync(0xffffffffu, ok);
       uint32_t pw[QC / 2], dw[QC / 2];
@@ -625,10 +644,12 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
           for (int e = 0; e < CW / 2; ++e) {
             const int ql = c2 * CW + 2 * e;  // query within this warpgroup's QC
             const int q0 = wg * QC + ql;     // query within the tile
-            const float2 l2 = *reinterpret_cast<const float2*>(lrow + ql);
-            const float2 dd = *reinterpret_cast<const float2*>(drow + ql);
-            float p0 = ex2(fmaf(__uint_as_float(s[2 * e]), sl2, -l2.x));
-            float p1 = ex2(fmaf(__uint_as_float(s[2 * e + 1]), sl2, -l2.y));
+            const float2 nl = *reinterpret_cast<const float2*>(lrow + ql);  // -lse2 of the two queries
+            const float2 nd = *reinterpret_cast<const float2*>(drow + ql);  // -D
+            const float2 arg = __ffma2_rn(make_float2(__uint_as_float(s[2 * e]), __uint_as_float(s[2 * e + 1])),
+                                          make_float2(sl2, sl2), nl);
+            float p0 = ex2(arg.x);
+            float p1 = ex2(arg.y);
             if (!key_ok) p0 = p1 = 0.0f;
             if (diag) {
               if constexpr (ACCUM) {
@@ -640,8 +661,10 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
               }
             }
             pw[c2 * (CW / 2) + e] = pack_pair(p0, p1, DT);
-            dw[c2 * (CW / 2) + e] = pack_pair(p0 * (__uint_as_float(g[2 * e]) - dd.x),
-                                        p1 * (__uint_as_float(g[2 * e + 1]) - dd.y), DT);
+            const float2 gd =
+                __fadd2_rn(make_float2(__uint_as_float(g[2 * e]), __uint_as_float(g[2 * e + 1])), nd);
+            const float2 ds = __fmul2_rn(make_float2(p0, p1), gd);
+            dw[c2 * (CW / 2) + e] = pack_pair(ds.x, ds.y, DT);
           }
         }
       }
@@ -678,7 +701,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         fence_proxy_async_smem();
         tc_fence_before();
         mbar_arrive(bar_ready);
-        if (t128 < 2 * QC) rows[(slot ^ 1) * 2 * QC + t128] = nrow;
+        put_rows(slot ^ 1, nrow);
       }
       if constexpr (HD == 128) {
         // this step's dQ, out of the dP^T columns before the next step's products may be issued
@@ -691,7 +714,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
           }
         }
       }
-      ok = wg_bar_and(wg, ok);
+      ok = __all_sync(0xffffffffu, ok);
     }
     if (HD == 64 && ok) {
       // last step: dQ, then dV_j and dK_j rows (key row = tensor-memory lane), written once
