@@ -61,7 +61,8 @@ constexpr int NBAR = 14;
 //   128 x 64 fp32 (195 KiB). Tensor memory: S^T, dP^T, dV, dK, dQ and P^T (16-bit pairs), 512 columns.
 // d = 128: every 128-row tile is two boxes, so K, V, one Q and one dO tile and dS^T take 160 KiB; dQ
 //   (128 x 128 fp32, 64 KiB) is staged over the dS^T tile and the 32 KiB behind it once the step's
-//   products have read dS^T. Tensor memory: S^T 0-127 (each warpgroup writes its P^T over the first
+//   products have read dS^T. Q and dO have their own load and release barriers (bar_q[0] / bar_q[1],
+//   bar_qfree[0] / bar_qfree[1]), released after dK and after dV, so each reloads as early as it can. Tensor memory: S^T 0-127 (each warpgroup writes its P^T over the first
 //   half of its own S^T columns), dP^T 128-255 (dQ is accumulated over it after dS is formed), dV
 //   256-383, dK 384-511.
 template <int HD>
@@ -398,17 +399,41 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
           tma_load_4d(sV + x * BOX, &tmV, bar_kv, x * 64, k0, h, b);
         }
       }
-      for (int it = 0; it < NSLOT && it < nit; ++it) load_q(it);
-      for (int it = 0; it + NSLOT < nit; ++it) {
-        // slot it % NSLOT is free once every MMA of step it has read it
-        if (!wait_abort(&bar_qfree[it % NSLOT], static_cast<uint32_t>((it / NSLOT) & 1), tmo, abort_flag,
-                        kBwdTimeoutLoad, 5))
-          break;
-        load_q(it + NSLOT);
+      if constexpr (HD == 64) {
+        for (int it = 0; it < NSLOT && it < nit; ++it) load_q(it);
+        for (int it = 0; it + NSLOT < nit; ++it) {
+          // slot it % NSLOT is free once every MMA of step it has read it
+          if (!wait_abort(&bar_qfree[it % NSLOT], static_cast<uint32_t>((it / NSLOT) & 1), tmo, abort_flag,
+                          kBwdTimeoutLoad, 5))
+            break;
+          load_q(it + NSLOT);
+        }
+      } else {
+        // d = 128, one tile each: dO (bar_q[1]) is refilled once dV of the step has read it, Q (bar_q[0])
+        // once dK has; the issuer commits the two releases separately (bar_qfree[1], bar_qfree[0])
+        auto load_one = [&](int it, int which) {
+          uint8_t* dst = which ? sG : sQ;
+          const CUtensorMap* map = which ? &tmG : &tmQ;
+          mbar_arrive_expect_tx(&bar_q[which], TILE);
+#pragma unroll
+          for (int x = 0; x < HD / 64; ++x)
+            tma_load_4d(dst + x * BOX, map, &bar_q[which], x * 64, (it0 + it) * BT, h, b);
+          ++issued[which];
+        };
+        if (nit > 0) {
+          load_one(0, 0);
+          load_one(0, 1);
+        }
+        for (int it = 0; it + 1 < nit; ++it) {
+          if (!wait_abort(&bar_qfree[1], static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutLoad, 5)) break;
+          load_one(it + 1, 1);
+          if (!wait_abort(&bar_qfree[0], static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutLoad, 5)) break;
+          load_one(it + 1, 0);
+        }
       }
       // every load issued lands before the CTA exits (bounded waits)
       if (!skip_kv) mbar_wait_bounded(bar_kv, 0, tmo);
-      for (int s = 0; s < NSLOT; ++s)
+      for (int s = 0; s < 2; ++s)
         if (issued[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued[s] - 1) & 1), tmo);
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
@@ -454,8 +479,52 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         }
         __syncwarp();
       };
+      // d = 128: the three gradient products one after another, with the release of dO (after dV) and of
+      // Q (after dK) committed in between, so that the producer refills each as early as possible
+      auto issue_grads_128 = [&](int it) {
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < BT / 16; ++ks) {
+            const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));
+            if (it == 0 && ks == 0) mma_ts_imm<0>(tmem + C::COL_DV, tmem + C::col_pt(ks), dG0_mn + off, IDESC_V);
+            else mma_ts_imm<1>(tmem + C::COL_DV, tmem + C::col_pt(ks), dG0_mn + off, IDESC_V);
+          }
+          tc_commit(&bar_qfree[1]);
+#pragma unroll
+          for (int ks = 0; ks < BT / 16; ++ks) {
+            const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));
+            const uint32_t koff = static_cast<uint32_t>((ks >> 2) * (BOX >> 4) + (ks & 3) * 2);
+            if (it == 0 && ks == 0) mma_ss_imm<0>(tmem + C::COL_DK, dS_k + koff, dQ0_mn + off, IDESC_V);
+            else mma_ss_imm<1>(tmem + C::COL_DK, dS_k + koff, dQ0_mn + off, IDESC_V);
+          }
+          tc_commit(&bar_qfree[0]);
+#pragma unroll
+          for (int ks = 0; ks < BT / 16; ++ks) {
+            const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));
+            if (ks == 0) mma_ss_imm<0>(tmem + C::COL_DQ, dS_mn + off, dK_mn + off, IDESC_Q);
+            else mma_ss_imm<1>(tmem + C::COL_DQ, dS_mn + off, dK_mn + off, IDESC_Q);
+          }
+          tc_commit(bar_m2);
+        }
+        __syncwarp();
+      };
+      auto issue_s_128 = [&]() {  // S^T of the next step, behind this thread's dV (P^T is over S^T)
+        tc_fence_after();
+        if (leader) issue_t<HD>(tmem + C::COL_S, dK_k, dQ0_k, IDESC_T);
+        __syncwarp();
+      };
+      auto issue_dp_128 = [&]() {  // dP^T of the next step, over the dQ columns once dQ is staged out
+        tc_fence_after();
+        if (leader) {
+          issue_t<HD>(tmem + C::COL_DP, dV_k, dG0_k, IDESC_T);
+          tc_commit(bar_m1);
+        }
+        __syncwarp();
+      };
       bool ok = wait_all(bar_kv, 0, kBwdTimeoutLoad, 1);
       if (ok) ok = wait_all(&bar_q[0], 0, kBwdTimeoutLoad, 2);
+      if (HD == 128 && ok) ok = wait_all(&bar_q[1], 0, kBwdTimeoutLoad, 2);
       if (ok) issue_m1(0);
       for (int it = 0; ok && it < nit; ++it) {
         if constexpr (HD == 64) {
@@ -472,11 +541,13 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
           // next S^T is issued behind it by this thread); the next step's S^T and dP^T once the single
           // Q/dO slot holds step it + 1 and dQ of step it has left the dP^T columns
           ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
-          if (ok) issue_m2(it);
+          if (ok) issue_grads_128(it);
           if (ok && it + 1 < nit) {
-            ok = wait_all(&bar_staged[0], static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 10);
-            if (ok) ok = wait_all(&bar_q[0], static_cast<uint32_t>((it + 1) & 1), kBwdTimeoutLoad, 2);
-            if (ok) issue_m1(it + 1);
+            ok = wait_all(&bar_q[0], static_cast<uint32_t>((it + 1) & 1), kBwdTimeoutLoad, 2);
+            if (ok) issue_s_128();
+            if (ok) ok = wait_all(&bar_staged[0], static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 10);
+            if (ok) ok = wait_all(&bar_q[1], static_cast<uint32_t>((it + 1) & 1), kBwdTimeoutLoad, 2);
+            if (ok) issue_dp_128();
           }
         }
       }
@@ -505,7 +576,6 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
     // [d/2 wg, d/2 wg + d/2) of the dQ, dK and dV read-outs; its warp q owns tensor-memory lanes [32q, 32q + 32)
     const int wg = (warp >> 2) - 1;
     const int quarter = warp & 3;
-    const int t128 = tid & 127;
     const int r = quarter * 32 + lane;  // key row (tensor-memory lane) of P^T / dS^T; query row of dQ
     const uint32_t trow = tmem + (static_cast<uint32_t>(quarter * 32) << 16);
     const bool key_ok = k0 + r < Nkv;
@@ -725,7 +795,6 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         ok = stage_dq(nit - 1);
       }
     }
-#pragma unroll
     if (NWG == 4 && ok) {
       // d = 64: features [16 wg, 16 wg + 16) of dV_j and dK_j
       const int fb = wg * 16;
