@@ -363,8 +363,10 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s_full[t], 1);
-      mbar_init(&bar_s_free[t], 128);
-      mbar_init(&bar_p_full[t], 128);
+      // P kept apart (fp16, d = 64): one arrival per softmax warp; P over S: one per thread (measured:
+      // per-warp arrivals gain 1% at fp16 d = 64 and lose 4% at bf16 d = 128)
+      mbar_init(&bar_s_free[t], ALIAS ? 128 : 4);
+      mbar_init(&bar_p_full[t], ALIAS ? 128 : 4);
       mbar_init(&bar_pv_done[t], 1);
       mbar_init(&bar_o_final[t], 1);
       mbar_init(&bar_mma_idle[t], 1);
@@ -631,7 +633,8 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
         for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         if (!ALIAS) {
           tc_fence_before();
-          mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
         }
 
         float x[128];
@@ -728,7 +731,12 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
         }
         tmem_wait_st();
         tc_fence_before();
-        mbar_arrive_a(a_p_full);
+        if (!ALIAS) {
+          __syncwarp();
+          if (lane == 0) mbar_arrive_a(a_p_full);
+        } else {
+          mbar_arrive_a(a_p_full);
+        }
       }
     }
 
