@@ -507,8 +507,11 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1, engine="classic
 
     mono_s = None
     if device_inputs:
+        # the call returns after its own streams drain, so each interval also holds its host-side work
+        # (schedule, pool, launches); median of 7
         call()
-        ms = statistics.median(_time_events(call, 3, stream))
+        samples = _time_events(call, 7, stream)
+        ms = statistics.median(samples)
         wall = ms / 1e3
         # the monolithic call on the same problem ([B,H,N,d] copies of the same device inputs)
         qb, kb, vb = (x.permute(0, 2, 1, 3).contiguous() for x in qkv)
@@ -519,7 +522,7 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1, engine="classic
             cq.cqsa_attn_fwd(qb, kb, vb, ob, lb, 1, Hs, n_tokens, Ds, True, 0.0, cq.CQSA_F16, stream)
 
         mono_call()
-        mono_s = statistics.median(_time_events(mono_call, 3, stream)) / 1e3
+        mono_s = statistics.median(_time_events(mono_call, 7, stream)) / 1e3
         del qb, kb, vb, ob
     else:
         t0 = time.perf_counter()
@@ -529,7 +532,8 @@ def measure_quorum(cq, dev, n_tokens, acc_on_host=False, npar=1, engine="classic
     where = "device-resident token-major Q/K/V/out" if device_inputs else "token-major pinned host Q/K/V/out"
     extra = {}
     if mono_s:
-        extra = {"mono_tflops": flop / mono_s / 1e12, "over_mono": mono_s / wall}
+        extra = {"mono_tflops": flop / mono_s / 1e12, "over_mono": mono_s / wall,
+                 "ms_samples": [round(x, 3) for x in samples]}
     return {"measure": "quorum", "workload": f"cyclic quorum decomposition, B=1 H=8 N={n_tokens} d=64 fp16 causal, "
             f"c={c} interest_set={D} itr={itr}, {where}", "wall_s": wall, **extra,
             "tflops": flop / wall / 1e12, "compute_s": st.compute_ms / 1e3, "copy_s": st.copy_ms / 1e3,

@@ -293,6 +293,7 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
   constexpr int STAGES = C::STAGES;
   constexpr int KSUB = C::KSUB;
   constexpr bool ALIAS = C::ALIAS;
+  constexpr bool WARP_ARRIVE = !ALIAS && MODE != kModeMulti;
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -363,10 +364,11 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
     }
     for (int t = 0; t < 2; ++t) {
       mbar_init(&bar_s_full[t], 1);
-      // P kept apart (fp16, d = 64): one arrival per softmax warp; P over S: one per thread (measured:
-      // per-warp arrivals gain 1% at fp16 d = 64 and lose 4% at bf16 d = 128)
-      mbar_init(&bar_s_free[t], ALIAS ? 128 : 4);
-      mbar_init(&bar_p_full[t], ALIAS ? 128 : 4);
+      // One arrival per softmax warp where P is kept apart (fp16, d = 64) in the single-pair kernel, one
+      // per thread otherwise (measured: per-warp arrivals gain 1% on the 32K bench shape and 4.5% at
+      // 262K tokens, and lose 4% at bf16 d = 128 and 13% in the multi-pair launch of the wave engine)
+      mbar_init(&bar_s_free[t], WARP_ARRIVE ? 4 : 128);
+      mbar_init(&bar_p_full[t], WARP_ARRIVE ? 4 : 128);
       mbar_init(&bar_pv_done[t], 1);
       mbar_init(&bar_o_final[t], 1);
       mbar_init(&bar_mma_idle[t], 1);
@@ -633,8 +635,12 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
         for (int c = 0; c < 4; ++c) reg_fence32(*reinterpret_cast<uint32_t(*)[32]>(&sr[c * 32]));
         if (!ALIAS) {
           tc_fence_before();
-          __syncwarp();
-          if (lane == 0) mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+          if (WARP_ARRIVE) {
+            __syncwarp();
+            if (lane == 0) mbar_arrive_a(a_s_free);  // S_t may now take S_t(j+1)
+          } else {
+            mbar_arrive_a(a_s_free);
+          }
         }
 
         float x[128];
@@ -731,7 +737,7 @@ __device__ __forceinline__ void attn_fwd2_body(const CUtensorMap& tmQ, const CUt
         }
         tmem_wait_st();
         tc_fence_before();
-        if (!ALIAS) {
+        if (WARP_ARRIVE) {
           __syncwarp();
           if (lane == 0) mbar_arrive_a(a_p_full);
         } else {
