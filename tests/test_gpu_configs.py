@@ -44,6 +44,17 @@ def test_causal_32k_d64_fp16(cq):
     ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=True, rows=rows)
     mx, mn = assert_close(_gather(out, rows), ro, _gather(lse, rows), rl, what="32K causal")
     print(f"\n32K causal d64 fp16 on {len(rows)} rows: max abs {mx:.2e} mean abs {mn:.2e}")
+    # the benchmark's end-to-end path on the same inputs: pinned host buffers through the streaming
+    # driver in 4,096-token chunks (inputs resident, one launch per query chunk over its key prefix)
+    # gives the monolithic call's bits
+    hq, hk, hv = (x.cpu().pin_memory() for x in (q, k, v))
+    hout = torch.empty((B, H, N, d), dtype=torch.float16).pin_memory()
+    hlse = torch.empty((B, H, N), dtype=torch.float32).pin_memory()
+    st = cq.cqsa_stream_stats()
+    cq.cqsa_stream_attn_fwd(hq, hk, hv, cq.CQSA_LAYOUT_BHND, hout, hlse, True, B, H, N, d, True, 0.0, cq.CQSA_F16,
+                            N // 8, st)
+    assert st.n_chunks == 8, "the 32K workload's inputs fit: one launch per query chunk"
+    assert torch.equal(hout.cuda(), out) and torch.equal(hlse.cuda(), lse)
 
 
 def test_noncausal_16k_d128_bf16_peaked(cq):
@@ -160,6 +171,27 @@ def test_chunked_131k_merge_equals_monolithic(cq):
     ro, rl, _ = oracle.attn_rows(qn, kn, vn, B=B, H=H, Nq=N, d=d, causal=True, rows=rows)
     mx, mn = assert_close(_gather(out, rows), ro, _gather(lse, rows), rl, what="131K chunked vs oracle")
     print(f"\n131K chunked: chunked-vs-mono worst row rel {worst:.2e}; vs oracle max abs {mx:.2e} mean abs {mn:.2e}")
+
+
+def test_wave_engine_262k_equals_monolithic(cq):
+    """The quorum decomposition of the bench's wave-engine line (B=1 H=8 N=262,144 d=64 fp16 causal,
+    c = 31, interest set (0, 1, 3, 8, 12, 18), token-major device inputs read in place): its adjacent key
+    chunks run as one key range per query chunk, so the result is the monolithic call's, bit for bit."""
+    B, H, N, d = 1, 8, 262_144, 64
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=3, layout=syn.LAYOUT_BNHD)
+    q, k, v = (to_dev(x, syn.F16) for x in (qn, kn, vn))
+    out = torch.empty((B, N, H, d), dtype=torch.float16, device="cuda")
+    lse = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    st = cq.cqsa_quorum_stats()
+    cq.cqsa_quorum_attn_fwd_ex(q, k, v, cq.CQSA_LAYOUT_BNHD, False, out, lse, False, B, H, N, d, True, 0.0,
+                               cq.CQSA_F16, 31, (0, 1, 3, 8, 12, 18), 1, engine=cq.CQSA_ENGINE_WAVE, stats=st)
+    assert st.n_pairs == 496
+    qb, kb, vb = (x.permute(0, 2, 1, 3).contiguous() for x in (q, k, v))
+    ob = torch.empty_like(qb)
+    lb = torch.empty((B, H, N), dtype=torch.float32, device="cuda")
+    cq.cqsa_attn_fwd(qb, kb, vb, ob, lb, B, H, N, d, True, 0.0, cq.CQSA_F16)
+    torch.cuda.synchronize()
+    assert torch.equal(out.permute(0, 2, 1, 3), ob) and torch.equal(lse, lb)
 
 
 def test_streaming_4m_host_resident(cq):
