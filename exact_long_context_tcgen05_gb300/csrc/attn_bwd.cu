@@ -887,15 +887,19 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
 }
 
 // D_i = dO_i . O_i in fp32: d/8 threads per row (8 for d = 64, 16 for d = 128), one 16-byte load of
-// each per thread, summed across the row's threads by shuffles.
+// each per thread, summed across the row's threads by shuffles. Row r of the `rows` = BH * n rows is
+// token t0 + r % n of head r / n of [BH, N, d] tensors (n = N, t0 = 0 for packed rows).
 template <int DT, int HD>
-__global__ void __launch_bounds__(256) bwd_dot_kernel(const uint4* o, const uint4* g, float* dvec, long long rows) {
+__global__ void __launch_bounds__(256) bwd_dot_kernel(const uint4* o, const uint4* g, float* dvec, long long rows,
+                                                      long long n, long long N, long long t0) {
   constexpr int TPR = HD / 8;
   const long long t = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x;
   const long long row = t / TPR;
+  const long long frow = (row / n) * N + t0 + row % n;  // the row's index in the [BH, N] tensors
+  const long long e = frow * TPR + t % TPR;            // this thread's 16-byte word
   float acc = 0.0f;
   if (row < rows) {
-    const uint4 a = __ldg(o + t), c = __ldg(g + t);
+    const uint4 a = __ldg(o + e), c = __ldg(g + e);
     const uint32_t aw[4] = {a.x, a.y, a.z, a.w}, cw[4] = {c.x, c.y, c.z, c.w};
 #pragma unroll
     for (int u = 0; u < 4; ++u) {
@@ -906,7 +910,7 @@ __global__ void __launch_bounds__(256) bwd_dot_kernel(const uint4* o, const uint
   }
 #pragma unroll
   for (int m = TPR / 2; m >= 1; m >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, m);
-  if (row < rows && (t % TPR) == 0) dvec[row] = acc;
+  if (row < rows && (t % TPR) == 0) dvec[frow] = acc;
 }
 
 // fp32 dQ accumulator -> input dtype, four elements per thread.
@@ -1070,21 +1074,27 @@ size_t attention_bwd_workspace(int B, int H, int N, int d) {
   return dq + rows * sizeof(float);
 }
 
-int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int d, int dtype,
-                    cudaStream_t stream) {
+int launch_bwd_dvec_range(const void* out, const void* dout, float* dvec, long long BH, long long n, long long N,
+                          long long t0, int d, int dtype, cudaStream_t stream) {
+  const long long rows = BH * n;
   if (rows <= 0) return CQSA_OK;
   const long long dot_threads = rows * (d / 8);
   const unsigned dot_blocks = static_cast<unsigned>((dot_threads + 255) / 256);
   const uint4* o = static_cast<const uint4*>(out);
   const uint4* g = static_cast<const uint4*>(dout);
   if (d == 128) {
-    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
-    else bwd_dot_kernel<0, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows, n, N, t0);
+    else bwd_dot_kernel<0, 128><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows, n, N, t0);
   } else {
-    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
-    else bwd_dot_kernel<0, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows);
+    if (dtype == CQSA_BF16) bwd_dot_kernel<1, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows, n, N, t0);
+    else bwd_dot_kernel<0, 64><<<dot_blocks, 256, 0, stream>>>(o, g, dvec, rows, n, N, t0);
   }
   return cuda_status(cudaGetLastError(), "attention backward dot kernel launch");
+}
+
+int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int d, int dtype,
+                    cudaStream_t stream) {
+  return launch_bwd_dvec_range(out, dout, dvec, 1, rows, rows, 0, d, dtype, stream);
 }
 
 int launch_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream) {

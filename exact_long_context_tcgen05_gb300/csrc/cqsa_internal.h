@@ -81,6 +81,15 @@ int launch_attention_bwd_chunk(const BwdArgs& a, cudaStream_t stream);
 // D_i = dout_i . out_i (fp32) for `rows` rows of 64 features; fp32 -> dtype for n elements (n % 4 == 0).
 int launch_bwd_dvec(const void* out, const void* dout, float* dvec, long long rows, int d, int dtype,
                     cudaStream_t stream);
+// Host-streaming helpers (stream_driver.cu): whether `bytes` of device memory fit the resident budget
+// (cqsa_set_stream_kv_resident_bytes), and a copy of tokens [t0, t0 + n) of a (layout, N tokens) tensor
+// into the same positions of another of the same shape; *bytes grows by the bytes copied.
+bool stream_resident_ok(size_t bytes);
+cudaError_t copy_range(void* dst, const void* src, int layout, int B, int H, long long N, int d, long long t0, int n,
+                       cudaMemcpyKind kind, cudaStream_t s, long long* bytes);
+// D for tokens [t0, t0 + n) of every head of [BH, N, d] out / dout, into dvec [BH, N] at the same rows.
+int launch_bwd_dvec_range(const void* out, const void* dout, float* dvec, long long BH, long long n, long long N,
+                          long long t0, int d, int dtype, cudaStream_t stream);
 int launch_bwd_cast(const float* acc, void* out, long long n, int dtype, cudaStream_t stream);
 
 // LSE merge of n partials (device pointer arrays passed by value).

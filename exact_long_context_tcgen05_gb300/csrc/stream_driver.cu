@@ -147,8 +147,9 @@ int launch_finalize(const float* acc, const float* lse_acc, void* out, float* ls
 // launch has fewer CTAs than the GPU has SMs, and one launch's last wave overlaps the next ones.
 namespace {
 std::atomic<long long> g_kv_resident_bytes{-1};
+}  // namespace
 
-bool kv_resident_ok(size_t bytes) {
+bool stream_resident_ok(size_t bytes) {
   const long long lim = g_kv_resident_bytes.load();
   if (lim == 0) return false;
   if (lim > 0) return static_cast<long long>(bytes) <= lim;
@@ -180,7 +181,6 @@ cudaError_t copy_range(void* dst, const void* src, int layout, int B, int H, lon
   return cudaMemcpy2DAsync(static_cast<char*>(dst) + off, pitch, static_cast<const char*>(src) + off, pitch, width,
                            height, kind, s);
 }
-}  // namespace
 
 int stream_fwd_resident(const void* q_host, const void* k_host, const void* v_host, int layout, void* out, float* lse,
                         int out_on_host, int B, int H, long long N, int d, int causal, float sc, int dtype, long long C,
@@ -460,7 +460,7 @@ extern "C" int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, cons
   // stay in L2 only then (4M tokens, 1 GB per head: 1,091 TFLOP/s resident against 1,145 accumulating).
   const bool kv_fits_l2 = 2.0 * static_cast<double>(N) * d * es <= 64.0 * 1024 * 1024;
   if (N <= 0x7fffffffLL && kv_fits_l2 &&
-      kv_resident_ok(4 * static_cast<size_t>(B) * H * N * d * es + static_cast<size_t>(B) * H * N * 4))
+      stream_resident_ok(4 * static_cast<size_t>(B) * H * N * d * es + static_cast<size_t>(B) * H * N * 4))
     return stream_fwd_resident(q_host, k_host, v_host, layout, out, lse, out_on_host, B, H, N, d, causal, sc, dtype, C,
                                nch, stats, stream, t_start);
 

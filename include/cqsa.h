@@ -116,7 +116,8 @@ int cqsa_stream_attn_fwd(const void* q_host, const void* k_host, const void* v_h
                          cudaStream_t stream);
 
 /*
- * Resident inputs for cqsa_stream_attn_fwd. When Q, K, V and the output (4 * B*H*N*d*2 bytes, plus
+ * Resident inputs for cqsa_stream_attn_fwd (and the budget of cqsa_stream_attn_bwd's resident schedule,
+ * described with it). When Q, K, V and the output (4 * B*H*N*d*2 bytes, plus
  * B*H*N*4 of lse) take at most `bytes` of device memory (bytes < 0, the default: at most half of the
  * device's free memory at the call; 0: never), and one head's K and V (2*N*d*2 bytes) fit the 64 MiB
  * of L2 the kernel groups heads by (longer prefixes would have every CTA sweep keys L2 cannot hold, and
@@ -289,13 +290,20 @@ int cqsa_attn_bwd_cast(const float* acc, void* out, long long n, int dtype, cuda
  * each streamed chunk (inputs, D, lse, the dq accumulator, output staging), from the library's pool
  * (CQSA_ERR_OOM if they do not fit). Synchronous; the result equals cqsa_attn_bwd's up to the fp32
  * summation order. Returns CQSA_ERR_TIMEOUT if a kernel's bounded wait gave up.
+  * When q, out, dout, lse, D, the fp32 dq accumulator, every K/V chunk and the dk/dv accumulators fit
+ * the resident budget (cqsa_set_stream_kv_resident_bytes; about 14 bytes of device memory per byte of
+ * one input tensor), every chunk is instead copied once and stays: key chunks go from the last to the
+ * first, the query side copied in the same order, and each key chunk is one launch of the chunk-pair
+ * kernel over every query it meets, the launches round-robin over up to four streams.
  */
 int cqsa_stream_attn_bwd(const void* q, const void* k, const void* v, const void* out, const void* dout,
                          const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d, int causal,
                          float scale, int dtype, long long chunk_tokens, cudaStream_t stream);
 /* The same call, filling *stats (may be NULL): compute_ms sums the event intervals of its kernel segments
  * (D and the dq zeroing of each query chunk, each pair, each output cast), h2d_ms those of its copy
- * groups, stall_ms the gaps between consecutive kernel segments, n_chunks the pairs run. */
+ * groups, stall_ms the gaps between consecutive kernel segments, n_chunks the pairs run. On the resident
+ * schedule compute_ms is the union of the kernel intervals (its launches overlap on several streams) and
+ * n_chunks the key-chunk launches. */
 int cqsa_stream_attn_bwd_ex(const void* q, const void* k, const void* v, const void* out, const void* dout,
                             const float* lse, void* dq, void* dk, void* dv, int B, int H, long long N, int d,
                             int causal, float scale, int dtype, long long chunk_tokens, cqsa_stream_stats* stats,

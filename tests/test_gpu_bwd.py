@@ -236,21 +236,28 @@ def test_chunk_pair_above_diagonal_adds_nothing(cq):
     assert all(bool((a == 0.5).all()) for a in accs)
 
 
+@pytest.mark.parametrize("resident", [True, False])
 @pytest.mark.parametrize("B,H,N,C,causal,d", [(2, 2, 640, 256, True, 64), (1, 2, 384, 128, False, 64),
                                              (1, 2, 640, 256, True, 128)])
-def test_stream_backward(cq, B, H, N, C, causal, d):
-    """Host-resident backward over chunks (ragged last chunk, several batches and heads): equal to the
-    monolithic device call within a few ulps (fp32 summation order differs)."""
+def test_stream_backward(cq, B, H, N, C, causal, d, resident):
+    """Host-resident backward over chunks (ragged last chunk, several batches and heads), with the inputs
+    kept resident (one launch per key chunk over every query) and through double-buffered chunk pairs:
+    equal to the monolithic device call within a few ulps (fp32 summation order differs)."""
     dtype = syn.F16
     (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, causal, dtype)
     q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
     out, lse = mono(cq, q, k, v, B, H, N, d, causal, dtype)
     host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
     grads = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
-    st = cq.cqsa_stream_attn_bwd_ex(*host, *grads, B, H, N, d, causal, 0.0, dtype, C)
+    cq.cqsa_set_stream_kv_resident_bytes(1 << 40 if resident else 0)
+    try:
+        st = cq.cqsa_stream_attn_bwd_ex(*host, *grads, B, H, N, d, causal, 0.0, dtype, C)
+    finally:
+        cq.cqsa_set_stream_kv_resident_bytes(-1)
     n_chunks = -(-N // C)
     pairs = n_chunks * (n_chunks + 1) // 2 if causal else n_chunks * n_chunks
-    assert st.n_chunks == pairs and st.compute_ms > 0 and st.wall_ms >= st.compute_ms * 0.5
+    assert st.n_chunks == (n_chunks if resident else pairs) and st.compute_ms > 0
+    assert st.wall_ms >= st.compute_ms * 0.5
     # every input crosses the link at least once: q, out, dout, k, v and lse
     assert st.h2d_bytes >= 5 * B * H * N * d * 2 + B * H * N * 4
     assert st.d2h_bytes == 3 * B * H * N * d * 2
