@@ -739,14 +739,43 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         }
       }
       if constexpr (HD == 64) {
-        // P^T and dS^T of the previous step are consumed once its products are done; its dQ is then read out
+        // P^T and dS^T of the previous step are consumed once its products are done; its dQ is read out of
+        // tensor memory while this step's P^T and dS^T go in, under one wait and one fence
         if (ok && it > 0) {
           ok = wait_abort(bar_m2, static_cast<uint32_t>((it - 1) & 1), tmo, abort_flag, kBwdTimeoutMMA, 4);
+          const int qs = (it - 1) & 1;
+          if (ok && it - 1 >= 2)
+            ok = wait_abort(&bar_dqfree[qs], static_cast<uint32_t>(((it - 3) >> 1) & 1), tmo, abort_flag,
+                            kBwdTimeoutSoftmax, 9);
           ok = __all_sync(0xffffffffu, ok);
           if (ok) {
             tc_fence_after();
-            ok = stage_dq(it - 1);
+            uint32_t o[16];
+            tmem_ld16(trow + C::COL_DQ + wg * 16, o);
+            tmem_st16(trow + 448u + static_cast<uint32_t>(wg * (QC / 2)), &pw[0]);
+#pragma unroll
+            for (int u = 0; u < QC / 8; ++u)
+              st_shared_v4(ds_row + static_cast<uint32_t>(((ds_c0 + u) ^ sw) * 16), dw[4 * u], dw[4 * u + 1],
+                           dw[4 * u + 2], dw[4 * u + 3]);
+            tmem_wait_ld();
+            reg_fence16(o);
+            const uint32_t dst = dq_row + static_cast<uint32_t>(qs * C::DQ_SLOT);
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+              st_shared_v4(dst + static_cast<uint32_t>(((dq_c0 + u) ^ sw) * 16),
+                           __float_as_uint(__uint_as_float(o[4 * u]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[4 * u + 1]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[4 * u + 2]) * p.scale),
+                           __float_as_uint(__uint_as_float(o[4 * u + 3]) * p.scale));
+            tmem_wait_st();
+            fence_proxy_async_smem();
+            tc_fence_before();
+            mbar_arrive(&bar_staged[qs]);
+            mbar_arrive(bar_ready);
+            put_rows(slot ^ 1, nrow);
           }
+          ok = __all_sync(0xffffffffu, ok);
+          continue;  // this step's hand-offs are done
         }
       } else {
         // the previous step's dQ, staged over the dS^T tile, must have been read by its reduction
