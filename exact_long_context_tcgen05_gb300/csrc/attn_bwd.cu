@@ -24,8 +24,8 @@
 //                    The dQ tile is scaled, staged in shared memory and added into an fp32
 //                    accumulator by TMA bulk reduce-add. S^T and dP^T of the next tile are computed
 //                    while the elementwise warps work on the current one. Roles: a TMA producer warp,
-//                    an MMA issuer warp, a dQ reduction warp and four (d = 128: two) elementwise
-//                    warpgroups, joined by mbarriers. dK_j, dV_j are written once, after the last
+//                    an MMA issuer warp (d = 64: a second one for dQ), a dQ reduction warp and four
+//                    (d = 128: two) elementwise warpgroups, joined by mbarriers. dK_j, dV_j are written once, after the last
 //                    query tile.
 //   bwd_dq_kernel    fp32 dQ accumulator -> dQ in the input dtype
 // P and dS enter the MMAs rounded to the input dtype; everything else is fp32. Head dimension 64 or 128
@@ -54,7 +54,7 @@ __device__ DevErr g_bwd_err;
 constexpr int BT = 128;                         // keys per CTA tile, queries per step
 constexpr uint32_t BOX = BT * 64 * 2;           // one 128 x 64 box of 16-bit elements (16 KiB)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NBAR = 14;
+constexpr int NBAR = 15;
 
 // Shared- and tensor-memory layout per head dimension.
 // d = 64: K, V, a two-slot ring of Q and dO tiles, the dS^T tile and two dQ staging slots of
@@ -108,7 +108,7 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                : "memory");
 }
 // Warp roles: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
-// reductions (warp 2), one idle warp; then the elementwise warpgroups, each on an equal share of the
+// reductions (warp 2), the dQ products' issuer at d = 64 (warp 3; idle at d = 128); then the elementwise warpgroups, each on an equal share of the
 // step's 128 query columns, so each tensor-memory lane quarter (SM sub-partition) interleaves one warp of
 // each: four at d = 64 (32 columns each; 640 threads), two at d = 128 (64 each; 384 threads, whose
 // tensor and shared memory leave no room for more). setmaxnreg moves registers from warpgroup 0 to the
@@ -259,7 +259,7 @@ __device__ __forceinline__ void issue_t(uint32_t dcol, uint64_t a0, uint64_t b0,
 // dQ = dS K (A = the same dS^T tile read MN-major): 8 steps of 16 queries (dV, dK) or keys (dQ); the
 // B operands dO, Q and K are MN-major with N = d (the second 64-feature box at the descriptor's
 // leading-byte offset when d = 128).
-template <int FIRST, int HD>
+template <int FIRST, int HD, bool DQ>
 __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t dQm, uint64_t dS_k, uint64_t dS_mn,
                                             uint64_t dK, uint32_t idesc_g, uint32_t idesc_q) {
   using C = BwdCfg<HD>;
@@ -274,8 +274,10 @@ __device__ __forceinline__ void issue_grads(uint32_t tmem, uint64_t dG, uint64_t
       mma_ts_imm<1>(tmem + C::COL_DV, tmem + C::col_pt(ks), dG + off, idesc_g);
       mma_ss_imm<1>(tmem + C::COL_DK, dS_k + koff, dQm + off, idesc_g);
     }
-    if (ks == 0) mma_ss_imm<0>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
-    else mma_ss_imm<1>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
+    if (DQ) {
+      if (ks == 0) mma_ss_imm<0>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
+      else mma_ss_imm<1>(tmem + C::COL_DQ, dS_mn + off, dK + off, idesc_q);
+    }
   }
 }
 
@@ -316,6 +318,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
                                     // also tells the MMA issuer that dQ has left the dP^T columns
   uint64_t* bar_dqfree = bars + 11; // [2] dQ staging slot read by its reduction
   uint64_t* bar_idle = bars + 13;   // every MMA done (commit)
+  uint64_t* bar_idle3 = bars + 14;  // d = 64: every dQ product of warp 3 done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -356,10 +359,11 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
       mbar_init(&bar_dqfree[s], 1);
     }
     mbar_init(bar_m1, 1);
-    mbar_init(bar_m2, 1);
+    mbar_init(bar_m2, HD == 64 ? 2 : 1);  // d = 64: dV / dK (warp 1) and dQ (warp 3) commit separately
     mbar_init(bar_sfree, NWG * 128);
     mbar_init(bar_ready, NWG * 128);
     mbar_init(bar_idle, 1);
+    mbar_init(bar_idle3, 1);
     *abort_flag = 0;
     fence_mbar_init();
   }
@@ -472,8 +476,8 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         const uint32_t so = static_cast<uint32_t>(it % NSLOT) * SLOT16;
         tc_fence_after();
         if (leader) {
-          if (it == 0) issue_grads<1, HD>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
-          else issue_grads<0, HD>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+          if (it == 0) issue_grads<1, HD, HD != 64>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
+          else issue_grads<0, HD, HD != 64>(tmem, dG0_mn + so, dQ0_mn + so, dS_k, dS_mn, dK_mn, IDESC_V, IDESC_Q);
           tc_commit(bar_m2);
           tc_commit(&bar_qfree[it % NSLOT]);
         }
@@ -568,6 +572,35 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
         mbar_arrive(&bar_dqfree[slot]);
       }
       bulk_wait_all();
+    } else if (HD == 64 && warp == 3) {
+      // ---------------------------------------------------------------- dQ products (d = 64)
+      // dQ = dS K of each step, issued beside warp 1's dV / dK (each issuing warp shares its sub-partition
+      // with four elementwise warps, so the step's 24 small products are issued from two of them); dQ of
+      // the previous step has left tensor memory once the step's P^T / dS^T hand-off has arrived
+      constexpr uint32_t IDESC_Q = idesc_f16(DT, 1, 128, HD) | (1u << 15);
+      const bool leader = elect_lane();
+      const uint64_t dK_mn = smem_desc_sw128(smem_u32(sK), 1024u, 1024);
+      const uint64_t dS_mn = smem_desc_sw128(smem_u32(sdS), BOX, 1024);
+      bool ok = __all_sync(0xffffffffu, wait_abort(bar_kv, 0, tmo, abort_flag, kBwdTimeoutLoad, 1));
+      for (int it = 0; ok && it < nit; ++it) {
+        ok = __all_sync(0xffffffffu,
+                        wait_abort(bar_ready, static_cast<uint32_t>(it & 1), tmo, abort_flag, kBwdTimeoutSoftmax, 7));
+        if (!ok) break;
+        tc_fence_after();
+        if (leader) {
+#pragma unroll
+          for (int ks = 0; ks < BT / 16; ++ks) {
+            const uint32_t off = static_cast<uint32_t>(ks * (2048 >> 4));
+            if (ks == 0) mma_ss_imm<0>(tmem + C::COL_DQ, dS_mn + off, dK_mn + off, IDESC_Q);
+            else mma_ss_imm<1>(tmem + C::COL_DQ, dS_mn + off, dK_mn + off, IDESC_Q);
+          }
+          tc_commit(bar_m2);
+        }
+        __syncwarp();
+      }
+      if (leader) tc_commit(bar_idle3);
+      __syncwarp();
+      mbar_wait_bounded(bar_idle3, 0, tmo);
     }
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(TH::HIGH));
