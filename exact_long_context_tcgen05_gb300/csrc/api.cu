@@ -58,6 +58,11 @@ static int report_device_error(const DevErr& e) {
               "fp32 summation order", "running-sum slots", e.block);
     return CQSA_ERR_DEVICE;
   }
+  if (e.code == kDevMisaligned) {
+    set_error("the backward kernel's dynamic shared memory base is not 1024-byte aligned (block %d): its "
+              "swizzled tiles need that alignment, and it stopped before computing anything", e.block);
+    return CQSA_ERR_DEVICE;
+  }
   set_error("device wait gave up (code %d, block %d, site %d)", e.code, e.block, e.where);
   return CQSA_ERR_TIMEOUT;
 }

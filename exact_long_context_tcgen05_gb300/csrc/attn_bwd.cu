@@ -54,11 +54,14 @@ __device__ DevErr g_bwd_err;
 constexpr int BT = 128;                         // keys per CTA tile, queries per step
 constexpr uint32_t BOX = BT * 64 * 2;           // one 128 x 64 box of 16-bit elements (16 KiB)
 constexpr uint32_t TMEM_COLS = 512;
-constexpr int NBAR = 15;
+constexpr int NBAR = 17;
 
 // Shared- and tensor-memory layout per head dimension.
-// d = 64: K, V, a two-slot ring of Q and dO tiles, the dS^T tile and two dQ staging slots of
-//   128 x 64 fp32 (195 KiB). Tensor memory: S^T, dP^T, dV, dK, dQ and P^T (16-bit pairs), 512 columns.
+// d = 64: K, V, a three-slot ring of Q and dO tiles (the tile two steps ahead loads while a step's
+//   products run: with two slots its load waited for them, ~0.3 us a step), the dS^T tile, two dQ
+//   staging slots of 128 x 64 fp32 and the row values (226 KiB, with no slack: the kernel checks that
+//   the dynamic shared memory base is 1024-byte aligned). Tensor memory: S^T, dP^T, dV, dK, dQ and
+//   P^T (16-bit pairs), 512 columns.
 // d = 128: every 128-row tile is two boxes, so K, V, one Q and one dO tile and dS^T take 160 KiB; dQ
 //   (128 x 128 fp32, 64 KiB) is staged over the dS^T tile and the 32 KiB behind it once the step's
 //   products have read dS^T. Q and dO have their own load and release barriers (bar_q[0] / bar_q[1],
@@ -67,7 +70,7 @@ constexpr int NBAR = 15;
 //   256-383, dK 384-511.
 template <int HD>
 struct BwdCfg {
-  static constexpr int NSLOT = HD == 64 ? 2 : 1;          // Q/dO ring slots
+  static constexpr int NSLOT = HD == 64 ? 3 : 1;          // Q/dO ring slots
   static constexpr uint32_t TILE = BOX * (HD / 64);       // one 128-row tile of Q, dO, K or V
   static constexpr uint32_t OFF_K = 0, OFF_V = TILE, OFF_Q = 2 * TILE;
   static constexpr uint32_t OFF_G = OFF_Q + NSLOT * TILE;
@@ -75,9 +78,10 @@ struct BwdCfg {
   static constexpr uint32_t OFF_DQ = OFF_DS + 2 * BOX;
   static constexpr uint32_t DQ_SLOT = BT * 64 * 4;        // d = 64: one staging slot (128 x 64 fp32)
   static constexpr uint32_t OFF_ROW = HD == 64 ? OFF_DQ + 2 * DQ_SLOT : OFF_DQ + 2 * BOX;
-  // row values: per elementwise warp and slot, lse2 and D of the step's 128 / NWG queries (8 KiB)
-  static constexpr uint32_t OFF_BAR = OFF_ROW + 2 * 256 * 4 * 4;
-  static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16 + 1024;  // + slack for 1024-byte alignment
+  // row values: per elementwise warpgroup and slot, lse2 and D of the step's 128 / NWG queries (2 KiB)
+  static constexpr uint32_t OFF_BAR = OFF_ROW + 2 * 2 * 128 * 4;
+  // the dynamic shared memory base is 1024-byte aligned (the kernel checks, and stops with an error if not)
+  static constexpr uint32_t SMEM_BYTES = OFF_BAR + NBAR * 8 + 16;
   static constexpr uint32_t COL_S = 0, COL_DP = 128;
   static constexpr uint32_t COL_DV = 256, COL_DK = 256 + HD;
   static constexpr uint32_t COL_DQ = HD == 64 ? 384 : 128;
@@ -295,8 +299,12 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
   constexpr int CW = NWG == 4 ? 16 : 32;  // columns per tensor-memory load
   constexpr int NSLOT = C::NSLOT;
   constexpr uint32_t TILE = C::TILE;
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  extern __shared__ __align__(1024) uint8_t smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {  // the 128-byte swizzled tiles need 1024-byte alignment
+    if (threadIdx.x == 0) record_bwd_error(kDevMisaligned, 0);
+    return;
+  }
+  uint8_t* sm = smem_raw;
   uint8_t* sK = sm + C::OFF_K;
   uint8_t* sV = sm + C::OFF_V;
   uint8_t* sQ = sm + C::OFF_Q;    // [NSLOT][TILE]
@@ -308,17 +316,17 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
   float* sRow = reinterpret_cast<float*>(sm + C::OFF_ROW);  // per elementwise warp: [slot 2][lse2 | D]
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + C::OFF_BAR);
   uint64_t* bar_kv = bars + 0;
-  uint64_t* bar_q = bars + 1;       // [NSLOT] Q/dO slot loaded
-  uint64_t* bar_qfree = bars + 3;   // [NSLOT] Q/dO slot read by every MMA (commit)
-  uint64_t* bar_m1 = bars + 5;      // S^T, dP^T ready (commit)
-  uint64_t* bar_m2 = bars + 6;      // dV, dK, dQ products done (commit)
-  uint64_t* bar_sfree = bars + 7;   // S^T, dP^T read into registers (256 elementwise threads)
-  uint64_t* bar_ready = bars + 8;   // P^T and dS^T written, previous dQ read out (256 threads)
-  uint64_t* bar_staged = bars + 9;  // [2] dQ staging slot written (256 threads); d = 128: slot 0 only, and it
+  uint64_t* bar_q = bars + 1;       // [3] Q/dO slot loaded (d = 128: [0] Q, [1] dO)
+  uint64_t* bar_qfree = bars + 4;   // [3] Q/dO slot read by every MMA (commit)
+  uint64_t* bar_m1 = bars + 7;      // S^T, dP^T ready (commit)
+  uint64_t* bar_m2 = bars + 8;      // dV, dK, dQ products done (commit)
+  uint64_t* bar_sfree = bars + 9;   // S^T, dP^T read into registers (256 elementwise threads)
+  uint64_t* bar_ready = bars + 10;  // P^T and dS^T written, previous dQ read out (256 threads)
+  uint64_t* bar_staged = bars + 11; // [2] dQ staging slot written (256 threads); d = 128: slot 0 only, and it
                                     // also tells the MMA issuer that dQ has left the dP^T columns
-  uint64_t* bar_dqfree = bars + 11; // [2] dQ staging slot read by its reduction
-  uint64_t* bar_idle = bars + 13;   // every MMA done (commit)
-  uint64_t* bar_idle3 = bars + 14;  // d = 64: every dQ product of warp 3 done (commit)
+  uint64_t* bar_dqfree = bars + 13; // [2] dQ staging slot read by its reduction
+  uint64_t* bar_idle = bars + 15;   // every MMA done (commit)
+  uint64_t* bar_idle3 = bars + 16;  // d = 64: every dQ product of warp 3 done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(bars + NBAR);
   volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_slot + 1);
 
@@ -352,9 +360,11 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
 
   if (tid == 0) {
     mbar_init(bar_kv, 1);
-    for (int s = 0; s < 2; ++s) {
+    for (int s = 0; s < 3; ++s) {
       mbar_init(&bar_q[s], 1);
       mbar_init(&bar_qfree[s], 1);
+    }
+    for (int s = 0; s < 2; ++s) {
       mbar_init(&bar_staged[s], NWG * 128);
       mbar_init(&bar_dqfree[s], 1);
     }
@@ -383,7 +393,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
       prefetch_tensormap(&tmK);
       prefetch_tensormap(&tmV);
       prefetch_tensormap(&tmG);
-      int issued[2] = {0, 0};
+      int issued[3] = {0, 0, 0};
       auto load_q = [&](int it) {
         const int slot = it % NSLOT;
         mbar_arrive_expect_tx(&bar_q[slot], 2 * TILE);
@@ -437,7 +447,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
       }
       // every load issued lands before the CTA exits (bounded waits)
       if (!skip_kv) mbar_wait_bounded(bar_kv, 0, tmo);
-      for (int s = 0; s < 2; ++s)
+      for (int s = 0; s < 3; ++s)
         if (issued[s] > 0) mbar_wait_bounded(&bar_q[s], static_cast<uint32_t>((issued[s] - 1) & 1), tmo);
     } else if (warp == 1) {
       // ---------------------------------------------------------------- MMA issuer
@@ -535,7 +545,7 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
           if (it + 1 < nit) {
             // S^T / dP^T of step it are in registers: the next step's products may overwrite them
             ok = wait_all(bar_sfree, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 6);
-            if (ok) ok = wait_all(&bar_q[(it + 1) & 1], static_cast<uint32_t>(((it + 1) >> 1) & 1), kBwdTimeoutLoad, 2);
+            if (ok) ok = wait_all(&bar_q[(it + 1) % NSLOT], static_cast<uint32_t>(((it + 1) / NSLOT) & 1), kBwdTimeoutLoad, 2);
             if (ok) issue_m1(it + 1);
           }
           if (ok) ok = wait_all(bar_ready, static_cast<uint32_t>(it & 1), kBwdTimeoutSoftmax, 7);
@@ -620,10 +630,12 @@ __global__ void __launch_bounds__(BwdThreads<HD>::NTHR, 1)
     const uint32_t dq_row = smem_u32(sdQ) + static_cast<uint32_t>((NWG == 4 ? wg / 2 : wg) * (BT * 128) + r * 128);
     const int dq_c0 = NWG == 4 ? (wg % 2) * 4 : 0;
     const int sw = r & 7;
-    // Row values private to this warp ([slot][lse2 QC | D QC]): each lane fetches QC / 32 queries' lse2
-    // and D one step ahead and the warp shares them through shared memory after a __syncwarp, so no
-    // barrier across the warpgroup is needed per step.
-    float* rows = sRow + (warp - 4) * 4 * QC;
+    // Row values of this warpgroup's queries ([slot][lse2 QC | D QC]): each lane fetches QC / 32 queries'
+    // lse2 and D one step ahead, and every warp of the warpgroup stores the same values after its step's
+    // hand-off, then reads them after a __syncwarp, so no barrier across the warpgroup is needed. A
+    // warp rewrites a slot only after the products of the step before, which wait for every warp's
+    // hand-off, and each warp reads the slot before its own hand-off.
+    float* rows = sRow + wg * 4 * QC;
     struct RowVals {
       float l[QC / 32], d[QC / 32];
     };

@@ -17,7 +17,8 @@ enum : int {
   kDevTimeoutKV = 2,      // a K/V stage never arrived or was never released
   kDevTimeoutMMA = 3,     // an MMA completion never arrived
   kDevTimeoutSoftmax = 4,  // softmax -> MMA hand-off never arrived
-  kDevSmSlot = 5           // an SM id beyond the running-sum slots (the fold was skipped)
+  kDevSmSlot = 5,          // an SM id beyond the running-sum slots (the fold was skipped)
+  kDevMisaligned = 6       // the dynamic shared memory base is not 1024-byte aligned (nothing was computed)
 };
 
 struct DevErr {
