@@ -715,6 +715,7 @@ def measure_stream_bwd(cq, dev, N=131072, C=16384, H=8):
             "n_pairs": st.n_chunks, "peak_device_bytes": st.peak_device_bytes,
             "device_resident_ms": dev_ms, "device_resident_tflops": flop / (dev_ms / 1e3) / 1e12,
             "wall_over_device_resident": wall / (dev_ms / 1e3),
+            "numa_nodes_of_host_pages": _numa_nodes(host[0]),
             "note": "resident schedule (inputs copied once and kept): one chunk-pair launch per key chunk over "
                     "every query it meets, on up to four streams; n_pairs counts those launches, compute_s is "
                     "the union of the call's kernel intervals (D, launches, output casts)"}
