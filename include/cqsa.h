@@ -43,7 +43,8 @@ typedef enum {
   CQSA_ERR_CUDA = -3,        /* a CUDA runtime/driver call failed */
   CQSA_ERR_OOM = -4,         /* a device or pinned allocation failed: the caller may re-plan */
   CQSA_ERR_TIMEOUT = -5,     /* a device-side bounded wait gave up (see cqsa_device_error) */
-  CQSA_ERR_DEVICE = -6       /* no usable sm_103 device */
+  CQSA_ERR_DEVICE = -6       /* no usable sm_103 device, or a device-side condition other than a wait
+                                (see cqsa_device_error) */
 } cqsa_status;
 
 typedef enum { CQSA_F16 = 0, CQSA_BF16 = 1, CQSA_F32 = 2 /* outputs only */ } cqsa_dtype;
@@ -343,7 +344,10 @@ const char* cqsa_last_error(void);
 /*
  * Device error word written by a kernel whose bounded wait gave up (instead of hanging the GPU):
  * synchronises the device, stores the code (0 = none) and the block index, optionally clears it.
- * Returns CQSA_OK, or CQSA_ERR_TIMEOUT if a code was set.
+ * Returns CQSA_OK, or CQSA_ERR_TIMEOUT if a code was set. Two codes return CQSA_ERR_DEVICE instead:
+ * 5, a d = 128 forward CTA that ran on an SM beyond its running-sum slots (the result is still exact),
+ * and 6, a backward kernel whose dynamic shared memory base was not 1024-byte aligned (it stopped
+ * before computing anything).
  */
 int cqsa_device_error(int* code, int* block, int clear);
 
