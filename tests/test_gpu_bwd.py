@@ -56,6 +56,7 @@ def _check(got: np.ndarray, ref: np.ndarray, dtype, what):
     (2, 3, 333, 64, True, syn.F16),      # ragged last tile, several heads and batches
     (1, 2, 200, 64, False, syn.F16),
     (1, 1, 77, 64, True, syn.F16),       # one partial tile
+    (1, 1, 1536, 64, False, syn.F16),    # twelve query tiles per key tile: the Q/dO ring wraps four times
     (1, 2, 512, 64, True, syn.BF16),
     (1, 1, 384, 64, False, syn.BF16),
     (1, 2, 640, 128, True, syn.F16),     # head dim 128: one Q/dO slot, dQ staged over dS^T
