@@ -267,3 +267,44 @@ def test_stream_backward(cq, B, H, N, C, causal, d, resident):
         m = m.float().cpu()
         diff = float((t.float() - m).abs().max())
         assert diff <= 4 * u * float(m.abs().max()), (name, diff)
+
+
+@pytest.mark.slow
+@pytest.mark.parametrize("resident", [True, False])
+def test_stream_backward_32k_sampled_vs_oracle(cq, resident):
+    """The host-resident backward at 32,768 tokens in 8,192-token chunks (B=1 H=4 d=64 fp16 causal), with
+    the inputs kept resident (one launch per key chunk) and through double-buffered chunk pairs: dq on
+    2,048+ seeded sampled query rows and dk, dv on sampled key columns of two heads against the FP64
+    oracle, and every gradient against the monolithic device call within a few ulps."""
+    B, H, N, d, C = 1, 4, 32768, 64, 8192
+    dtype = syn.F16
+    (qn, kn, vn, gn), mono_grads = _run(cq, B, H, N, d, True, dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, True, dtype)
+    host = [t.cpu().pin_memory() for t in (q, k, v, out, g, lse)]
+    grads = [torch.empty(q.shape, dtype=q.dtype).pin_memory() for _ in range(3)]
+    cq.cqsa_set_stream_kv_resident_bytes(1 << 40 if resident else 0)
+    try:
+        st = cq.cqsa_stream_attn_bwd_ex(*host, *grads, B, H, N, d, True, 0.0, dtype, C)
+    finally:
+        cq.cqsa_set_stream_kv_resident_bytes(-1)
+    n_chunks = N // C
+    assert st.n_chunks == (n_chunks if resident else n_chunks * (n_chunks + 1) // 2)
+    dq, dk, dv = grads
+    rows = syn.sample_rows(B, H, N, 2048, chunk=C, causal_tile=128)
+    js = syn.sample_rows(1, 1, N, 128, seed=5, must_i=(C - 1, C, N - 128, N // 2))[:, 2]
+    cols = np.concatenate([np.stack([np.zeros_like(js), np.full_like(js, hh), js], axis=1) for hh in (0, H - 1)])
+
+    def gather(t, idx):
+        return t[torch.as_tensor(idx[:, 0]), torch.as_tensor(idx[:, 1]), torch.as_tensor(idx[:, 2])].float().numpy().astype(np.float64)
+
+    ref_dq = oracle.attn_bwd_rows(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=True, rows=rows)
+    ref_dk, ref_dv = oracle.attn_bwd_cols(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=True, cols=cols)
+    for name, got, ref in (("dq", gather(dq, rows), ref_dq), ("dk", gather(dk, cols), ref_dk),
+                           ("dv", gather(dv, cols), ref_dv)):
+        _check(got, ref, dtype, f"stream 32K {name} resident={resident}")
+    u = U[dtype]
+    for name, t, m in zip(("dq", "dk", "dv"), grads, mono_grads):
+        m = m.float().cpu()
+        diff = float((t.float() - m).abs().max())
+        assert diff <= 4 * u * float(m.abs().max()), (name, diff)
