@@ -163,6 +163,35 @@ def test_backward_d128_8k_sampled_vs_oracle(cq):
         _check(got, ref, dtype, f"8K d=128 {name}")
 
 
+@pytest.mark.slow
+def test_backward_bf16_d128_bench_shape_sampled_vs_oracle(cq):
+    """The benchmark's head-dim-128 backward (B=2 H=32 N=16,384 d=128 bf16 non-causal, K scaled by 3, the
+    inputs of its bench line) against the FP64 oracle on 512+ sampled query rows (dq) and 64 sampled key
+    columns of the first and last head (dk, dv)."""
+    B, H, N, d, dtype = 2, 32, 16384, 128, syn.BF16
+    qn, kn, vn = syn.qkv(B, H, N, d, seed=0, dtype=dtype, k_mul=3.0)
+    gn = syn.normal(B, H, N, d, seed=0, tensor_id=syn.TID_DO, dtype=dtype)
+    q, k, v, g = (to_dev(x, dtype) for x in (qn, kn, vn, gn))
+    out, lse = mono(cq, q, k, v, B, H, N, d, False, dtype)
+    dq, dk, dv = cq.attention_backward(q, k, v, out, g, lse, causal=False)
+    torch.cuda.synchronize()
+    rc, code, _ = cq.cqsa_device_error()
+    assert rc == cq.CQSA_OK and code == 0
+    rows = syn.sample_rows(B, H, N, 512, seed=11)
+    js = syn.sample_rows(1, 1, N, 32, seed=12, must_i=(0, N - 1, N // 2))[:, 2]
+    cols = np.concatenate([np.stack([np.full_like(js, bb), np.full_like(js, hh), js], axis=1)
+                           for bb, hh in ((0, 0), (B - 1, H - 1))])
+
+    def gather(t, idx):
+        return to_np64(t[torch.as_tensor(idx[:, 0]), torch.as_tensor(idx[:, 1]), torch.as_tensor(idx[:, 2])])
+
+    ref_dq = oracle.attn_bwd_rows(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=False, rows=rows, dtype=dtype)
+    ref_dk, ref_dv = oracle.attn_bwd_cols(qn, kn, vn, gn, B=B, H=H, N=N, d=d, causal=False, cols=cols, dtype=dtype)
+    for name, got, ref in (("dq", gather(dq, rows), ref_dq), ("dk", gather(dk, cols), ref_dk),
+                           ("dv", gather(dv, cols), ref_dv)):
+        _check(got, ref, dtype, f"bf16 d=128 16K {name}")
+
+
 def _chunked_backward(cq, q, k, v, g, out, lse, B, H, N, d, C, causal, dtype, skip_masked=True):
     """The backward over (query chunk, key chunk) pairs of C tokens through cqsa_attn_bwd_chunk, with
     per-chunk fp32 accumulators cast to dtype at the end."""
