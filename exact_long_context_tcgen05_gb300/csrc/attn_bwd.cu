@@ -112,18 +112,20 @@ __device__ __forceinline__ void reg_fence16(uint32_t (&r)[16]) {
                : "memory");
 }
 // Warp roles: warpgroup 0 = TMA producer (warp 0), MMA issuer and tensor-memory owner (warp 1), dQ
-// reductions (warp 2), the dQ products' issuer at d = 64 (warp 3; idle at d = 128); then the elementwise warpgroups, each on an equal share of the
-// step's 128 query columns, so each tensor-memory lane quarter (SM sub-partition) interleaves one warp of
-// each: four at d = 64 (32 columns each; 640 threads), two at d = 128 (64 each; 384 threads, whose
-// tensor and shared memory leave no room for more). setmaxnreg moves registers from warpgroup 0 to the
-// elementwise warpgroups: d = 64, 128 * 64 + 512 * 104 <= 640 * 96; d = 128, 128 * 96 + 256 * 200 <=
-// 384 * 168. (Two warpgroups at d = 64: 860 TFLOP/s on the 32K causal backward; four: 913, with
-// 104 registers; four with 96: 888.)
+// reductions (warp 2), the dQ products' issuer at d = 64 (warp 3; idle at d = 128); then the
+// elementwise warpgroups, each on an equal share of the step's 128 query columns, so each tensor-memory
+// lane quarter (SM sub-partition) interleaves one warp of each: four at d = 64 (32 columns each; 640
+// threads), two at d = 128 (64 each; 384 threads, whose tensor and shared memory leave no room for
+// more). setmaxnreg splits the launch's registers between warpgroup 0 and the elementwise warpgroups:
+// d = 64, 128 * 64 + 512 * 104 <= 640 * 96; d = 128, 128 * 152 + 256 * 176 = 384 * 168. (Two warpgroups
+// at d = 64: 860 TFLOP/s on the 32K causal backward; four: 913, with 104 registers; four with 96: 888.
+// At d = 128 warpgroup 0's unrolled product issue spilled below ~150 registers: 96 / 200 spilled 350
+// bytes, 152 / 176 none, 960 -> 1,002 TFLOP/s on the 32K causal backward.)
 template <int HD>
 struct BwdThreads {
   static constexpr int NWG = HD == 64 ? 4 : 2;
   static constexpr int NTHR = 128 * (NWG + 1);
-  static constexpr int LOW = HD == 64 ? 64 : 96, HIGH = HD == 64 ? 104 : 200;
+  static constexpr int LOW = HD == 64 ? 64 : 152, HIGH = HD == 64 ? 104 : 176;
   static constexpr int LAUNCH_REGS = HD == 64 ? 96 : 168;
   static_assert(128 * LOW + 128 * NWG * HIGH <= NTHR * LAUNCH_REGS, "register split exceeds the launch allocation");
 };
